@@ -1,0 +1,181 @@
+/*
+ * specoptim -- GB300 (sm_103a) kernels for the fast-circuit hot path of
+ * "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes"
+ * (NeurIPS 2026, arXiv 2609.14339; papernotes.org notes):
+ *
+ *   * the spectral-correction optimizer step (key design 2: anchor EMA;
+ *     key design 3: SVD of the anchor momentum, Tikhonov filter, two-sided
+ *     projection, convex blend, AdamW), and
+ *   * the in-graph activation mask (key design 1: keep K = round((1-p)H)
+ *     dims per token chosen by a shared deterministic function g; only the K
+ *     kept values are sent; the backward pass reuses the same indices).
+ *
+ * Conventions for every entry point below
+ *   - Pointers named as device pointers must point to GPU memory of the
+ *     current device; they are owned by the caller unless stated otherwise.
+ *     Matrices are fp32, row-major, m x n with leading dimension n (as in
+ *     torch.nn.Linear.weight: m = out_features, n = in_features), and must be
+ *     16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream unless stated otherwise.
+ *   - Every call returns a status code and never throws or aborts.  On a
+ *     non-zero status, specoptim_last_error() gives a message (per thread).
+ *   - A handle serves one weight matrix and is not thread-safe.
+ */
+#ifndef SPECOPTIM_H
+#define SPECOPTIM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SPECOPTIM_OK                  0
+#define SPECOPTIM_ERR_INVALID_ARG     1 /* null pointer, bad size or hyperparameter   */
+#define SPECOPTIM_ERR_MISALIGNED      2 /* a pointer is not 16-byte aligned           */
+#define SPECOPTIM_ERR_CUDA            3 /* a CUDA call failed (text in last_error)    */
+#define SPECOPTIM_ERR_NOT_CONVERGED   4 /* SVD hit svd_max_sweeps; old factors kept   */
+#define SPECOPTIM_ERR_NOT_IMPLEMENTED 5
+#define SPECOPTIM_ERR_TIMEOUT         6 /* a bounded device-side wait gave up         */
+
+/* GEMM arithmetic of the projection (key design 3, projection equation) */
+#define SPECOPTIM_PREC_TF32 0  /* tcgen05 kind::tf32 tensor cores, fp32 accumulate */
+#define SPECOPTIM_PREC_FP32 1  /* fp32 FMA on the SIMT cores (slow, exact fp32)    */
+
+typedef struct specoptim specoptim_t;
+
+typedef struct {
+    int32_t m, n;           /* weight shape, m = out_features, n = in_features (>= 1) */
+    float beta_anc;         /* anchor EMA coefficient (default 0.9)                   */
+    float tau_p;            /* Tikhonov threshold on raw singular values (1e-3), > 0  */
+    float alpha;            /* blend weight of the masked gradient (0.3), in [0,1]    */
+    float beta1, beta2;     /* AdamW moment coefficients (0.9, 0.999)                 */
+    float eps;              /* AdamW epsilon (1e-8)                                   */
+    float weight_decay;     /* AdamW decoupled weight decay (0.01)                    */
+    int32_t precision;      /* SPECOPTIM_PREC_TF32 (default) or SPECOPTIM_PREC_FP32    */
+    int32_t svd_max_sweeps; /* Jacobi sweep limit of the SVD refresh (default 20)      */
+    float svd_tol;          /* off-diagonal / total Frobenius norm to stop at (1e-5)  */
+} specoptim_config;
+
+/* Fills *cfg with the defaults above for an m x n weight.  The defaults are
+ * the pages' recipe: tau_p = 1e-3, alpha = 0.3, beta_anc = 0.9 ("loss
+ * function / training strategy"); AdamW betas / eps / weight decay are the
+ * usual AdamW values the workloads state. */
+int specoptim_config_default(specoptim_config *cfg, int32_t m, int32_t n);
+
+/* Creates the optimizer state of one weight matrix.  Allocates on the current
+ * device, zero-initialised on `stream`: anchor momentum M (m x n), SVD factors
+ * U (m x r), s (r), V (n x r), filter d (r) with r = min(m, n), AdamW moments
+ * (m x n) and a workspace.  The step counter starts at 0.  Before the first
+ * svd_refresh all factors are zero, so the filtered gradient is 0 and a step
+ * applies AdamW to alpha * G_mask.  *out receives the handle (owned by the
+ * library until specoptim_destroy). */
+int specoptim_create(specoptim_t **out, const specoptim_config *cfg, void *stream);
+
+/* Frees the handle and its device memory (synchronises the device first). */
+int specoptim_destroy(specoptim_t *h);
+
+/* Anchor momentum update, key design 2, EMA equation:
+ *   M <- beta_anc * M + (1 - beta_anc) * G_anc
+ * G_anc: device, m x n fp32, read only.  No bias correction. */
+int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void *stream);
+
+/* SVD refresh, key design 3: thin SVD M = U diag(s) V^T (r = min(m, n),
+ * s descending) and the Tikhonov filter d_i = s_i / (s_i + tau_p).
+ * Computed as the eigen-decomposition of the Gram matrix of M on its short
+ * side (fp32) by block Jacobi, then the long-side factor as M V / s (or
+ * M^T U / s).  Columns with s_i = 0 are left zero (their d_i is 0).
+ * Synchronises `stream` once per Jacobi sweep to test convergence.
+ * sweeps_out (host pointer, may be NULL) receives the number of sweeps.
+ * Returns SPECOPTIM_ERR_NOT_CONVERGED, keeping the previous factors, if the
+ * off-diagonal norm is still above svd_tol after svd_max_sweeps sweeps. */
+int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out);
+
+/* Spectral-corrected step, key design 3 (projection and blend equations)
+ * followed by AdamW:
+ *   X = U^T G V,  X_filt = diag(d) X diag(d),  G_filt = U X_filt V^T,
+ *   G_proj = alpha G + (1 - alpha) G_filt,
+ *   t += 1;  W <- W (1 - lr wd);  m1 <- b1 m1 + (1-b1) G_proj;
+ *   m2 <- b2 m2 + (1-b2) G_proj^2;
+ *   W <- W - lr (m1 / (1-b1^t)) / (sqrt(m2 / (1-b2^t)) + eps).
+ * W: device m x n, updated in place.  G_mask: device m x n, read only.
+ * lr: this step's learning rate (a schedule stays on the host).
+ * G_filt_out, G_proj_out: optional device m x n outputs (NULL to skip).
+ * The four products are evaluated in the cheaper association for the shape
+ * (U^T G first when m >= n, G V first when m < n); the blend and the AdamW
+ * update run in the epilogue of the last product. */
+int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr, void *stream,
+                   float *G_filt_out, float *G_proj_out);
+
+/* Copies the current factors to caller device buffers (any may be NULL):
+ * U m x r, s r, V n x r, d r (row-major fp32). */
+int specoptim_get_factors(const specoptim_t *h, float *U, float *s, float *V, float *d,
+                          void *stream);
+
+/* Copies the state to caller device buffers (any may be NULL): anchor
+ * momentum M, AdamW moments exp_avg / exp_avg_sq (m x n each); *t (host,
+ * may be NULL) receives the step counter. */
+int specoptim_get_state(const specoptim_t *h, float *M, float *exp_avg, float *exp_avg_sq,
+                        int64_t *t, void *stream);
+
+/* Restores a state saved by specoptim_get_state (checkpoint resume); the SVD
+ * factors must be recomputed with specoptim_svd_refresh afterwards. */
+int specoptim_set_state(specoptim_t *h, const float *M, const float *exp_avg,
+                        const float *exp_avg_sq, int64_t t, void *stream);
+
+/* Plain AdamW (same update as in specoptim_step, with G_proj replaced by g)
+ * for tensors outside the spectral correction (embedding, norm vectors).
+ * W, g, exp_avg, exp_avg_sq: device fp32 arrays of numel elements, 16-byte
+ * aligned; t is the step number after increment (>= 1). */
+int specoptim_adamw(float *W, const float *g, float *exp_avg, float *exp_avg_sq, int64_t numel,
+                    int64_t t, float lr, float beta1, float beta2, float eps, float weight_decay,
+                    void *stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *specoptim_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Activation mask, key design 1: h~ = h (.) m, K = round((1-p) H) kept dims
+ * per token, m = g(layer, step, batch metadata, S, H) regenerated on both
+ * sides; backward dL/dh = (dL/dh~) (.) m with the same indices.
+ *
+ * g: row r (flattened token index b*T + t of the call) keeps the dims
+ * pi_r(0), ..., pi_r(K-1) of a keyed pseudo-random permutation pi_r of
+ * [0, H).  Keys: seed = sm64(sm64(sm64(layer) ^ step) ^ batch_id),
+ * rowkey = sm64(seed ^ r), k_i = low32(sm64(rowkey + i)), i < 4, with sm64
+ * the SplitMix64 output function.  pi_r: 4 alternating Feistel rounds on
+ * w = ceil(log2 H) bits (hi = w/2 bits, lo = w - w/2 bits; rounds
+ * hi ^= f(lo ^ k0), lo ^= f(hi ^ k1), hi ^= f(lo ^ k2), lo ^= f(hi ^ k3),
+ * f = MurmurHash3 fmix32 masked to the half width), repeated while the
+ * value is >= H.  Packed order is k order.
+ *
+ * dense: [rows][H], packed: [rows][K], element size elem_bytes (2 = bf16 /
+ * fp16, 4 = fp32); values are copied bit for bit.  0 <= K <= H <= 2^30.
+ * ------------------------------------------------------------------------ */
+
+/* K = floor((1 - p) * H + 0.5) evaluated in double; -1 if p is outside
+ * [0, 1] or H < 1. */
+int32_t mask_keep_count(double p, int32_t H);
+
+/* Forward (or activation-gradient) pack: packed[r][k] = dense[r][pi_r(k)]. */
+int mask_pack(const void *dense, void *packed, int64_t rows, int32_t H, int32_t K,
+              int32_t elem_bytes, uint32_t layer, uint64_t step, uint64_t batch_id, void *stream);
+
+/* Receiver unpack: dense[r][pi_r(k)] = packed[r][k]; all other entries are
+ * written as +0 (all-zero bits), whatever the sign or NaN-ness of h. */
+int mask_unpack(const void *packed, void *dense, int64_t rows, int32_t H, int32_t K,
+                int32_t elem_bytes, uint32_t layer, uint64_t step, uint64_t batch_id,
+                void *stream);
+
+/* The kept indices themselves: idx_out[r][k] = pi_r(k), int32, device
+ * (for tests and for callers that build their own fused ops). */
+int mask_indices(int32_t *idx_out, int64_t rows, int32_t H, int32_t K, uint32_t layer,
+                 uint64_t step, uint64_t batch_id, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECOPTIM_H */

@@ -1,0 +1,136 @@
+// HBM-bound element-wise kernels: the anchor EMA (key design 2 of
+// "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes") and
+// plain AdamW for tensors outside the spectral correction.  128-bit loads and
+// stores, grid sized to a multiple of the SM count, scalar tail.
+#include <algorithm>
+
+#include "common.cuh"
+#include "elementwise.cuh"
+
+namespace spco {
+namespace {
+
+int stream_grid(int64_t vec_items) {
+    int64_t g = (vec_items + 255) / 256;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(g, (int64_t)num_sms() * 8));
+}
+
+// M <- beta M + (1 - beta) G
+__global__ void __launch_bounds__(256)
+ema_kernel(float *__restrict__ M, const float *__restrict__ G, int64_t n, float beta) {
+    const float one_minus = 1.f - beta;
+    const int64_t nv = n / 4;
+    float4 *M4 = reinterpret_cast<float4 *>(M);
+    const float4 *G4 = reinterpret_cast<const float4 *>(G);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += stride) {
+        float4 m = M4[i];
+        const float4 g = __ldcs(&G4[i]);
+        m.x = beta * m.x + one_minus * g.x;
+        m.y = beta * m.y + one_minus * g.y;
+        m.z = beta * m.z + one_minus * g.z;
+        m.w = beta * m.w + one_minus * g.w;
+        M4[i] = m;
+    }
+    for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride)
+        M[i] = beta * M[i] + one_minus * G[i];
+}
+
+__device__ __forceinline__ void adamw_one(float &w, float g, float &m, float &v, const AdamWScalars &s) {
+    w *= s.decay;
+    m = s.beta1 * m + (1.f - s.beta1) * g;
+    v = s.beta2 * v + (1.f - s.beta2) * g * g;
+    w -= s.step_size * m / (sqrtf(v) * s.inv_sqrt_bc2 + s.eps);
+}
+
+__global__ void __launch_bounds__(256)
+adamw_kernel(float *__restrict__ W, const float *__restrict__ G, float *__restrict__ M1,
+             float *__restrict__ M2, int64_t n, AdamWScalars s) {
+    const int64_t nv = n / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += stride) {
+        float4 w = reinterpret_cast<float4 *>(W)[i];
+        const float4 g = __ldcs(reinterpret_cast<const float4 *>(G) + i);
+        float4 m = reinterpret_cast<float4 *>(M1)[i];
+        float4 v = reinterpret_cast<float4 *>(M2)[i];
+        adamw_one(w.x, g.x, m.x, v.x, s);
+        adamw_one(w.y, g.y, m.y, v.y, s);
+        adamw_one(w.z, g.z, m.z, v.z, s);
+        adamw_one(w.w, g.w, m.w, v.w, s);
+        reinterpret_cast<float4 *>(W)[i] = w;
+        reinterpret_cast<float4 *>(M1)[i] = m;
+        reinterpret_cast<float4 *>(M2)[i] = v;
+    }
+    for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride)
+        adamw_one(W[i], G[i], M1[i], M2[i], s);
+}
+
+// dst (cols x rows) = src (rows x cols)^T through a 32 x 33 shared tile,
+// optionally rounded to TF32 (round to nearest, ties away)
+__global__ void __launch_bounds__(256)
+transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows, int cols,
+                 int round) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
+    const int64_t tiles_c = (cols + 31) / 32, tiles = tiles_c * ((rows + 31) / 32);
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int r0 = (int)(t / tiles_c) * 32, c0 = (int)(t % tiles_c) * 32;
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int r = r0 + i, c = c0 + tx;
+            float v = (r < rows && c < cols) ? __ldcs(&src[(int64_t)r * cols + c]) : 0.f;
+            if (round) {
+                uint32_t b;
+                asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(v));
+                v = __uint_as_float(b);
+            }
+            tile[i][tx] = v;
+        }
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int c = c0 + i, r = r0 + tx;
+            if (c < cols && r < rows) dst[(int64_t)c * rows + r] = tile[tx][i];
+        }
+    }
+}
+
+}  // namespace
+
+int transpose_run(const float *src, float *dst, int rows, int cols, bool round, cudaStream_t st) {
+    if (rows <= 0 || cols <= 0) return SPECOPTIM_OK;
+    const int64_t tiles = (int64_t)((rows + 31) / 32) * ((cols + 31) / 32);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 16));
+    transpose_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, round ? 1 : 0);
+    SPECOPTIM_LAUNCHED("transpose_kernel");
+    return SPECOPTIM_OK;
+}
+
+AdamWScalars adamw_scalars(int64_t t, float lr, float beta1, float beta2, float eps, float wd) {
+    AdamWScalars s;
+    const double bc1 = 1.0 - std::pow((double)beta1, (double)t);
+    const double bc2 = 1.0 - std::pow((double)beta2, (double)t);
+    s.beta1 = beta1;
+    s.beta2 = beta2;
+    s.eps = eps;
+    s.decay = (float)(1.0 - (double)lr * (double)wd);
+    s.step_size = (float)((double)lr / bc1);
+    s.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    return s;
+}
+
+int ema_run(float *M, const float *G, int64_t n, float beta, cudaStream_t st) {
+    if (n <= 0) return SPECOPTIM_OK;
+    ema_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(M, G, n, beta);
+    SPECOPTIM_LAUNCHED("ema_kernel");
+    return SPECOPTIM_OK;
+}
+
+int adamw_run(float *W, const float *G, float *m1, float *m2, int64_t n, const AdamWScalars &s,
+              cudaStream_t st) {
+    if (n <= 0) return SPECOPTIM_OK;
+    adamw_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(W, G, m1, m2, n, s);
+    SPECOPTIM_LAUNCHED("adamw_kernel");
+    return SPECOPTIM_OK;
+}
+
+}  // namespace spco

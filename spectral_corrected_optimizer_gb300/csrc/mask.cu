@@ -1,0 +1,452 @@
+// In-graph activation mask: pack / unpack / indices.
+//
+// "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes",
+// key design 1: h~ = h (.) m keeps K = round((1-p)H) dims of every token; the
+// mask m = g(layer, step, batch metadata, S, H) is regenerated locally by
+// sender and receiver, only the K kept values are sent, and the backward pass
+// dL/dh = (dL/dh~) (.) m uses the same index set.
+//
+// g (this library's definition; the pages fix only its properties): row r
+// keeps pi_r(0..K-1) of a keyed permutation pi_r of [0, H), built from four
+// alternating Feistel rounds over ceil(log2 H) bits with MurmurHash3's fmix32
+// as round function and SplitMix64-derived round keys; values >= H are walked
+// on through the permutation's cycle.  Costs K permutation evaluations per row
+// (no sort, no per-dim hash of all H dims), and for H a power of two no cycle
+// walking at all.
+//
+// Data path (HBM-bound streaming): a persistent CTA takes chunks of CH rows
+// (CH * elem_bytes = 16, so every chunk of dense and of packed rows starts and
+// ends on a 16-byte boundary).  Dense chunks move between HBM and shared memory
+// with 1D bulk copies (cp.async.bulk) in a multi-stage pipeline; the gather
+// (pack) or the zero-fill + scatter (unpack) happens in shared memory; the
+// result leaves with one bulk store per chunk.  Rows that do not fill a chunk,
+// unaligned pointers and very long rows take a plain per-row kernel.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace spco {
+namespace {
+
+// ---- g: keyed permutation ---------------------------------------------------
+
+__host__ __device__ __forceinline__ uint64_t splitmix_out(uint64_t state) {
+    uint64_t z = state + 0x9e3779b97f4a7c15ULL;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ uint32_t murmur_fmix(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x85ebca6bu;
+    x ^= x >> 13;
+    x *= 0xc2b2ae35u;
+    x ^= x >> 16;
+    return x;
+}
+
+struct RowKeys {
+    uint32_t k[4];
+};
+
+__device__ __forceinline__ RowKeys row_keys(uint64_t seed, uint64_t row) {
+    uint64_t rk = splitmix_out(seed ^ row);
+    RowKeys out;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out.k[i] = static_cast<uint32_t>(splitmix_out(rk + (uint64_t)i));
+    return out;
+}
+
+// permutation geometry for a given H
+struct PermShape {
+    uint32_t H;
+    int lo_bits;
+    uint32_t hi_mask, lo_mask;
+    uint32_t walk_limit;
+};
+
+__host__ __device__ inline PermShape perm_shape(uint32_t H) {
+    int w = 0;
+    while ((1ull << w) < (unsigned long long)H) ++w;
+    PermShape s;
+    s.H = H;
+    s.lo_bits = w - w / 2;
+    s.hi_mask = (1u << (w / 2)) - 1u;
+    s.lo_mask = (1u << s.lo_bits) - 1u;
+    s.walk_limit = 1u << w;
+    return s;
+}
+
+__device__ __forceinline__ uint32_t feistel4(const RowKeys &key, const PermShape &ps, uint32_t x) {
+    uint32_t lo = x & ps.lo_mask;
+    uint32_t hi = x >> ps.lo_bits;
+    hi ^= murmur_fmix(lo ^ key.k[0]) & ps.hi_mask;
+    lo ^= murmur_fmix(hi ^ key.k[1]) & ps.lo_mask;
+    hi ^= murmur_fmix(lo ^ key.k[2]) & ps.hi_mask;
+    lo ^= murmur_fmix(hi ^ key.k[3]) & ps.lo_mask;
+    return (hi << ps.lo_bits) | lo;
+}
+
+// pi_r(k): the k-th kept dim of the row (cycle walking bounded by the domain size)
+__device__ __forceinline__ uint32_t kept_dim(const RowKeys &key, const PermShape &ps, uint32_t k) {
+    uint32_t x = feistel4(key, ps, k);
+    for (uint32_t g = 0; x >= ps.H && g < ps.walk_limit; ++g) x = feistel4(key, ps, x);
+    return x;
+}
+
+// ---- pipelined bulk-copy kernels --------------------------------------------
+
+constexpr int kThreads = 256;
+constexpr int kMaxStages = 4;
+constexpr size_t kSmemBudget = 200 * 1024;
+
+__host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
+
+// shared memory carve-up, identical on host and device
+struct PackLayout {
+    size_t keys, pk, dense, total;
+};
+
+__host__ __device__ inline PackLayout pack_layout(int CH, int H, int K, int esz, int stages) {
+    PackLayout L;
+    L.keys = 128;  // mbarriers live in the first 128 bytes
+    L.pk = L.keys + align128((size_t)CH * 16);
+    L.dense = L.pk + align128((size_t)CH * K * esz);
+    L.total = L.dense + (size_t)stages * align128((size_t)CH * H * esz);
+    return L;
+}
+
+struct UnpackLayout {
+    size_t keys, dense, pk, total;
+};
+
+__host__ __device__ inline UnpackLayout unpack_layout(int CH, int H, int K, int esz, int stages) {
+    UnpackLayout L;
+    L.keys = 128;
+    L.dense = L.keys + align128((size_t)CH * 16);
+    L.pk = L.dense + 2 * align128((size_t)CH * H * esz);
+    L.total = L.pk + (size_t)stages * align128((size_t)CH * K * esz);
+    return L;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nchunks, int H,
+                 int K, uint64_t seed, int stages, unsigned *flag) {
+    constexpr int CH = 16 / sizeof(T);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const PackLayout L = pack_layout(CH, H, K, sizeof(T), stages);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    RowKeys *keys = reinterpret_cast<RowKeys *>(smem + L.keys);
+    T *pk = reinterpret_cast<T *>(smem + L.pk);
+    const size_t stage_elems = align128((size_t)CH * H * sizeof(T)) / sizeof(T);
+    T *dsm = reinterpret_cast<T *>(smem + L.dense);
+    const uint32_t dense_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
+    const uint32_t pk_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
+    const PermShape ps = perm_shape((uint32_t)H);
+    const int tid = threadIdx.x;
+    const int64_t grid = gridDim.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            int64_t c = blockIdx.x + s * grid;
+            if (c < nchunks) {
+                mbar_arrive_expect_tx(&bar[s], dense_bytes);
+                bulk_load(dsm + s * stage_elems, dense + c * CH * (int64_t)H, dense_bytes, &bar[s]);
+            }
+        }
+    }
+    bool ok = true;
+    int it = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += grid, ++it) {
+        const int stage = it % stages;
+        const uint32_t parity = (uint32_t)(it / stages) & 1u;
+        if (tid < CH) keys[tid] = row_keys(seed, (uint64_t)(c * CH + tid));
+        if (tid == 0) bulk_wait_read<0>();  // previous packed store has left pk
+        if (ok) ok = mbar_wait_bounded(&bar[stage], parity, flag, 1u);
+        ok = __syncthreads_and(ok) != 0;  // keep the block's control flow uniform
+        const T *src = dsm + stage * stage_elems;
+        if (ok) {
+            for (int j = tid; j < CH * K; j += kThreads) {
+                int r = j / K, k = j - r * K;
+                pk[j] = src[(size_t)r * H + kept_dim(keys[r], ps, (uint32_t)k)];
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            bulk_store(packed + c * CH * (int64_t)K, pk, pk_bytes);
+            bulk_commit();
+            int64_t nxt = c + stages * grid;
+            if (nxt < nchunks) {
+                mbar_arrive_expect_tx(&bar[stage], dense_bytes);
+                bulk_load(dsm + stage * stage_elems, dense + nxt * CH * (int64_t)H, dense_bytes,
+                          &bar[stage]);
+            }
+        }
+        if (!ok) break;
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t nchunks, int H,
+                   int K, uint64_t seed, int stages, unsigned *flag) {
+    constexpr int CH = 16 / sizeof(T);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const UnpackLayout L = unpack_layout(CH, H, K, sizeof(T), stages);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    RowKeys *keys = reinterpret_cast<RowKeys *>(smem + L.keys);
+    const size_t dbuf_elems = align128((size_t)CH * H * sizeof(T)) / sizeof(T);
+    T *dsm = reinterpret_cast<T *>(smem + L.dense);
+    const size_t pk_elems = align128((size_t)CH * K * sizeof(T)) / sizeof(T);
+    T *pks = reinterpret_cast<T *>(smem + L.pk);
+    const uint32_t dense_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
+    const uint32_t pk_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
+    const PermShape ps = perm_shape((uint32_t)H);
+    const int tid = threadIdx.x;
+    const int64_t grid = gridDim.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            int64_t c = blockIdx.x + s * grid;
+            if (c < nchunks) {
+                mbar_arrive_expect_tx(&bar[s], pk_bytes);
+                bulk_load(pks + s * pk_elems, packed + c * CH * (int64_t)K, pk_bytes, &bar[s]);
+            }
+        }
+    }
+    bool ok = true;
+    int it = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += grid, ++it) {
+        const int stage = it % stages;
+        const uint32_t parity = (uint32_t)(it / stages) & 1u;
+        T *dst = dsm + (it & 1) * dbuf_elems;
+        if (tid < CH) keys[tid] = row_keys(seed, (uint64_t)(c * CH + tid));
+        if (tid == 0) bulk_wait_read<1>();  // the store that used this buffer is done reading
+        __syncthreads();
+        // zero-fill the dense chunk (exact +0 off the mask)
+        uint4 *z = reinterpret_cast<uint4 *>(dst);
+        for (uint32_t j = tid; j < dense_bytes / 16; j += kThreads) z[j] = make_uint4(0, 0, 0, 0);
+        if (ok) ok = mbar_wait_bounded(&bar[stage], parity, flag, 2u);
+        ok = __syncthreads_and(ok) != 0;  // keep the block's control flow uniform
+        const T *src = pks + stage * pk_elems;
+        if (ok) {
+            for (int j = tid; j < CH * K; j += kThreads) {
+                int r = j / K, k = j - r * K;
+                dst[(size_t)r * H + kept_dim(keys[r], ps, (uint32_t)k)] = src[j];
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            bulk_store(dense + c * CH * (int64_t)H, dst, dense_bytes);
+            bulk_commit();
+            int64_t nxt = c + stages * grid;
+            if (nxt < nchunks) {
+                mbar_arrive_expect_tx(&bar[stage], pk_bytes);
+                bulk_load(pks + stage * pk_elems, packed + nxt * CH * (int64_t)K, pk_bytes,
+                          &bar[stage]);
+            }
+        }
+        if (!ok) break;
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
+// ---- plain per-row kernels (ragged tails, unaligned pointers, long rows) ----
+
+template <typename T>
+__global__ void pack_rows_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t row0,
+                                 int64_t rows, int H, int K, uint64_t seed) {
+    const PermShape ps = perm_shape((uint32_t)H);
+    for (int64_t r = row0 + blockIdx.x; r < rows; r += gridDim.x) {
+        RowKeys key = row_keys(seed, (uint64_t)r);
+        for (int k = threadIdx.x; k < K; k += blockDim.x)
+            packed[r * K + k] = dense[r * H + kept_dim(key, ps, (uint32_t)k)];
+    }
+}
+
+template <typename T>
+__global__ void unpack_rows_kernel(const T *__restrict__ packed, T *__restrict__ dense,
+                                   int64_t row0, int64_t rows, int H, int K, uint64_t seed) {
+    const PermShape ps = perm_shape((uint32_t)H);
+    for (int64_t r = row0 + blockIdx.x; r < rows; r += gridDim.x) {
+        for (int j = threadIdx.x; j < H; j += blockDim.x) dense[r * H + j] = T(0);
+        __syncthreads();
+        RowKeys key = row_keys(seed, (uint64_t)r);
+        for (int k = threadIdx.x; k < K; k += blockDim.x)
+            dense[r * H + kept_dim(key, ps, (uint32_t)k)] = packed[r * K + k];
+        __syncthreads();
+    }
+}
+
+__global__ void indices_kernel(int32_t *__restrict__ idx, int64_t rows, int H, int K,
+                               uint64_t seed) {
+    const PermShape ps = perm_shape((uint32_t)H);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        RowKeys key = row_keys(seed, (uint64_t)r);
+        for (int k = threadIdx.x; k < K; k += blockDim.x)
+            idx[r * K + k] = (int32_t)kept_dim(key, ps, (uint32_t)k);
+    }
+}
+
+uint64_t mask_seed(uint32_t layer, uint64_t step, uint64_t batch_id) {
+    return splitmix_out(splitmix_out(splitmix_out((uint64_t)layer) ^ step) ^ batch_id);
+}
+
+int check_args(int64_t rows, int32_t H, int32_t K, int32_t elem_bytes) {
+    if (rows < 0) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask: rows < 0");
+    if (H < 1 || H > (1 << 30)) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask: H outside [1, 2^30]");
+    if (K < 0 || K > H) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask: K outside [0, H]");
+    if (elem_bytes != 2 && elem_bytes != 4)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "mask: elem_bytes must be 2 or 4");
+    return SPECOPTIM_OK;
+}
+
+int row_grid(int64_t rows) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * 16));
+}
+
+// stages that fit the shared-memory budget (0 = the bulk path does not fit)
+int pick_stages(size_t (*total)(int, int, int, int, int), int CH, int H, int K, int esz) {
+    for (int s = kMaxStages; s >= 1; --s)
+        if (total(CH, H, K, esz, s) <= kSmemBudget) return s;
+    return 0;
+}
+
+size_t pack_total(int CH, int H, int K, int esz, int s) { return pack_layout(CH, H, K, esz, s).total; }
+size_t unpack_total(int CH, int H, int K, int esz, int s) {
+    return unpack_layout(CH, H, K, esz, s).total;
+}
+
+template <typename T>
+int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64_t seed,
+             cudaStream_t st) {
+    constexpr int CH = 16 / sizeof(T);
+    const T *d = static_cast<const T *>(dense);
+    T *p = static_cast<T *>(packed);
+    int stages = pick_stages(pack_total, CH, H, K, sizeof(T));
+    int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
+    if (nfull > 0) {
+        size_t smem = pack_layout(CH, H, K, sizeof(T), stages).total;
+        static bool attr = false;
+        if (!attr) {
+            SPECOPTIM_CUDA(cudaFuncSetAttribute(pack_bulk_kernel<T>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)kSmemBudget));
+            attr = true;
+        }
+        int grid = (int)std::min<int64_t>(nfull, num_sms());
+        pack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(d, p, nfull, H, K, seed, stages,
+                                                          device_flag_ptr());
+        SPECOPTIM_LAUNCHED("mask_pack bulk kernel");
+    }
+    int64_t row0 = nfull * CH;
+    if (row0 < rows) {
+        pack_rows_kernel<T><<<row_grid(rows - row0), 128, 0, st>>>(d, p, row0, rows, H, K, seed);
+        SPECOPTIM_LAUNCHED("mask_pack row kernel");
+    }
+    return SPECOPTIM_OK;
+}
+
+template <typename T>
+int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint64_t seed,
+               cudaStream_t st) {
+    constexpr int CH = 16 / sizeof(T);
+    const T *p = static_cast<const T *>(packed);
+    T *d = static_cast<T *>(dense);
+    int stages = pick_stages(unpack_total, CH, H, K, sizeof(T));
+    int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
+    if (nfull > 0) {
+        size_t smem = unpack_layout(CH, H, K, sizeof(T), stages).total;
+        static bool attr = false;
+        if (!attr) {
+            SPECOPTIM_CUDA(cudaFuncSetAttribute(unpack_bulk_kernel<T>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)kSmemBudget));
+            attr = true;
+        }
+        int grid = (int)std::min<int64_t>(nfull, num_sms());
+        unpack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(p, d, nfull, H, K, seed, stages,
+                                                            device_flag_ptr());
+        SPECOPTIM_LAUNCHED("mask_unpack bulk kernel");
+    }
+    int64_t row0 = nfull * CH;
+    if (row0 < rows) {
+        unpack_rows_kernel<T><<<row_grid(rows - row0), 256, 0, st>>>(p, d, row0, rows, H, K, seed);
+        SPECOPTIM_LAUNCHED("mask_unpack row kernel");
+    }
+    return SPECOPTIM_OK;
+}
+
+}  // namespace
+}  // namespace spco
+
+using namespace spco;
+
+extern "C" int32_t mask_keep_count(double p, int32_t H) {
+    if (!(p >= 0.0 && p <= 1.0) || H < 1) return -1;
+    double x = (1.0 - p) * (double)H + 0.5;
+    int32_t K = (int32_t)x;  // x >= 0.5, truncation = floor
+    return K > H ? H : K;
+}
+
+extern "C" int mask_pack(const void *dense, void *packed, int64_t rows, int32_t H, int32_t K,
+                         int32_t elem_bytes, uint32_t layer, uint64_t step, uint64_t batch_id,
+                         void *stream) {
+    clear_error();
+    int rc = check_args(rows, H, K, elem_bytes);
+    if (rc) return rc;
+    if (rows == 0 || K == 0) return SPECOPTIM_OK;
+    if (!dense || !packed) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask_pack: null pointer");
+    uint64_t seed = mask_seed(layer, step, batch_id);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return elem_bytes == 2 ? run_pack<uint16_t>(dense, packed, rows, H, K, seed, st)
+                           : run_pack<uint32_t>(dense, packed, rows, H, K, seed, st);
+}
+
+extern "C" int mask_unpack(const void *packed, void *dense, int64_t rows, int32_t H, int32_t K,
+                           int32_t elem_bytes, uint32_t layer, uint64_t step, uint64_t batch_id,
+                           void *stream) {
+    clear_error();
+    int rc = check_args(rows, H, K, elem_bytes);
+    if (rc) return rc;
+    if (rows == 0) return SPECOPTIM_OK;
+    if (!dense || (K > 0 && !packed))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "mask_unpack: null pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        SPECOPTIM_CUDA(cudaMemsetAsync(dense, 0, (size_t)rows * H * elem_bytes, st));
+        return SPECOPTIM_OK;
+    }
+    uint64_t seed = mask_seed(layer, step, batch_id);
+    return elem_bytes == 2 ? run_unpack<uint16_t>(packed, dense, rows, H, K, seed, st)
+                           : run_unpack<uint32_t>(packed, dense, rows, H, K, seed, st);
+}
+
+extern "C" int mask_indices(int32_t *idx_out, int64_t rows, int32_t H, int32_t K, uint32_t layer,
+                            uint64_t step, uint64_t batch_id, void *stream) {
+    clear_error();
+    int rc = check_args(rows, H, K, 4);
+    if (rc) return rc;
+    if (rows == 0 || K == 0) return SPECOPTIM_OK;
+    if (!idx_out) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask_indices: null pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    indices_kernel<<<row_grid(rows), 128, 0, st>>>(idx_out, rows, H, K,
+                                                   mask_seed(layer, step, batch_id));
+    SPECOPTIM_LAUNCHED("mask_indices kernel");
+    return SPECOPTIM_OK;
+}

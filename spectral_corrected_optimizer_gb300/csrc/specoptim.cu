@@ -1,0 +1,346 @@
+// C-ABI of the spectral-corrected optimizer ("Communication-Efficient LLM
+// Adaptation over Decentralized GPU Meshes", key designs 2 and 3): handle
+// lifecycle, anchor EMA, SVD refresh, and the step orchestration.
+//
+// Step (key design 3, projection + blend equations, then AdamW), evaluated as
+// four GEMMs whose operands are all stored K-contiguous (the layout the
+// tcgen05 path reads with TMA; the SIMT path reads the same buffers):
+//   m > n (tall, r = n):  G^T = transpose(G)
+//       T1  = U^T G          (r x n, K = m)
+//       Xf  = (T1 V) o dd^T  (r x r, K = n)      diag(d) X diag(d) in the epilogue
+//       Z^T = V Xf^T         (n x r, K = r)
+//       Gf  = U Z            (m x n, K = r)      blend + AdamW in the epilogue
+//   m <= n (wide, r = m):
+//       T^T = V^T G^T        (r x m, K = n)      G read as the K-contiguous operand
+//       Xf^T= (T^T U) o dd^T (r x r, K = m)
+//       Y   = U Xf           (m x r, K = r)
+//       Gf  = Y V^T          (m x n, K = r)      blend + AdamW in the epilogue
+// Both orders cost 4 r^2 max(m,n) + 4 r^3 flops, the cheaper of the two
+// associations of U^T G V and U X V^T for their shape.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "elementwise.cuh"
+#include "gemm.cuh"
+#include "svd.cuh"
+
+struct specoptim {
+    specoptim_config cfg;
+    int m, n, r;
+    bool tall;
+    int64_t t;
+    float *M, *U, *s, *V, *d, *m1, *m2;
+    float *Uo, *UTo, *Vo, *VTo;  // GEMM operand copies of the factors (TF32-rounded on the TC path)
+    float *ws_g, *ws_a, *ws_x;   // step workspace: G^T (tall), T1/Z^T or T^T/Y, Xf
+    float *ws_svd;
+    bool have_factors;
+};
+
+namespace spco {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+void clear_error() { g_last_error.clear(); }
+
+static __device__ unsigned g_timeout_flag;
+
+unsigned *device_flag_ptr() {
+    static unsigned *ptr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_timeout_flag) == cudaSuccess) ptr = static_cast<unsigned *>(p);
+    });
+    return ptr;
+}
+
+int check_device_flag(cudaStream_t st) {
+    unsigned *p = device_flag_ptr();
+    if (!p) return SPECOPTIM_OK;
+    unsigned v = 0;
+    SPECOPTIM_CUDA(cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, st));
+    SPECOPTIM_CUDA(cudaStreamSynchronize(st));
+    if (v) {
+        unsigned zero = 0;
+        cudaMemcpyAsync(p, &zero, sizeof(zero), cudaMemcpyHostToDevice, st);
+        cudaStreamSynchronize(st);
+        return fail(SPECOPTIM_ERR_TIMEOUT, "a bounded device-side wait gave up (code " +
+                                               std::to_string(v) + ")");
+    }
+    return SPECOPTIM_OK;
+}
+
+int transpose_run(const float *src, float *dst, int rows, int cols, bool round, cudaStream_t st);
+int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
+            cudaStream_t stream);
+bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, Operand A, Operand B);
+
+// C = A . B^T with A (M x K) and B (N x K) both K-contiguous
+static int gemm_nt(const specoptim_t *h, int64_t M, int64_t N, int64_t K, const float *A,
+                   int64_t lda, const float *B, int64_t ldb, const Epilogue &e, cudaStream_t st) {
+    Operand a{A, lda, false}, b{B, ldb, true};
+    if (h->cfg.precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(M, N, K, a, b))
+        return gemm_tc(M, N, K, a, b, e, st);
+    return gemm_simt(M, N, K, a, b, e, st);
+}
+
+}  // namespace spco
+
+using namespace spco;
+
+namespace {
+
+int validate_cfg(const specoptim_config *c) {
+    if (!c) return fail(SPECOPTIM_ERR_INVALID_ARG, "config is null");
+    if (c->m < 1 || c->n < 1) return fail(SPECOPTIM_ERR_INVALID_ARG, "m and n must be >= 1");
+    if ((int64_t)c->m * c->n > (int64_t)1 << 34) return fail(SPECOPTIM_ERR_INVALID_ARG, "matrix too large");
+    if (!(c->tau_p > 0.f) || !std::isfinite(c->tau_p))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "tau_p must be finite and > 0");
+    if (!(c->alpha >= 0.f && c->alpha <= 1.f)) return fail(SPECOPTIM_ERR_INVALID_ARG, "alpha must be in [0,1]");
+    if (!(c->beta_anc >= 0.f && c->beta_anc <= 1.f))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "beta_anc must be in [0,1]");
+    if (!(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "AdamW betas must be in [0,1)");
+    if (!(c->eps >= 0.f)) return fail(SPECOPTIM_ERR_INVALID_ARG, "eps must be >= 0");
+    if (c->precision != SPECOPTIM_PREC_TF32 && c->precision != SPECOPTIM_PREC_FP32)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "unknown precision");
+    if (c->svd_max_sweeps < 1) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_max_sweeps must be >= 1");
+    if (!(c->svd_tol >= 0.f)) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_tol must be >= 0");
+    return SPECOPTIM_OK;
+}
+
+void free_all(specoptim_t *h) {
+    float *bufs[] = {h->M, h->U, h->s, h->V, h->d, h->m1, h->m2, h->Uo, h->UTo,
+                     h->Vo, h->VTo, h->ws_g, h->ws_a, h->ws_x, h->ws_svd};
+    for (float *p : bufs)
+        if (p) cudaFree(p);
+}
+
+}  // namespace
+
+extern "C" const char *specoptim_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int specoptim_config_default(specoptim_config *cfg, int32_t m, int32_t n) {
+    clear_error();
+    if (!cfg) return fail(SPECOPTIM_ERR_INVALID_ARG, "config is null");
+    std::memset(cfg, 0, sizeof(*cfg));
+    cfg->m = m;
+    cfg->n = n;
+    cfg->beta_anc = 0.9f;
+    cfg->tau_p = 1e-3f;
+    cfg->alpha = 0.3f;
+    cfg->beta1 = 0.9f;
+    cfg->beta2 = 0.999f;
+    cfg->eps = 1e-8f;
+    cfg->weight_decay = 0.01f;
+    cfg->precision = SPECOPTIM_PREC_TF32;
+    cfg->svd_max_sweeps = 20;
+    cfg->svd_tol = 1e-5f;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_create(specoptim_t **out, const specoptim_config *cfg, void *stream) {
+    clear_error();
+    if (!out) return fail(SPECOPTIM_ERR_INVALID_ARG, "out is null");
+    *out = nullptr;
+    int rc = validate_cfg(cfg);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    specoptim_t *h = new specoptim_t();
+    std::memset(h, 0, sizeof(*h));
+    h->cfg = *cfg;
+    h->m = cfg->m;
+    h->n = cfg->n;
+    h->r = std::min(cfg->m, cfg->n);
+    h->tall = cfg->m > cfg->n;
+    const size_t mn = (size_t)h->m * h->n, mr = (size_t)h->m * h->r, nr = (size_t)h->n * h->r;
+    const size_t rr = (size_t)h->r * h->r;
+    struct {
+        float **p;
+        size_t count;
+    } plan[] = {
+        {&h->M, mn}, {&h->U, mr}, {&h->s, (size_t)h->r}, {&h->V, nr}, {&h->d, (size_t)h->r},
+        {&h->m1, mn}, {&h->m2, mn}, {&h->Uo, mr}, {&h->UTo, mr}, {&h->Vo, nr}, {&h->VTo, nr},
+        {&h->ws_g, h->tall ? mn : 4}, {&h->ws_a, h->tall ? (size_t)h->n * h->r : mr},
+        {&h->ws_x, rr}, {&h->ws_svd, svd_workspace_floats(h->r)},
+    };
+    for (auto &b : plan) {
+        cudaError_t e = cudaMalloc(reinterpret_cast<void **>(b.p), b.count * sizeof(float));
+        if (e == cudaSuccess) e = cudaMemsetAsync(*b.p, 0, b.count * sizeof(float), st);
+        if (e != cudaSuccess) {
+            free_all(h);
+            delete h;
+            return cuda_status(e, "specoptim_create: allocation");
+        }
+    }
+    *out = h;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_destroy(specoptim_t *h) {
+    clear_error();
+    if (!h) return SPECOPTIM_OK;
+    cudaDeviceSynchronize();
+    free_all(h);
+    delete h;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void *stream) {
+    clear_error();
+    if (!h || !G_anc) return fail(SPECOPTIM_ERR_INVALID_ARG, "anchor_update: null argument");
+    if (!aligned16(G_anc)) return fail(SPECOPTIM_ERR_MISALIGNED, "anchor_update: G_anc not 16-byte aligned");
+    return ema_run(h->M, G_anc, (int64_t)h->m * h->n, h->cfg.beta_anc,
+                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out) {
+    clear_error();
+    if (!h) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: null handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SvdArgs a;
+    a.M = h->M;
+    a.m = h->m;
+    a.n = h->n;
+    a.U = h->U;
+    a.s = h->s;
+    a.V = h->V;
+    a.d = h->d;
+    a.work = h->ws_svd;
+    a.tau = h->cfg.tau_p;
+    a.max_sweeps = h->cfg.svd_max_sweeps;
+    a.tol = h->cfg.svd_tol;
+    int sweeps = 0;
+    int rc = svd_refresh_run(a, st, &sweeps);
+    if (sweeps_out) *sweeps_out = sweeps;
+    if (rc) return rc;
+    // operand copies for the step's GEMMs
+    const bool round = h->cfg.precision == SPECOPTIM_PREC_TF32;
+    if ((rc = transpose_run(h->U, h->UTo, h->m, h->r, round, st))) return rc;
+    if ((rc = transpose_run(h->V, h->VTo, h->n, h->r, round, st))) return rc;
+    if ((rc = transpose_run(h->UTo, h->Uo, h->r, h->m, false, st))) return rc;
+    if ((rc = transpose_run(h->VTo, h->Vo, h->r, h->n, false, st))) return rc;
+    h->have_factors = true;
+    return check_device_flag(st);
+}
+
+extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr,
+                              void *stream, float *G_filt_out, float *G_proj_out) {
+    clear_error();
+    if (!h || !W || !G_mask) return fail(SPECOPTIM_ERR_INVALID_ARG, "step: null argument");
+    if (!aligned16(W) || !aligned16(G_mask) || (G_filt_out && !aligned16(G_filt_out)) ||
+        (G_proj_out && !aligned16(G_proj_out)))
+        return fail(SPECOPTIM_ERR_MISALIGNED, "step: pointers must be 16-byte aligned");
+    if (!std::isfinite(lr)) return fail(SPECOPTIM_ERR_INVALID_ARG, "step: lr is not finite");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t m = h->m, n = h->n, r = h->r;
+    const bool round = h->cfg.precision == SPECOPTIM_PREC_TF32;
+    h->t += 1;
+    AdamWScalars sc = adamw_scalars(h->t, lr, h->cfg.beta1, h->cfg.beta2, h->cfg.eps,
+                                    h->cfg.weight_decay);
+    Epilogue plain;
+    plain.round_tf32 = round;
+    Epilogue scaled = plain;
+    scaled.mode = EPI_SCALE;
+    scaled.row_scale = h->d;
+    scaled.col_scale = h->d;
+    Epilogue last;
+    last.mode = EPI_ADAMW;
+    last.G = G_mask;
+    last.W = W;
+    last.m1 = h->m1;
+    last.m2 = h->m2;
+    last.Gf_out = G_filt_out;
+    last.Gp_out = G_proj_out;
+    last.ld = n;
+    last.alpha = h->cfg.alpha;
+    last.beta1 = sc.beta1;
+    last.beta2 = sc.beta2;
+    last.eps = sc.eps;
+    last.decay = sc.decay;
+    last.step_size = sc.step_size;
+    last.inv_sqrt_bc2 = sc.inv_sqrt_bc2;
+    int rc;
+    if (h->tall) {
+        float *GT = h->ws_g, *T1 = h->ws_a, *Xf = h->ws_x, *ZT = h->ws_a;
+        if ((rc = transpose_run(G_mask, GT, (int)m, (int)n, round, st))) return rc;
+        plain.C = T1;
+        plain.ldc = n;
+        if ((rc = gemm_nt(h, r, n, m, h->UTo, m, GT, m, plain, st))) return rc;
+        scaled.C = Xf;
+        scaled.ldc = r;
+        if ((rc = gemm_nt(h, r, r, n, T1, n, h->VTo, n, scaled, st))) return rc;
+        plain.C = ZT;
+        plain.ldc = r;
+        if ((rc = gemm_nt(h, n, r, r, h->Vo, r, Xf, r, plain, st))) return rc;
+        return gemm_nt(h, m, n, r, h->Uo, r, ZT, r, last, st);
+    }
+    float *TT = h->ws_a, *XfT = h->ws_x, *Y = h->ws_a;
+    plain.C = TT;
+    plain.ldc = m;
+    if ((rc = gemm_nt(h, r, m, n, h->VTo, n, G_mask, n, plain, st))) return rc;
+    scaled.C = XfT;
+    scaled.ldc = r;
+    if ((rc = gemm_nt(h, r, r, m, TT, m, h->UTo, m, scaled, st))) return rc;
+    plain.C = Y;
+    plain.ldc = r;
+    if ((rc = gemm_nt(h, m, r, r, h->Uo, r, XfT, r, plain, st))) return rc;
+    return gemm_nt(h, m, n, r, Y, r, h->Vo, r, last, st);
+}
+
+extern "C" int specoptim_get_factors(const specoptim_t *h, float *U, float *s, float *V, float *d,
+                                     void *stream) {
+    clear_error();
+    if (!h) return fail(SPECOPTIM_ERR_INVALID_ARG, "get_factors: null handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t mr = (size_t)h->m * h->r, nr = (size_t)h->n * h->r;
+    if (U) SPECOPTIM_CUDA(cudaMemcpyAsync(U, h->U, mr * 4, cudaMemcpyDeviceToDevice, st));
+    if (s) SPECOPTIM_CUDA(cudaMemcpyAsync(s, h->s, (size_t)h->r * 4, cudaMemcpyDeviceToDevice, st));
+    if (V) SPECOPTIM_CUDA(cudaMemcpyAsync(V, h->V, nr * 4, cudaMemcpyDeviceToDevice, st));
+    if (d) SPECOPTIM_CUDA(cudaMemcpyAsync(d, h->d, (size_t)h->r * 4, cudaMemcpyDeviceToDevice, st));
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_get_state(const specoptim_t *h, float *M, float *exp_avg,
+                                   float *exp_avg_sq, int64_t *t, void *stream) {
+    clear_error();
+    if (!h) return fail(SPECOPTIM_ERR_INVALID_ARG, "get_state: null handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)h->m * h->n * 4;
+    if (M) SPECOPTIM_CUDA(cudaMemcpyAsync(M, h->M, bytes, cudaMemcpyDeviceToDevice, st));
+    if (exp_avg) SPECOPTIM_CUDA(cudaMemcpyAsync(exp_avg, h->m1, bytes, cudaMemcpyDeviceToDevice, st));
+    if (exp_avg_sq) SPECOPTIM_CUDA(cudaMemcpyAsync(exp_avg_sq, h->m2, bytes, cudaMemcpyDeviceToDevice, st));
+    if (t) *t = h->t;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_set_state(specoptim_t *h, const float *M, const float *exp_avg,
+                                   const float *exp_avg_sq, int64_t t, void *stream) {
+    clear_error();
+    if (!h || !M || !exp_avg || !exp_avg_sq || t < 0)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "set_state: null argument or t < 0");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)h->m * h->n * 4;
+    SPECOPTIM_CUDA(cudaMemcpyAsync(h->M, M, bytes, cudaMemcpyDeviceToDevice, st));
+    SPECOPTIM_CUDA(cudaMemcpyAsync(h->m1, exp_avg, bytes, cudaMemcpyDeviceToDevice, st));
+    SPECOPTIM_CUDA(cudaMemcpyAsync(h->m2, exp_avg_sq, bytes, cudaMemcpyDeviceToDevice, st));
+    h->t = t;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_adamw(float *W, const float *g, float *exp_avg, float *exp_avg_sq,
+                               int64_t numel, int64_t t, float lr, float beta1, float beta2,
+                               float eps, float weight_decay, void *stream) {
+    clear_error();
+    if (numel < 0 || t < 1) return fail(SPECOPTIM_ERR_INVALID_ARG, "adamw: numel < 0 or t < 1");
+    if (numel == 0) return SPECOPTIM_OK;
+    if (!W || !g || !exp_avg || !exp_avg_sq) return fail(SPECOPTIM_ERR_INVALID_ARG, "adamw: null pointer");
+    if (!aligned16(W) || !aligned16(g) || !aligned16(exp_avg) || !aligned16(exp_avg_sq))
+        return fail(SPECOPTIM_ERR_MISALIGNED, "adamw: pointers must be 16-byte aligned");
+    return adamw_run(W, g, exp_avg, exp_avg_sq, numel,
+                     adamw_scalars(t, lr, beta1, beta2, eps, weight_decay),
+                     static_cast<cudaStream_t>(stream));
+}

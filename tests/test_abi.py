@@ -1,0 +1,81 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+entry point that include/*.h declares, and validates arguments on the host
+(no compute call here: these run on machines without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import oracle
+import spectral_corrected_optimizer_gb300 as so
+from spectral_corrected_optimizer_gb300 import build as sob
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sob.build()
+    return so.lib()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(lib, name), name
+    # and the binding declares a signature for each of them
+    assert {s[0] for s in so.SIGNATURES} == set(names)
+
+
+def test_keep_count_matches_oracle(lib):
+    for p in (0.0, 0.5, 0.9, 0.95, 0.99, 1.0):
+        for H in (1, 2, 7, 256, 2048, 3000, 4096):
+            assert so.mask_keep_count(p, H) == oracle.mask_K(p, H)
+    assert so.mask_keep_count(-0.1, 10) == -1 and so.mask_keep_count(0.5, 0) == -1
+
+
+def test_mask_argument_errors_are_reported_without_a_gpu(lib):
+    vp = ctypes.c_void_p(16)
+    assert lib.mask_pack(vp, vp, 4, 8, 9, 2, 0, 0, 0, None) == so.ERR_INVALID_ARG   # K > H
+    assert b"K outside" in lib.specoptim_last_error()
+    assert lib.mask_pack(vp, vp, 4, 8, 2, 3, 0, 0, 0, None) == so.ERR_INVALID_ARG   # elem_bytes
+    assert lib.mask_unpack(vp, vp, -1, 8, 2, 2, 0, 0, 0, None) == so.ERR_INVALID_ARG
+    assert lib.mask_indices(None, 4, 8, 2, 0, 0, 0, None) == so.ERR_INVALID_ARG
+    # empty work is a no-op success
+    assert lib.mask_pack(None, None, 0, 8, 2, 2, 0, 0, 0, None) == so.OK
+
+
+def test_config_defaults_are_the_pages_recipe(lib):
+    cfg = so.config_default(256, 128)
+    assert (cfg.m, cfg.n) == (256, 128)
+    assert cfg.tau_p == pytest.approx(1e-3) and cfg.alpha == pytest.approx(0.3)
+    assert cfg.beta_anc == pytest.approx(0.9)
+    assert cfg.precision == so.PREC_TF32
+
+
+@pytest.mark.parametrize("field,value", [("m", 0), ("tau_p", 0.0), ("alpha", 1.5), ("beta2", 1.0),
+                                         ("precision", 7), ("svd_max_sweeps", 0)])
+def test_create_rejects_bad_config_before_touching_the_gpu(lib, field, value):
+    cfg = so.config_default(16, 8)
+    setattr(cfg, field, value)
+    h = ctypes.c_void_p()
+    assert lib.specoptim_create(ctypes.byref(h), ctypes.byref(cfg), None) == so.ERR_INVALID_ARG
+    assert h.value is None
+
+
+def test_null_handles_are_rejected(lib):
+    assert lib.specoptim_step(None, None, None, 1e-3, None, None, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_svd_refresh(None, None, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_destroy(None) == so.OK

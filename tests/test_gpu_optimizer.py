@@ -1,0 +1,169 @@
+"""GPU parity of the spectral-corrected optimizer against the float64 oracle
+(key designs 2 and 3 of "Communication-Efficient LLM Adaptation over
+Decentralized GPU Meshes").
+
+Comparisons go through G_filt and G_proj, which are unique even where the SVD
+factors are not (sign and order of repeated singular values).  Tolerance:
+relative Frobenius error <= 2e-3 for the TF32 tensor-core path (the bar the
+workload sets for the optimizer output); the fp32 SIMT path is held to 5e-4
+(its floor, about 1.4e-4 on the toy case in a float32 emulation, comes from the
+fp32 block-Jacobi eigen-solve of the Gram matrix, not from the GEMMs).
+The AdamW state (m, v) is linear / quadratic in G_proj and held to the same
+bar; the weight update itself is compared with alpha = 1, where G_proj equals
+G_mask exactly and the update is well conditioned.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import spectral_corrected_optimizer_gb300 as so
+import synthetic
+from gpu_util import dev, ensure_lib, host, rel
+
+pytestmark = pytest.mark.gpu
+
+TOL = {so.PREC_TF32: 2e-3, so.PREC_FP32: 5e-4}
+PRECS = [so.PREC_FP32, so.PREC_TF32]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def run_case(inp, prec, steps=1, lr=2e-5, refresh=True, **cfg):
+    """One anchor update (+ refresh) and `steps` steps on GPU and in the oracle."""
+    m, n = inp.m, inp.n
+    gpu = so.SpectralOptimizer(m, n, precision=prec, **cfg)
+    ora = oracle.SpectralOptimizer(m, n, **{k: v for k, v in cfg.items() if k in (
+        "tau_p", "alpha", "beta_anc", "beta1", "beta2", "eps", "weight_decay")})
+    G_anc = inp.anchor_grad(0)
+    gpu.anchor_update(dev(G_anc))
+    ora.anchor_update(G_anc)
+    if refresh:
+        gpu.svd_refresh()
+        ora.svd_refresh()
+    W0 = inp.weights()
+    Wd = dev(W0)
+    Wo = W0.astype(np.float64)
+    out = []
+    for t in range(steps):
+        G = inp.masked_grad(t)
+        gf = torch.empty(m, n, device="cuda")
+        gp = torch.empty(m, n, device="cuda")
+        Wprev = host(Wd).copy()
+        gpu.step(Wd, dev(G), lr, gf, gp)
+        Wo_prev = Wo
+        Wo, Gf_o, Gp_o = ora.step(Wo, G, lr)
+        out.append(dict(Gf=host(gf), Gp=host(gp), W=host(Wd), Wprev=Wprev, Gf_o=Gf_o, Gp_o=Gp_o,
+                        W_o=Wo, W_o_prev=Wo_prev))
+    torch.cuda.synchronize()
+    return gpu, ora, out
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("shape", [(256, 128), (200, 72), (72, 200), (130, 130), (300, 33), (1, 5)])
+def test_step_matches_oracle(prec, shape):
+    inp = synthetic.MatrixInputs(*shape, seed=3, rank=min(8, min(shape)), factor_norm=shape[0])
+    gpu, ora, out = run_case(inp, prec, steps=3)
+    tol = TOL[prec]
+    for o in out:
+        assert rel(o["Gf"], o["Gf_o"]) <= tol
+        assert rel(o["Gp"], o["Gp_o"]) <= tol
+    M, m1, m2, t = gpu.get_state()
+    assert t == 3
+    assert rel(host(M), ora.M) <= 1e-6
+    assert rel(host(m1), ora.exp_avg) <= tol
+    assert rel(host(m2), ora.exp_avg_sq) <= tol
+    assert rel(out[-1]["W"], out[-1]["W_o"]) <= tol
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_toy_case(prec):
+    inp = synthetic.toy_matrix_inputs()
+    gpu, ora, out = run_case(inp, prec, steps=1)
+    U, s, V, d = (host(x) for x in gpu.get_factors())
+    assert np.abs(s - ora.s).max() <= 1e-4 * ora.s[0]
+    assert np.abs(d - ora.d).max() <= 1e-3
+    assert (d >= 0).all() and (d <= 1).all() and (np.diff(s) <= 0).all()
+    Mh = 0.1 * inp.anchor_grad(0).astype(np.float64)
+    assert rel(U.astype(np.float64) * s @ V.T, Mh) <= 1e-5
+    assert np.abs(V.T.astype(np.float64) @ V - np.eye(128)).max() <= 1e-4
+    assert rel(out[0]["Gf"], out[0]["Gf_o"]) <= TOL[prec]
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_weight_update_with_alpha_one_is_plain_adamw(prec):
+    # alpha = 1: G_proj = G_mask exactly, so the fused AdamW epilogue can be held tight
+    inp = synthetic.MatrixInputs(96, 160, seed=9, rank=4)
+    gpu, ora, out = run_case(inp, prec, steps=3, alpha=1.0)
+    for t, o in enumerate(out):
+        G = inp.masked_grad(t)
+        assert np.array_equal(o["Gp"], G)
+        dW = o["W"].astype(np.float64) - o["Wprev"]
+        dW_o = o["W_o"] - o["W_o_prev"]
+        assert rel(dW, dW_o) <= 1e-3
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_step_before_first_refresh(prec):
+    inp = synthetic.MatrixInputs(64, 48, seed=1)
+    gpu, ora, out = run_case(inp, prec, steps=1, refresh=False)
+    assert not out[0]["Gf"].any()
+    assert np.array_equal(out[0]["Gp"], np.float32(0.3) * inp.masked_grad(0))
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_large_tau_filters_everything(prec):
+    inp = synthetic.MatrixInputs(128, 64, seed=2)
+    gpu, ora, out = run_case(inp, prec, steps=1, tau_p=1e6)
+    assert np.linalg.norm(out[0]["Gf"]) <= 1e-6 * np.linalg.norm(inp.masked_grad(0))
+
+
+def test_ema_and_plain_adamw_kernels():
+    rng = np.random.default_rng(0)
+    n = 1000003  # ragged tail after the float4 body
+    W, g, m, v = (rng.standard_normal(n).astype(np.float32) for _ in range(4))
+    v = np.abs(v)
+    Wd, gd, md, vd = dev(W), dev(g), dev(m), dev(v)
+    so.adamw(Wd, gd, md, vd, 5, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    Wo, mo, vo = oracle.adamw(W, m, v, g, 5, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert rel(host(Wd) - W, Wo - W) <= 1e-5
+    assert rel(host(md), mo) <= 1e-6 and rel(host(vd), vo) <= 1e-6
+    opt = so.SpectralOptimizer(1000, 1003)
+    M = np.zeros((1000, 1003))
+    for k in range(3):
+        G = rng.standard_normal((1000, 1003)).astype(np.float32)
+        opt.anchor_update(dev(G))
+        M = oracle.anchor_ema(M, G, 0.9)
+    assert rel(host(opt.get_state()[0]), M) <= 1e-6
+
+
+def test_state_round_trip():
+    inp = synthetic.MatrixInputs(64, 32, seed=4)
+    a = so.SpectralOptimizer(64, 32)
+    a.anchor_update(dev(inp.anchor_grad(0)))
+    a.svd_refresh()
+    W = dev(inp.weights())
+    a.step(W, dev(inp.masked_grad(0)), 1e-3)
+    M, m1, m2, t = a.get_state()
+    b = so.SpectralOptimizer(64, 32)
+    b.set_state(M, m1, m2, t)
+    b.svd_refresh()
+    Wa, Wb = W.clone(), W.clone()
+    G = dev(inp.masked_grad(1))
+    a.step(Wa, G, 1e-3)
+    b.step(Wb, G, 1e-3)
+    assert torch.equal(Wa, Wb)
+
+
+def test_invalid_arguments_on_gpu():
+    opt = so.SpectralOptimizer(32, 16)
+    W = torch.zeros(32, 16, device="cuda")
+    with pytest.raises(ValueError):
+        opt.step(W, torch.zeros(16, 32, device="cuda"), 1e-3)
+    raw = torch.zeros(32 * 16 + 1, device="cuda")
+    lib = so.lib()
+    rc = lib.specoptim_step(opt._h, raw.data_ptr() + 4, raw.data_ptr(), 1e-3, None, None, None)
+    assert rc == so.ERR_MISALIGNED
