@@ -1,0 +1,489 @@
+"""Benchmark of the spectral-corrected optimizer + activation-mask hot path.
+
+Method: "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes"
+(arXiv 2609.14339): key design 1 (in-graph activation mask, pack / unpack at
+pipeline-stage boundaries, backward with the same indices), key design 2
+(anchor EMA) and key design 3 (SVD of the anchor momentum, Tikhonov filter,
+two-sided projection, blend, AdamW).
+
+Workload (one bench "step" = one pass of the whole hot path):
+  * one Llama-3.2-1B decoder layer, 7 fp32 weights (q, o 2048x2048; k, v
+    512x2048; gate, up 8192x2048; down 2048x8192), rank-32 anchor signal +
+    N(0,1e-4) noise, masked gradients with fresh N(0,1e-2) noise;
+  * every step: the spectral-corrected step of all 7 matrices, and the
+    stage-boundary mask round trip of a bf16 [32*2048, 2048] activation at
+    p = 0.95 (forward pack, receiver unpack, backward pack of the bf16
+    activation gradient, sender unpack);
+  * every 20th step (the anchor delay of the pages): anchor EMA + SVD refresh
+    of the 7 matrices.
+value = steps/s of the whole job.  Separate timed loops give the steady step
+(no refresh), the refresh, and the activation-mask sweep (15 boundaries x
+{pack, unpack, backward pack, backward unpack} at p = 0.90 and 0.95) in GB/s.
+
+With torchrun (N > 1) every rank runs its own replica of the layer (the
+optimizer state of different matrices is independent; no data-path
+collective): weak scaling, time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Llama-3.2-1B-shaped spectral-corrected steps/s; mask pack/unpack HBM GB/s"
+REFRESH_EVERY = 20
+MASK_ROWS, MASK_H, MASK_P = 32 * 2048, 2048, 0.95
+MASK_BOUNDARIES = 15
+POOL = 4               # distinct masked-gradient sets kept resident in HBM
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor throughput ratio
+FP32_FMA_PEAK_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s, SIMT fp32
+
+WORKLOAD = ("llama-3.2-1b decoder layer (q,o 2048x2048; k,v 512x2048; gate,up 8192x2048; "
+            "down 2048x8192), rank-32 anchor signal, SVD refresh every 20 steps, "
+            "mask round trip bf16 [65536,2048] p=0.95 per step")
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ the layer on the GPU
+
+def gemm_flops(m: int, n: int) -> float:
+    """Algorithmic flops of one matrix's step in the executed association
+    (4 r^2 max(m,n) + 4 r^3 with r = min(m,n)); equals 2 sum(M N K) of its 4 GEMMs."""
+    r, L = min(m, n), max(m, n)
+    return 4.0 * r * r * L + 4.0 * r ** 3
+
+
+def step_bytes(m: int, n: int) -> float:
+    """Algorithmic HBM bytes of one matrix's step: G read, W/m/v read+write
+    (28 B per element), U and V read twice, intermediates written and read once,
+    G^T written and read for m > n."""
+    r, mn = min(m, n), m * n
+    b = 28.0 * mn + 8.0 * (m + n) * r + 8.0 * (2 * r * max(m, n) + r * r)
+    if m > n:
+        b += 8.0 * mn
+    return b
+
+
+class Layer:
+    def __init__(self, seed: int):
+        import numpy as np
+        import torch
+        import spectral_corrected_optimizer_gb300 as so
+        import synthetic
+
+        self.so, self.torch = so, torch
+        self.names = list(synthetic.LLAMA_1B_LAYER)
+        self.inputs = synthetic.layer_inputs(synthetic.LLAMA_1B_LAYER, seed=seed, rank=32)
+        self.opt, self.W, self.Ganc, self.Gpool = {}, {}, {}, {}
+        for name, inp in self.inputs.items():
+            self.opt[name] = so.SpectralOptimizer(inp.m, inp.n)
+            self.W[name] = torch.from_numpy(inp.weights()).cuda()
+            self.Ganc[name] = [torch.from_numpy(inp.anchor_grad(i)).cuda() for i in range(2)]
+            self.Gpool[name] = [torch.from_numpy(inp.masked_grad(t)).cuda() for t in range(POOL)]
+        self.K = so.mask_keep_count(MASK_P, MASK_H)
+        self.h = torch.from_numpy(synthetic.activations_bf16(MASK_ROWS, MASK_H, seed=seed).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        self.g = torch.from_numpy(synthetic.act_grads_bf16(MASK_ROWS, MASK_H, seed=seed).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        self.hp = torch.empty(MASK_ROWS, self.K, dtype=torch.bfloat16, device="cuda")
+        self.gp = torch.empty_like(self.hp)
+        self.hd = torch.empty_like(self.h)
+        self.gd = torch.empty_like(self.g)
+        self.lr = 2e-5
+        self.flops = sum(gemm_flops(i.m, i.n) for i in self.inputs.values())
+        self.bytes = sum(step_bytes(i.m, i.n) for i in self.inputs.values())
+        self.params = sum(i.m * i.n for i in self.inputs.values())
+
+    def refresh(self, idx: int, G=None):
+        for name in self.names:
+            self.opt[name].anchor_update(G[name] if G else self.Ganc[name][idx % 2])
+            self.opt[name].svd_refresh()
+
+    def spectral(self, i: int, G=None):
+        for name in self.names:
+            self.opt[name].step(self.W[name], G[name] if G else self.Gpool[name][i % POOL], self.lr)
+
+    def mask_round_trip(self, i: int, h=None, g=None):
+        so, layer = self.so, i % MASK_BOUNDARIES
+        so.mask_pack(self.h if h is None else h, self.K, layer, i, 0, out=self.hp)
+        so.mask_unpack(self.hp, MASK_H, layer, i, 0, out=self.hd)
+        so.mask_pack(self.g if g is None else g, self.K, layer, i, 0, out=self.gp)
+        so.mask_unpack(self.gp, MASK_H, layer, i, 0, out=self.gd)
+
+    def step(self, i: int):
+        if i % REFRESH_EVERY == 0:
+            self.refresh(i // REFRESH_EVERY)
+        self.spectral(i)
+        self.mask_round_trip(i)
+
+
+def timed(torch, fn, dist_ok):
+    """Device time of fn() with a barrier and a synchronize on both sides (ms)."""
+    torch.cuda.synchronize()
+    if dist_ok:
+        import torch.distributed as dist
+        dist.barrier()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    fn()
+    stop.record()
+    torch.cuda.synchronize()
+    if dist_ok:
+        import torch.distributed as dist
+        dist.barrier()
+    return start.elapsed_time(stop)
+
+
+def max_over_ranks(x: float, dist_ok: bool) -> float:
+    if not dist_ok:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def mask_sweep(layer: Layer, p: float):
+    """15 boundaries x {fwd pack, unpack, bwd pack, bwd unpack}; returns GB/s figures."""
+    so, torch = layer.so, layer.torch
+    K = so.mask_keep_count(p, MASK_H)
+    hp = torch.empty(MASK_ROWS, K, dtype=torch.bfloat16, device="cuda")
+    gp = torch.empty_like(hp)
+
+    def sweep():
+        for b in range(MASK_BOUNDARIES):
+            so.mask_pack(layer.h, K, b, 0, 0, out=hp)
+            so.mask_unpack(hp, MASK_H, b, 0, 0, out=layer.hd)
+            so.mask_pack(layer.g, K, b, 0, 0, out=gp)
+            so.mask_unpack(gp, MASK_H, b, 0, 0, out=layer.gd)
+
+    sweep()  # warm-up
+    so.trace_enable(True)
+    ms = timed(torch, sweep, False)
+    rep = so.trace_report()
+    so.trace_enable(False)
+    e = 2  # bf16
+    dense, packed = MASK_ROWS * MASK_H * e, MASK_ROWS * K * e
+    op_bytes = dense + packed  # pack: dense read + packed write; unpack: packed read + dense write
+    out = {"K": K, "sweep_ms": ms, "ops": 4 * MASK_BOUNDARIES,
+           "effective_GBps": 4 * MASK_BOUNDARIES * op_bytes / (ms * 1e-3) / 1e9}
+    for kind in ("mask_pack_bulk", "mask_unpack_bulk"):
+        if kind in rep:
+            n, t = rep[kind]
+            out[kind] = {"launches": n, "avg_us": 1e3 * t / n, "GBps": n * op_bytes / (t * 1e-3) / 1e9}
+    return out
+
+
+def run_ours(args, rank, world, local_rank, dist_ok):
+    import torch
+
+    import spectral_corrected_optimizer_gb300 as so
+    from spectral_corrected_optimizer_gb300 import build as sob
+
+    if not os.path.exists(sob.LIB) or sob.needs_build():
+        if rank == 0:
+            sob.build()
+        if dist_ok:
+            import torch.distributed as dist
+            dist.barrier()
+    torch.cuda.set_device(local_rank)
+    peaks, peak_src = read_peaks()
+    layer = Layer(seed=rank)
+    K, W = args.steps, args.warmup
+
+    # warm-up (step 0 carries the first anchor update + SVD refresh)
+    for i in range(W):
+        layer.step(i)
+    torch.cuda.synchronize()
+
+    # ---- the timed region: K whole-hot-path steps
+    so.trace_reset()
+    with ClockSampler(local_rank) as clocks:
+        ms = timed(torch, lambda: [layer.step(W + i) for i in range(K)], dist_ok)
+    launches = so.launch_count()
+    ms_max = max_over_ranks(ms, dist_ok)
+    value = world * K / (ms_max * 1e-3)
+
+    # ---- breakdown: steady spectral step (traced), refresh, mask sweep
+    steady_n = max(3, min(K, 10))
+    so.trace_enable(True)
+    steady_ms = timed(torch, lambda: [layer.spectral(1000 + i) for i in range(steady_n)], False) / steady_n
+    rep = so.trace_report()
+    so.trace_enable(False)
+    refresh_ms = timed(torch, lambda: layer.refresh(7), False)
+    mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
+    mask_frac = mask["p0.95"]["effective_GBps"] / peaks["hbm_gbs"]
+
+    # roofline of the dominant kernel of the steady step
+    dom = max(rep.items(), key=lambda kv: kv[1][1])
+    name, (n_launch, t_ms) = dom
+    total_ms = sum(v[1] for v in rep.values())
+    tf32_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
+    if name == "gemm_tf32":
+        achieved = layer.flops * steady_n / (t_ms * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": tf32_peak,
+                "unit": "TFLOP/s", "frac": achieved / tf32_peak,
+                "peak_source": "%s bf16 sustained x nominal tf32/bf16 %.3f" % (peak_src, TF32_OVER_BF16)}
+    elif name == "gemm_simt":
+        achieved = layer.flops * steady_n / (t_ms * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "alu", "achieved": achieved, "peak": FP32_FMA_PEAK_NOMINAL,
+                "unit": "TFLOP/s", "frac": achieved / FP32_FMA_PEAK_NOMINAL,
+                "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x 2.07 GHz"}
+    else:
+        roof = {"kernel": name, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": None}
+    roof.update({"launches_per_step": n_launch / steady_n, "avg_launch_ms": t_ms / n_launch,
+                 "share_of_step": t_ms / total_ms, "traffic": None})
+    step_bound_ms = 1e3 * max(layer.flops / (tf32_peak * 1e12), layer.bytes / (peaks["hbm_gbs"] * 1e9))
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (tf32 tensor-core products, fp32 accumulate; bf16 mask copies)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "parallelism": "replicas (one layer per GPU)",
+                   "l2": "inputs larger than L2: each step streams 0.97 GB of distinct gradients and "
+                         "optimizer state and 1 GB of activations"},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "roofline": roof,
+        "breakdown": {"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
+                      "step_roofline_ms": step_bound_ms, "step_frac": step_bound_ms / steady_ms,
+                      "refresh_ms": refresh_ms, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()}},
+        "mask": dict(mask, frac_of_hbm=mask_frac, hbm_peak_GBps=peaks["hbm_gbs"]),
+        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak},
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(layer, K, W, dist_ok, world)
+    return result
+
+
+def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
+    """Same steps with host buffers: every step copies its masked gradients and
+    activations host -> device from pinned memory and reads the updated weights
+    back (the parameter snapshot the anchor circuit pulls), inside the timed region."""
+    torch = layer.torch
+    hostG = {n: [g.cpu().pin_memory() for g in layer.Gpool[n][:2]] for n in layer.names}
+    hostA = {n: [g.cpu().pin_memory() for g in layer.Ganc[n]] for n in layer.names}
+    devG = {n: torch.empty_like(layer.Gpool[n][0]) for n in layer.names}
+    hostW = {n: torch.empty(layer.W[n].shape, dtype=torch.float32).pin_memory() for n in layer.names}
+    host_h, host_g = layer.h.cpu().pin_memory(), layer.g.cpu().pin_memory()
+    dev_h, dev_g = torch.empty_like(layer.h), torch.empty_like(layer.g)
+    stats = {"h2d": 0, "d2h": 0}
+
+    def one(i):
+        G = None
+        if i % REFRESH_EVERY == 0:
+            for n in layer.names:
+                devG[n].copy_(hostA[n][(i // REFRESH_EVERY) % 2], non_blocking=True)
+                stats["h2d"] += devG[n].numel() * 4
+            layer.refresh(0, G=devG)
+        for n in layer.names:
+            devG[n].copy_(hostG[n][i % 2], non_blocking=True)
+            stats["h2d"] += devG[n].numel() * 4
+        layer.spectral(i, G=devG)
+        dev_h.copy_(host_h, non_blocking=True)
+        dev_g.copy_(host_g, non_blocking=True)
+        stats["h2d"] += 2 * dev_h.numel() * 2
+        layer.mask_round_trip(i, h=dev_h, g=dev_g)
+        for n in layer.names:
+            hostW[n].copy_(layer.W[n], non_blocking=True)
+            stats["d2h"] += layer.W[n].numel() * 4
+
+    for i in range(W):
+        one(10_000 + i)
+    stats["h2d"] = stats["d2h"] = 0
+    ms = timed(torch, lambda: [one(10_000 + W + i) for i in range(K)], dist_ok)
+    ms = max_over_ranks(ms, dist_ok)
+    return {"value": world * K / (ms * 1e-3), "unit": "steps/s",
+            "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K}
+
+
+# ------------------------------------------------------------------ the oracle on the host
+
+class OracleSample:
+    """The oracle as it stands, on a bounded sample of the workload: one steady
+    spectral step of the 7-matrix layer (projection, blend, AdamW in float64)
+    plus one stage-boundary mask round trip.  The SVD factors are random
+    matrices of the right shapes (the step's cost does not depend on their
+    values); the oracle's SVD refresh is not in the sample."""
+
+    def __init__(self, seed=0):
+        import numpy as np
+
+        import oracle
+        import synthetic
+
+        self.np, self.oracle = np, oracle
+        rng = np.random.default_rng(seed)
+        self.mats = []
+        for name, inp in synthetic.layer_inputs(synthetic.LLAMA_1B_LAYER, seed=seed, rank=32).items():
+            opt = oracle.SpectralOptimizer(inp.m, inp.n)
+            r = min(inp.m, inp.n)
+            opt.U = rng.standard_normal((inp.m, r)) / np.sqrt(inp.m)
+            opt.V = rng.standard_normal((inp.n, r)) / np.sqrt(inp.n)
+            opt.d = rng.uniform(0.0, 1.0, r)
+            self.mats.append((opt, inp.weights().astype(np.float64), inp.masked_grad(0)))
+        self.K = oracle.mask_K(MASK_P, MASK_H)
+        self.h = synthetic.activations_bf16(MASK_ROWS, MASK_H, seed=seed)
+        self.g = synthetic.act_grads_bf16(MASK_ROWS, MASK_H, seed=seed)
+
+    def step(self, i: int):
+        oracle = self.oracle
+        for opt, W, G in self.mats:
+            opt.step(W, G, 2e-5)
+        b = i % MASK_BOUNDARIES
+        hp = oracle.mask_pack(self.h, self.K, b, i)
+        oracle.mask_unpack(hp, MASK_H, b, i)
+        gp = oracle.mask_pack(self.g, self.K, b, i)
+        oracle.mask_unpack(gp, MASK_H, b, i)
+
+    def describe(self):
+        return ("one steady step of the 7-matrix Llama-3.2-1B layer (float64 projection, blend, "
+                "AdamW with random factors of the right shapes; SVD refresh excluded) + one bf16 [65536,2048] "
+                "p=0.95 mask round trip; steps/s = 1 / seconds per sample")
+
+
+def cpu_baseline():
+    s = OracleSample()
+    t = time.perf_counter()
+    s.step(0)
+    dt = time.perf_counter() - t
+    return {"value": 1.0 / dt, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": s.describe(), "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    s = OracleSample()
+    for i in range(args.warmup):
+        s.step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        s.step(args.warmup + i)
+    dt = time.perf_counter() - t
+    value = args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": 1,
+                                            "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": s.describe()},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local_rank = env_int("LOCAL_RANK", 0)
+    dist_ok = False
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        dist_ok = True
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank, dist_ok)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+    if dist_ok:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

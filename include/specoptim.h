@@ -133,6 +133,32 @@ int specoptim_adamw(float *W, const float *g, float *exp_avg, float *exp_avg_sq,
                     int64_t t, float lr, float beta1, float beta2, float eps, float weight_decay,
                     void *stream);
 
+/* C (M x N) = A (M x K) . B (N x K)^T, fp32 row-major with leading
+ * dimensions lda, ldb, ldc (device pointers).  The building block of the
+ * projection (key design 3, projection equation).  precision
+ * SPECOPTIM_PREC_TF32 runs the tcgen05 tensor-core kernel and requires
+ * lda, ldb multiples of 4 and 16-byte aligned A, B (else
+ * SPECOPTIM_ERR_NOT_IMPLEMENTED); SPECOPTIM_PREC_FP32 runs the fp32 SIMT
+ * kernel for any layout. */
+int specoptim_gemm_nt(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, int32_t precision,
+                      void *stream);
+
+/* Tracing of the library's own kernels.  Every kernel launch is counted;
+ * while tracing is enabled each launch is also bracketed by two CUDA events
+ * recorded on its stream.  specoptim_trace_enable(1) synchronises the device,
+ * clears earlier records and the launch counter, and starts recording;
+ * specoptim_trace_enable(0) stops recording (records are kept).
+ * specoptim_launch_count() returns the launches since the last reset.
+ * specoptim_trace_reset() synchronises and clears records and counter.
+ * specoptim_trace_report() synchronises the device and writes one line per
+ * kernel name, "name launches total_ms\n", into buf (len bytes, NUL
+ * terminated); SPECOPTIM_ERR_INVALID_ARG if it does not fit. */
+int specoptim_trace_enable(int32_t enable);
+int64_t specoptim_launch_count(void);
+int specoptim_trace_reset(void);
+int specoptim_trace_report(char *buf, int64_t len);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *specoptim_last_error(void);
 

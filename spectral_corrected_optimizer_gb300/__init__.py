@@ -56,6 +56,11 @@ SIGNATURES = [
     ("specoptim_get_state", _int, [_vp, _vp, _vp, _vp, ctypes.POINTER(_i64), _vp]),
     ("specoptim_set_state", _int, [_vp, _vp, _vp, _vp, _i64, _vp]),
     ("specoptim_adamw", _int, [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _f32, _f32, _f32, _f32, _vp]),
+    ("specoptim_gemm_nt", _int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
+    ("specoptim_trace_enable", _int, [_i32]),
+    ("specoptim_launch_count", _i64, []),
+    ("specoptim_trace_reset", _int, []),
+    ("specoptim_trace_report", _int, [ctypes.c_char_p, _i64]),
     ("specoptim_last_error", ctypes.c_char_p, []),
     ("mask_keep_count", _i32, [_f64, _i32]),
     ("mask_pack", _int, [_vp, _vp, _i64, _i32, _i32, _i32, _u32, _u64, _u64, _vp]),
@@ -201,6 +206,43 @@ def adamw(W, g, exp_avg, exp_avg_sq, t: int, lr: float, beta1=0.9, beta2=0.999, 
             raise ValueError("%s has %d elements, W has %d" % (name, x.numel(), n))
     _check(lib().specoptim_adamw(_ptr(W), _ptr(g), _ptr(exp_avg), _ptr(exp_avg_sq), n, int(t), lr,
                                  beta1, beta2, eps, weight_decay, _stream(stream)), "specoptim_adamw")
+
+
+def gemm_nt(A, B, precision: int = PREC_TF32, out=None, stream=None):
+    """C = A @ B.T for fp32 CUDA matrices A (M x K), B (N x K)."""
+    torch = _torch()
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2 or A.dtype != torch.float32 or B.dtype != torch.float32:
+        raise ValueError("gemm_nt: A (M x K) and B (N x K) must be float32 with equal K")
+    if out is None:
+        out = torch.empty((M, N), device=A.device)
+    _check(lib().specoptim_gemm_nt(M, N, K, _ptr(A), K, _ptr(B), K, _ptr(out), N, precision,
+                                   _stream(stream)), "specoptim_gemm_nt")
+    return out
+
+
+def trace_enable(on: bool = True):
+    _check(lib().specoptim_trace_enable(1 if on else 0), "specoptim_trace_enable")
+
+
+def launch_count() -> int:
+    return int(lib().specoptim_launch_count())
+
+
+def trace_reset():
+    _check(lib().specoptim_trace_reset(), "specoptim_trace_reset")
+
+
+def trace_report() -> dict:
+    """{kernel name: (launches, total device ms)} of the traced launches."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check(lib().specoptim_trace_report(buf, len(buf)), "specoptim_trace_report")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out
 
 
 # ---------------------------------------------------------------- activation mask

@@ -58,6 +58,19 @@ inline int num_sms() {
 int check_device_flag(cudaStream_t stream);
 unsigned *device_flag_ptr();
 
+// Tracing: every kernel launch of the library goes through SPCO_LAUNCH, which
+// counts it and, while tracing is enabled, brackets it with CUDA events on the
+// launching stream so that per-kernel device time can be reported.
+int trace_begin(const char *name, cudaStream_t st);
+void trace_end(int token, cudaStream_t st);
+
+#define SPCO_LAUNCH(name, st, ...)                                            \
+    do {                                                                      \
+        int _tk = ::spco::trace_begin(name, st);                             \
+        __VA_ARGS__;                                                          \
+        ::spco::trace_end(_tk, st);                                          \
+    } while (0)
+
 // iteration limit of every spin on an mbarrier (each probe also sleeps a little)
 constexpr uint32_t kSpinLimit = 1u << 22;
 

@@ -100,7 +100,7 @@ int transpose_run(const float *src, float *dst, int rows, int cols, bool round, 
     if (rows <= 0 || cols <= 0) return SPECOPTIM_OK;
     const int64_t tiles = (int64_t)((rows + 31) / 32) * ((cols + 31) / 32);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 16));
-    transpose_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, round ? 1 : 0);
+    SPCO_LAUNCH("transpose", st, transpose_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, round ? 1 : 0));
     SPECOPTIM_LAUNCHED("transpose_kernel");
     return SPECOPTIM_OK;
 }
@@ -120,7 +120,7 @@ AdamWScalars adamw_scalars(int64_t t, float lr, float beta1, float beta2, float 
 
 int ema_run(float *M, const float *G, int64_t n, float beta, cudaStream_t st) {
     if (n <= 0) return SPECOPTIM_OK;
-    ema_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(M, G, n, beta);
+    SPCO_LAUNCH("anchor_ema", st, ema_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(M, G, n, beta));
     SPECOPTIM_LAUNCHED("ema_kernel");
     return SPECOPTIM_OK;
 }
@@ -128,7 +128,7 @@ int ema_run(float *M, const float *G, int64_t n, float beta, cudaStream_t st) {
 int adamw_run(float *W, const float *G, float *m1, float *m2, int64_t n, const AdamWScalars &s,
               cudaStream_t st) {
     if (n <= 0) return SPECOPTIM_OK;
-    adamw_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(W, G, m1, m2, n, s);
+    SPCO_LAUNCH("adamw", st, adamw_kernel<<<stream_grid(n / 4 + 1), 256, 0, st>>>(W, G, m1, m2, n, s));
     SPECOPTIM_LAUNCHED("adamw_kernel");
     return SPECOPTIM_OK;
 }

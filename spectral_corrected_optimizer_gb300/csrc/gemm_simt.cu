@@ -105,7 +105,7 @@ int gemm_simt(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilo
     Operand Bt = B;
     Bt.trans = !B.trans;
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    gemm_simt_kernel<<<grid, NT, 0, stream>>>(M, N, K, A, Bt, epi);
+    SPCO_LAUNCH("gemm_simt", stream, gemm_simt_kernel<<<grid, NT, 0, stream>>>(M, N, K, A, Bt, epi));
     SPECOPTIM_LAUNCHED("gemm_simt_kernel");
     return SPECOPTIM_OK;
 }

@@ -1,12 +1,384 @@
-// tcgen05 (kind::tf32) GEMM -- not built yet: every shape reports "unsupported".
+// tcgen05 tensor-core GEMM, kind::tf32 with fp32 accumulation in TMEM.
+//
+//   C (M x N) = A (M x K) . B (N x K)^T      A, B fp32 row-major, K contiguous
+//
+// These are the four products of the two-sided projection of key design 3
+// ("Communication-Efficient LLM Adaptation over Decentralized GPU Meshes":
+// X = U^T G V, X_filt = diag(d) X diag(d), G_filt = U X_filt V^T), with the
+// diagonal scaling, the convex blend and the AdamW update as epilogues.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: 2D tiled loads (128B swizzle) of a 128 x 32 slab
+//               of A and a 256 x 32 slab of B per stage, 4 stages, completion
+//               counted on the stage's "full" mbarrier.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators);
+//               one lane issues tcgen05.mma (M=128, N=256, K=8) four times per
+//               stage and frees the stage with tcgen05.commit; after the last
+//               stage of a tile it commits to the accumulator's "full" barrier.
+//   warps 2-9   epilogue: tcgen05.ld of their TMEM lane quarter and column
+//               half, element-wise epilogue, global stores; then release the
+//               accumulator, so tile i's epilogue overlaps tile i+1's MMAs.
+// Every wait on an mbarrier is bounded; a wait that gives up records a code in
+// the library's device flag and the CTA winds down (TMEM freed) instead of
+// hanging.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "gemm.cuh"
 
 namespace spco {
+namespace {
 
-bool gemm_tc_supported(int64_t, int64_t, int64_t, Operand, Operand) { return false; }
+constexpr int BM = 128, BN = 256, BK = 32;  // BK fp32 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = (2 + EPI_WARPS) * 32;
+constexpr uint32_t A_BYTES = BM * BK * 4;
+constexpr uint32_t B_BYTES = BN * BK * 4;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-int gemm_tc(int64_t, int64_t, int64_t, Operand, Operand, const Epilogue &, cudaStream_t) {
-    return fail(SPECOPTIM_ERR_NOT_IMPLEMENTED, "tcgen05 GEMM not built");
+// ---- PTX wrappers ------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::tf32: D fp32, A and B tf32, both K-major, M x N.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// ---- epilogue of one row segment (32 accumulator columns) ---------------------
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4_stream(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+__device__ __forceinline__ void adamw4(const Epilogue &e, float *W, float *M1, float *M2,
+                                       const float *G, float *Gf, float *Gp, const float *acc) {
+    const float4 g = ld4_stream(G);
+    float4 w = ld4(W), m = ld4(M1), v = ld4(M2);
+    float gv[4] = {g.x, g.y, g.z, g.w}, wv[4] = {w.x, w.y, w.z, w.w};
+    float mv[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w}, pv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        pv[q] = e.alpha * gv[q] + (1.f - e.alpha) * acc[q];
+        mv[q] = e.beta1 * mv[q] + (1.f - e.beta1) * pv[q];
+        vv[q] = e.beta2 * vv[q] + (1.f - e.beta2) * pv[q] * pv[q];
+        wv[q] = wv[q] * e.decay - e.step_size * mv[q] / (sqrtf(vv[q]) * e.inv_sqrt_bc2 + e.eps);
+    }
+    st4(W, make_float4(wv[0], wv[1], wv[2], wv[3]));
+    st4(M1, make_float4(mv[0], mv[1], mv[2], mv[3]));
+    st4(M2, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    if (Gf) st4(Gf, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    if (Gp) st4(Gp, make_float4(pv[0], pv[1], pv[2], pv[3]));
+}
+
+__device__ __forceinline__ void epilogue_segment(const Epilogue &e, int64_t row, int64_t col0,
+                                                 int64_t M, int64_t N, const float (&v)[32]) {
+    if (row >= M || col0 >= N) return;
+    const bool full = col0 + 32 <= N;
+    if (e.mode == EPI_ADAMW) {
+        if (full && (e.ld & 3) == 0) {
+            const int64_t o = row * e.ld + col0;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+                adamw4(e, e.W + o + q, e.m1 + o + q, e.m2 + o + q, e.G + o + q,
+                       e.Gf_out ? e.Gf_out + o + q : nullptr, e.Gp_out ? e.Gp_out + o + q : nullptr,
+                       &v[q]);
+        } else {
+            for (int q = 0; q < 32 && col0 + q < N; ++q) epilogue_apply(e, row, col0 + q, v[q]);
+        }
+        return;
+    }
+    if (full && (e.ldc & 3) == 0) {
+        float rs = (e.mode == EPI_SCALE && e.row_scale) ? e.row_scale[row] : 1.f;
+        float *dst = e.C + row * e.ldc + col0;
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+            float c[4] = {v[q] * rs, v[q + 1] * rs, v[q + 2] * rs, v[q + 3] * rs};
+            if (e.mode == EPI_SCALE && e.col_scale) {
+                const float4 cs = ld4(e.col_scale + col0 + q);
+                c[0] *= cs.x;
+                c[1] *= cs.y;
+                c[2] *= cs.z;
+                c[3] *= cs.w;
+            }
+            if (e.round_tf32) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) c[t] = round_to_tf32(c[t]);
+            }
+            st4(dst + q, make_float4(c[0], c[1], c[2], c[3]));
+        }
+    } else {
+        for (int q = 0; q < 32 && col0 + q < N; ++q) epilogue_apply(e, row, col0 + q, v[q]);
+    }
+}
+
+// ---- the kernel ----------------------------------------------------------------
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 int M, int N, int K, Epilogue epi, unsigned *flag) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int tiles = tiles_m * tiles_n;
+    const int num_kb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], EPI_WARPS * 32);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, flag, 0x101u)) { ok = false; break; }
+                unsigned char *sa = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                tma_load_2d(sa, &tmA, kb * BK, m0, &full[s]);
+                tma_load_2d(sa + A_BYTES, &tmB, kb * BK, n0, &full[s]);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        uint32_t it = 0, local = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
+            const uint32_t acc = local & 1u;
+            const uint32_t aph = (local >> 1) & 1u;
+            if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, flag, 0x102u)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!mbar_wait_bounded(&full[s], ph, flag, 0x103u)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 8; ++k)
+                    mma_tf32(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32),
+                             kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&empty[s]);  // stage free once these MMAs have read it
+            }
+            mma_commit(&tfull[acc]);    // accumulator ready once all MMAs completed
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue
+        const int q = warp % 4;          // TMEM lane quarter this warp may access
+        const int half = (warp - 2) / 4; // column half of the 256-wide tile
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+            const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+            const uint32_t acc = local & 1u;
+            const uint32_t aph = (local >> 1) & 1u;
+            if (!mbar_wait_bounded(&tfull[acc], aph, flag, 0x104u)) break;
+            tc_fence_after();
+            const int64_t row = m0 + q * 32 + lane;
+            for (int c = 0; c < BN / 2 / 32; ++c) {
+                const int col = half * (BN / 2) + c * 32;
+                float v[32];
+                tmem_ld32(tmem_base + acc * BN + col + ((uint32_t)(q * 32) << 16), v);
+                epilogue_segment(epi, row, (int64_t)n0 + col, M, N, v);
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// rows x K fp32 matrix (K contiguous, leading dimension ld), box 32 (K) x box_rows
+int make_tmap(CUtensorMap *map, const float *ptr, int64_t rows, int64_t K, int64_t ld,
+              uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(SPECOPTIM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SPECOPTIM_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SPECOPTIM_OK;
+}
+
+}  // namespace
+
+// The tensor-core path takes C = A . B^T with A and B both K-contiguous, row
+// pitches that are multiples of 16 bytes and 16-byte aligned bases (TMA rules).
+bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, Operand A, Operand B) {
+    if (M < 1 || N < 1 || K < 1) return false;
+    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return false;
+    if (A.trans || !B.trans) return false;
+    if ((A.ld & 3) || (B.ld & 3) || !aligned16(A.ptr) || !aligned16(B.ptr)) return false;
+    return encode_fn() != nullptr;
+}
+
+int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
+            cudaStream_t stream) {
+    if (!gemm_tc_supported(M, N, K, A, B))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_tc: operand layout not supported");
+    CUtensorMap ta, tb;
+    int rc = make_tmap(&ta, A.ptr, M, K, A.ld, BM);
+    if (rc) return rc;
+    if ((rc = make_tmap(&tb, B.ptr, N, K, B.ld, BN))) return rc;
+    static bool attr = false;
+    if (!attr) {
+        SPECOPTIM_CUDA(cudaFuncSetAttribute(gemm_tf32_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)SMEM_BYTES));
+        attr = true;
+    }
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = (int)std::min<int64_t>(tiles, num_sms());
+    SPCO_LAUNCH("gemm_tf32", stream, gemm_tf32_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, (int)M, (int)N, (int)K, epi,
+                                                             device_flag_ptr()));
+    SPECOPTIM_LAUNCHED("gemm_tf32_kernel");
+    return SPECOPTIM_OK;
 }
 
 }  // namespace spco

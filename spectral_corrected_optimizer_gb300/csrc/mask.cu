@@ -350,13 +350,13 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
             attr = true;
         }
         int grid = (int)std::min<int64_t>(nfull, num_sms());
-        pack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(d, p, nfull, H, K, seed, stages,
-                                                          device_flag_ptr());
+        SPCO_LAUNCH("mask_pack_bulk", st, pack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(d, p, nfull, H, K, seed, stages,
+                                                          device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_pack bulk kernel");
     }
     int64_t row0 = nfull * CH;
     if (row0 < rows) {
-        pack_rows_kernel<T><<<row_grid(rows - row0), 128, 0, st>>>(d, p, row0, rows, H, K, seed);
+        SPCO_LAUNCH("mask_pack_rows", st, pack_rows_kernel<T><<<row_grid(rows - row0), 128, 0, st>>>(d, p, row0, rows, H, K, seed));
         SPECOPTIM_LAUNCHED("mask_pack row kernel");
     }
     return SPECOPTIM_OK;
@@ -380,13 +380,13 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
             attr = true;
         }
         int grid = (int)std::min<int64_t>(nfull, num_sms());
-        unpack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(p, d, nfull, H, K, seed, stages,
-                                                            device_flag_ptr());
+        SPCO_LAUNCH("mask_unpack_bulk", st, unpack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(p, d, nfull, H, K, seed, stages,
+                                                            device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_unpack bulk kernel");
     }
     int64_t row0 = nfull * CH;
     if (row0 < rows) {
-        unpack_rows_kernel<T><<<row_grid(rows - row0), 256, 0, st>>>(p, d, row0, rows, H, K, seed);
+        SPCO_LAUNCH("mask_unpack_rows", st, unpack_rows_kernel<T><<<row_grid(rows - row0), 256, 0, st>>>(p, d, row0, rows, H, K, seed));
         SPECOPTIM_LAUNCHED("mask_unpack row kernel");
     }
     return SPECOPTIM_OK;
@@ -445,8 +445,8 @@ extern "C" int mask_indices(int32_t *idx_out, int64_t rows, int32_t H, int32_t K
     if (rows == 0 || K == 0) return SPECOPTIM_OK;
     if (!idx_out) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask_indices: null pointer");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    indices_kernel<<<row_grid(rows), 128, 0, st>>>(idx_out, rows, H, K,
-                                                   mask_seed(layer, step, batch_id));
+    SPCO_LAUNCH("mask_indices", st, indices_kernel<<<row_grid(rows), 128, 0, st>>>(idx_out, rows, H, K,
+                                                   mask_seed(layer, step, batch_id)));
     SPECOPTIM_LAUNCHED("mask_indices kernel");
     return SPECOPTIM_OK;
 }

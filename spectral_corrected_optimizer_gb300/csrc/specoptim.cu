@@ -165,7 +165,7 @@ extern "C" int specoptim_create(specoptim_t **out, const specoptim_config *cfg, 
         {&h->M, mn}, {&h->U, mr}, {&h->s, (size_t)h->r}, {&h->V, nr}, {&h->d, (size_t)h->r},
         {&h->m1, mn}, {&h->m2, mn}, {&h->Uo, mr}, {&h->UTo, mr}, {&h->Vo, nr}, {&h->VTo, nr},
         {&h->ws_g, h->tall ? mn : 4}, {&h->ws_a, h->tall ? (size_t)h->n * h->r : mr},
-        {&h->ws_x, rr}, {&h->ws_svd, svd_workspace_floats(h->r)},
+        {&h->ws_x, rr}, {&h->ws_svd, svd_workspace_floats(h->m, h->n)},
     };
     for (auto &b : plan) {
         cudaError_t e = cudaMalloc(reinterpret_cast<void **>(b.p), b.count * sizeof(float));
@@ -343,4 +343,27 @@ extern "C" int specoptim_adamw(float *W, const float *g, float *exp_avg, float *
     return adamw_run(W, g, exp_avg, exp_avg_sq, numel,
                      adamw_scalars(t, lr, beta1, beta2, eps, weight_decay),
                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int specoptim_gemm_nt(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                 const float *B, int64_t ldb, float *C, int64_t ldc,
+                                 int32_t precision, void *stream) {
+    clear_error();
+    if (M < 0 || N < 0 || K < 0) return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_nt: negative size");
+    if (M == 0 || N == 0) return SPECOPTIM_OK;
+    if (!A || !B || !C) return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_nt: null pointer");
+    if (lda < K || ldb < K || ldc < N) return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_nt: leading dimension too small");
+    Operand a{A, lda, false}, b{B, ldb, true};
+    Epilogue e;
+    e.C = C;
+    e.ldc = ldc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (precision == SPECOPTIM_PREC_TF32) {
+        if (!gemm_tc_supported(M, N, K, a, b))
+            return fail(SPECOPTIM_ERR_NOT_IMPLEMENTED,
+                        "gemm_nt: the tensor-core path needs K >= 1, lda/ldb multiples of 4 and 16-byte aligned A, B");
+        return gemm_tc(M, N, K, a, b, e, st);
+    }
+    if (precision != SPECOPTIM_PREC_FP32) return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_nt: unknown precision");
+    return gemm_simt(M, N, K, a, b, e, st);
 }

@@ -15,9 +15,9 @@
 //      off-diagonal Frobenius norm falls below tol times the total norm.
 //      Padded indices have exactly zero rows and columns, so they are never
 //      rotated and stay out of the real eigenvectors.
-//   3. s_i = sqrt(max(lambda_i, 0)) sorted descending; d_i = s_i/(s_i+tau_p).
-//   4. The long-side factor: U = M V diag(1/s) (or V = M^T U diag(1/s)), with
-//      zero columns where s_i = 0.
+//   3. The eigenvectors are re-orthonormalised by two Newton-Schulz steps.
+//   4. P = M V (or M^T U); s_i = |P e_i| sorted descending, d_i = s_i/(s_i+tau_p),
+//      and the long-side factor is P diag(1/s), zero columns where s_i = 0.
 // The fp32 Gram squares the condition number; the filter makes that harmless
 // (d_i ~ s_i/tau_p for the small directions, so the error of those directions
 // enters G_filt multiplied by d_i).
@@ -229,41 +229,69 @@ __global__ void offnorm_kernel(const float *__restrict__ A, int Np, double *out)
     }
 }
 
-// rank of each real eigenvalue (descending, ties by index) -> order[rank] = index
-__global__ void rank_kernel(const float *__restrict__ A, int Np, int r, int *__restrict__ order) {
+// short-side factor before sorting: out[row][c] = Qacc[row][c], row, c < r
+__global__ void extract_kernel(const float *__restrict__ Qacc, int Np, int r, float *__restrict__ out) {
+    const int64_t total = (int64_t)r * r;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x)
+        out[e] = Qacc[(e / r) * Np + e % r];
+}
+
+// Newton-Schulz orthogonalisation step: X <- 1.5 X - 0.5 T with T = X (X^T X)
+__global__ void ns_update_kernel(float *__restrict__ X, const float *__restrict__ T, int64_t n) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x)
+        X[e] = 1.5f * X[e] - 0.5f * T[e];
+}
+
+// column norms of P (rows x r, row-major): thread per column, coalesced across columns
+__global__ void colnorm_kernel(const float *__restrict__ P, int64_t rows, int r, float *__restrict__ out) {
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < r; j += gridDim.x * blockDim.x) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < rows; ++i) {
+            const double v = P[i * r + j];
+            acc += v * v;
+        }
+        out[j] = (float)sqrt(acc);
+    }
+}
+
+// rank of each singular value (descending, ties by index) -> order[rank] = index
+__global__ void rank_kernel(const float *__restrict__ sv, int r, int *__restrict__ order) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < r; i += gridDim.x * blockDim.x) {
-        const float li = A[(size_t)i * Np + i];
+        const float si = sv[i];
         int rank = 0;
         for (int j = 0; j < r; ++j) {
-            const float lj = A[(size_t)j * Np + j];
-            rank += (lj > li) || (lj == li && j < i);
+            const float sj = sv[j];
+            rank += (sj > si) || (sj == si && j < i);
         }
         order[rank] = i;
     }
 }
 
-// s, d, 1/s in sorted order
-__global__ void spectrum_kernel(const float *__restrict__ A, int Np, int r,
-                                const int *__restrict__ order, float tau, float *__restrict__ s,
-                                float *__restrict__ d, float *__restrict__ inv_s) {
+// sorted s, d = s / (s + tau), and 1/s
+__global__ void spectrum_kernel(const float *__restrict__ sv, int r, const int *__restrict__ order,
+                                float tau, float *__restrict__ s, float *__restrict__ d,
+                                float *__restrict__ inv_s) {
     for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < r; c += gridDim.x * blockDim.x) {
-        const int i = order[c];
-        const float lam = A[(size_t)i * Np + i];
-        const float sv = lam > 0.f ? sqrtf(lam) : 0.f;
-        s[c] = sv;
-        d[c] = (sv + tau) > 0.f ? sv / (sv + tau) : 0.f;
-        inv_s[c] = sv > 0.f ? 1.f / sv : 0.f;
+        const float v = sv[order[c]];
+        s[c] = v;
+        d[c] = (v + tau) > 0.f ? v / (v + tau) : 0.f;
+        inv_s[c] = v > 0.f ? 1.f / v : 0.f;
     }
 }
 
-// short-side factor: out[row][c] = Qacc[row][order[c]], row < r (row-major r x r)
-__global__ void gather_vectors_kernel(const float *__restrict__ Qacc, int Np, int r,
-                                      const int *__restrict__ order, float *__restrict__ out) {
-    const int64_t total = (int64_t)r * r;
+// out[row][c] = in[row][order[c]] * (scale ? scale[c] : 1), rows x r row-major
+__global__ void permute_cols_kernel(const float *__restrict__ in, int64_t rows, int r,
+                                    const int *__restrict__ order, const float *__restrict__ scale,
+                                    float *__restrict__ out) {
+    const int64_t total = rows * r;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
-        const int row = (int)(e / r), c = (int)(e % r);
-        out[e] = Qacc[(size_t)row * Np + order[c]];
+        const int64_t row = e / r;
+        const int c = (int)(e % r);
+        const float v = in[row * r + order[c]];
+        out[e] = scale ? v * scale[c] : v;
     }
 }
 
@@ -274,22 +302,29 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-size_t svd_workspace_floats(int r) {
+size_t svd_workspace_floats(int m, int n) {
+    const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = ((r + kP - 1) / kP) * kP;
     const int64_t np = Np / kP;
-    // A, Qacc, rotations, inv_s, order (int), 2 doubles
-    return (size_t)(2 * Np * Np + np * kP * kP + r + r + 8);
+    // A, Qacc, rotations, short factor + NS temp (2 r^2), long factor P (L r),
+    // s_raw, inv_s, order (int), 2 doubles
+    return (size_t)(2 * Np * Np + np * kP * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
 }
 
 int svd_refresh_run(const SvdArgs &a, cudaStream_t st, int *sweeps_out) {
-    const int r = a.m >= a.n ? a.n : a.m;
     const bool tall = a.m >= a.n;
+    const int r = tall ? a.n : a.m;
+    const int64_t L = tall ? a.m : a.n;  // long side
     const int Np = ((r + kP - 1) / kP) * kP;
     const int nb = Np / kB, np = nb / 2;
     float *A = a.work;
     float *Qacc = A + (size_t)Np * Np;
     float *R = Qacc + (size_t)Np * Np;
-    float *inv_s = R + (size_t)np * kP * kP;
+    float *Sf = R + (size_t)np * kP * kP;  // short-side factor, unsorted (r x r)
+    float *Tmp = Sf + (size_t)r * r;       // r x r scratch
+    float *P = Tmp + (size_t)r * r;        // long-side M V (or M^T U), unsorted (L x r)
+    float *s_raw = P + (size_t)L * r;
+    float *inv_s = s_raw + r;
     int *order = reinterpret_cast<int *>(inv_s + r);
     double *norms = reinterpret_cast<double *>(
         (reinterpret_cast<uintptr_t>(order + r) + 15) & ~uintptr_t(15));
@@ -307,7 +342,7 @@ int svd_refresh_run(const SvdArgs &a, cudaStream_t st, int *sweeps_out) {
     if (rc) return rc;
 
     // 2. block Jacobi
-    eye_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(Qacc, Np);
+    SPCO_LAUNCH("svd_eye", st, eye_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(Qacc, Np));
     SPECOPTIM_LAUNCHED("eye_kernel");
     const int solve_blocks = (np + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t apply_work = (int64_t)np * np + (int64_t)(Np / kP) * np;
@@ -317,12 +352,12 @@ int svd_refresh_run(const SvdArgs &a, cudaStream_t st, int *sweeps_out) {
     double host_norms[2] = {0.0, 0.0};
     for (sweep = 0; sweep < a.max_sweeps && !converged; ++sweep) {
         for (int round = 0; round < nb - 1; ++round) {
-            jacobi_solve_kernel<<<solve_blocks, 32 * kWarpsPerBlock, 0, st>>>(A, Np, round, R, 4);
-            jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(A, Qacc, Np, round, R);
+            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_blocks, 32 * kWarpsPerBlock, 0, st>>>(A, Np, round, R, 4));
+            SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(A, Qacc, Np, round, R));
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         SPECOPTIM_CUDA(cudaMemsetAsync(norms, 0, 2 * sizeof(double), st));
-        offnorm_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(A, Np, norms);
+        SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(A, Np, norms));
         SPECOPTIM_LAUNCHED("offnorm_kernel");
         SPECOPTIM_CUDA(cudaMemcpyAsync(host_norms, norms, 2 * sizeof(double),
                                        cudaMemcpyDeviceToHost, st));
@@ -335,27 +370,44 @@ int svd_refresh_run(const SvdArgs &a, cudaStream_t st, int *sweeps_out) {
                     "svd_refresh: Jacobi did not reach svd_tol within svd_max_sweeps; "
                     "previous factors kept");
 
-    // 3. spectrum, filter, short-side factor
-    rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(A, Np, r, order);
-    spectrum_kernel<<<grid_for(r, 128), 128, 0, st>>>(A, Np, r, order, a.tau, a.s, a.d, inv_s);
-    float *short_f = tall ? a.V : a.U;  // r x r
-    gather_vectors_kernel<<<grid_for((int64_t)r * r, 256), 256, 0, st>>>(Qacc, Np, r, order,
-                                                                          short_f);
-    SPECOPTIM_LAUNCHED("svd spectrum kernels");
-
-    // 4. long-side factor with column scale 1/s
-    Epilogue f;
-    f.mode = EPI_SCALE;
-    f.col_scale = inv_s;
-    f.ldc = r;
-    if (tall) {  // U (m x r) = M (m x n) V (n x r) diag(1/s)
-        f.C = a.U;
-        rc = gemm_simt(a.m, r, a.n, Operand{a.M, a.n, false}, Operand{a.V, r, false}, f, st);
-    } else {     // V (n x r) = M^T (n x m) U (m x r) diag(1/s)
-        f.C = a.V;
-        rc = gemm_simt(a.n, r, a.m, Operand{a.M, a.n, true}, Operand{a.U, r, false}, f, st);
+    // 3. short-side factor, re-orthonormalised: two Newton-Schulz steps
+    //    X <- X (3 I - X^T X) / 2 remove the drift that thousands of fp32
+    //    rotations leave in the accumulated eigenvectors.
+    const int64_t rr = (int64_t)r * r;
+    SPCO_LAUNCH("svd_extract", st, extract_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Qacc, Np, r, Sf));
+    SPECOPTIM_LAUNCHED("extract_kernel");
+    for (int it = 0; it < 2; ++it) {
+        Epilogue g;
+        g.C = A;  // X^T X (r x r, ld r) reuses the Gram buffer
+        g.ldc = r;
+        if ((rc = gemm_simt(r, r, r, Operand{Sf, r, true}, Operand{Sf, r, false}, g, st))) return rc;
+        Epilogue t;
+        t.C = Tmp;
+        t.ldc = r;
+        if ((rc = gemm_simt(r, r, r, Operand{Sf, r, false}, Operand{A, r, false}, t, st))) return rc;
+        SPCO_LAUNCH("svd_ns_update", st, ns_update_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Sf, Tmp, rr));
+        SPECOPTIM_LAUNCHED("ns_update_kernel");
     }
-    return rc;
+
+    // 4. long side P = M X (tall) or M^T X (wide); s_i = |P e_i|, sorted descending;
+    //    long factor = P diag(1/s), zero columns where s_i = 0
+    Epilogue f;
+    f.C = P;
+    f.ldc = r;
+    if (tall)
+        rc = gemm_simt(L, r, a.n, Operand{a.M, a.n, false}, Operand{Sf, r, false}, f, st);
+    else
+        rc = gemm_simt(L, r, a.m, Operand{a.M, a.n, true}, Operand{Sf, r, false}, f, st);
+    if (rc) return rc;
+    SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid_for(r, 128), 128, 0, st>>>(P, L, r, s_raw));
+    SPCO_LAUNCH("svd_rank", st, rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(s_raw, r, order));
+    SPCO_LAUNCH("svd_spectrum", st, spectrum_kernel<<<grid_for(r, 128), 128, 0, st>>>(s_raw, r, order, a.tau, a.s, a.d, inv_s));
+    float *short_out = tall ? a.V : a.U;
+    float *long_out = tall ? a.U : a.V;
+    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Sf, r, r, order, nullptr, short_out));
+    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(L * r, 256), 256, 0, st>>>(P, L, r, order, inv_s, long_out));
+    SPECOPTIM_LAUNCHED("svd spectrum kernels");
+    return SPECOPTIM_OK;
 }
 
 }  // namespace spco

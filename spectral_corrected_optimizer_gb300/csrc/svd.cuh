@@ -15,7 +15,7 @@ struct SvdArgs {
     float tol;
 };
 
-size_t svd_workspace_floats(int r);
+size_t svd_workspace_floats(int m, int n);
 int svd_refresh_run(const SvdArgs &args, cudaStream_t stream, int *sweeps_out);
 
 }  // namespace spco

@@ -1,0 +1,113 @@
+// Launch counting and per-kernel CUDA-event timing of the library's kernels
+// (specoptim_trace_* in the C-ABI).
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace spco {
+namespace {
+
+struct Rec {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<bool> g_enabled{false};
+std::mutex g_mu;
+std::vector<Rec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t take_event() {
+    if (!g_pool.empty()) {
+        cudaEvent_t e = g_pool.back();
+        g_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+void recycle_all() {
+    for (auto &r : g_recs) {
+        g_pool.push_back(r.start);
+        g_pool.push_back(r.stop);
+    }
+    g_recs.clear();
+}
+
+}  // namespace
+
+int trace_begin(const char *name, cudaStream_t st) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_enabled.load(std::memory_order_relaxed)) return -1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Rec r{name, take_event(), take_event()};
+    cudaEventRecord(r.start, st);
+    g_recs.push_back(r);
+    return (int)g_recs.size() - 1;
+}
+
+void trace_end(int token, cudaStream_t st) {
+    if (token < 0) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (token < (int)g_recs.size()) cudaEventRecord(g_recs[token].stop, st);
+}
+
+}  // namespace spco
+
+using namespace spco;
+
+extern "C" int specoptim_trace_enable(int32_t enable) {
+    clear_error();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (enable) {
+        cudaDeviceSynchronize();
+        recycle_all();
+        g_launches.store(0);
+    }
+    g_enabled.store(enable != 0);
+    return SPECOPTIM_OK;
+}
+
+extern "C" int64_t specoptim_launch_count(void) { return g_launches.load(); }
+
+extern "C" int specoptim_trace_reset(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaDeviceSynchronize();
+    recycle_all();
+    g_launches.store(0);
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_trace_report(char *buf, int64_t len) {
+    clear_error();
+    if (!buf || len < 1) return fail(SPECOPTIM_ERR_INVALID_ARG, "trace_report: no buffer");
+    std::lock_guard<std::mutex> lk(g_mu);
+    SPECOPTIM_CUDA(cudaDeviceSynchronize());
+    std::map<std::string, std::pair<int64_t, double>> agg;
+    for (auto &r : g_recs) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) ms = 0.f;
+        auto &a = agg[r.name];
+        a.first += 1;
+        a.second += ms;
+    }
+    std::string out;
+    for (auto &kv : agg) {
+        char line[256];
+        std::snprintf(line, sizeof(line), "%s %lld %.6f\n", kv.first.c_str(),
+                      (long long)kv.second.first, kv.second.second);
+        out += line;
+    }
+    if ((int64_t)out.size() + 1 > len) return fail(SPECOPTIM_ERR_INVALID_ARG, "trace_report: buffer too small");
+    std::memcpy(buf, out.c_str(), out.size() + 1);
+    return SPECOPTIM_OK;
+}

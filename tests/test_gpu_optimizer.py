@@ -129,7 +129,8 @@ def test_ema_and_plain_adamw_kernels():
     Wd, gd, md, vd = dev(W), dev(g), dev(m), dev(v)
     so.adamw(Wd, gd, md, vd, 5, 1e-3, 0.9, 0.999, 1e-8, 0.01)
     Wo, mo, vo = oracle.adamw(W, m, v, g, 5, 1e-3, 0.9, 0.999, 1e-8, 0.01)
-    assert rel(host(Wd) - W, Wo - W) <= 1e-5
+    # W is stored in fp32 (ulp ~6e-8 at |W| ~ 1) while the update is ~1e-3
+    assert rel(host(Wd) - W, Wo - W) <= 5e-4
     assert rel(host(md), mo) <= 1e-6 and rel(host(vd), vo) <= 1e-6
     opt = so.SpectralOptimizer(1000, 1003)
     M = np.zeros((1000, 1003))
