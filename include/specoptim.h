@@ -144,6 +144,26 @@ int specoptim_gemm_nt(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
                       const float *B, int64_t ldb, float *C, int64_t ldc, int32_t precision,
                       void *stream);
 
+/* The filtered gradient alone, without allocating device memory.
+ * The paper has no counterpart of this entry point; it exists for callers
+ * that cannot call cudaMalloc -- code inside a framework that owns all device
+ * memory through its own pool, or on a latency-critical path where the device
+ * synchronisation of cudaMalloc / cudaFree is not acceptable.
+ *   G_filt = U diag(d) U^T G V diag(d) V^T
+ * U (m x r), V (n x r), d (r), G (m x n), G_filt (m x n, written) with
+ * r = min(m, n): device pointers, fp32 row-major, U, V, G, G_filt 16-byte
+ * aligned; precision SPECOPTIM_PREC_TF32 or SPECOPTIM_PREC_FP32 as in
+ * specoptim_step (same association and rounding).
+ * Intermediates live in one 16 MiB file-scope device array that every GPU
+ * loading the library holds until exit; shapes whose intermediates do not fit
+ * (about r * (2 max(m,n) + 2 r) floats, plus m n when m > n) are rejected with
+ * SPECOPTIM_ERR_INVALID_ARG.  All calls share the array: calls that overlap on
+ * the GPU race and give wrong results.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and should come before
+ * any stream capture. */
+int specoptim_filter_noalloc(const float *U, const float *V, const float *d, const float *G,
+                             float *G_filt, int32_t m, int32_t n, int32_t precision, void *stream);
+
 /* Tracing of the library's own kernels.  Every kernel launch is counted;
  * while tracing is enabled each launch is also bracketed by two CUDA events
  * recorded on its stream.  specoptim_trace_enable(1) synchronises the device,
