@@ -450,6 +450,39 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """Small cases for ncu captures (a few hundred MB on the device):
+    'gate': steady spectral steps of one 8192x2048 matrix (transpose + 4 GEMMs per step);
+    'mask': pack / unpack of one bf16 [65536, 2048] boundary at p = 0.95."""
+    import numpy as np
+    import torch
+
+    import spectral_corrected_optimizer_gb300 as so
+    import synthetic
+
+    torch.cuda.set_device(env_int("LOCAL_RANK", 0))
+    n_iter = args.warmup + args.steps
+    if args.profile == "gate":
+        inp = synthetic.MatrixInputs(8192, 2048, seed=0, rank=32)
+        opt = so.SpectralOptimizer(8192, 2048)
+        opt.anchor_update(torch.from_numpy(inp.anchor_grad(0)).cuda())
+        W = torch.from_numpy(inp.weights()).cuda()
+        G = [torch.from_numpy(inp.masked_grad(t)).cuda() for t in range(2)]
+        for i in range(n_iter):
+            opt.step(W, G[i % 2], 2e-5)
+    else:
+        K = so.mask_keep_count(MASK_P, MASK_H)
+        h = torch.from_numpy(synthetic.activations_bf16(MASK_ROWS, MASK_H).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        hp = torch.empty(MASK_ROWS, K, dtype=torch.bfloat16, device="cuda")
+        hd = torch.empty_like(h)
+        for i in range(n_iter):
+            so.mask_pack(h, K, i % MASK_BOUNDARIES, 0, 0, out=hp)
+            so.mask_unpack(hp, MASK_H, i % MASK_BOUNDARIES, 0, 0, out=hd)
+    torch.cuda.synchronize()
+    return {"profile": args.profile, "iterations": n_iter, "launches": so.launch_count()}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,6 +491,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["gate", "mask"], default=None,
+                    help="run a small case for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -471,6 +506,9 @@ def main():
         dist.init_process_group("gloo")
         dist_ok = True
 
+    if args.profile:
+        print(json.dumps(run_profile_case(args)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

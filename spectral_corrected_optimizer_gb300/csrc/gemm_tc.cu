@@ -39,7 +39,11 @@ constexpr uint32_t A_BYTES = BM * BK * 4;
 constexpr uint32_t B_BYTES = BN * BK * 4;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int TPITCH = 33;  // padded row of an epilogue transpose tile (conflict-free both ways)
+constexpr size_t TILE_BYTES = (size_t)EPI_WARPS * 32 * TPITCH * 4;
+constexpr size_t SMEM_BYTES =
+    (size_t)STAGES * STAGE_BYTES + TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 // ---- PTX wrappers ------------------------------------------------------------
 
@@ -155,45 +159,62 @@ __device__ __forceinline__ void adamw4(const Epilogue &e, float *W, float *M1, f
     if (Gp) st4(Gp, make_float4(pv[0], pv[1], pv[2], pv[3]));
 }
 
-__device__ __forceinline__ void epilogue_segment(const Epilogue &e, int64_t row, int64_t col0,
-                                                 int64_t M, int64_t N, const float (&v)[32]) {
-    if (row >= M || col0 >= N) return;
-    const bool full = col0 + 32 <= N;
+// Coalesced epilogue of a 32 x 32 accumulator block.  The block arrives from
+// tcgen05.ld as "thread = row, registers = 32 columns"; it is transposed
+// through a padded shared tile so that each warp instruction then touches four
+// rows x 32 consecutive columns (four full 128-byte lines per array).
+__device__ __forceinline__ void epilogue_block(const Epilogue &e, float *tile, int lane,
+                                               int64_t row0, int64_t col0, int64_t M, int64_t N,
+                                               const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) tile[lane * TPITCH + j] = v[j];
+    __syncwarp();
+    const int sub = lane >> 3;        // row within a group of 4
+    const int cq = (lane & 7) * 4;    // first of this thread's 4 columns
+    const int64_t col = col0 + cq;
+    const bool vec = (col + 4 <= N) &&
+                     (((e.mode == EPI_ADAMW) ? e.ld : e.ldc) & 3) == 0;
     if (e.mode == EPI_ADAMW) {
-        if (full && (e.ld & 3) == 0) {
-            const int64_t o = row * e.ld + col0;
-#pragma unroll
-            for (int q = 0; q < 32; q += 4)
-                adamw4(e, e.W + o + q, e.m1 + o + q, e.m2 + o + q, e.G + o + q,
-                       e.Gf_out ? e.Gf_out + o + q : nullptr, e.Gp_out ? e.Gp_out + o + q : nullptr,
-                       &v[q]);
-        } else {
-            for (int q = 0; q < 32 && col0 + q < N; ++q) epilogue_apply(e, row, col0 + q, v[q]);
-        }
-        return;
-    }
-    if (full && (e.ldc & 3) == 0) {
-        float rs = (e.mode == EPI_SCALE && e.row_scale) ? e.row_scale[row] : 1.f;
-        float *dst = e.C + row * e.ldc + col0;
-#pragma unroll
-        for (int q = 0; q < 32; q += 4) {
-            float c[4] = {v[q] * rs, v[q + 1] * rs, v[q + 2] * rs, v[q + 3] * rs};
-            if (e.mode == EPI_SCALE && e.col_scale) {
-                const float4 cs = ld4(e.col_scale + col0 + q);
-                c[0] *= cs.x;
-                c[1] *= cs.y;
-                c[2] *= cs.z;
-                c[3] *= cs.w;
+#pragma unroll 4
+        for (int g = 0; g < 8; ++g) {
+            const int i = g * 4 + sub;
+            const int64_t row = row0 + i;
+            if (row >= M) continue;
+            const float a[4] = {tile[i * TPITCH + cq], tile[i * TPITCH + cq + 1],
+                                tile[i * TPITCH + cq + 2], tile[i * TPITCH + cq + 3]};
+            if (vec) {
+                const int64_t o = row * e.ld + col;
+                adamw4(e, e.W + o, e.m1 + o, e.m2 + o, e.G + o, e.Gf_out ? e.Gf_out + o : nullptr,
+                       e.Gp_out ? e.Gp_out + o : nullptr, a);
+            } else {
+                for (int t = 0; t < 4; ++t)
+                    if (col + t < N) epilogue_apply(e, row, col + t, a[t]);
             }
-            if (e.round_tf32) {
-#pragma unroll
-                for (int t = 0; t < 4; ++t) c[t] = round_to_tf32(c[t]);
-            }
-            st4(dst + q, make_float4(c[0], c[1], c[2], c[3]));
         }
     } else {
-        for (int q = 0; q < 32 && col0 + q < N; ++q) epilogue_apply(e, row, col0 + q, v[q]);
+        float cs[4] = {1.f, 1.f, 1.f, 1.f};
+        if (e.mode == EPI_SCALE && e.col_scale)
+            for (int t = 0; t < 4; ++t) cs[t] = (col + t < N) ? e.col_scale[col + t] : 0.f;
+#pragma unroll 4
+        for (int g = 0; g < 8; ++g) {
+            const int i = g * 4 + sub;
+            const int64_t row = row0 + i;
+            if (row >= M) continue;
+            const float rs = (e.mode == EPI_SCALE && e.row_scale) ? e.row_scale[row] : 1.f;
+            float c[4];
+            for (int t = 0; t < 4; ++t) {
+                c[t] = tile[i * TPITCH + cq + t] * rs * cs[t];
+                if (e.round_tf32) c[t] = round_to_tf32(c[t]);
+            }
+            if (vec) {
+                st4(e.C + row * e.ldc + col, make_float4(c[0], c[1], c[2], c[3]));
+            } else {
+                for (int t = 0; t < 4; ++t)
+                    if (col + t < N) e.C[row * e.ldc + col + t] = c[t];
+            }
+        }
     }
+    __syncwarp();
 }
 
 // ---- the kernel ----------------------------------------------------------------
@@ -204,7 +225,8 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    float *tbuf = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + TILE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
@@ -212,7 +234,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int tiles = tiles_m * tiles_n;
+    const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -241,7 +263,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ---------------- TMA producer
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % STAGES;
@@ -257,7 +279,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ---------------- MMA issuer
         uint32_t it = 0, local = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
             const uint32_t acc = local & 1u;
             const uint32_t aph = (local >> 1) & 1u;
             if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, flag, 0x102u)) break;
@@ -283,18 +305,18 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int q = warp % 4;          // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4; // column half of the 256-wide tile
         uint32_t local = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
             const uint32_t acc = local & 1u;
             const uint32_t aph = (local >> 1) & 1u;
             if (!mbar_wait_bounded(&tfull[acc], aph, flag, 0x104u)) break;
             tc_fence_after();
-            const int64_t row = m0 + q * 32 + lane;
+            float *tbuf_w = tbuf + (warp - 2) * 32 * TPITCH;
             for (int c = 0; c < BN / 2 / 32; ++c) {
                 const int col = half * (BN / 2) + c * 32;
                 float v[32];
                 tmem_ld32(tmem_base + acc * BN + col + ((uint32_t)(q * 32) << 16), v);
-                epilogue_segment(epi, row, (int64_t)n0 + col, M, N, v);
+                epilogue_block(epi, tbuf_w, lane, (int64_t)m0 + q * 32, (int64_t)n0 + col, M, N, v);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);

@@ -15,8 +15,7 @@
 // walking at all.
 //
 // Data path (HBM-bound streaming): a persistent CTA takes chunks of CH rows
-// (CH * elem_bytes = 16, so every chunk of dense and of packed rows starts and
-// ends on a 16-byte boundary).  Dense chunks move between HBM and shared memory
+// (see the pipelined kernels below).  Dense chunks move between HBM and shared memory
 // with 1D bulk copies (cp.async.bulk) in a multi-stage pipeline; the gather
 // (pack) or the zero-fill + scatter (unpack) happens in shared memory; the
 // result leaves with one bulk store per chunk.  Rows that do not fill a chunk,
@@ -96,56 +95,52 @@ __device__ __forceinline__ uint32_t kept_dim(const RowKeys &key, const PermShape
 }
 
 // ---- pipelined bulk-copy kernels --------------------------------------------
+//
+// A CTA of CH = 8 warps takes chunks of 8 rows (8 * elem_bytes * X is a
+// multiple of 16 bytes for any X, so every chunk of dense and of packed rows
+// starts and ends 16-byte aligned).  Warp w owns row w of the chunk: it derives
+// the row's keys in registers and gathers / scatters that row, so no block
+// barrier is needed inside a row.  Dense (pack) or packed (unpack) input chunks
+// arrive by 1D bulk copies into a ring of `stages` buffers, each with its own
+// mbarrier; outputs leave by bulk stores from a ring of kOutBufs buffers.
+// Thread 0 lets at most one store group stay in flight after issuing a store,
+// so by the next block barrier the buffer two iterations ahead is free: one
+// __syncthreads per chunk.
 
-constexpr int kThreads = 256;
+constexpr int CH = 8;                   // rows per chunk = warps per CTA
+constexpr int kThreads = CH * 32;
 constexpr int kMaxStages = 4;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr int kOutBufs = 3;
+constexpr size_t kSmemBudget = 232448;  // 227 KB, one CTA per SM
 
 __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
-// shared memory carve-up, identical on host and device
-struct PackLayout {
-    size_t keys, pk, dense, total;
+// shared memory carve-up (identical on host and device): barriers, input ring, output ring
+struct RingLayout {
+    size_t in, out, in_stride, out_stride, total;
 };
 
-__host__ __device__ inline PackLayout pack_layout(int CH, int H, int K, int esz, int stages) {
-    PackLayout L;
-    L.keys = 128;  // mbarriers live in the first 128 bytes
-    L.pk = L.keys + align128((size_t)CH * 16);
-    L.dense = L.pk + align128((size_t)CH * K * esz);
-    L.total = L.dense + (size_t)stages * align128((size_t)CH * H * esz);
-    return L;
-}
-
-struct UnpackLayout {
-    size_t keys, dense, pk, total;
-};
-
-__host__ __device__ inline UnpackLayout unpack_layout(int CH, int H, int K, int esz, int stages) {
-    UnpackLayout L;
-    L.keys = 128;
-    L.dense = L.keys + align128((size_t)CH * 16);
-    L.pk = L.dense + 2 * align128((size_t)CH * H * esz);
-    L.total = L.pk + (size_t)stages * align128((size_t)CH * K * esz);
+__host__ __device__ inline RingLayout ring_layout(size_t in_bytes, size_t out_bytes, int stages) {
+    RingLayout L;
+    L.in = 128;  // mbarriers live in the first 128 bytes
+    L.in_stride = align128(in_bytes);
+    L.out = L.in + (size_t)stages * L.in_stride;
+    L.out_stride = align128(out_bytes);
+    L.total = L.out + (size_t)kOutBufs * L.out_stride;
     return L;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nchunks, int H,
                  int K, uint64_t seed, int stages, unsigned *flag) {
-    constexpr int CH = 16 / sizeof(T);
     extern __shared__ __align__(128) unsigned char smem[];
-    const PackLayout L = pack_layout(CH, H, K, sizeof(T), stages);
+    const uint32_t in_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
+    const uint32_t out_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
+    const RingLayout L = ring_layout(in_bytes, out_bytes, stages);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    RowKeys *keys = reinterpret_cast<RowKeys *>(smem + L.keys);
-    T *pk = reinterpret_cast<T *>(smem + L.pk);
-    const size_t stage_elems = align128((size_t)CH * H * sizeof(T)) / sizeof(T);
-    T *dsm = reinterpret_cast<T *>(smem + L.dense);
-    const uint32_t dense_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
-    const uint32_t pk_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
     const PermShape ps = perm_shape((uint32_t)H);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int64_t grid = gridDim.x;
 
     if (tid == 0) {
@@ -157,8 +152,8 @@ pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nc
         for (int s = 0; s < stages; ++s) {
             int64_t c = blockIdx.x + s * grid;
             if (c < nchunks) {
-                mbar_arrive_expect_tx(&bar[s], dense_bytes);
-                bulk_load(dsm + s * stage_elems, dense + c * CH * (int64_t)H, dense_bytes, &bar[s]);
+                mbar_arrive_expect_tx(&bar[s], in_bytes);
+                bulk_load(smem + L.in + s * L.in_stride, dense + c * CH * (int64_t)H, in_bytes, &bar[s]);
             }
         }
     }
@@ -167,52 +162,43 @@ pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nc
     for (int64_t c = blockIdx.x; c < nchunks; c += grid, ++it) {
         const int stage = it % stages;
         const uint32_t parity = (uint32_t)(it / stages) & 1u;
-        if (tid < CH) keys[tid] = row_keys(seed, (uint64_t)(c * CH + tid));
-        if (tid == 0) bulk_wait_read<0>();  // previous packed store has left pk
+        const RowKeys key = row_keys(seed, (uint64_t)(c * CH + warp));
+        const T *src = reinterpret_cast<const T *>(smem + L.in + stage * L.in_stride) + (size_t)warp * H;
+        T *out = reinterpret_cast<T *>(smem + L.out + (it % kOutBufs) * L.out_stride);
         if (ok) ok = mbar_wait_bounded(&bar[stage], parity, flag, 1u);
-        ok = __syncthreads_and(ok) != 0;  // keep the block's control flow uniform
-        const T *src = dsm + stage * stage_elems;
-        if (ok) {
-            for (int j = tid; j < CH * K; j += kThreads) {
-                int r = j / K, k = j - r * K;
-                pk[j] = src[(size_t)r * H + kept_dim(keys[r], ps, (uint32_t)k)];
-            }
-        }
+        if (ok)
+            for (int k = lane; k < K; k += 32) out[warp * K + k] = src[kept_dim(key, ps, (uint32_t)k)];
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0 && ok) {
-            bulk_store(packed + c * CH * (int64_t)K, pk, pk_bytes);
+        ok = __syncthreads_and(ok) != 0;  // row gathers done; block control flow stays uniform
+        if (!ok) break;
+        if (tid == 0) {
+            bulk_store(packed + c * CH * (int64_t)K, out, out_bytes);
             bulk_commit();
+            bulk_wait_read<1>();  // the buffer of iteration it-1 is free again
             int64_t nxt = c + stages * grid;
             if (nxt < nchunks) {
-                mbar_arrive_expect_tx(&bar[stage], dense_bytes);
-                bulk_load(dsm + stage * stage_elems, dense + nxt * CH * (int64_t)H, dense_bytes,
+                mbar_arrive_expect_tx(&bar[stage], in_bytes);
+                bulk_load(smem + L.in + stage * L.in_stride, dense + nxt * CH * (int64_t)H, in_bytes,
                           &bar[stage]);
             }
         }
-        if (!ok) break;
     }
     if (tid == 0) bulk_wait_all();
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t nchunks, int H,
                    int K, uint64_t seed, int stages, unsigned *flag) {
-    constexpr int CH = 16 / sizeof(T);
     extern __shared__ __align__(128) unsigned char smem[];
-    const UnpackLayout L = unpack_layout(CH, H, K, sizeof(T), stages);
+    const uint32_t in_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
+    const uint32_t out_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
+    const RingLayout L = ring_layout(in_bytes, out_bytes, stages);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    RowKeys *keys = reinterpret_cast<RowKeys *>(smem + L.keys);
-    const size_t dbuf_elems = align128((size_t)CH * H * sizeof(T)) / sizeof(T);
-    T *dsm = reinterpret_cast<T *>(smem + L.dense);
-    const size_t pk_elems = align128((size_t)CH * K * sizeof(T)) / sizeof(T);
-    T *pks = reinterpret_cast<T *>(smem + L.pk);
-    const uint32_t dense_bytes = (uint32_t)((size_t)CH * H * sizeof(T));
-    const uint32_t pk_bytes = (uint32_t)((size_t)CH * K * sizeof(T));
     const PermShape ps = perm_shape((uint32_t)H);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int64_t grid = gridDim.x;
+    const uint32_t row_bytes = (uint32_t)(H * sizeof(T));
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&bar[s], 1);
@@ -223,8 +209,8 @@ unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t 
         for (int s = 0; s < stages; ++s) {
             int64_t c = blockIdx.x + s * grid;
             if (c < nchunks) {
-                mbar_arrive_expect_tx(&bar[s], pk_bytes);
-                bulk_load(pks + s * pk_elems, packed + c * CH * (int64_t)K, pk_bytes, &bar[s]);
+                mbar_arrive_expect_tx(&bar[s], in_bytes);
+                bulk_load(smem + L.in + s * L.in_stride, packed + c * CH * (int64_t)K, in_bytes, &bar[s]);
             }
         }
     }
@@ -233,35 +219,36 @@ unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t 
     for (int64_t c = blockIdx.x; c < nchunks; c += grid, ++it) {
         const int stage = it % stages;
         const uint32_t parity = (uint32_t)(it / stages) & 1u;
-        T *dst = dsm + (it & 1) * dbuf_elems;
-        if (tid < CH) keys[tid] = row_keys(seed, (uint64_t)(c * CH + tid));
-        if (tid == 0) bulk_wait_read<1>();  // the store that used this buffer is done reading
-        __syncthreads();
-        // zero-fill the dense chunk (exact +0 off the mask)
-        uint4 *z = reinterpret_cast<uint4 *>(dst);
-        for (uint32_t j = tid; j < dense_bytes / 16; j += kThreads) z[j] = make_uint4(0, 0, 0, 0);
+        const RowKeys key = row_keys(seed, (uint64_t)(c * CH + warp));
+        unsigned char *row = smem + L.out + (it % kOutBufs) * L.out_stride + (size_t)warp * row_bytes;
+        // exact +0 off the mask: zero the row (16-byte stores when the row allows it)
+        if ((row_bytes & 15u) == 0) {
+            uint4 *z = reinterpret_cast<uint4 *>(row);
+            for (uint32_t j = lane; j < row_bytes / 16; j += 32) z[j] = make_uint4(0, 0, 0, 0);
+        } else {
+            for (uint32_t j = lane; j < row_bytes; j += 32) row[j] = 0;
+        }
+        __syncwarp();
         if (ok) ok = mbar_wait_bounded(&bar[stage], parity, flag, 2u);
-        ok = __syncthreads_and(ok) != 0;  // keep the block's control flow uniform
-        const T *src = pks + stage * pk_elems;
         if (ok) {
-            for (int j = tid; j < CH * K; j += kThreads) {
-                int r = j / K, k = j - r * K;
-                dst[(size_t)r * H + kept_dim(keys[r], ps, (uint32_t)k)] = src[j];
-            }
+            const T *src = reinterpret_cast<const T *>(smem + L.in + stage * L.in_stride) + (size_t)warp * K;
+            T *dst = reinterpret_cast<T *>(row);
+            for (int k = lane; k < K; k += 32) dst[kept_dim(key, ps, (uint32_t)k)] = src[k];
         }
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0 && ok) {
-            bulk_store(dense + c * CH * (int64_t)H, dst, dense_bytes);
+        ok = __syncthreads_and(ok) != 0;
+        if (!ok) break;
+        if (tid == 0) {
+            bulk_store(dense + c * CH * (int64_t)H, smem + L.out + (it % kOutBufs) * L.out_stride, out_bytes);
             bulk_commit();
+            bulk_wait_read<1>();
             int64_t nxt = c + stages * grid;
             if (nxt < nchunks) {
-                mbar_arrive_expect_tx(&bar[stage], pk_bytes);
-                bulk_load(pks + stage * pk_elems, packed + nxt * CH * (int64_t)K, pk_bytes,
+                mbar_arrive_expect_tx(&bar[stage], in_bytes);
+                bulk_load(smem + L.in + stage * L.in_stride, packed + nxt * CH * (int64_t)K, in_bytes,
                           &bar[stage]);
             }
         }
-        if (!ok) break;
     }
     if (tid == 0) bulk_wait_all();
 }
@@ -320,28 +307,23 @@ int row_grid(int64_t rows) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * 16));
 }
 
-// stages that fit the shared-memory budget (0 = the bulk path does not fit)
-int pick_stages(size_t (*total)(int, int, int, int, int), int CH, int H, int K, int esz) {
-    for (int s = kMaxStages; s >= 1; --s)
-        if (total(CH, H, K, esz, s) <= kSmemBudget) return s;
+// input-ring stages that fit the shared-memory budget (0 = the bulk path does not fit)
+int pick_stages(size_t in_bytes, size_t out_bytes) {
+    for (int st = kMaxStages; st >= 1; --st)
+        if (ring_layout(in_bytes, out_bytes, st).total <= kSmemBudget) return st;
     return 0;
-}
-
-size_t pack_total(int CH, int H, int K, int esz, int s) { return pack_layout(CH, H, K, esz, s).total; }
-size_t unpack_total(int CH, int H, int K, int esz, int s) {
-    return unpack_layout(CH, H, K, esz, s).total;
 }
 
 template <typename T>
 int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64_t seed,
              cudaStream_t st) {
-    constexpr int CH = 16 / sizeof(T);
     const T *d = static_cast<const T *>(dense);
     T *p = static_cast<T *>(packed);
-    int stages = pick_stages(pack_total, CH, H, K, sizeof(T));
+    const size_t in_b = (size_t)CH * H * sizeof(T), out_b = (size_t)CH * K * sizeof(T);
+    int stages = pick_stages(in_b, out_b);
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
-        size_t smem = pack_layout(CH, H, K, sizeof(T), stages).total;
+        size_t smem = ring_layout(in_b, out_b, stages).total;
         static bool attr = false;
         if (!attr) {
             SPECOPTIM_CUDA(cudaFuncSetAttribute(pack_bulk_kernel<T>,
@@ -365,13 +347,13 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
 template <typename T>
 int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint64_t seed,
                cudaStream_t st) {
-    constexpr int CH = 16 / sizeof(T);
     const T *p = static_cast<const T *>(packed);
     T *d = static_cast<T *>(dense);
-    int stages = pick_stages(unpack_total, CH, H, K, sizeof(T));
+    const size_t in_b = (size_t)CH * K * sizeof(T), out_b = (size_t)CH * H * sizeof(T);
+    int stages = pick_stages(in_b, out_b);
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
-        size_t smem = unpack_layout(CH, H, K, sizeof(T), stages).total;
+        size_t smem = ring_layout(in_b, out_b, stages).total;
         static bool attr = false;
         if (!attr) {
             SPECOPTIM_CUDA(cudaFuncSetAttribute(unpack_bulk_kernel<T>,
