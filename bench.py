@@ -172,7 +172,7 @@ class Layer:
     def refresh(self, idx: int, G=None):
         for name in self.names:
             self.opt[name].anchor_update(G[name] if G else self.Ganc[name][idx % 2])
-            self.opt[name].svd_refresh()
+        self.so.svd_refresh_many([self.opt[name] for name in self.names])
 
     def spectral(self, i: int, G=None):
         for name in self.names:

@@ -85,13 +85,26 @@ int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void *stream);
 /* SVD refresh, key design 3: thin SVD M = U diag(s) V^T (r = min(m, n),
  * s descending) and the Tikhonov filter d_i = s_i / (s_i + tau_p).
  * Computed as the eigen-decomposition of the Gram matrix of M on its short
- * side (fp32) by block Jacobi, then the long-side factor as M V / s (or
- * M^T U / s).  Columns with s_i = 0 are left zero (their d_i is 0).
+ * side (fp32) by block Jacobi, re-orthonormalised by Newton-Schulz; then
+ * s_i = |M v_i| and the long-side factor M V / s (or M^T U / s).  Columns
+ * with s_i = 0 are left zero (their d_i is 0).
  * Synchronises `stream` once per Jacobi sweep to test convergence.
  * sweeps_out (host pointer, may be NULL) receives the number of sweeps.
  * Returns SPECOPTIM_ERR_NOT_CONVERGED, keeping the previous factors, if the
  * off-diagonal norm is still above svd_tol after svd_max_sweeps sweeps. */
 int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out);
+
+/* The same refresh for 1 to 16 handles at once (e.g. the 7 weights of one
+ * decoder layer): their Jacobi rounds share kernel launches, so the GPU is
+ * filled by the whole batch instead of one matrix at a time.  handles: host
+ * array of distinct handles; sweeps_out: host array of `count` ints or NULL.
+ * A handle that already holds factors starts its Jacobi from its previous
+ * short-side factor (the anchor momentum moves slowly between anchors), which
+ * shortens the iteration; the result is the same decomposition.  Matrices
+ * that do not converge keep their previous factors and the call returns
+ * SPECOPTIM_ERR_NOT_CONVERGED after finishing the others. */
+int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
+                               int32_t *sweeps_out);
 
 /* Spectral-corrected step, key design 3 (projection and blend equations)
  * followed by AdamW:

@@ -51,6 +51,7 @@ SIGNATURES = [
     ("specoptim_destroy", _int, [_vp]),
     ("specoptim_anchor_update", _int, [_vp, _vp, _vp]),
     ("specoptim_svd_refresh", _int, [_vp, _vp, ctypes.POINTER(_i32)]),
+    ("specoptim_svd_refresh_many", _int, [ctypes.POINTER(_vp), _i32, _vp, ctypes.POINTER(_i32)]),
     ("specoptim_step", _int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp]),
     ("specoptim_get_factors", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     ("specoptim_get_state", _int, [_vp, _vp, _vp, _vp, ctypes.POINTER(_i64), _vp]),
@@ -196,6 +197,15 @@ class SpectralOptimizer:
         _check(lib().specoptim_set_state(self._h, _f32_2d(M, shape, "M"), _f32_2d(exp_avg, shape, "exp_avg"),
                                          _f32_2d(exp_avg_sq, shape, "exp_avg_sq"), int(t), _stream(stream)),
                "specoptim_set_state")
+
+
+def svd_refresh_many(optimizers, stream=None):
+    """One batched SVD refresh of several SpectralOptimizer handles (at most 16)."""
+    n = len(optimizers)
+    arr = (ctypes.c_void_p * n)(*[o._h.value for o in optimizers])
+    sweeps = (ctypes.c_int32 * n)()
+    _check(lib().specoptim_svd_refresh_many(arr, n, _stream(stream), sweeps), "specoptim_svd_refresh_many")
+    return list(sweeps)
 
 
 def adamw(W, g, exp_avg, exp_avg_sq, t: int, lr: float, beta1=0.9, beta2=0.999, eps=1e-8,

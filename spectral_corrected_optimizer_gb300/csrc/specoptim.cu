@@ -197,34 +197,59 @@ extern "C" int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void 
                    static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out) {
+extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
+                                          int32_t *sweeps_out) {
     clear_error();
-    if (!h) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: null handle");
+    if (!handles || count < 1 || count > 16)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: 1 to 16 handles");
+    for (int i = 0; i < count; ++i) {
+        if (!handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: null handle");
+        for (int k = 0; k < i; ++k)
+            if (handles[k] == handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: repeated handle");
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SvdArgs a;
-    a.M = h->M;
-    a.m = h->m;
-    a.n = h->n;
-    a.U = h->U;
-    a.s = h->s;
-    a.V = h->V;
-    a.d = h->d;
-    a.work = h->ws_svd;
-    a.tau = h->cfg.tau_p;
-    a.max_sweeps = h->cfg.svd_max_sweeps;
-    a.tol = h->cfg.svd_tol;
-    int sweeps = 0;
-    int rc = svd_refresh_run(a, st, &sweeps);
-    if (sweeps_out) *sweeps_out = sweeps;
-    if (rc) return rc;
-    // operand copies for the step's GEMMs
-    const bool round = h->cfg.precision == SPECOPTIM_PREC_TF32;
-    if ((rc = transpose_run(h->U, h->UTo, h->m, h->r, round, st))) return rc;
-    if ((rc = transpose_run(h->V, h->VTo, h->n, h->r, round, st))) return rc;
-    if ((rc = transpose_run(h->UTo, h->Uo, h->r, h->m, false, st))) return rc;
-    if ((rc = transpose_run(h->VTo, h->Vo, h->r, h->n, false, st))) return rc;
-    h->have_factors = true;
-    return check_device_flag(st);
+    SvdJob jobs[16];
+    for (int i = 0; i < count; ++i) {
+        specoptim_t *h = handles[i];
+        SvdJob &a = jobs[i];
+        a.M = h->M;
+        a.m = h->m;
+        a.n = h->n;
+        a.U = h->U;
+        a.s = h->s;
+        a.V = h->V;
+        a.d = h->d;
+        a.work = h->ws_svd;
+        a.warm = h->have_factors ? (h->tall || h->m == h->n ? h->V : h->U) : nullptr;
+        a.tau = h->cfg.tau_p;
+        a.tol = h->cfg.svd_tol;
+        a.max_sweeps = h->cfg.svd_max_sweeps;
+    }
+    int rc = svd_refresh_batch(jobs, count, st);
+    if (sweeps_out)
+        for (int i = 0; i < count; ++i) sweeps_out[i] = jobs[i].sweeps;
+    if (rc && rc != SPECOPTIM_ERR_NOT_CONVERGED) return rc;
+    std::string err = rc ? std::string(specoptim_last_error()) : std::string();
+    for (int i = 0; i < count; ++i) {
+        specoptim_t *h = handles[i];
+        if (jobs[i].status != SPECOPTIM_OK) continue;
+        // operand copies for the step's GEMMs
+        const bool round = h->cfg.precision == SPECOPTIM_PREC_TF32;
+        int r2;
+        if ((r2 = transpose_run(h->U, h->UTo, h->m, h->r, round, st))) return r2;
+        if ((r2 = transpose_run(h->V, h->VTo, h->n, h->r, round, st))) return r2;
+        if ((r2 = transpose_run(h->UTo, h->Uo, h->r, h->m, false, st))) return r2;
+        if ((r2 = transpose_run(h->VTo, h->Vo, h->r, h->n, false, st))) return r2;
+        h->have_factors = true;
+    }
+    int r3 = check_device_flag(st);
+    if (r3) return r3;
+    if (rc) return fail(rc, err);
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out) {
+    return specoptim_svd_refresh_many(&h, 1, stream, sweeps_out);
 }
 
 extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr,

@@ -22,6 +22,7 @@
 // (d_i ~ s_i/tau_p for the small directions, so the error of those directions
 // enters G_filt multiplied by d_i).
 #include <algorithm>
+#include <cstring>
 #include <vector>
 
 #include "gemm.cuh"
@@ -30,8 +31,9 @@
 namespace spco {
 namespace {
 
-constexpr int kB = 16;      // block size of the block-Jacobi
-constexpr int kP = 2 * kB;  // subproblem size (one warp)
+constexpr int kB = 32;      // block size of the block-Jacobi
+constexpr int kP = 2 * kB;  // subproblem size (one CTA)
+constexpr int kMaxBatch = 16;
 
 // round-robin schedule over `players` (even): pair i of round k
 __host__ __device__ __forceinline__ void rr_pair(int players, int round, int i, int &a, int &b) {
@@ -43,13 +45,6 @@ __host__ __device__ __forceinline__ void rr_pair(int players, int round, int i, 
         a = (round + i) % n1;
         b = (round - i + n1) % n1;
     }
-}
-
-// global index of local index l (0..31) of pair p in round `round` (nb blocks)
-__device__ __forceinline__ int pair_index(int nb, int round, int p, int l) {
-    int a, b;
-    rr_pair(nb, round, p, a, b);
-    return (l < kB ? a : b) * kB + (l & (kB - 1));
 }
 
 // Jacobi rotation (c, s) that zeroes the (p,q) entry of [[app, apq], [apq, aqq]]
@@ -67,139 +62,246 @@ __device__ __forceinline__ void jacobi_cs(float app, float aqq, float apq, float
         t = 1.f / (fabsf(theta) + sqrtf(1.f + theta * theta));
         if (theta < 0.f) t = -t;
     }
-    c = rsqrtf(1.f + t * t);
+    c = 1.f / sqrtf(1.f + t * t);
     s = t * c;
 }
 
-constexpr int kWarpsPerBlock = 4;
+// All matrices of one batched refresh.  Each matrix i has Np[i] (a multiple of
+// 64) padded indices in nb = Np/32 blocks; in its round `round[i]` the blocks
+// meet in Np/64 pairs.  Work items of every kernel are numbered over the whole
+// batch through the prefix arrays.
+struct JacBatch {
+    int count;
+    float *A[kMaxBatch];
+    float *Q[kMaxBatch];
+    float *R[kMaxBatch];
+    int Np[kMaxBatch];
+    int round[kMaxBatch];
+    int active[kMaxBatch];
+    int pair_off[kMaxBatch + 1];   // solve: one CTA per pair
+    int row_off[kMaxBatch + 1];    // rows pass: pairs x (Np/64) column chunks, then Q items
+    int q_off[kMaxBatch + 1];      // Q items: (Np/64) row chunks x pairs
+    int col_off[kMaxBatch + 1];    // cols pass: (Np/64) row chunks x pairs
+};
 
-// One warp per pair: load the 32x32 subproblem, run `inner_sweeps` cyclic
-// Jacobi sweeps (parallel order, 16 disjoint rotations per step), write R.
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
-jacobi_solve_kernel(const float *__restrict__ A, int Np, int round, float *__restrict__ R,
-                    int inner_sweeps) {
-    __shared__ float S[kWarpsPerBlock][kP][kP + 1];
-    __shared__ float Q[kWarpsPerBlock][kP][kP + 1];
-    __shared__ float cs[kWarpsPerBlock][kB][2];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int nb = Np / kB;
-    const int pair = blockIdx.x * kWarpsPerBlock + warp;
-    if (pair >= nb / 2) return;  // whole warp leaves together
-    float(*s)[kP + 1] = S[warp];
-    float(*q)[kP + 1] = Q[warp];
-    const int gl = pair_index(nb, round, pair, lane);
-    for (int i = 0; i < kP; ++i) {
-        const int gi = pair_index(nb, round, pair, i);
-        s[i][lane] = A[(size_t)gi * Np + gl];
-        q[i][lane] = (i == lane) ? 1.f : 0.f;
-    }
-    __syncwarp();
-    for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
-        float offmax = 0.f;
-        for (int step = 0; step < kP - 1; ++step) {
-            if (lane < kB) {
-                int p, r;
-                rr_pair(kP, step, lane, p, r);
-                const float apq = s[p][r];
-                float c, sn;
-                jacobi_cs(s[p][p], s[r][r], apq, c, sn);
-                cs[warp][lane][0] = c;
-                cs[warp][lane][1] = sn;
-                offmax = fmaxf(offmax, fabsf(apq));
-            }
-            __syncwarp();
-            // rows: lane owns column `lane`
-            for (int i = 0; i < kB; ++i) {
-                int p, r;
-                rr_pair(kP, step, i, p, r);
-                const float c = cs[warp][i][0], sn = cs[warp][i][1];
-                const float x = s[p][lane], y = s[r][lane];
-                s[p][lane] = c * x - sn * y;
-                s[r][lane] = sn * x + c * y;
-            }
-            __syncwarp();
-            // columns of S and of Q: lane owns row `lane`
-            for (int i = 0; i < kB; ++i) {
-                int p, r;
-                rr_pair(kP, step, i, p, r);
-                const float c = cs[warp][i][0], sn = cs[warp][i][1];
-                float x = s[lane][p], y = s[lane][r];
-                s[lane][p] = c * x - sn * y;
-                s[lane][r] = sn * x + c * y;
-                x = q[lane][p];
-                y = q[lane][r];
-                q[lane][p] = c * x - sn * y;
-                q[lane][r] = sn * x + c * y;
-            }
-            __syncwarp();
-        }
-        // stop early once no off-diagonal entry is above fp32 noise of the diagonal
-        float dmax = fabsf(s[lane][lane]);
-        for (int o = 16; o > 0; o >>= 1) {
-            offmax = fmaxf(offmax, __shfl_xor_sync(0xffffffffu, offmax, o));
-            dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
-        }
-        if (offmax <= 1e-7f * dmax) break;
-    }
-    float *Rp = R + (size_t)pair * kP * kP;
-    for (int i = 0; i < kP; ++i) Rp[i * kP + lane] = q[i][lane];
+__device__ __forceinline__ int find_job(const int *off, int count, int item) {
+    int i = 0;
+    while (i + 1 < count && item >= off[i + 1]) ++i;
+    return i;
 }
 
-// Applies the round's rotations: tiles of A (pair x pair) and 32-row slabs of Qacc.
-__global__ void __launch_bounds__(256)
-jacobi_apply_kernel(float *__restrict__ A, float *__restrict__ Qacc, int Np, int round,
-                    const float *__restrict__ R) {
-    __shared__ float X[kP][kP + 1];
-    __shared__ float T[kP][kP + 1];
-    __shared__ float R1[kP][kP + 1];
-    __shared__ float R2[kP][kP + 1];
-    const int nb = Np / kB, np = nb / 2;
-    const int64_t atiles = (int64_t)np * np;
+// global index of local index l (0..63) of pair p of the given round (nb blocks)
+__device__ __forceinline__ int pair_index(int nb, int round, int p, int l) {
+    int a, b;
+    rr_pair(nb, round, p, a, b);
+    return (l < kB ? a : b) * kB + (l & (kB - 1));
+}
+
+constexpr int kSolveThreads = 512;
+constexpr int kSP = kP + 1;  // padded pitch of the subproblem tiles
+
+// One CTA per pair: load the 64 x 64 subproblem, run up to `inner_sweeps`
+// cyclic Jacobi sweeps in parallel order (32 disjoint rotations per step), and
+// write the accumulated rotation R (64 x 64).
+__global__ void __launch_bounds__(kSolveThreads)
+jacobi_solve_kernel(const JacBatch jb, int inner_sweeps) {
+    __shared__ float S[kP * kSP];
+    __shared__ float Q[kP * kSP];
+    __shared__ float cs[kB][2];
+    __shared__ int pq[kB][2];
+    __shared__ float red[2][kSolveThreads / 32];
+    const int job = find_job(jb.pair_off, jb.count, blockIdx.x);
+    if (!jb.active[job]) return;
+    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
+    const int pair = blockIdx.x - jb.pair_off[job];
+    const float *A = jb.A[job];
     const int tid = threadIdx.x;
-    const int tx = tid % kP, ty = tid / kP;  // 32 x 8
-    for (int64_t t = blockIdx.x; t < atiles + (int64_t)(Np / kP) * np; t += gridDim.x) {
-        __syncthreads();
-        if (t < atiles) {
-            const int p1 = (int)(t / np), p2 = (int)(t % np);
-            for (int i = ty; i < kP; i += 8) {
-                const int gi = pair_index(nb, round, p1, i), gj = pair_index(nb, round, p2, tx);
-                X[i][tx] = A[(size_t)gi * Np + gj];
-                R1[i][tx] = R[(size_t)p1 * kP * kP + i * kP + tx];
-                R2[i][tx] = R[(size_t)p2 * kP * kP + i * kP + tx];
+    for (int e = tid; e < kP * kP; e += kSolveThreads) {
+        const int i = e / kP, j = e % kP;
+        S[i * kSP + j] = A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j)];
+        Q[i * kSP + j] = (i == j) ? 1.f : 0.f;
+    }
+    __syncthreads();
+    for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
+        float offmax = 0.f, dmax = 0.f;
+        for (int step = 0; step < kP - 1; ++step) {
+            if (tid < kB) {
+                int p, q;
+                rr_pair(kP, step, tid, p, q);
+                const float apq = S[p * kSP + q];
+                float c, sn;
+                jacobi_cs(S[p * kSP + p], S[q * kSP + q], apq, c, sn);
+                cs[tid][0] = c;
+                cs[tid][1] = sn;
+                pq[tid][0] = p;
+                pq[tid][1] = q;
+                offmax = fmaxf(offmax, fabsf(apq));
+                dmax = fmaxf(dmax, fmaxf(fabsf(S[p * kSP + p]), fabsf(S[q * kSP + q])));
             }
             __syncthreads();
-            for (int i = ty; i < kP; i += 8) {  // T = R1^T X
-                float acc = 0.f;
-#pragma unroll 8
-                for (int k = 0; k < kP; ++k) acc = fmaf(R1[k][i], X[k][tx], acc);
-                T[i][tx] = acc;
+            // rows p, q of S: 32 pairs x 64 columns, 4 element pairs per thread
+#pragma unroll
+            for (int u = 0; u < (kB * kP) / kSolveThreads; ++u) {
+                const int e = tid + u * kSolveThreads;
+                const int k = e / kP, j = e % kP;
+                const int p = pq[k][0], q = pq[k][1];
+                const float c = cs[k][0], sn = cs[k][1];
+                const float x = S[p * kSP + j], y = S[q * kSP + j];
+                S[p * kSP + j] = c * x - sn * y;
+                S[q * kSP + j] = sn * x + c * y;
             }
             __syncthreads();
-            for (int i = ty; i < kP; i += 8) {  // A' = T R2
-                float acc = 0.f;
-#pragma unroll 8
-                for (int k = 0; k < kP; ++k) acc = fmaf(T[i][k], R2[k][tx], acc);
-                const int gi = pair_index(nb, round, p1, i), gj = pair_index(nb, round, p2, tx);
-                A[(size_t)gi * Np + gj] = acc;
-            }
-        } else {
-            const int64_t u = t - atiles;
-            const int slab = (int)(u / np), p = (int)(u % np);
-            for (int i = ty; i < kP; i += 8) {
-                const int gj = pair_index(nb, round, p, tx);
-                X[i][tx] = Qacc[(size_t)(slab * kP + i) * Np + gj];
-                R2[i][tx] = R[(size_t)p * kP * kP + i * kP + tx];
+            // columns p, q of S and of Q
+#pragma unroll
+            for (int u = 0; u < (kB * kP) / kSolveThreads; ++u) {
+                const int e = tid + u * kSolveThreads;
+                const int k = e / kP, i = e % kP;
+                const int p = pq[k][0], q = pq[k][1];
+                const float c = cs[k][0], sn = cs[k][1];
+                float x = S[i * kSP + p], y = S[i * kSP + q];
+                S[i * kSP + p] = c * x - sn * y;
+                S[i * kSP + q] = sn * x + c * y;
+                x = Q[i * kSP + p];
+                y = Q[i * kSP + q];
+                Q[i * kSP + p] = c * x - sn * y;
+                Q[i * kSP + q] = sn * x + c * y;
             }
             __syncthreads();
-            for (int i = ty; i < kP; i += 8) {
-                float acc = 0.f;
-#pragma unroll 8
-                for (int k = 0; k < kP; ++k) acc = fmaf(X[i][k], R2[k][tx], acc);
-                const int gj = pair_index(nb, round, p, tx);
-                Qacc[(size_t)(slab * kP + i) * Np + gj] = acc;
+        }
+        // stop once no off-diagonal entry rotated in this sweep was above fp32 noise
+        if (tid < 32) {
+            for (int o = 16; o > 0; o >>= 1) {
+                offmax = fmaxf(offmax, __shfl_xor_sync(0xffffffffu, offmax, o));
+                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+            }
+            if (tid == 0) {
+                red[0][0] = offmax;
+                red[1][0] = dmax;
             }
         }
+        __syncthreads();
+        const bool done = red[0][0] <= 1e-7f * red[1][0];
+        __syncthreads();
+        if (done) break;
     }
+    float *Rp = jb.R[job] + (size_t)pair * kP * kP;
+    for (int e = tid; e < kP * kP; e += kSolveThreads) Rp[e] = Q[(e / kP) * kSP + (e % kP)];
+}
+
+// 64 x 64 x 64 product of two shared tiles into registers, 4 x 4 outputs per
+// thread (256 threads): out[i][j] = sum_k L(i,k) Rt(k,j), where L is read
+// either as X[i][k] (left_t = false) or X[k][i] (left_t = true).
+template <bool left_t>
+__device__ __forceinline__ void tile_product(const float *X, const float *Y, int ti, int tj,
+                                             float (&acc)[4][4]) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kP; ++k) {
+        float l[4], r[4];
+        if (left_t) {
+            const float4 v = *reinterpret_cast<const float4 *>(&X[k * kP + 4 * ti]);
+            l[0] = v.x; l[1] = v.y; l[2] = v.z; l[3] = v.w;
+        } else {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) l[a] = X[(4 * ti + a) * (kP + 4) + k];
+        }
+        const float4 w = *reinterpret_cast<const float4 *>(&Y[k * kP + 4 * tj]);
+        r[0] = w.x; r[1] = w.y; r[2] = w.z; r[3] = w.w;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(l[a], r[b], acc[a][b]);
+    }
+}
+
+// Rows pass (A <- R_p^T A on the rows of each pair, 64-column chunks) and the
+// accumulation Q <- Q R_p (64-row chunks): both read what the previous round
+// left and touch disjoint elements.
+__global__ void __launch_bounds__(256)
+jacobi_rows_kernel(const JacBatch jb) {
+    __shared__ __align__(16) float Rs[kP * kP];
+    __shared__ __align__(16) float Xs[kP * (kP + 4)];
+    const int item = blockIdx.x;
+    const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
+    const int total_rows = jb.row_off[jb.count];
+    if (item < total_rows) {
+        const int job = find_job(jb.row_off, jb.count, item);
+        if (!jb.active[job]) return;
+        const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], chunks = Np / kP;
+        const int local = item - jb.row_off[job];
+        const int pair = local / chunks, c0 = (local % chunks) * kP;
+        float *A = jb.A[job];
+        const float *R = jb.R[job] + (size_t)pair * kP * kP;
+        for (int e = tid; e < kP * kP; e += 256) {
+            Rs[e] = R[e];
+            const int l = e / kP, j = e % kP;
+            Xs[l * kP + j] = A[(size_t)pair_index(nb, round, pair, l) * Np + c0 + j];
+        }
+        __syncthreads();
+        float acc[4][4];
+        tile_product<true>(Rs, Xs, ti, tj, acc);  // (R^T X)[i][j] = sum_k R[k][i] X[k][j]
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int gi = pair_index(nb, round, pair, 4 * ti + a);
+            *reinterpret_cast<float4 *>(&A[(size_t)gi * Np + c0 + 4 * tj]) =
+                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
+        return;
+    }
+    // Q items
+    const int qitem = item - total_rows;
+    const int job = find_job(jb.q_off, jb.count, qitem);
+    if (!jb.active[job]) return;
+    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], pairs = Np / kP;
+    const int local = qitem - jb.q_off[job];
+    const int r0 = (local / pairs) * kP, pair = local % pairs;
+    float *Qm = jb.Q[job];
+    const float *R = jb.R[job] + (size_t)pair * kP * kP;
+    for (int e = tid; e < kP * kP; e += 256) {
+        Rs[e] = R[e];
+        const int rr = e / kP, l = e % kP;
+        Xs[rr * (kP + 4) + l] = Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l)];
+    }
+    __syncthreads();
+    float acc[4][4];
+    tile_product<false>(Xs, Rs, ti, tj, acc);  // (X R)[i][j]
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            Qm[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj + b)] = acc[a][b];
+}
+
+// Columns pass: A <- A R_p on the columns of each pair, 64-row chunks.
+__global__ void __launch_bounds__(256)
+jacobi_cols_kernel(const JacBatch jb) {
+    __shared__ __align__(16) float Rs[kP * kP];
+    __shared__ __align__(16) float Xs[kP * (kP + 4)];
+    const int item = blockIdx.x;
+    const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
+    const int job = find_job(jb.col_off, jb.count, item);
+    if (!jb.active[job]) return;
+    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], pairs = Np / kP;
+    const int local = item - jb.col_off[job];
+    const int r0 = (local / pairs) * kP, pair = local % pairs;
+    float *A = jb.A[job];
+    const float *R = jb.R[job] + (size_t)pair * kP * kP;
+    for (int e = tid; e < kP * kP; e += 256) {
+        Rs[e] = R[e];
+        const int rr = e / kP, l = e % kP;
+        Xs[rr * (kP + 4) + l] = A[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l)];
+    }
+    __syncthreads();
+    float acc[4][4];
+    tile_product<false>(Xs, Rs, ti, tj, acc);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            A[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj + b)] = acc[a][b];
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -207,6 +309,16 @@ __global__ void eye_kernel(float *__restrict__ Q, int Np) {
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x)
         Q[e] = (e / Np == e % Np) ? 1.f : 0.f;
+}
+
+// Qacc = [W 0; 0 I] with W the previous short-side factor (r x r, row-major)
+__global__ void init_q_kernel(float *__restrict__ Q, int Np, int r, const float *__restrict__ W) {
+    const int64_t total = (int64_t)Np * Np;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(e / Np), j = (int)(e % Np);
+        Q[e] = (i < r && j < r) ? W[(size_t)i * r + j] : (i == j ? 1.f : 0.f);
+    }
 }
 
 // sums of squares: out[0] = off-diagonal, out[1] = all (double atomics)
@@ -305,108 +417,194 @@ int grid_for(int64_t work, int threads) {
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = ((r + kP - 1) / kP) * kP;
-    const int64_t np = Np / kP;
-    // A, Qacc, rotations, short factor + NS temp (2 r^2), long factor P (L r),
-    // s_raw, inv_s, order (int), 2 doubles
-    return (size_t)(2 * Np * Np + np * kP * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
+    // A, Qacc, rotations (Np/64 x 64 x 64), short factor + scratch (2 r^2), long factor P
+    // (L r), s_raw, inv_s, order (int), 2 doubles
+    return (size_t)(2 * Np * Np + Np * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
 }
 
-int svd_refresh_run(const SvdArgs &a, cudaStream_t st, int *sweeps_out) {
-    const bool tall = a.m >= a.n;
-    const int r = tall ? a.n : a.m;
-    const int64_t L = tall ? a.m : a.n;  // long side
-    const int Np = ((r + kP - 1) / kP) * kP;
-    const int nb = Np / kB, np = nb / 2;
-    float *A = a.work;
-    float *Qacc = A + (size_t)Np * Np;
-    float *R = Qacc + (size_t)Np * Np;
-    float *Sf = R + (size_t)np * kP * kP;  // short-side factor, unsorted (r x r)
-    float *Tmp = Sf + (size_t)r * r;       // r x r scratch
-    float *P = Tmp + (size_t)r * r;        // long-side M V (or M^T U), unsorted (L x r)
-    float *s_raw = P + (size_t)L * r;
-    float *inv_s = s_raw + r;
-    int *order = reinterpret_cast<int *>(inv_s + r);
-    double *norms = reinterpret_cast<double *>(
-        (reinterpret_cast<uintptr_t>(order + r) + 15) & ~uintptr_t(15));
+namespace {
 
-    // 1. Gram matrix of the short side into the padded A
-    SPECOPTIM_CUDA(cudaMemsetAsync(A, 0, sizeof(float) * (size_t)Np * Np, st));
+struct JobBufs {
+    int r, Np, nb;
+    int64_t L;
+    bool tall;
+    float *A, *Qacc, *R, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    int *order;
+    double *norms;
+};
+
+JobBufs carve(const SvdJob &a) {
+    JobBufs b;
+    b.tall = a.m >= a.n;
+    b.r = b.tall ? a.n : a.m;
+    b.L = b.tall ? a.m : a.n;
+    b.Np = ((b.r + kP - 1) / kP) * kP;
+    b.nb = b.Np / kB;
+    b.A = a.work;
+    b.Qacc = b.A + (size_t)b.Np * b.Np;
+    b.R = b.Qacc + (size_t)b.Np * b.Np;
+    b.Sf = b.R + (size_t)b.Np * kP;
+    b.Tmp = b.Sf + (size_t)b.r * b.r;
+    b.P = b.Tmp + (size_t)b.r * b.r;
+    b.s_raw = b.P + (size_t)b.L * b.r;
+    b.inv_s = b.s_raw + b.r;
+    b.order = reinterpret_cast<int *>(b.inv_s + b.r);
+    b.norms = reinterpret_cast<double *>((reinterpret_cast<uintptr_t>(b.order + b.r) + 15) & ~uintptr_t(15));
+    return b;
+}
+
+// Gram matrix of the short side into the padded A, and the starting basis:
+// identity, or the previous short-side factor W with A <- W^T A W.
+int prepare(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
+    SPECOPTIM_CUDA(cudaMemsetAsync(b.A, 0, sizeof(float) * (size_t)b.Np * b.Np, st));
     Epilogue e;
-    e.C = A;
-    e.ldc = Np;
+    e.C = b.A;
+    e.ldc = b.Np;
     int rc;
-    if (tall)  // A = M^T M : op(A)(i,k) = M[k][i], op(B)(k,j) = M[k][j]
-        rc = gemm_simt(r, r, a.m, Operand{a.M, a.n, true}, Operand{a.M, a.n, false}, e, st);
-    else       // A = M M^T
-        rc = gemm_simt(r, r, a.n, Operand{a.M, a.n, false}, Operand{a.M, a.n, true}, e, st);
+    if (b.tall)  // A = M^T M : op(A)(i,k) = M[k][i], op(B)(k,j) = M[k][j]
+        rc = gemm_simt(b.r, b.r, a.m, Operand{a.M, a.n, true}, Operand{a.M, a.n, false}, e, st);
+    else         // A = M M^T
+        rc = gemm_simt(b.r, b.r, a.n, Operand{a.M, a.n, false}, Operand{a.M, a.n, true}, e, st);
     if (rc) return rc;
-
-    // 2. block Jacobi
-    SPCO_LAUNCH("svd_eye", st, eye_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(Qacc, Np));
-    SPECOPTIM_LAUNCHED("eye_kernel");
-    const int solve_blocks = (np + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int64_t apply_work = (int64_t)np * np + (int64_t)(Np / kP) * np;
-    const int apply_grid = (int)std::min<int64_t>(apply_work, (int64_t)num_sms() * 8);
-    int sweep = 0;
-    bool converged = false;
-    double host_norms[2] = {0.0, 0.0};
-    for (sweep = 0; sweep < a.max_sweeps && !converged; ++sweep) {
-        for (int round = 0; round < nb - 1; ++round) {
-            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_blocks, 32 * kWarpsPerBlock, 0, st>>>(A, Np, round, R, 4));
-            SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(A, Qacc, Np, round, R));
-        }
-        SPECOPTIM_LAUNCHED("jacobi sweep");
-        SPECOPTIM_CUDA(cudaMemsetAsync(norms, 0, 2 * sizeof(double), st));
-        SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for((int64_t)Np * Np, 256), 256, 0, st>>>(A, Np, norms));
-        SPECOPTIM_LAUNCHED("offnorm_kernel");
-        SPECOPTIM_CUDA(cudaMemcpyAsync(host_norms, norms, 2 * sizeof(double),
-                                       cudaMemcpyDeviceToHost, st));
-        SPECOPTIM_CUDA(cudaStreamSynchronize(st));
-        converged = host_norms[0] <= (double)a.tol * a.tol * host_norms[1];
+    const int64_t NN = (int64_t)b.Np * b.Np;
+    if (!a.warm) {
+        SPCO_LAUNCH("svd_eye", st, eye_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b.Qacc, b.Np));
+        SPECOPTIM_LAUNCHED("eye_kernel");
+        return SPECOPTIM_OK;
     }
-    if (sweeps_out) *sweeps_out = sweep;
-    if (!converged)
-        return fail(SPECOPTIM_ERR_NOT_CONVERGED,
-                    "svd_refresh: Jacobi did not reach svd_tol within svd_max_sweeps; "
-                    "previous factors kept");
+    SPCO_LAUNCH("svd_init_q", st, init_q_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b.Qacc, b.Np, b.r, a.warm));
+    SPECOPTIM_LAUNCHED("init_q_kernel");
+    Epilogue t;
+    t.C = b.Tmp;
+    t.ldc = b.r;
+    if ((rc = gemm_simt(b.r, b.r, b.r, Operand{b.A, b.Np, false}, Operand{a.warm, b.r, false}, t, st)))
+        return rc;  // T = A W
+    Epilogue w;
+    w.C = b.A;
+    w.ldc = b.Np;
+    return gemm_simt(b.r, b.r, b.r, Operand{a.warm, b.r, true}, Operand{b.Tmp, b.r, false}, w, st);  // W^T T
+}
 
-    // 3. short-side factor, re-orthonormalised: two Newton-Schulz steps
-    //    X <- X (3 I - X^T X) / 2 remove the drift that thousands of fp32
-    //    rotations leave in the accumulated eigenvectors.
-    const int64_t rr = (int64_t)r * r;
-    SPCO_LAUNCH("svd_extract", st, extract_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Qacc, Np, r, Sf));
+// re-orthonormalised short factor, s_i = |M v_i| sorted descending, d, long factor
+int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
+    const int r = b.r;
+    const int64_t rr = (int64_t)r * r, L = b.L;
+    int rc;
+    SPCO_LAUNCH("svd_extract", st, extract_kernel<<<grid_for(rr, 256), 256, 0, st>>>(b.Qacc, b.Np, r, b.Sf));
     SPECOPTIM_LAUNCHED("extract_kernel");
+    // two Newton-Schulz steps X <- X (3 I - X^T X) / 2 remove the drift that the
+    // fp32 rotations leave in the accumulated eigenvectors
     for (int it = 0; it < 2; ++it) {
         Epilogue g;
-        g.C = A;  // X^T X (r x r, ld r) reuses the Gram buffer
+        g.C = b.A;  // X^T X (r x r, ld r) reuses the Gram buffer
         g.ldc = r;
-        if ((rc = gemm_simt(r, r, r, Operand{Sf, r, true}, Operand{Sf, r, false}, g, st))) return rc;
+        if ((rc = gemm_simt(r, r, r, Operand{b.Sf, r, true}, Operand{b.Sf, r, false}, g, st))) return rc;
         Epilogue t;
-        t.C = Tmp;
+        t.C = b.Tmp;
         t.ldc = r;
-        if ((rc = gemm_simt(r, r, r, Operand{Sf, r, false}, Operand{A, r, false}, t, st))) return rc;
-        SPCO_LAUNCH("svd_ns_update", st, ns_update_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Sf, Tmp, rr));
+        if ((rc = gemm_simt(r, r, r, Operand{b.Sf, r, false}, Operand{b.A, r, false}, t, st))) return rc;
+        SPCO_LAUNCH("svd_ns_update", st, ns_update_kernel<<<grid_for(rr, 256), 256, 0, st>>>(b.Sf, b.Tmp, rr));
         SPECOPTIM_LAUNCHED("ns_update_kernel");
     }
-
-    // 4. long side P = M X (tall) or M^T X (wide); s_i = |P e_i|, sorted descending;
-    //    long factor = P diag(1/s), zero columns where s_i = 0
     Epilogue f;
-    f.C = P;
+    f.C = b.P;
     f.ldc = r;
-    if (tall)
-        rc = gemm_simt(L, r, a.n, Operand{a.M, a.n, false}, Operand{Sf, r, false}, f, st);
+    if (b.tall)
+        rc = gemm_simt(L, r, a.n, Operand{a.M, a.n, false}, Operand{b.Sf, r, false}, f, st);
     else
-        rc = gemm_simt(L, r, a.m, Operand{a.M, a.n, true}, Operand{Sf, r, false}, f, st);
+        rc = gemm_simt(L, r, a.m, Operand{a.M, a.n, true}, Operand{b.Sf, r, false}, f, st);
     if (rc) return rc;
-    SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid_for(r, 128), 128, 0, st>>>(P, L, r, s_raw));
-    SPCO_LAUNCH("svd_rank", st, rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(s_raw, r, order));
-    SPCO_LAUNCH("svd_spectrum", st, spectrum_kernel<<<grid_for(r, 128), 128, 0, st>>>(s_raw, r, order, a.tau, a.s, a.d, inv_s));
-    float *short_out = tall ? a.V : a.U;
-    float *long_out = tall ? a.U : a.V;
-    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(rr, 256), 256, 0, st>>>(Sf, r, r, order, nullptr, short_out));
-    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(L * r, 256), 256, 0, st>>>(P, L, r, order, inv_s, long_out));
+    SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.P, L, r, b.s_raw));
+    SPCO_LAUNCH("svd_rank", st, rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.s_raw, r, b.order));
+    SPCO_LAUNCH("svd_spectrum", st, spectrum_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.s_raw, r, b.order, a.tau, a.s, a.d, b.inv_s));
+    float *short_out = b.tall ? a.V : a.U;
+    float *long_out = b.tall ? a.U : a.V;
+    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(rr, 256), 256, 0, st>>>(b.Sf, r, r, b.order, nullptr, short_out));
+    SPCO_LAUNCH("svd_permute", st, permute_cols_kernel<<<grid_for(L * r, 256), 256, 0, st>>>(b.P, L, r, b.order, b.inv_s, long_out));
     SPECOPTIM_LAUNCHED("svd spectrum kernels");
+    return SPECOPTIM_OK;
+}
+
+}  // namespace
+
+int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
+    if (count < 1 || count > kMaxBatch)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: 1 to 16 matrices per batch");
+    JobBufs b[kMaxBatch];
+    int rc;
+    for (int i = 0; i < count; ++i) {
+        b[i] = carve(jobs[i]);
+        jobs[i].sweeps = 0;
+        jobs[i].status = SPECOPTIM_OK;
+        if ((rc = prepare(jobs[i], b[i], st))) return rc;
+    }
+    JacBatch jb;
+    std::memset(&jb, 0, sizeof(jb));
+    jb.count = count;
+    int max_sweeps = 1, rounds = 1;
+    for (int i = 0; i < count; ++i) {
+        jb.A[i] = b[i].A;
+        jb.Q[i] = b[i].Qacc;
+        jb.R[i] = b[i].R;
+        jb.Np[i] = b[i].Np;
+        jb.active[i] = 1;
+        const int pairs = b[i].Np / kP, chunks = b[i].Np / kP;
+        jb.pair_off[i + 1] = jb.pair_off[i] + pairs;
+        jb.row_off[i + 1] = jb.row_off[i] + pairs * chunks;
+        jb.q_off[i + 1] = jb.q_off[i] + chunks * pairs;
+        jb.col_off[i + 1] = jb.col_off[i] + chunks * pairs;
+        max_sweeps = std::max(max_sweeps, jobs[i].max_sweeps);
+        rounds = std::max(rounds, b[i].nb - 1);
+    }
+    const int solve_grid = jb.pair_off[count];
+    const int rows_grid = jb.row_off[count] + jb.q_off[count];
+    const int cols_grid = jb.col_off[count];
+    std::vector<double> host(2 * count);
+    int active = count;
+    for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
+        for (int g = 0; g < rounds; ++g) {
+            for (int i = 0; i < count; ++i) jb.round[i] = g % (b[i].nb - 1);
+            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, 0, st>>>(jb, 2));
+            SPCO_LAUNCH("svd_jacobi_rows", st, jacobi_rows_kernel<<<rows_grid, 256, 0, st>>>(jb));
+            SPCO_LAUNCH("svd_jacobi_cols", st, jacobi_cols_kernel<<<cols_grid, 256, 0, st>>>(jb));
+        }
+        SPECOPTIM_LAUNCHED("jacobi sweep");
+        for (int i = 0; i < count; ++i) {
+            if (!jb.active[i]) continue;
+            jobs[i].sweeps = sweep + 1;
+            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), st));
+            const int64_t NN = (int64_t)b[i].Np * b[i].Np;
+            SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b[i].A, b[i].Np, b[i].norms));
+            SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
+                                           cudaMemcpyDeviceToHost, st));
+        }
+        SPECOPTIM_LAUNCHED("offnorm_kernel");
+        SPECOPTIM_CUDA(cudaStreamSynchronize(st));
+        for (int i = 0; i < count; ++i) {
+            if (!jb.active[i]) continue;
+            const double tol = jobs[i].tol;
+            if (host[2 * i] <= tol * tol * host[2 * i + 1]) {
+                jb.active[i] = 0;
+                --active;
+            } else if (jobs[i].sweeps >= jobs[i].max_sweeps) {
+                jb.active[i] = 0;
+                --active;
+                jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
+            }
+        }
+    }
+    int first_bad = SPECOPTIM_OK;
+    for (int i = 0; i < count; ++i) {
+        if (jb.active[i]) jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
+        if (jobs[i].status != SPECOPTIM_OK) {
+            if (!first_bad) first_bad = jobs[i].status;
+            continue;
+        }
+        if ((rc = finish(jobs[i], b[i], st))) return rc;
+    }
+    if (first_bad)
+        return fail(first_bad, "svd_refresh: Jacobi did not reach svd_tol within svd_max_sweeps; "
+                               "previous factors kept for the matrices concerned");
     return SPECOPTIM_OK;
 }
 

@@ -5,17 +5,21 @@
 
 namespace spco {
 
-struct SvdArgs {
-    const float *M;  // m x n anchor momentum
+// One matrix of a (batched) refresh.
+struct SvdJob {
+    const float *M;        // m x n anchor momentum
     int m, n;
     float *U, *s, *V, *d;  // outputs: U m x r, s r, V n x r, d r (written only on success)
-    float *work;           // svd_workspace_floats(r) floats, 16-byte aligned
-    float tau;
+    float *work;           // svd_workspace_floats(m, n) floats, 16-byte aligned
+    const float *warm;     // previous short-side factor (r x r) to start from, or null
+    float tau, tol;
     int max_sweeps;
-    float tol;
+    int sweeps;            // out: Jacobi sweeps run
+    int status;            // out: SPECOPTIM_OK or SPECOPTIM_ERR_NOT_CONVERGED
 };
 
 size_t svd_workspace_floats(int m, int n);
-int svd_refresh_run(const SvdArgs &args, cudaStream_t stream, int *sweeps_out);
+// Refreshes up to 16 matrices; their Jacobi rounds share kernel launches.
+int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t stream);
 
 }  // namespace spco

@@ -168,3 +168,42 @@ def test_invalid_arguments_on_gpu():
     lib = so.lib()
     rc = lib.specoptim_step(opt._h, raw.data_ptr() + 4, raw.data_ptr(), 1e-3, None, None, None)
     assert rc == so.ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_batched_and_warm_started_refresh(prec):
+    # three matrices refreshed in one batched call, twice (the second refresh starts
+    # from the first one's factors); each step is compared with the oracle
+    shapes = [(256, 128), (96, 192), (160, 160)]
+    inps = [synthetic.MatrixInputs(m, n, seed=40 + i, rank=6) for i, (m, n) in enumerate(shapes)]
+    gpus = [so.SpectralOptimizer(i.m, i.n, precision=prec) for i in inps]
+    oras = [oracle.SpectralOptimizer(i.m, i.n) for i in inps]
+    Ws = [dev(i.weights()) for i in inps]
+    Wo = [i.weights().astype(np.float64) for i in inps]
+    for anchor in range(2):
+        for g, o, i in zip(gpus, oras, inps):
+            G = i.anchor_grad(anchor)
+            g.anchor_update(dev(G))
+            o.anchor_update(G)
+            o.svd_refresh()
+        sweeps = so.svd_refresh_many(gpus)
+        assert all(1 <= s_ <= 20 for s_ in sweeps)
+        for k, (g, o, i) in enumerate(zip(gpus, oras, inps)):
+            G = i.masked_grad(10 * anchor)
+            gf = torch.empty(i.m, i.n, device="cuda")
+            g.step(Ws[k], dev(G), 2e-5, gf)
+            Wo[k], Gf_o, _ = o.step(Wo[k], G, 2e-5)
+            assert rel(host(gf), Gf_o) <= TOL[prec]
+            _, s_, _, d_ = g.get_factors()
+            # an fp32 Gram matrix fixes s only to about sqrt(eps_fp32) * s_max in
+            # absolute terms (2.4e-4 s_max); d = s / (s + tau) is what the step uses
+            assert np.abs(host(s_) - o.s).max() <= 5e-4 * o.s[0]
+            assert np.abs(host(d_) - o.d).max() <= 1e-3
+
+
+def test_refresh_many_rejects_bad_batches():
+    a = so.SpectralOptimizer(32, 16)
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_many([a, a])
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_many([so.SpectralOptimizer(8, 8) for _ in range(17)])
