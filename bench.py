@@ -286,7 +286,10 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     steady_ms = timed(torch, lambda: [layer.spectral(1000 + i) for i in range(steady_n)], False) / steady_n
     rep = so.trace_report()
     so.trace_enable(False)
+    so.trace_enable(True)
     refresh_ms = timed(torch, lambda: layer.refresh(7), False)
+    refresh_rep = so.trace_report()
+    so.trace_enable(False)
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
     mask_frac = mask["p0.95"]["effective_GBps"] / peaks["hbm_gbs"]
 
@@ -325,7 +328,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "roofline": roof,
         "breakdown": {"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
                       "step_roofline_ms": step_bound_ms, "step_frac": step_bound_ms / steady_ms,
-                      "refresh_ms": refresh_ms, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()}},
+                      "refresh_ms": refresh_ms, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()},
+                      "refresh_kernels": {k: {"launches": v[0], "ms": round(v[1], 3)} for k, v in refresh_rep.items()}},
         "mask": dict(mask, frac_of_hbm=mask_frac, hbm_peak_GBps=peaks["hbm_gbs"]),
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak},
     }
@@ -453,7 +457,8 @@ def run_reference(args, rank, world):
 def run_profile_case(args):
     """Small cases for ncu captures (a few hundred MB on the device):
     'gate': steady spectral steps of one 8192x2048 matrix (transpose + 4 GEMMs per step);
-    'mask': pack / unpack of one bf16 [65536, 2048] boundary at p = 0.95."""
+    'mask': pack / unpack of one bf16 [65536, 2048] boundary at p = 0.95;
+    'refresh': anchor EMA + SVD refresh of one 2048x2048 matrix, twice (the second warm)."""
     import numpy as np
     import torch
 
@@ -470,6 +475,12 @@ def run_profile_case(args):
         G = [torch.from_numpy(inp.masked_grad(t)).cuda() for t in range(2)]
         for i in range(n_iter):
             opt.step(W, G[i % 2], 2e-5)
+    elif args.profile == "refresh":
+        inp = synthetic.MatrixInputs(2048, 2048, seed=0, rank=32)
+        opt = so.SpectralOptimizer(2048, 2048)
+        for i in range(2):
+            opt.anchor_update(torch.from_numpy(inp.anchor_grad(i)).cuda())
+            opt.svd_refresh()
     else:
         K = so.mask_keep_count(MASK_P, MASK_H)
         h = torch.from_numpy(synthetic.activations_bf16(MASK_ROWS, MASK_H).view(np.int16)).view(
@@ -491,7 +502,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["gate", "mask"], default=None,
+    ap.add_argument("--profile", choices=["gate", "mask", "refresh"], default=None,
                     help="run a small case for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

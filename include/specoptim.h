@@ -57,6 +57,7 @@ typedef struct {
     int32_t precision;      /* SPECOPTIM_PREC_TF32 (default) or SPECOPTIM_PREC_FP32    */
     int32_t svd_max_sweeps; /* Jacobi sweep limit of the SVD refresh (default 20)      */
     float svd_tol;          /* off-diagonal / total Frobenius norm to stop at (1e-5)  */
+    int32_t svd_inner_sweeps; /* Jacobi sweeps on each 64 x 64 subproblem per round (1) */
 } specoptim_config;
 
 /* Fills *cfg with the defaults above for an m x n weight.  The defaults are

@@ -37,7 +37,7 @@ class Config(ctypes.Structure):
                 ("tau_p", ctypes.c_float), ("alpha", ctypes.c_float), ("beta1", ctypes.c_float),
                 ("beta2", ctypes.c_float), ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
                 ("precision", ctypes.c_int32), ("svd_max_sweeps", ctypes.c_int32),
-                ("svd_tol", ctypes.c_float)]
+                ("svd_tol", ctypes.c_float), ("svd_inner_sweeps", ctypes.c_int32)]
 
 
 # (name, restype, argtypes) of every exported entry point of include/specoptim.h

@@ -109,6 +109,8 @@ int validate_cfg(const specoptim_config *c) {
         return fail(SPECOPTIM_ERR_INVALID_ARG, "unknown precision");
     if (c->svd_max_sweeps < 1) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_max_sweeps must be >= 1");
     if (!(c->svd_tol >= 0.f)) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_tol must be >= 0");
+    if (c->svd_inner_sweeps < 1 || c->svd_inner_sweeps > 16)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_inner_sweeps must be in [1, 16]");
     return SPECOPTIM_OK;
 }
 
@@ -139,6 +141,7 @@ extern "C" int specoptim_config_default(specoptim_config *cfg, int32_t m, int32_
     cfg->precision = SPECOPTIM_PREC_TF32;
     cfg->svd_max_sweeps = 20;
     cfg->svd_tol = 1e-5f;
+    cfg->svd_inner_sweeps = 1;
     return SPECOPTIM_OK;
 }
 
@@ -224,6 +227,7 @@ extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t c
         a.tau = h->cfg.tau_p;
         a.tol = h->cfg.svd_tol;
         a.max_sweeps = h->cfg.svd_max_sweeps;
+        a.inner_sweeps = h->cfg.svd_inner_sweeps;
     }
     int rc = svd_refresh_batch(jobs, count, st);
     if (sweeps_out)

@@ -79,9 +79,8 @@ struct JacBatch {
     int round[kMaxBatch];
     int active[kMaxBatch];
     int pair_off[kMaxBatch + 1];   // solve: one CTA per pair
-    int row_off[kMaxBatch + 1];    // rows pass: pairs x (Np/64) column chunks, then Q items
-    int q_off[kMaxBatch + 1];      // Q items: (Np/64) row chunks x pairs
-    int col_off[kMaxBatch + 1];    // cols pass: (Np/64) row chunks x pairs
+    int row_off[kMaxBatch + 1];    // apply: upper-triangle A tiles (pair p1 <= pair p2)
+    int q_off[kMaxBatch + 1];      // apply: Q slabs, (Np/64) row chunks x pairs
 };
 
 __device__ __forceinline__ int find_job(const int *off, int count, int item) {
@@ -102,25 +101,34 @@ constexpr int kSP = kP + 1;  // padded pitch of the subproblem tiles
 
 // One CTA per pair: load the 64 x 64 subproblem, run up to `inner_sweeps`
 // cyclic Jacobi sweeps in parallel order (32 disjoint rotations per step), and
-// write the accumulated rotation R (64 x 64).
+// write the accumulated rotation R (64 x 64).  Each step has two phases: 32
+// threads compute the rotations; then every 2 x 2 block (p_a, q_a) x (p_b, q_b)
+// of S receives the row rotation of pair a and the column rotation of pair b
+// at once, and Q's columns p_b, q_b the rotation of pair b.
 __global__ void __launch_bounds__(kSolveThreads)
 jacobi_solve_kernel(const JacBatch jb, int inner_sweeps) {
     __shared__ float S[kP * kSP];
     __shared__ float Q[kP * kSP];
     __shared__ float cs[kB][2];
     __shared__ int pq[kB][2];
-    __shared__ float red[2][kSolveThreads / 32];
+    __shared__ float red[2];
     const int job = find_job(jb.pair_off, jb.count, blockIdx.x);
     if (!jb.active[job]) return;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
     const int pair = blockIdx.x - jb.pair_off[job];
     const float *A = jb.A[job];
     const int tid = threadIdx.x;
-    for (int e = tid; e < kP * kP; e += kSolveThreads) {
-        const int i = e / kP, j = e % kP;
-        S[i * kSP + j] = A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j)];
-        Q[i * kSP + j] = (i == j) ? 1.f : 0.f;
+    // 64 rows x 16 float4 (each row of the subproblem is two runs of 32 floats)
+    for (int e = tid; e < kP * (kP / 4); e += kSolveThreads) {
+        const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
+        const float4 v = *reinterpret_cast<const float4 *>(
+            &A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j4)]);
+        S[i * kSP + j4] = v.x;
+        S[i * kSP + j4 + 1] = v.y;
+        S[i * kSP + j4 + 2] = v.z;
+        S[i * kSP + j4 + 3] = v.w;
     }
+    for (int e = tid; e < kP * kP; e += kSolveThreads) Q[(e / kP) * kSP + e % kP] = (e / kP == e % kP) ? 1.f : 0.f;
     __syncthreads();
     for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
         float offmax = 0.f, dmax = 0.f;
@@ -128,43 +136,63 @@ jacobi_solve_kernel(const JacBatch jb, int inner_sweeps) {
             if (tid < kB) {
                 int p, q;
                 rr_pair(kP, step, tid, p, q);
-                const float apq = S[p * kSP + q];
+                const float app = S[p * kSP + p], aqq = S[q * kSP + q], apq = S[p * kSP + q];
                 float c, sn;
-                jacobi_cs(S[p * kSP + p], S[q * kSP + q], apq, c, sn);
+                jacobi_cs(app, aqq, apq, c, sn);
                 cs[tid][0] = c;
                 cs[tid][1] = sn;
                 pq[tid][0] = p;
                 pq[tid][1] = q;
                 offmax = fmaxf(offmax, fabsf(apq));
-                dmax = fmaxf(dmax, fmaxf(fabsf(S[p * kSP + p]), fabsf(S[q * kSP + q])));
+                dmax = fmaxf(dmax, fmaxf(fabsf(app), fabsf(aqq)));
             }
             __syncthreads();
-            // rows p, q of S: 32 pairs x 64 columns, 4 element pairs per thread
+            // S: 32 x 32 blocks of 2 x 2, two per thread
+            float z[2][4];
+            int addr[2][4];
 #pragma unroll
-            for (int u = 0; u < (kB * kP) / kSolveThreads; ++u) {
-                const int e = tid + u * kSolveThreads;
-                const int k = e / kP, j = e % kP;
-                const int p = pq[k][0], q = pq[k][1];
-                const float c = cs[k][0], sn = cs[k][1];
-                const float x = S[p * kSP + j], y = S[q * kSP + j];
-                S[p * kSP + j] = c * x - sn * y;
-                S[q * kSP + j] = sn * x + c * y;
+            for (int u = 0; u < 2; ++u) {
+                const int b = tid + u * kSolveThreads;
+                const int ka = b / kB, kb = b % kB;
+                const int pa = pq[ka][0], qa = pq[ka][1], pb = pq[kb][0], qb = pq[kb][1];
+                const float ca = cs[ka][0], sa = cs[ka][1], cb = cs[kb][0], sb = cs[kb][1];
+                addr[u][0] = pa * kSP + pb;
+                addr[u][1] = pa * kSP + qb;
+                addr[u][2] = qa * kSP + pb;
+                addr[u][3] = qa * kSP + qb;
+                const float x11 = S[addr[u][0]], x12 = S[addr[u][1]], x21 = S[addr[u][2]], x22 = S[addr[u][3]];
+                const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
+                const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
+                z[u][0] = cb * y11 - sb * y12;
+                z[u][1] = sb * y11 + cb * y12;
+                z[u][2] = cb * y21 - sb * y22;
+                z[u][3] = sb * y21 + cb * y22;
+                if (ka == kb) z[u][1] = z[u][2] = 0.f;  // the rotated pair is now decoupled
             }
-            __syncthreads();
-            // columns p, q of S and of Q
+            // Q: columns p_b, q_b of 64 rows, four element pairs per thread
+            float qv[4][2];
+            int qa_[4][2];
 #pragma unroll
-            for (int u = 0; u < (kB * kP) / kSolveThreads; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int e = tid + u * kSolveThreads;
-                const int k = e / kP, i = e % kP;
-                const int p = pq[k][0], q = pq[k][1];
-                const float c = cs[k][0], sn = cs[k][1];
-                float x = S[i * kSP + p], y = S[i * kSP + q];
-                S[i * kSP + p] = c * x - sn * y;
-                S[i * kSP + q] = sn * x + c * y;
-                x = Q[i * kSP + p];
-                y = Q[i * kSP + q];
-                Q[i * kSP + p] = c * x - sn * y;
-                Q[i * kSP + q] = sn * x + c * y;
+                const int kb = e / kP, i = e % kP;
+                const int pb = pq[kb][0], qb = pq[kb][1];
+                const float cb = cs[kb][0], sb = cs[kb][1];
+                qa_[u][0] = i * kSP + pb;
+                qa_[u][1] = i * kSP + qb;
+                const float x = Q[qa_[u][0]], y = Q[qa_[u][1]];
+                qv[u][0] = cb * x - sb * y;
+                qv[u][1] = sb * x + cb * y;
+            }
+            __syncthreads();  // every read of this step is done before any write
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) S[addr[u][t]] = z[u][t];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                Q[qa_[u][0]] = qv[u][0];
+                Q[qa_[u][1]] = qv[u][1];
             }
             __syncthreads();
         }
@@ -175,133 +203,142 @@ jacobi_solve_kernel(const JacBatch jb, int inner_sweeps) {
                 dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
             }
             if (tid == 0) {
-                red[0][0] = offmax;
-                red[1][0] = dmax;
+                red[0] = offmax;
+                red[1] = dmax;
             }
         }
         __syncthreads();
-        const bool done = red[0][0] <= 1e-7f * red[1][0];
+        const bool done = red[0] <= 1e-7f * red[1];
         __syncthreads();
         if (done) break;
     }
     float *Rp = jb.R[job] + (size_t)pair * kP * kP;
-    for (int e = tid; e < kP * kP; e += kSolveThreads) Rp[e] = Q[(e / kP) * kSP + (e % kP)];
+    for (int e = tid; e < kP * kP / 4; e += kSolveThreads) {
+        const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
+        *reinterpret_cast<float4 *>(&Rp[i * kP + j4]) =
+            make_float4(Q[i * kSP + j4], Q[i * kSP + j4 + 1], Q[i * kSP + j4 + 2], Q[i * kSP + j4 + 3]);
+    }
 }
 
 // 64 x 64 x 64 product of two shared tiles into registers, 4 x 4 outputs per
-// thread (256 threads): out[i][j] = sum_k L(i,k) Rt(k,j), where L is read
-// either as X[i][k] (left_t = false) or X[k][i] (left_t = true).
-template <bool left_t>
-__device__ __forceinline__ void tile_product(const float *X, const float *Y, int ti, int tj,
-                                             float (&acc)[4][4]) {
+// thread (256 threads): acc[a][b] = sum_k L[k][4 ti + a] * Rt[k][4 tj + b]
+// (both tiles stored k-major with pitch kQ, so each k step is two float4 loads).
+constexpr int kQ = kP + 4;
+__device__ __forceinline__ void tile_product_kt(const float *L, const float *Rt, int ti, int tj,
+                                                float (&acc)[4][4]) {
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll 8
     for (int k = 0; k < kP; ++k) {
-        float l[4], r[4];
-        if (left_t) {
-            const float4 v = *reinterpret_cast<const float4 *>(&X[k * kP + 4 * ti]);
-            l[0] = v.x; l[1] = v.y; l[2] = v.z; l[3] = v.w;
-        } else {
-#pragma unroll
-            for (int a = 0; a < 4; ++a) l[a] = X[(4 * ti + a) * (kP + 4) + k];
-        }
-        const float4 w = *reinterpret_cast<const float4 *>(&Y[k * kP + 4 * tj]);
-        r[0] = w.x; r[1] = w.y; r[2] = w.z; r[3] = w.w;
+        const float4 l = *reinterpret_cast<const float4 *>(&L[k * kQ + 4 * ti]);
+        const float4 r = *reinterpret_cast<const float4 *>(&Rt[k * kQ + 4 * tj]);
+        const float lv[4] = {l.x, l.y, l.z, l.w}, rv[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(l[a], r[b], acc[a][b]);
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(lv[a], rv[b], acc[a][b]);
     }
 }
 
-// Rows pass (A <- R_p^T A on the rows of each pair, 64-column chunks) and the
-// accumulation Q <- Q R_p (64-row chunks): both read what the previous round
-// left and touch disjoint elements.
+// load a 64 x 64 fp32 tile (row-major, pitch 64) into shared memory with pitch kQ
+__device__ __forceinline__ void load_tile64(float *dst, const float *src, int tid) {
+    for (int e = tid; e < kP * kP / 4; e += 256) {
+        const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
+        *reinterpret_cast<float4 *>(&dst[i * kQ + j4]) = *reinterpret_cast<const float4 *>(&src[i * kP + j4]);
+    }
+}
+
+// One round's rotations, applied in one pass:
+//  * A tiles (p1 <= p2): A'[p1,p2] = R1^T A[p1,p2] R2, also written transposed
+//    into [p2,p1] (A stays symmetric, so only the upper triangle is computed);
+//  * Q slabs (64 rows x pair p): Q' = Q R_p.
+// Every item reads only what the previous round left and writes disjoint elements.
 __global__ void __launch_bounds__(256)
-jacobi_rows_kernel(const JacBatch jb) {
-    __shared__ __align__(16) float Rs[kP * kP];
-    __shared__ __align__(16) float Xs[kP * (kP + 4)];
-    const int item = blockIdx.x;
+jacobi_apply_kernel(const JacBatch jb) {
+    __shared__ __align__(16) float T0[kP * kQ];
+    __shared__ __align__(16) float T1[kP * kQ];
+    __shared__ __align__(16) float T2[kP * kQ];
     const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
-    const int total_rows = jb.row_off[jb.count];
-    if (item < total_rows) {
+    const int total_a = jb.row_off[jb.count];
+    int item = blockIdx.x;
+    if (item < total_a) {
         const int job = find_job(jb.row_off, jb.count, item);
         if (!jb.active[job]) return;
-        const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], chunks = Np / kP;
-        const int local = item - jb.row_off[job];
-        const int pair = local / chunks, c0 = (local % chunks) * kP;
+        const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
+        int local = item - jb.row_off[job];
+        // local -> (p1, p2) with p1 <= p2, row by row of the upper triangle
+        int p1 = 0;
+        while (local >= np - p1) {
+            local -= np - p1;
+            ++p1;
+        }
+        const int p2 = p1 + local;
         float *A = jb.A[job];
-        const float *R = jb.R[job] + (size_t)pair * kP * kP;
-        for (int e = tid; e < kP * kP; e += 256) {
-            Rs[e] = R[e];
-            const int l = e / kP, j = e % kP;
-            Xs[l * kP + j] = A[(size_t)pair_index(nb, round, pair, l) * Np + c0 + j];
+        const float *R1 = jb.R[job] + (size_t)p1 * kP * kP;
+        const float *R2 = jb.R[job] + (size_t)p2 * kP * kP;
+        load_tile64(T0, R1, tid);  // T0[k][i] = R1[k][i]
+        // T1[k][j] = A[g1(k)][g2(j)] (rows of pair p1, columns of pair p2)
+        for (int e = tid; e < kP * kP / 4; e += 256) {
+            const int k = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
+            *reinterpret_cast<float4 *>(&T1[k * kQ + j4]) = *reinterpret_cast<const float4 *>(
+                &A[(size_t)pair_index(nb, round, p1, k) * Np + pair_index(nb, round, p2, j4)]);
         }
         __syncthreads();
         float acc[4][4];
-        tile_product<true>(Rs, Xs, ti, tj, acc);  // (R^T X)[i][j] = sum_k R[k][i] X[k][j]
+        tile_product_kt(T0, T1, ti, tj, acc);  // Y = R1^T X  (Y[i][j])
+        __syncthreads();
+        // store Y transposed: T1[j][i] = Y[i][j]  (so the next product is k-major in j)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) T1[(4 * tj + b) * kQ + 4 * ti + a] = acc[a][b];
+        load_tile64(T2, R2, tid);  // T2[k][j] = R2[k][j]
+        __syncthreads();
+        // Z[i][j] = sum_k Y[i][k] R2[k][j] = sum_k T1[k][i] T2[k][j]
+        tile_product_kt(T1, T2, ti, tj, acc);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int gi = pair_index(nb, round, pair, 4 * ti + a);
-            *reinterpret_cast<float4 *>(&A[(size_t)gi * Np + c0 + 4 * tj]) =
+            const int gi = pair_index(nb, round, p1, 4 * ti + a);
+            *reinterpret_cast<float4 *>(&A[(size_t)gi * Np + pair_index(nb, round, p2, 4 * tj)]) =
                 make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
+        if (p1 != p2) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int gj = pair_index(nb, round, p2, 4 * tj + b);
+                *reinterpret_cast<float4 *>(&A[(size_t)gj * Np + pair_index(nb, round, p1, 4 * ti)]) =
+                    make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
+            }
         }
         return;
     }
-    // Q items
-    const int qitem = item - total_rows;
-    const int job = find_job(jb.q_off, jb.count, qitem);
+    // Q slabs
+    item -= total_a;
+    const int job = find_job(jb.q_off, jb.count, item);
     if (!jb.active[job]) return;
-    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], pairs = Np / kP;
-    const int local = qitem - jb.q_off[job];
-    const int r0 = (local / pairs) * kP, pair = local % pairs;
+    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
+    const int local = item - jb.q_off[job];
+    const int r0 = (local / np) * kP, pair = local % np;
     float *Qm = jb.Q[job];
-    const float *R = jb.R[job] + (size_t)pair * kP * kP;
-    for (int e = tid; e < kP * kP; e += 256) {
-        Rs[e] = R[e];
-        const int rr = e / kP, l = e % kP;
-        Xs[rr * (kP + 4) + l] = Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l)];
+    load_tile64(T2, jb.R[job] + (size_t)pair * kP * kP, tid);
+    // T1[l][rr] = Q[r0 + rr][g(l)]  (transposed so the product is k-major in rr)
+    for (int e = tid; e < kP * kP / 4; e += 256) {
+        const int rr = e % kP, l4 = (e / kP) * 4;
+        const float4 v = *reinterpret_cast<const float4 *>(&Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l4)]);
+        T1[(l4 + 0) * kQ + rr] = v.x;
+        T1[(l4 + 1) * kQ + rr] = v.y;
+        T1[(l4 + 2) * kQ + rr] = v.z;
+        T1[(l4 + 3) * kQ + rr] = v.w;
     }
     __syncthreads();
     float acc[4][4];
-    tile_product<false>(Xs, Rs, ti, tj, acc);  // (X R)[i][j]
+    tile_product_kt(T1, T2, ti, tj, acc);  // (Q R)[rr][j]
 #pragma unroll
     for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            Qm[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj + b)] = acc[a][b];
-}
-
-// Columns pass: A <- A R_p on the columns of each pair, 64-row chunks.
-__global__ void __launch_bounds__(256)
-jacobi_cols_kernel(const JacBatch jb) {
-    __shared__ __align__(16) float Rs[kP * kP];
-    __shared__ __align__(16) float Xs[kP * (kP + 4)];
-    const int item = blockIdx.x;
-    const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
-    const int job = find_job(jb.col_off, jb.count, item);
-    if (!jb.active[job]) return;
-    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], pairs = Np / kP;
-    const int local = item - jb.col_off[job];
-    const int r0 = (local / pairs) * kP, pair = local % pairs;
-    float *A = jb.A[job];
-    const float *R = jb.R[job] + (size_t)pair * kP * kP;
-    for (int e = tid; e < kP * kP; e += 256) {
-        Rs[e] = R[e];
-        const int rr = e / kP, l = e % kP;
-        Xs[rr * (kP + 4) + l] = A[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l)];
-    }
-    __syncthreads();
-    float acc[4][4];
-    tile_product<false>(Xs, Rs, ti, tj, acc);
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            A[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj + b)] = acc[a][b];
+        *reinterpret_cast<float4 *>(&Qm[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj)]) =
+            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -548,25 +585,24 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         jb.R[i] = b[i].R;
         jb.Np[i] = b[i].Np;
         jb.active[i] = 1;
-        const int pairs = b[i].Np / kP, chunks = b[i].Np / kP;
+        const int pairs = b[i].Np / kP;
         jb.pair_off[i + 1] = jb.pair_off[i] + pairs;
-        jb.row_off[i + 1] = jb.row_off[i] + pairs * chunks;
-        jb.q_off[i + 1] = jb.q_off[i] + chunks * pairs;
-        jb.col_off[i + 1] = jb.col_off[i] + chunks * pairs;
+        jb.row_off[i + 1] = jb.row_off[i] + pairs * (pairs + 1) / 2;  // A tiles p1 <= p2
+        jb.q_off[i + 1] = jb.q_off[i] + pairs * pairs;                // Q slabs
         max_sweeps = std::max(max_sweeps, jobs[i].max_sweeps);
         rounds = std::max(rounds, b[i].nb - 1);
     }
     const int solve_grid = jb.pair_off[count];
-    const int rows_grid = jb.row_off[count] + jb.q_off[count];
-    const int cols_grid = jb.col_off[count];
+    const int apply_grid = jb.row_off[count] + jb.q_off[count];
+    int inner = 1;
+    for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
     std::vector<double> host(2 * count);
     int active = count;
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int g = 0; g < rounds; ++g) {
             for (int i = 0; i < count; ++i) jb.round[i] = g % (b[i].nb - 1);
-            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, 0, st>>>(jb, 2));
-            SPCO_LAUNCH("svd_jacobi_rows", st, jacobi_rows_kernel<<<rows_grid, 256, 0, st>>>(jb));
-            SPCO_LAUNCH("svd_jacobi_cols", st, jacobi_cols_kernel<<<cols_grid, 256, 0, st>>>(jb));
+            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, 0, st>>>(jb, inner));
+            SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(jb));
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {

@@ -14,6 +14,7 @@ struct SvdJob {
     const float *warm;     // previous short-side factor (r x r) to start from, or null
     float tau, tol;
     int max_sweeps;
+    int inner_sweeps;      // Jacobi sweeps per 64 x 64 subproblem and round
     int sweeps;            // out: Jacobi sweeps run
     int status;            // out: SPECOPTIM_OK or SPECOPTIM_ERR_NOT_CONVERGED
 };
