@@ -139,26 +139,6 @@ __device__ __forceinline__ float4 ld4_stream(const float *p) {
 }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 
-__device__ __forceinline__ void adamw4(const Epilogue &e, float *W, float *M1, float *M2,
-                                       const float *G, float *Gf, float *Gp, const float *acc) {
-    const float4 g = ld4_stream(G);
-    float4 w = ld4(W), m = ld4(M1), v = ld4(M2);
-    float gv[4] = {g.x, g.y, g.z, g.w}, wv[4] = {w.x, w.y, w.z, w.w};
-    float mv[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w}, pv[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        pv[q] = e.alpha * gv[q] + (1.f - e.alpha) * acc[q];
-        mv[q] = e.beta1 * mv[q] + (1.f - e.beta1) * pv[q];
-        vv[q] = e.beta2 * vv[q] + (1.f - e.beta2) * pv[q] * pv[q];
-        wv[q] = wv[q] * e.decay - e.step_size * mv[q] / (sqrtf(vv[q]) * e.inv_sqrt_bc2 + e.eps);
-    }
-    st4(W, make_float4(wv[0], wv[1], wv[2], wv[3]));
-    st4(M1, make_float4(mv[0], mv[1], mv[2], mv[3]));
-    st4(M2, make_float4(vv[0], vv[1], vv[2], vv[3]));
-    if (Gf) st4(Gf, make_float4(acc[0], acc[1], acc[2], acc[3]));
-    if (Gp) st4(Gp, make_float4(pv[0], pv[1], pv[2], pv[3]));
-}
-
 // Coalesced epilogue of a 32 x 32 accumulator block.  The block arrives from
 // tcgen05.ld as "thread = row, registers = 32 columns"; it is transposed
 // through a padded shared tile so that each warp instruction then touches four
@@ -175,20 +155,56 @@ __device__ __forceinline__ void epilogue_block(const Epilogue &e, float *tile, i
     const bool vec = (col + 4 <= N) &&
                      (((e.mode == EPI_ADAMW) ? e.ld : e.ldc) & 3) == 0;
     if (e.mode == EPI_ADAMW) {
-#pragma unroll 4
-        for (int g = 0; g < 8; ++g) {
-            const int i = g * 4 + sub;
-            const int64_t row = row0 + i;
-            if (row >= M) continue;
-            const float a[4] = {tile[i * TPITCH + cq], tile[i * TPITCH + cq + 1],
-                                tile[i * TPITCH + cq + 2], tile[i * TPITCH + cq + 3]};
-            if (vec) {
-                const int64_t o = row * e.ld + col;
-                adamw4(e, e.W + o, e.m1 + o, e.m2 + o, e.G + o, e.Gf_out ? e.Gf_out + o : nullptr,
-                       e.Gp_out ? e.Gp_out + o : nullptr, a);
-            } else {
+        if (vec) {
+            // four row groups at a time: every load is issued before any store, so
+            // 16 independent 16-byte loads per thread are in flight
+#pragma unroll
+            for (int gb = 0; gb < 8; gb += 4) {
+                float4 g4[4], w4[4], m4[4], v4[4];
+                int64_t off[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t row = row0 + (gb + u) * 4 + sub;
+                    off[u] = row < M ? row * e.ld + col : -1;
+                    if (off[u] >= 0) {
+                        g4[u] = ld4_stream(e.G + off[u]);
+                        w4[u] = ld4(e.W + off[u]);
+                        m4[u] = ld4(e.m1 + off[u]);
+                        v4[u] = ld4(e.m2 + off[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (off[u] < 0) continue;
+                    const int i = (gb + u) * 4 + sub;
+                    const float a[4] = {tile[i * TPITCH + cq], tile[i * TPITCH + cq + 1],
+                                        tile[i * TPITCH + cq + 2], tile[i * TPITCH + cq + 3]};
+                    const float gv[4] = {g4[u].x, g4[u].y, g4[u].z, g4[u].w};
+                    float wv[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
+                    float mv[4] = {m4[u].x, m4[u].y, m4[u].z, m4[u].w};
+                    float vv[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w}, pv[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        pv[t] = e.alpha * gv[t] + (1.f - e.alpha) * a[t];
+                        mv[t] = e.beta1 * mv[t] + (1.f - e.beta1) * pv[t];
+                        vv[t] = e.beta2 * vv[t] + (1.f - e.beta2) * pv[t] * pv[t];
+                        wv[t] = wv[t] * e.decay - e.step_size * mv[t] / (sqrtf(vv[t]) * e.inv_sqrt_bc2 + e.eps);
+                    }
+                    const int64_t o = off[u];
+                    st4(e.W + o, make_float4(wv[0], wv[1], wv[2], wv[3]));
+                    st4(e.m1 + o, make_float4(mv[0], mv[1], mv[2], mv[3]));
+                    st4(e.m2 + o, make_float4(vv[0], vv[1], vv[2], vv[3]));
+                    if (e.Gf_out) st4(e.Gf_out + o, make_float4(a[0], a[1], a[2], a[3]));
+                    if (e.Gp_out) st4(e.Gp_out + o, make_float4(pv[0], pv[1], pv[2], pv[3]));
+                }
+            }
+        } else {
+            for (int g = 0; g < 8; ++g) {
+                const int i = g * 4 + sub;
+                const int64_t row = row0 + i;
+                if (row >= M) continue;
                 for (int t = 0; t < 4; ++t)
-                    if (col + t < N) epilogue_apply(e, row, col + t, a[t]);
+                    if (col + t < N) epilogue_apply(e, row, col + t, tile[i * TPITCH + cq + t]);
             }
         }
     } else {
@@ -264,7 +280,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+            const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;  // N fastest: the A slab stays hot in L2
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
@@ -306,7 +322,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int half = (warp - 2) / 4; // column half of the 256-wide tile
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-            const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+            const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;  // N fastest: the A slab stays hot in L2
             const uint32_t acc = local & 1u;
             const uint32_t aph = (local >> 1) & 1u;
             if (!mbar_wait_bounded(&tfull[acc], aph, flag, 0x104u)) break;
@@ -397,7 +413,10 @@ int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogu
     }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)std::min<int64_t>(tiles, num_sms());
-    SPCO_LAUNCH("gemm_tf32", stream, gemm_tf32_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, (int)M, (int)N, (int)K, epi,
+    const char *name = epi.mode == EPI_ADAMW ? "gemm_tf32_adamw"
+                       : epi.mode == EPI_SCALE ? "gemm_tf32_scale"
+                                               : "gemm_tf32";
+    SPCO_LAUNCH(name, stream, gemm_tf32_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, (int)M, (int)N, (int)K, epi,
                                                              device_flag_ptr()));
     SPECOPTIM_LAUNCHED("gemm_tf32_kernel");
     return SPECOPTIM_OK;

@@ -131,7 +131,7 @@ __host__ __device__ inline RingLayout ring_layout(size_t in_bytes, size_t out_by
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nchunks, int H,
                  int K, uint64_t seed, int stages, unsigned *flag) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -187,7 +187,7 @@ pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nc
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t nchunks, int H,
                    int K, uint64_t seed, int stages, unsigned *flag) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -307,11 +307,20 @@ int row_grid(int64_t rows) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * 16));
 }
 
-// input-ring stages that fit the shared-memory budget (0 = the bulk path does not fit)
-int pick_stages(size_t in_bytes, size_t out_bytes) {
+// Ring configuration: two CTAs per SM (16 warps to hide the hash latency) when
+// a ring of at least 3 input stages fits in half the shared memory, else one
+// CTA per SM with as many stages as fit; stages = 0 means the bulk path does
+// not fit at all.
+struct RingPlan {
+    int stages, ctas_per_sm;
+};
+
+RingPlan pick_ring(size_t in_bytes, size_t out_bytes) {
+    for (int st = kMaxStages; st >= 3; --st)
+        if (ring_layout(in_bytes, out_bytes, st).total <= kSmemBudget / 2 - 1024) return {st, 2};
     for (int st = kMaxStages; st >= 1; --st)
-        if (ring_layout(in_bytes, out_bytes, st).total <= kSmemBudget) return st;
-    return 0;
+        if (ring_layout(in_bytes, out_bytes, st).total <= kSmemBudget) return {st, 1};
+    return {0, 1};
 }
 
 template <typename T>
@@ -320,7 +329,8 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
     const T *d = static_cast<const T *>(dense);
     T *p = static_cast<T *>(packed);
     const size_t in_b = (size_t)CH * H * sizeof(T), out_b = (size_t)CH * K * sizeof(T);
-    int stages = pick_stages(in_b, out_b);
+    const RingPlan plan = pick_ring(in_b, out_b);
+    const int stages = plan.stages;
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
         size_t smem = ring_layout(in_b, out_b, stages).total;
@@ -331,7 +341,7 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
                                                 (int)kSmemBudget));
             attr = true;
         }
-        int grid = (int)std::min<int64_t>(nfull, num_sms());
+        int grid = (int)std::min<int64_t>(nfull, (int64_t)num_sms() * plan.ctas_per_sm);
         SPCO_LAUNCH("mask_pack_bulk", st, pack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(d, p, nfull, H, K, seed, stages,
                                                           device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_pack bulk kernel");
@@ -350,7 +360,8 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
     const T *p = static_cast<const T *>(packed);
     T *d = static_cast<T *>(dense);
     const size_t in_b = (size_t)CH * K * sizeof(T), out_b = (size_t)CH * H * sizeof(T);
-    int stages = pick_stages(in_b, out_b);
+    const RingPlan plan = pick_ring(in_b, out_b);
+    const int stages = plan.stages;
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
         size_t smem = ring_layout(in_b, out_b, stages).total;
@@ -361,7 +372,7 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
                                                 (int)kSmemBudget));
             attr = true;
         }
-        int grid = (int)std::min<int64_t>(nfull, num_sms());
+        int grid = (int)std::min<int64_t>(nfull, (int64_t)num_sms() * plan.ctas_per_sm);
         SPCO_LAUNCH("mask_unpack_bulk", st, unpack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(p, d, nfull, H, K, seed, stages,
                                                             device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_unpack bulk kernel");
