@@ -175,8 +175,8 @@ class Layer:
         self.so.svd_refresh_many([self.opt[name] for name in self.names])
 
     def spectral(self, i: int, G=None):
-        for name in self.names:
-            self.opt[name].step(self.W[name], G[name] if G else self.Gpool[name][i % POOL], self.lr)
+        self.so.step_many([self.opt[n] for n in self.names], [self.W[n] for n in self.names],
+                          [G[n] if G else self.Gpool[n][i % POOL] for n in self.names], self.lr)
 
     def mask_round_trip(self, i: int, h=None, g=None):
         so, layer = self.so, i % MASK_BOUNDARIES

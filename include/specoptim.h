@@ -123,6 +123,15 @@ int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void 
 int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr, void *stream,
                    float *G_filt_out, float *G_proj_out);
 
+/* The same step for 1 to 16 handles at once (e.g. the 7 weights of one
+ * decoder layer), all with learning rate lr: W[i] and G_mask[i] (host arrays
+ * of device pointers) belong to handles[i].  Each of the four products runs
+ * for all handles in one persistent tensor-core launch (largest problems
+ * first), so small matrices fill the SMs the large ones leave idle.  Same
+ * results as calling specoptim_step on each handle (without debug outputs). */
+int specoptim_step_many(specoptim_t *const *handles, int32_t count, float *const *W,
+                        const float *const *G_mask, float lr, void *stream);
+
 /* Copies the current factors to caller device buffers (any may be NULL):
  * U m x r, s r, V n x r, d r (row-major fp32). */
 int specoptim_get_factors(const specoptim_t *h, float *U, float *s, float *V, float *d,

@@ -53,6 +53,7 @@ SIGNATURES = [
     ("specoptim_svd_refresh", _int, [_vp, _vp, ctypes.POINTER(_i32)]),
     ("specoptim_svd_refresh_many", _int, [ctypes.POINTER(_vp), _i32, _vp, ctypes.POINTER(_i32)]),
     ("specoptim_step", _int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp]),
+    ("specoptim_step_many", _int, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _f32, _vp]),
     ("specoptim_get_factors", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     ("specoptim_get_state", _int, [_vp, _vp, _vp, _vp, ctypes.POINTER(_i64), _vp]),
     ("specoptim_set_state", _int, [_vp, _vp, _vp, _vp, _i64, _vp]),
@@ -206,6 +207,17 @@ def svd_refresh_many(optimizers, stream=None):
     sweeps = (ctypes.c_int32 * n)()
     _check(lib().specoptim_svd_refresh_many(arr, n, _stream(stream), sweeps), "specoptim_svd_refresh_many")
     return list(sweeps)
+
+
+def step_many(optimizers, Ws, Gs, lr: float, stream=None):
+    """One spectral-corrected step of several handles (at most 16) in shared launches."""
+    n = len(optimizers)
+    if len(Ws) != n or len(Gs) != n:
+        raise ValueError("step_many: one W and one G_mask per optimizer")
+    hs = (ctypes.c_void_p * n)(*[o._h.value for o in optimizers])
+    wp = (ctypes.c_void_p * n)(*[_f32_2d(w, (o.m, o.n), "W") for o, w in zip(optimizers, Ws)])
+    gp = (ctypes.c_void_p * n)(*[_f32_2d(g, (o.m, o.n), "G_mask") for o, g in zip(optimizers, Gs)])
+    _check(lib().specoptim_step_many(hs, n, wp, gp, float(lr), _stream(stream)), "specoptim_step_many")
 
 
 def adamw(W, g, exp_avg, exp_avg_sq, t: int, lr: float, beta1=0.9, beta2=0.999, eps=1e-8,

@@ -74,6 +74,20 @@ __device__ __forceinline__ void epilogue_apply(const Epilogue &e, int64_t i, int
     e.C[i * e.ldc + j] = c;
 }
 
+// One product of a grouped launch: C = op(A) op(B) with its own epilogue.
+struct GemmProblem {
+    int64_t M, N, K;
+    Operand A, B;
+    Epilogue epi;
+};
+
+// tcgen05 TF32 path (C = A B^T, both K-contiguous, 16-byte rows): one product,
+// or up to 8 independent products sharing one persistent launch.
+bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, Operand A, Operand B);
+int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
+            cudaStream_t stream);
+int gemm_tc_group(int count, const GemmProblem *probs, cudaStream_t stream);
+
 // fp32 SIMT GEMM (any shape, any transposition, any alignment)
 int gemm_simt(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
               cudaStream_t stream);

@@ -24,6 +24,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "gemm.cuh"
@@ -39,6 +40,7 @@ constexpr uint32_t A_BYTES = BM * BK * 4;
 constexpr uint32_t B_BYTES = BN * BK * 4;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int kMaxGroup = 8;
 constexpr int TPITCH = 33;  // padded row of an epilogue transpose tile (conflict-free both ways)
 constexpr size_t TILE_BYTES = (size_t)EPI_WARPS * 32 * TPITCH * 4;
 constexpr size_t SMEM_BYTES =
@@ -235,9 +237,29 @@ __device__ __forceinline__ void epilogue_block(const Epilogue &e, float *tile, i
 
 // ---- the kernel ----------------------------------------------------------------
 
+// Up to kMaxGroup independent products in one persistent launch.  Tiles are
+// numbered problem by problem (N fastest inside a problem); every role walks
+// the same sequence, so each CTA knows which problem a tile belongs to.
+struct GemmGroup {
+    CUtensorMap tmA[kMaxGroup];
+    CUtensorMap tmB[kMaxGroup];
+    Epilogue epi[kMaxGroup];
+    int M[kMaxGroup], N[kMaxGroup], K[kMaxGroup];
+    int tiles_n[kMaxGroup];
+    int tile_off[kMaxGroup + 1];
+    int count;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmGroup &g, int tile, int &p, int &m0, int &n0) {
+    p = 0;
+    while (p + 1 < g.count && tile >= g.tile_off[p + 1]) ++p;
+    const int local = tile - g.tile_off[p];
+    n0 = (local % g.tiles_n[p]) * BN;  // N fastest: the A slab stays hot in L2
+    m0 = (local / g.tiles_n[p]) * BM;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 int M, int N, int K, Epilogue epi, unsigned *flag) {
+gemm_tf32_kernel(const __grid_constant__ GemmGroup grp, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -249,9 +271,7 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int num_tiles = tiles_m * tiles_n;
-    const int num_kb = (K + BK - 1) / BK;
+    const int num_tiles = grp.tile_off[grp.count];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -263,8 +283,10 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(&tempty[a], EPI_WARPS * 32);
         }
         fence_mbar_init();
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
+        for (int p = 0; p < grp.count; ++p) {
+            prefetch_tmap(&grp.tmA[p]);
+            prefetch_tmap(&grp.tmB[p]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -280,15 +302,17 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;  // N fastest: the A slab stays hot in L2
+            int p, m0, n0;
+            tile_coords(grp, tile, p, m0, n0);
+            const int num_kb = (grp.K[p] + BK - 1) / BK;
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait_bounded(&empty[s], ph ^ 1u, flag, 0x101u)) { ok = false; break; }
                 unsigned char *sa = smem + s * STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                tma_load_2d(sa, &tmA, kb * BK, m0, &full[s]);
-                tma_load_2d(sa + A_BYTES, &tmB, kb * BK, n0, &full[s]);
+                tma_load_2d(sa, &grp.tmA[p], kb * BK, m0, &full[s]);
+                tma_load_2d(sa + A_BYTES, &grp.tmB[p], kb * BK, n0, &full[s]);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -301,6 +325,9 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!mbar_wait_bounded(&tempty[acc], aph ^ 1u, flag, 0x102u)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
+            int p, m0, n0;
+            tile_coords(grp, tile, p, m0, n0);
+            const int num_kb = (grp.K[p] + BK - 1) / BK;
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
@@ -322,7 +349,8 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int half = (warp - 2) / 4; // column half of the 256-wide tile
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-            const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;  // N fastest: the A slab stays hot in L2
+            int p, m0, n0;
+            tile_coords(grp, tile, p, m0, n0);
             const uint32_t acc = local & 1u;
             const uint32_t aph = (local >> 1) & 1u;
             if (!mbar_wait_bounded(&tfull[acc], aph, flag, 0x104u)) break;
@@ -332,7 +360,8 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int col = half * (BN / 2) + c * 32;
                 float v[32];
                 tmem_ld32(tmem_base + acc * BN + col + ((uint32_t)(q * 32) << 16), v);
-                epilogue_block(epi, tbuf_w, lane, (int64_t)m0 + q * 32, (int64_t)n0 + col, M, N, v);
+                epilogue_block(grp.epi[p], tbuf_w, lane, (int64_t)m0 + q * 32, (int64_t)n0 + col, grp.M[p],
+                               grp.N[p], v);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -396,14 +425,27 @@ bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, Operand A, Operand B) {
     return encode_fn() != nullptr;
 }
 
-int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
-            cudaStream_t stream) {
-    if (!gemm_tc_supported(M, N, K, A, B))
-        return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_tc: operand layout not supported");
-    CUtensorMap ta, tb;
-    int rc = make_tmap(&ta, A.ptr, M, K, A.ld, BM);
-    if (rc) return rc;
-    if ((rc = make_tmap(&tb, B.ptr, N, K, B.ld, BN))) return rc;
+int gemm_tc_group(int count, const GemmProblem *probs, cudaStream_t stream) {
+    if (count < 1 || count > kMaxGroup) return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_tc: 1 to 8 problems");
+    GemmGroup g;
+    std::memset(&g, 0, sizeof(g));
+    g.count = count;
+    int mode_mask = 0;
+    for (int p = 0; p < count; ++p) {
+        const GemmProblem &q = probs[p];
+        if (!gemm_tc_supported(q.M, q.N, q.K, q.A, q.B))
+            return fail(SPECOPTIM_ERR_INVALID_ARG, "gemm_tc: operand layout not supported");
+        int rc = make_tmap(&g.tmA[p], q.A.ptr, q.M, q.K, q.A.ld, BM);
+        if (rc) return rc;
+        if ((rc = make_tmap(&g.tmB[p], q.B.ptr, q.N, q.K, q.B.ld, BN))) return rc;
+        g.epi[p] = q.epi;
+        g.M[p] = (int)q.M;
+        g.N[p] = (int)q.N;
+        g.K[p] = (int)q.K;
+        g.tiles_n[p] = (int)((q.N + BN - 1) / BN);
+        g.tile_off[p + 1] = g.tile_off[p] + g.tiles_n[p] * (int)((q.M + BM - 1) / BM);
+        mode_mask |= 1 << q.epi.mode;
+    }
     static bool attr = false;
     if (!attr) {
         SPECOPTIM_CUDA(cudaFuncSetAttribute(gemm_tf32_kernel,
@@ -411,15 +453,19 @@ int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogu
                                             (int)SMEM_BYTES));
         attr = true;
     }
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = (int)std::min<int64_t>(tiles, num_sms());
-    const char *name = epi.mode == EPI_ADAMW ? "gemm_tf32_adamw"
-                       : epi.mode == EPI_SCALE ? "gemm_tf32_scale"
-                                               : "gemm_tf32";
-    SPCO_LAUNCH(name, stream, gemm_tf32_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, (int)M, (int)N, (int)K, epi,
-                                                             device_flag_ptr()));
+    const int grid = std::min(g.tile_off[count], num_sms());
+    const char *name = (mode_mask & (1 << EPI_ADAMW)) ? "gemm_tf32_adamw"
+                       : (mode_mask & (1 << EPI_SCALE)) ? "gemm_tf32_scale"
+                                                        : "gemm_tf32";
+    SPCO_LAUNCH(name, stream, gemm_tf32_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(g, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("gemm_tf32_kernel");
     return SPECOPTIM_OK;
+}
+
+int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
+            cudaStream_t stream) {
+    GemmProblem q{M, N, K, A, B, epi};
+    return gemm_tc_group(1, &q, stream);
 }
 
 }  // namespace spco

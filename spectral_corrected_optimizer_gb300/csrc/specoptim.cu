@@ -17,6 +17,7 @@
 //       Gf  = Y V^T          (m x n, K = r)      blend + AdamW in the epilogue
 // Both orders cost 4 r^2 max(m,n) + 4 r^3 flops, the cheaper of the two
 // associations of U^T G V and U X V^T for their shape.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -77,15 +78,6 @@ int transpose_run(const float *src, float *dst, int rows, int cols, bool round, 
 int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
             cudaStream_t stream);
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, Operand A, Operand B);
-
-// C = A . B^T with A (M x K) and B (N x K) both K-contiguous
-static int gemm_nt(const specoptim_t *h, int64_t M, int64_t N, int64_t K, const float *A,
-                   int64_t lda, const float *B, int64_t ldb, const Epilogue &e, cudaStream_t st) {
-    Operand a{A, lda, false}, b{B, ldb, true};
-    if (h->cfg.precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(M, N, K, a, b))
-        return gemm_tc(M, N, K, a, b, e, st);
-    return gemm_simt(M, N, K, a, b, e, st);
-}
 
 }  // namespace spco
 
@@ -256,22 +248,46 @@ extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *swee
     return specoptim_svd_refresh_many(&h, 1, stream, sweeps_out);
 }
 
-extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr,
-                              void *stream, float *G_filt_out, float *G_proj_out) {
-    clear_error();
+namespace {
+
+// The four products of one handle's step, in the order they must run, with
+// their epilogues; `transpose` is set when G^T must be formed first (m > n).
+struct StepPlan {
+    GemmProblem stage[4];
+    bool transpose;
+    const float *G;
+    float *GT;
+    int m, n;
+    bool round;
+};
+
+int check_step_args(const specoptim_t *h, const float *W, const float *G_mask, float lr,
+                    const float *G_filt_out, const float *G_proj_out) {
     if (!h || !W || !G_mask) return fail(SPECOPTIM_ERR_INVALID_ARG, "step: null argument");
     if (!aligned16(W) || !aligned16(G_mask) || (G_filt_out && !aligned16(G_filt_out)) ||
         (G_proj_out && !aligned16(G_proj_out)))
         return fail(SPECOPTIM_ERR_MISALIGNED, "step: pointers must be 16-byte aligned");
     if (!std::isfinite(lr)) return fail(SPECOPTIM_ERR_INVALID_ARG, "step: lr is not finite");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return SPECOPTIM_OK;
+}
+
+// Advances the step counter and fills the plan (C = A . B^T problems, every
+// operand K-contiguous).
+StepPlan plan_step(specoptim_t *h, float *W, const float *G_mask, float lr, float *G_filt_out,
+                   float *G_proj_out) {
     const int64_t m = h->m, n = h->n, r = h->r;
-    const bool round = h->cfg.precision == SPECOPTIM_PREC_TF32;
+    StepPlan P;
+    P.round = h->cfg.precision == SPECOPTIM_PREC_TF32;
+    P.G = G_mask;
+    P.GT = h->ws_g;
+    P.m = h->m;
+    P.n = h->n;
+    P.transpose = h->tall;
     h->t += 1;
-    AdamWScalars sc = adamw_scalars(h->t, lr, h->cfg.beta1, h->cfg.beta2, h->cfg.eps,
-                                    h->cfg.weight_decay);
+    const AdamWScalars sc = adamw_scalars(h->t, lr, h->cfg.beta1, h->cfg.beta2, h->cfg.eps,
+                                          h->cfg.weight_decay);
     Epilogue plain;
-    plain.round_tf32 = round;
+    plain.round_tf32 = P.round;
     Epilogue scaled = plain;
     scaled.mode = EPI_SCALE;
     scaled.row_scale = h->d;
@@ -292,32 +308,102 @@ extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, flo
     last.decay = sc.decay;
     last.step_size = sc.step_size;
     last.inv_sqrt_bc2 = sc.inv_sqrt_bc2;
-    int rc;
+    auto nt = [](int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                 int64_t ldb, const Epilogue &e) {
+        return GemmProblem{M, N, K, Operand{A, lda, false}, Operand{B, ldb, true}, e};
+    };
     if (h->tall) {
-        float *GT = h->ws_g, *T1 = h->ws_a, *Xf = h->ws_x, *ZT = h->ws_a;
-        if ((rc = transpose_run(G_mask, GT, (int)m, (int)n, round, st))) return rc;
+        float *T1 = h->ws_a, *Xf = h->ws_x, *ZT = h->ws_a;
         plain.C = T1;
         plain.ldc = n;
-        if ((rc = gemm_nt(h, r, n, m, h->UTo, m, GT, m, plain, st))) return rc;
+        P.stage[0] = nt(r, n, m, h->UTo, m, P.GT, m, plain);      // T1  = U^T G
         scaled.C = Xf;
         scaled.ldc = r;
-        if ((rc = gemm_nt(h, r, r, n, T1, n, h->VTo, n, scaled, st))) return rc;
+        P.stage[1] = nt(r, r, n, T1, n, h->VTo, n, scaled);       // Xf  = (T1 V) o dd^T
         plain.C = ZT;
         plain.ldc = r;
-        if ((rc = gemm_nt(h, n, r, r, h->Vo, r, Xf, r, plain, st))) return rc;
-        return gemm_nt(h, m, n, r, h->Uo, r, ZT, r, last, st);
+        P.stage[2] = nt(n, r, r, h->Vo, r, Xf, r, plain);         // Z^T = V Xf^T
+        P.stage[3] = nt(m, n, r, h->Uo, r, ZT, r, last);          // G_filt = U Z -> AdamW
+    } else {
+        float *TT = h->ws_a, *XfT = h->ws_x, *Y = h->ws_a;
+        plain.C = TT;
+        plain.ldc = m;
+        P.stage[0] = nt(r, m, n, h->VTo, n, G_mask, n, plain);    // T^T = V^T G^T
+        scaled.C = XfT;
+        scaled.ldc = r;
+        P.stage[1] = nt(r, r, m, TT, m, h->UTo, m, scaled);       // Xf^T = (T^T U) o dd^T
+        plain.C = Y;
+        plain.ldc = r;
+        P.stage[2] = nt(m, r, r, h->Uo, r, XfT, r, plain);        // Y = U Xf
+        P.stage[3] = nt(m, n, r, Y, r, h->Vo, r, last);           // G_filt = Y V^T -> AdamW
     }
-    float *TT = h->ws_a, *XfT = h->ws_x, *Y = h->ws_a;
-    plain.C = TT;
-    plain.ldc = m;
-    if ((rc = gemm_nt(h, r, m, n, h->VTo, n, G_mask, n, plain, st))) return rc;
-    scaled.C = XfT;
-    scaled.ldc = r;
-    if ((rc = gemm_nt(h, r, r, m, TT, m, h->UTo, m, scaled, st))) return rc;
-    plain.C = Y;
-    plain.ldc = r;
-    if ((rc = gemm_nt(h, m, r, r, h->Uo, r, XfT, r, plain, st))) return rc;
-    return gemm_nt(h, m, n, r, Y, r, h->Vo, r, last, st);
+    return P;
+}
+
+int run_problem(int precision, const GemmProblem &q, cudaStream_t st) {
+    if (precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(q.M, q.N, q.K, q.A, q.B))
+        return gemm_tc(q.M, q.N, q.K, q.A, q.B, q.epi, st);
+    return gemm_simt(q.M, q.N, q.K, q.A, q.B, q.epi, st);
+}
+
+}  // namespace
+
+extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr,
+                              void *stream, float *G_filt_out, float *G_proj_out) {
+    clear_error();
+    int rc = check_step_args(h, W, G_mask, lr, G_filt_out, G_proj_out);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const StepPlan P = plan_step(h, W, G_mask, lr, G_filt_out, G_proj_out);
+    if (P.transpose && (rc = transpose_run(P.G, P.GT, P.m, P.n, P.round, st))) return rc;
+    for (int s = 0; s < 4; ++s)
+        if ((rc = run_problem(h->cfg.precision, P.stage[s], st))) return rc;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_step_many(specoptim_t *const *handles, int32_t count, float *const *W,
+                                   const float *const *G_mask, float lr, void *stream) {
+    clear_error();
+    if (!handles || !W || !G_mask || count < 1 || count > 16)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "step_many: 1 to 16 handles with W and G_mask arrays");
+    int rc;
+    for (int i = 0; i < count; ++i) {
+        if ((rc = check_step_args(handles[i], W[i], G_mask[i], lr, nullptr, nullptr))) return rc;
+        for (int k = 0; k < i; ++k)
+            if (handles[k] == handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, "step_many: repeated handle");
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    StepPlan plans[16];
+    for (int i = 0; i < count; ++i) plans[i] = plan_step(handles[i], W[i], G_mask[i], lr, nullptr, nullptr);
+    for (int i = 0; i < count; ++i)
+        if (plans[i].transpose &&
+            (rc = transpose_run(plans[i].G, plans[i].GT, plans[i].m, plans[i].n, plans[i].round, st)))
+            return rc;
+    for (int s = 0; s < 4; ++s) {
+        // tensor-core problems of this stage share launches (largest first, 8 per launch);
+        // the rest run one by one on the SIMT path
+        GemmProblem group[16];
+        double work[16];
+        int ng = 0;
+        for (int i = 0; i < count; ++i) {
+            const GemmProblem &q = plans[i].stage[s];
+            if (handles[i]->cfg.precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(q.M, q.N, q.K, q.A, q.B)) {
+                group[ng] = q;
+                work[ng] = (double)q.M * q.N * q.K;
+                ++ng;
+            } else if ((rc = gemm_simt(q.M, q.N, q.K, q.A, q.B, q.epi, st))) {
+                return rc;
+            }
+        }
+        for (int a = 1; a < ng; ++a)  // insertion sort by work, descending
+            for (int b = a; b > 0 && work[b] > work[b - 1]; --b) {
+                std::swap(work[b], work[b - 1]);
+                std::swap(group[b], group[b - 1]);
+            }
+        for (int off = 0; off < ng; off += 8)
+            if ((rc = gemm_tc_group(std::min(8, ng - off), group + off, st))) return rc;
+    }
+    return SPECOPTIM_OK;
 }
 
 extern "C" int specoptim_get_factors(const specoptim_t *h, float *U, float *s, float *V, float *d,

@@ -207,3 +207,29 @@ def test_refresh_many_rejects_bad_batches():
         so.svd_refresh_many([a, a])
     with pytest.raises(so.SpecOptimError):
         so.svd_refresh_many([so.SpectralOptimizer(8, 8) for _ in range(17)])
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_step_many_equals_single_steps(prec):
+    shapes = [(384, 128), (128, 512), (256, 256), (64, 72)]
+    inps = [synthetic.MatrixInputs(m, n, seed=60 + i, rank=4) for i, (m, n) in enumerate(shapes)]
+    a = [so.SpectralOptimizer(i.m, i.n, precision=prec) for i in inps]
+    b = [so.SpectralOptimizer(i.m, i.n, precision=prec) for i in inps]
+    for x, y, i in zip(a, b, inps):
+        G = dev(i.anchor_grad(0))
+        x.anchor_update(G)
+        y.anchor_update(G)
+    so.svd_refresh_many(a)
+    so.svd_refresh_many(b)
+    Wa = [dev(i.weights()) for i in inps]
+    Wb = [w.clone() for w in Wa]
+    for t in range(2):
+        Gs = [dev(i.masked_grad(t)) for i in inps]
+        for x, w, g in zip(a, Wa, Gs):
+            x.step(w, g, 2e-5)
+        so.step_many(b, Wb, Gs, 2e-5)
+    torch.cuda.synchronize()
+    for x, y, wa, wb in zip(a, b, Wa, Wb):
+        assert torch.equal(wa, wb)
+        for sa, sb in zip(x.get_state()[:3], y.get_state()[:3]):
+            assert torch.equal(sa, sb)
