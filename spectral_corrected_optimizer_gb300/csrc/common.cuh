@@ -71,6 +71,12 @@ void trace_end(int token, cudaStream_t st);
         ::spco::trace_end(_tk, st);                                          \
     } while (0)
 
+// Library-wide scratch for transient operands (the split copies of 3xTF32
+// products in the SVD refresh): grown on demand with cudaMalloc on the current
+// device, never shrunk, shared by all handles.  Callers use it only between
+// stream syncs of the same host thread (the refresh synchronises every sweep).
+int scratch_floats(size_t n, float **out);
+
 // iteration limit of every spin on an mbarrier (each probe also sleeps a little)
 constexpr uint32_t kSpinLimit = 1u << 22;
 

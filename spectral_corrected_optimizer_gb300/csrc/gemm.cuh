@@ -88,6 +88,13 @@ int gemm_tc(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogu
             cudaStream_t stream);
 int gemm_tc_group(int count, const GemmProblem *probs, cudaStream_t stream);
 
+// fp32-accurate product on the tensor cores (3xTF32 with K-concatenated split
+// operands); needs gemm3_workspace_floats(M, N, K) floats of 16-byte aligned
+// workspace.  Falls back to gemm_simt when the shape does not allow it.
+size_t gemm3_workspace_floats(int64_t M, int64_t N, int64_t K);
+int gemm_fp32x3(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
+                float *ws, cudaStream_t st);
+
 // fp32 SIMT GEMM (any shape, any transposition, any alignment)
 int gemm_simt(int64_t M, int64_t N, int64_t K, Operand A, Operand B, const Epilogue &epi,
               cudaStream_t stream);

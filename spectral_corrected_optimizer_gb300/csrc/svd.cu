@@ -498,10 +498,12 @@ int prepare(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
     e.C = b.A;
     e.ldc = b.Np;
     int rc;
+    float *ws = nullptr;
+    if ((rc = scratch_floats(gemm3_workspace_floats(b.r, b.r, b.L), &ws))) return rc;
     if (b.tall)  // A = M^T M : op(A)(i,k) = M[k][i], op(B)(k,j) = M[k][j]
-        rc = gemm_simt(b.r, b.r, a.m, Operand{a.M, a.n, true}, Operand{a.M, a.n, false}, e, st);
+        rc = gemm_fp32x3(b.r, b.r, a.m, Operand{a.M, a.n, true}, Operand{a.M, a.n, false}, e, ws, st);
     else         // A = M M^T
-        rc = gemm_simt(b.r, b.r, a.n, Operand{a.M, a.n, false}, Operand{a.M, a.n, true}, e, st);
+        rc = gemm_fp32x3(b.r, b.r, a.n, Operand{a.M, a.n, false}, Operand{a.M, a.n, true}, e, ws, st);
     if (rc) return rc;
     const int64_t NN = (int64_t)b.Np * b.Np;
     if (!a.warm) {
@@ -514,12 +516,12 @@ int prepare(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
     Epilogue t;
     t.C = b.Tmp;
     t.ldc = b.r;
-    if ((rc = gemm_simt(b.r, b.r, b.r, Operand{b.A, b.Np, false}, Operand{a.warm, b.r, false}, t, st)))
+    if ((rc = gemm_fp32x3(b.r, b.r, b.r, Operand{b.A, b.Np, false}, Operand{a.warm, b.r, false}, t, ws, st)))
         return rc;  // T = A W
     Epilogue w;
     w.C = b.A;
     w.ldc = b.Np;
-    return gemm_simt(b.r, b.r, b.r, Operand{a.warm, b.r, true}, Operand{b.Tmp, b.r, false}, w, st);  // W^T T
+    return gemm_fp32x3(b.r, b.r, b.r, Operand{a.warm, b.r, true}, Operand{b.Tmp, b.r, false}, w, ws, st);  // W^T T
 }
 
 // re-orthonormalised short factor, s_i = |M v_i| sorted descending, d, long factor
@@ -527,6 +529,9 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
     const int r = b.r;
     const int64_t rr = (int64_t)r * r, L = b.L;
     int rc;
+    float *ws = nullptr;
+    if ((rc = scratch_floats(std::max(gemm3_workspace_floats(r, r, r), gemm3_workspace_floats(L, r, b.tall ? a.n : a.m)), &ws)))
+        return rc;
     SPCO_LAUNCH("svd_extract", st, extract_kernel<<<grid_for(rr, 256), 256, 0, st>>>(b.Qacc, b.Np, r, b.Sf));
     SPECOPTIM_LAUNCHED("extract_kernel");
     // two Newton-Schulz steps X <- X (3 I - X^T X) / 2 remove the drift that the
@@ -535,11 +540,11 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
         Epilogue g;
         g.C = b.A;  // X^T X (r x r, ld r) reuses the Gram buffer
         g.ldc = r;
-        if ((rc = gemm_simt(r, r, r, Operand{b.Sf, r, true}, Operand{b.Sf, r, false}, g, st))) return rc;
+        if ((rc = gemm_fp32x3(r, r, r, Operand{b.Sf, r, true}, Operand{b.Sf, r, false}, g, ws, st))) return rc;
         Epilogue t;
         t.C = b.Tmp;
         t.ldc = r;
-        if ((rc = gemm_simt(r, r, r, Operand{b.Sf, r, false}, Operand{b.A, r, false}, t, st))) return rc;
+        if ((rc = gemm_fp32x3(r, r, r, Operand{b.Sf, r, false}, Operand{b.A, r, false}, t, ws, st))) return rc;
         SPCO_LAUNCH("svd_ns_update", st, ns_update_kernel<<<grid_for(rr, 256), 256, 0, st>>>(b.Sf, b.Tmp, rr));
         SPECOPTIM_LAUNCHED("ns_update_kernel");
     }
@@ -547,9 +552,9 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
     f.C = b.P;
     f.ldc = r;
     if (b.tall)
-        rc = gemm_simt(L, r, a.n, Operand{a.M, a.n, false}, Operand{b.Sf, r, false}, f, st);
+        rc = gemm_fp32x3(L, r, a.n, Operand{a.M, a.n, false}, Operand{b.Sf, r, false}, f, ws, st);
     else
-        rc = gemm_simt(L, r, a.m, Operand{a.M, a.n, true}, Operand{b.Sf, r, false}, f, st);
+        rc = gemm_fp32x3(L, r, a.m, Operand{a.M, a.n, true}, Operand{b.Sf, r, false}, f, ws, st);
     if (rc) return rc;
     SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.P, L, r, b.s_raw));
     SPCO_LAUNCH("svd_rank", st, rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.s_raw, r, b.order));

@@ -61,6 +61,28 @@ void trace_end(int token, cudaStream_t st) {
     if (token < (int)g_recs.size()) cudaEventRecord(g_recs[token].stop, st);
 }
 
+namespace {
+std::mutex g_scratch_mu;
+float *g_scratch = nullptr;
+size_t g_scratch_n = 0;
+}  // namespace
+
+int scratch_floats(size_t n, float **out) {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (n > g_scratch_n) {
+        if (g_scratch) {
+            SPECOPTIM_CUDA(cudaDeviceSynchronize());
+            cudaFree(g_scratch);
+            g_scratch = nullptr;
+            g_scratch_n = 0;
+        }
+        SPECOPTIM_CUDA(cudaMalloc(reinterpret_cast<void **>(&g_scratch), n * sizeof(float)));
+        g_scratch_n = n;
+    }
+    *out = g_scratch;
+    return SPECOPTIM_OK;
+}
+
 }  // namespace spco
 
 using namespace spco;
