@@ -105,17 +105,18 @@ constexpr int kSP = kP + 1;  // padded pitch of the subproblem tiles
 // threads compute the rotations; then every 2 x 2 block (p_a, q_a) x (p_b, q_b)
 // of S receives the row rotation of pair a and the column rotation of pair b
 // at once, and Q's columns p_b, q_b the rotation of pair b.
-__global__ void __launch_bounds__(kSolveThreads)
-jacobi_solve_kernel(const JacBatch jb, int inner_sweeps) {
-    __shared__ float S[kP * kSP];
-    __shared__ float Q[kP * kSP];
-    __shared__ float cs[kB][2];
-    __shared__ int pq[kB][2];
-    __shared__ float red[2];
-    const int job = find_job(jb.pair_off, jb.count, blockIdx.x);
+constexpr size_t kSolveSmem = 2 * kP * kSP * 4 + kB * 2 * 4 + kB * 2 * 4 + 16;
+
+__device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsigned char *smem) {
+    float *S = reinterpret_cast<float *>(smem);
+    float *Q = S + kP * kSP;
+    float(*cs)[2] = reinterpret_cast<float(*)[2]>(Q + kP * kSP);
+    int(*pq)[2] = reinterpret_cast<int(*)[2]>(cs + kB);
+    float *red = reinterpret_cast<float *>(pq + kB);
+    const int job = find_job(jb.pair_off, jb.count, item);
     if (!jb.active[job]) return;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
-    const int pair = blockIdx.x - jb.pair_off[job];
+    const int pair = item - jb.pair_off[job];
     const float *A = jb.A[job];
     const int tid = threadIdx.x;
     // 64 rows x 16 float4 (each row of the subproblem is two runs of 32 floats)
@@ -263,7 +264,7 @@ jacobi_apply_kernel(const JacBatch jb) {
     const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
     const int total_a = jb.row_off[jb.count];
     int item = blockIdx.x;
-    if (item < total_a) {
+    {
         const int job = find_job(jb.row_off, jb.count, item);
         if (!jb.active[job]) return;
         const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
@@ -312,33 +313,65 @@ jacobi_apply_kernel(const JacBatch jb) {
                     make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
             }
         }
-        return;
     }
-    // Q slabs
-    item -= total_a;
+}
+
+// Q slab of round k (64 rows x pair p, Q' = Q R_p) computed by 256 threads
+// (`tid` in 0..255) that synchronise on their own named barrier `bar`.
+__device__ void q_slab(const JacBatch &jb, int item, int tid, int bar, float *T1, float *T2) {
+    const int ti = tid / 16, tj = tid % 16;
     const int job = find_job(jb.q_off, jb.count, item);
-    if (!jb.active[job]) return;
+    const bool live = jb.active[job] != 0;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
     const int local = item - jb.q_off[job];
     const int r0 = (local / np) * kP, pair = local % np;
     float *Qm = jb.Q[job];
-    load_tile64(T2, jb.R[job] + (size_t)pair * kP * kP, tid);
-    // T1[l][rr] = Q[r0 + rr][g(l)]  (transposed so the product is k-major in rr)
-    for (int e = tid; e < kP * kP / 4; e += 256) {
-        const int rr = e % kP, l4 = (e / kP) * 4;
-        const float4 v = *reinterpret_cast<const float4 *>(&Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l4)]);
-        T1[(l4 + 0) * kQ + rr] = v.x;
-        T1[(l4 + 1) * kQ + rr] = v.y;
-        T1[(l4 + 2) * kQ + rr] = v.z;
-        T1[(l4 + 3) * kQ + rr] = v.w;
+    if (live) {
+        const float *R = jb.R[job] + (size_t)pair * kP * kP;
+        for (int e = tid; e < kP * kP / 4; e += 256) {
+            const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
+            *reinterpret_cast<float4 *>(&T2[i * kQ + j4]) = *reinterpret_cast<const float4 *>(&R[i * kP + j4]);
+        }
+        // T1[l][rr] = Q[r0 + rr][g(l)]  (transposed so the product is k-major in rr)
+        for (int e = tid; e < kP * kP / 4; e += 256) {
+            const int rr = e % kP, l4 = (e / kP) * 4;
+            const float4 v = *reinterpret_cast<const float4 *>(&Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l4)]);
+            T1[(l4 + 0) * kQ + rr] = v.x;
+            T1[(l4 + 1) * kQ + rr] = v.y;
+            T1[(l4 + 2) * kQ + rr] = v.z;
+            T1[(l4 + 3) * kQ + rr] = v.w;
+        }
     }
-    __syncthreads();
+    asm volatile("bar.sync %0, 256;" ::"r"(bar) : "memory");
+    if (!live) return;
     float acc[4][4];
     tile_product_kt(T1, T2, ti, tj, acc);  // (Q R)[rr][j]
 #pragma unroll
     for (int a = 0; a < 4; ++a)
         *reinterpret_cast<float4 *>(&Qm[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj)]) =
             make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+}
+
+constexpr size_t kQSolveSmem = 4 * (size_t)kP * kQ * 4;  // two Q slabs of two tiles (>= kSolveSmem)
+static_assert(kQSolveSmem >= kSolveSmem, "q_solve shared memory");
+
+// The subproblem solves of round k+1 (first ns CTAs, dispatched first so that
+// their long sequential work starts at once) and the Q accumulation of round k
+// (remaining CTAs, two slabs each) in one launch: the solve of round k+1
+// depends only on A after round k, the Q update only on round k's R, and the
+// two rounds use different R buffers.
+__global__ void __launch_bounds__(kSolveThreads)
+jacobi_q_solve_kernel(const JacBatch jq, const JacBatch js, int ns, int inner_sweeps) {
+    extern __shared__ __align__(16) unsigned char qs_smem[];
+    if ((int)blockIdx.x < ns) {
+        solve_pair(js, blockIdx.x, inner_sweeps, qs_smem);
+        return;
+    }
+    const int half = threadIdx.x / 256;
+    float *T1 = reinterpret_cast<float *>(qs_smem) + half * 2 * kP * kQ;
+    float *T2 = T1 + kP * kQ;
+    const int item = 2 * (blockIdx.x - ns) + half;
+    if (item < jq.q_off[jq.count]) q_slab(jq, item, threadIdx.x % 256, 1 + half, T1, T2);
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -393,16 +426,31 @@ __global__ void ns_update_kernel(float *__restrict__ X, const float *__restrict_
         X[e] = 1.5f * X[e] - 0.5f * T[e];
 }
 
-// column norms of P (rows x r, row-major): thread per column, coalesced across columns
-__global__ void colnorm_kernel(const float *__restrict__ P, int64_t rows, int r, float *__restrict__ out) {
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < r; j += gridDim.x * blockDim.x) {
-        double acc = 0.0;
-        for (int64_t i = 0; i < rows; ++i) {
+// squared column norms of P (rows x r, row-major) accumulated in double:
+// block (x, y) covers 32 columns and a 1/gridDim.y share of the rows
+__global__ void __launch_bounds__(256)
+colnorm_kernel(const float *__restrict__ P, int64_t rows, int r, double *__restrict__ out2) {
+    __shared__ double part[8][33];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    const int j = blockIdx.x * 32 + tx;
+    double acc = 0.0;
+    if (j < r)
+        for (int64_t i = blockIdx.y * 8 + ty; i < rows; i += (int64_t)gridDim.y * 8) {
             const double v = P[i * r + j];
             acc += v * v;
         }
-        out[j] = (float)sqrt(acc);
+    part[ty][tx] = acc;
+    __syncthreads();
+    if (ty == 0 && j < r) {
+        double t = 0.0;
+        for (int y = 0; y < 8; ++y) t += part[y][tx];
+        atomicAdd(&out2[j], t);
     }
+}
+
+__global__ void sqrt_kernel(const double *__restrict__ in2, int r, float *__restrict__ out) {
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < r; j += gridDim.x * blockDim.x)
+        out[j] = (float)sqrt(in2[j]);
 }
 
 // rank of each singular value (descending, ties by index) -> order[rank] = index
@@ -454,9 +502,9 @@ int grid_for(int64_t work, int threads) {
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = ((r + kP - 1) / kP) * kP;
-    // A, Qacc, rotations (Np/64 x 64 x 64), short factor + scratch (2 r^2), long factor P
+    // A, Qacc, two rotation buffers (Np/64 x 64 x 64 each), short factor + scratch (2 r^2), long factor P
     // (L r), s_raw, inv_s, order (int), 2 doubles
-    return (size_t)(2 * Np * Np + Np * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
+    return (size_t)(2 * Np * Np + 2 * Np * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
 }
 
 namespace {
@@ -465,7 +513,7 @@ struct JobBufs {
     int r, Np, nb;
     int64_t L;
     bool tall;
-    float *A, *Qacc, *R, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    float *A, *Qacc, *R, *R2, *Sf, *Tmp, *P, *s_raw, *inv_s;
     int *order;
     double *norms;
 };
@@ -480,7 +528,8 @@ JobBufs carve(const SvdJob &a) {
     b.A = a.work;
     b.Qacc = b.A + (size_t)b.Np * b.Np;
     b.R = b.Qacc + (size_t)b.Np * b.Np;
-    b.Sf = b.R + (size_t)b.Np * kP;
+    b.R2 = b.R + (size_t)b.Np * kP;
+    b.Sf = b.R2 + (size_t)b.Np * kP;
     b.Tmp = b.Sf + (size_t)b.r * b.r;
     b.P = b.Tmp + (size_t)b.r * b.r;
     b.s_raw = b.P + (size_t)b.L * b.r;
@@ -556,7 +605,14 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
     else
         rc = gemm_fp32x3(L, r, a.m, Operand{a.M, a.n, true}, Operand{b.Sf, r, false}, f, ws, st);
     if (rc) return rc;
-    SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.P, L, r, b.s_raw));
+    // squared norms in double, in the (now free) Gram buffer
+    double *norm2 = reinterpret_cast<double *>(b.A);
+    SPECOPTIM_CUDA(cudaMemsetAsync(norm2, 0, sizeof(double) * (size_t)r, st));
+    {
+        const dim3 grid((unsigned)((r + 31) / 32), (unsigned)std::max<int64_t>(1, std::min<int64_t>(L / 64, 64)));
+        SPCO_LAUNCH("svd_colnorm", st, colnorm_kernel<<<grid, 256, 0, st>>>(b.P, L, r, norm2));
+        SPCO_LAUNCH("svd_colnorm", st, sqrt_kernel<<<grid_for(r, 128), 128, 0, st>>>(norm2, r, b.s_raw));
+    }
     SPCO_LAUNCH("svd_rank", st, rank_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.s_raw, r, b.order));
     SPCO_LAUNCH("svd_spectrum", st, spectrum_kernel<<<grid_for(r, 128), 128, 0, st>>>(b.s_raw, r, b.order, a.tau, a.s, a.d, b.inv_s));
     float *short_out = b.tall ? a.V : a.U;
@@ -598,16 +654,36 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         rounds = std::max(rounds, b[i].nb - 1);
     }
     const int solve_grid = jb.pair_off[count];
-    const int apply_grid = jb.row_off[count] + jb.q_off[count];
+    const int apply_grid = jb.row_off[count];
+    const int nq = (jb.q_off[count] + 1) / 2;
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
+    static bool attr = false;
+    if (!attr) {
+        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_q_solve_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSolveSmem));
+        attr = true;
+    }
+    // rounds of matrix i at global round g: g mod (nb_i - 1); rotations of round g in R[g % 2]
+    auto set_round = [&](JacBatch &x, long g) {
+        for (int i = 0; i < count; ++i) {
+            x.round[i] = (int)(g % (b[i].nb - 1));
+            x.R[i] = (g % 2) ? b[i].R2 : b[i].R;
+        }
+    };
+    JacBatch js = jb, jq = jb;
+    set_round(js, 0);
+    SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
     std::vector<double> host(2 * count);
     int active = count;
+    long g = 0;
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
-        for (int g = 0; g < rounds; ++g) {
-            for (int i = 0; i < count; ++i) jb.round[i] = g % (b[i].nb - 1);
-            SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, 0, st>>>(jb, inner));
+        for (int k = 0; k < rounds; ++k, ++g) {
+            set_round(jb, g);
             SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(jb));
+            jq = jb;
+            set_round(js, g + 1);
+            SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid + nq, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {
@@ -624,13 +700,16 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             const double tol = jobs[i].tol;
+            int now_active = 1;
             if (host[2 * i] <= tol * tol * host[2 * i + 1]) {
-                jb.active[i] = 0;
-                --active;
+                now_active = 0;
             } else if (jobs[i].sweeps >= jobs[i].max_sweeps) {
-                jb.active[i] = 0;
-                --active;
+                now_active = 0;
                 jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
+            }
+            if (!now_active) {
+                jb.active[i] = js.active[i] = jq.active[i] = 0;
+                --active;
             }
         }
     }
