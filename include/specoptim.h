@@ -202,6 +202,15 @@ int64_t specoptim_launch_count(void);
 int specoptim_trace_reset(void);
 int specoptim_trace_report(char *buf, int64_t len);
 
+/* Failure-detection self-test: launches one kernel that waits on a device
+ * barrier nothing ever completes, with the same bounded-spin mechanism every
+ * kernel of the library uses (spin_limit probes of ~64 ns, in [1, 2^24]).
+ * The wait gives up, records its code in the library's device error flag and
+ * the kernel returns; the call then synchronises `stream`, reads and clears
+ * the flag and returns SPECOPTIM_ERR_TIMEOUT.  The CUDA context stays usable.
+ * Any other return value means the mechanism is broken. */
+int specoptim_selftest_wait_timeout(uint32_t spin_limit, void *stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *specoptim_last_error(void);
 

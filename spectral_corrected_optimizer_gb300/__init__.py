@@ -60,6 +60,7 @@ SIGNATURES = [
     ("specoptim_adamw", _int, [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _f32, _f32, _f32, _f32, _vp]),
     ("specoptim_gemm_nt", _int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     ("specoptim_filter_noalloc", _int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]),
+    ("specoptim_selftest_wait_timeout", _int, [_u32, _vp]),
     ("specoptim_trace_enable", _int, [_i32]),
     ("specoptim_launch_count", _i64, []),
     ("specoptim_trace_reset", _int, []),

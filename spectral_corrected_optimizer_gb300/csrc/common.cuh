@@ -135,6 +135,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Same wait with an explicit probe limit (used by the timeout self-test).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned *flag,
+                                                unsigned code, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(64);
+    }
+    if (flag) atomicExch(flag, code);
+    return false;
+}
+
 // 1D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned)
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes,

@@ -83,9 +83,31 @@ int scratch_floats(size_t n, float **out) {
     return SPECOPTIM_OK;
 }
 
+namespace {
+// waits on an mbarrier phase that nothing completes, with a bounded spin
+__global__ void wait_timeout_kernel(unsigned *flag, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait_limit(&bar, 0, flag, 0x1FFu, limit);
+    }
+}
+}  // namespace
+
 }  // namespace spco
 
 using namespace spco;
+
+extern "C" int specoptim_selftest_wait_timeout(uint32_t spin_limit, void *stream) {
+    clear_error();
+    if (spin_limit < 1 || spin_limit > (1u << 24))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "selftest: spin_limit must be in [1, 2^24]");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SPCO_LAUNCH("selftest_wait", st, wait_timeout_kernel<<<1, 32, 0, st>>>(device_flag_ptr(), spin_limit));
+    SPECOPTIM_LAUNCHED("wait_timeout_kernel");
+    return check_device_flag(st);
+}
 
 extern "C" int specoptim_trace_enable(int32_t enable) {
     clear_error();
