@@ -65,31 +65,64 @@ adamw_kernel(float *__restrict__ W, const float *__restrict__ G, float *__restri
         adamw_one(W[i], G[i], M1[i], M2[i], s);
 }
 
-// dst (cols x rows) = src (rows x cols)^T through a 32 x 33 shared tile,
-// optionally rounded to TF32 (round to nearest, ties away)
+// dst (cols x rows) = src (rows x cols)^T, optionally rounded to TF32 (round to
+// nearest, ties away).  64 x 64 tiles through a padded shared tile; when both
+// dimensions are multiples of 4 each thread moves four float4 in and four
+// float4 out (16 values in flight per thread), else the scalar path runs.
+__device__ __forceinline__ float maybe_round(float v, int round) {
+    if (round) {
+        uint32_t b;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(v));
+        v = __uint_as_float(b);
+    }
+    return v;
+}
+
 __global__ void __launch_bounds__(256)
 transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows, int cols,
                  int round) {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
-    const int64_t tiles_c = (cols + 31) / 32, tiles = tiles_c * ((rows + 31) / 32);
+    __shared__ float tile[64][65];
+    const int tid = threadIdx.x;
+    const int64_t tiles_c = (cols + 63) / 64, tiles = tiles_c * ((rows + 63) / 64);
+    const bool vec = ((rows | cols) & 3) == 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int r0 = (int)(t / tiles_c) * 32, c0 = (int)(t % tiles_c) * 32;
+        const int r0 = (int)(t / tiles_c) * 64, c0 = (int)(t % tiles_c) * 64;
         __syncthreads();
-        for (int i = ty; i < 32; i += 8) {
-            const int r = r0 + i, c = c0 + tx;
-            float v = (r < rows && c < cols) ? __ldcs(&src[(int64_t)r * cols + c]) : 0.f;
-            if (round) {
-                uint32_t b;
-                asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(v));
-                v = __uint_as_float(b);
+        if (vec) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // 16 threads per row, 16 rows per pass
+                const int r = r0 + u * 16 + tid / 16, c = c0 + (tid % 16) * 4;
+                v[u] = (r < rows && c < cols) ? __ldcs(reinterpret_cast<const float4 *>(&src[(int64_t)r * cols + c]))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            tile[i][tx] = v;
-        }
-        __syncthreads();
-        for (int i = ty; i < 32; i += 8) {
-            const int c = c0 + i, r = r0 + tx;
-            if (c < cols && r < rows) dst[(int64_t)c * rows + r] = tile[tx][i];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int rr = u * 16 + tid / 16, cc = (tid % 16) * 4;
+                tile[rr][cc] = maybe_round(v[u].x, round);
+                tile[rr][cc + 1] = maybe_round(v[u].y, round);
+                tile[rr][cc + 2] = maybe_round(v[u].z, round);
+                tile[rr][cc + 3] = maybe_round(v[u].w, round);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // output row = input column
+                const int cc = u * 16 + tid / 16, rr = (tid % 16) * 4;
+                const int c = c0 + cc, r = r0 + rr;
+                if (c < cols && r < rows)
+                    *reinterpret_cast<float4 *>(&dst[(int64_t)c * rows + r]) =
+                        make_float4(tile[rr][cc], tile[rr + 1][cc], tile[rr + 2][cc], tile[rr + 3][cc]);
+            }
+        } else {
+            for (int e = tid; e < 64 * 64; e += 256) {
+                const int rr = e / 64, cc = e % 64, r = r0 + rr, c = c0 + cc;
+                tile[rr][cc] = (r < rows && c < cols) ? maybe_round(src[(int64_t)r * cols + c], round) : 0.f;
+            }
+            __syncthreads();
+            for (int e = tid; e < 64 * 64; e += 256) {
+                const int cc = e / 64, rr = e % 64, r = r0 + rr, c = c0 + cc;
+                if (c < cols && r < rows) dst[(int64_t)c * rows + r] = tile[rr][cc];
+            }
         }
     }
 }
@@ -98,8 +131,8 @@ transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int row
 
 int transpose_run(const float *src, float *dst, int rows, int cols, bool round, cudaStream_t st) {
     if (rows <= 0 || cols <= 0) return SPECOPTIM_OK;
-    const int64_t tiles = (int64_t)((rows + 31) / 32) * ((cols + 31) / 32);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 16));
+    const int64_t tiles = (int64_t)((rows + 63) / 64) * ((cols + 63) / 64);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 4));
     SPCO_LAUNCH("transpose", st, transpose_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, round ? 1 : 0));
     SPECOPTIM_LAUNCHED("transpose_kernel");
     return SPECOPTIM_OK;

@@ -131,7 +131,7 @@ __host__ __device__ inline RingLayout ring_layout(size_t in_bytes, size_t out_by
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nchunks, int H,
                  int K, uint64_t seed, int stages, unsigned *flag) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -315,7 +315,8 @@ struct RingPlan {
     int stages, ctas_per_sm;
 };
 
-RingPlan pick_ring(size_t in_bytes, size_t out_bytes) {
+RingPlan pick_ring(size_t in_bytes, size_t out_bytes, int max_ctas) {
+    if (max_ctas >= 3 && ring_layout(in_bytes, out_bytes, 2).total <= kSmemBudget / 3 - 1024) return {2, 3};
     for (int st = kMaxStages; st >= 3; --st)
         if (ring_layout(in_bytes, out_bytes, st).total <= kSmemBudget / 2 - 1024) return {st, 2};
     for (int st = kMaxStages; st >= 1; --st)
@@ -329,7 +330,7 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
     const T *d = static_cast<const T *>(dense);
     T *p = static_cast<T *>(packed);
     const size_t in_b = (size_t)CH * H * sizeof(T), out_b = (size_t)CH * K * sizeof(T);
-    const RingPlan plan = pick_ring(in_b, out_b);
+    const RingPlan plan = pick_ring(in_b, out_b, 3);
     const int stages = plan.stages;
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
@@ -360,7 +361,7 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
     const T *p = static_cast<const T *>(packed);
     T *d = static_cast<T *>(dense);
     const size_t in_b = (size_t)CH * K * sizeof(T), out_b = (size_t)CH * H * sizeof(T);
-    const RingPlan plan = pick_ring(in_b, out_b);
+    const RingPlan plan = pick_ring(in_b, out_b, 2);
     const int stages = plan.stages;
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
