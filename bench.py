@@ -58,6 +58,27 @@ def env_int(name, default):
         return default
 
 
+def gemm_traffic_per_launch():
+    """DRAM bytes per grouped gemm_tf32 launch from the committed ncu summary, or None
+    when the kernel or its orchestration changed since the counters were taken."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "spectral_corrected_optimizer_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("gemm_tc.cu", "gemm.cuh", "specoptim.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_tf32_layer_step.md")) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch=([0-9.e+]+) sources_sha256_16=([0-9a-f]+)", text)
+    if not m or m.group(2) != h.hexdigest()[:16]:
+        return None
+    return float(m.group(1))
+
+
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -336,7 +357,9 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         roof = {"kernel": name, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": None}
     roof.update({"launches_per_step": n_launch / steady_n, "avg_launch_ms": t_ms / n_launch,
-                 "share_of_step": t_ms / total_ms, "traffic": None})
+                 "share_of_step": t_ms / total_ms,
+                 "traffic": gemm_traffic_per_launch() if name == "gemm_tf32" else None,
+                 "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"})
     step_bound_ms = 1e3 * max(layer.flops / (tf32_peak * 1e12), layer.bytes / (peaks["hbm_gbs"] * 1e9))
 
     result = {
