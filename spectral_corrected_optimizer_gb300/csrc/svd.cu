@@ -4,17 +4,17 @@
 //
 // GPU formulation (fp32):
 //   1. Gram matrix of the short side, A = M^T M (m >= n) or M M^T (m < n),
-//      r x r, zero-padded to Np (a multiple of 32).
-//   2. Block-Jacobi eigen-decomposition A = Q diag(lambda) Q^T.  The Np/16
-//      blocks of 16 indices meet in round-robin order; in each round every
-//      pair of blocks forms a 32 x 32 subproblem that one warp diagonalises in
-//      shared memory (cyclic Jacobi, parallel order), giving a 32 x 32
-//      rotation R_p per pair.  A second kernel applies all rotations at once:
-//      every 32 x 32 tile (pair p1, pair p2) of A becomes R_p1^T A R_p2 and
-//      every 32-row slab of Q becomes Q R_p.  Sweeps repeat until the
-//      off-diagonal Frobenius norm falls below tol times the total norm.
-//      Padded indices have exactly zero rows and columns, so they are never
-//      rotated and stay out of the real eigenvectors.
+//      r x r, zero-padded to Np (a multiple of 64), in fp32-accurate 3xTF32
+//      tensor-core products; with a previous factor W the start is W^T A W.
+//   2. Block-Jacobi eigen-decomposition A = Q diag(lambda) Q^T.  The Np/32
+//      blocks of 32 indices meet in round-robin order; in each round every
+//      pair of blocks forms a 64 x 64 subproblem that one CTA sweeps in shared
+//      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
+//      per pair.  The rotations are then applied: every 64 x 64 tile (pair p1,
+//      pair p2) of A becomes R_p1^T A R_p2 and every 64-row slab of Q becomes
+//      Q R_p.  Sweeps repeat until the off-diagonal Frobenius norm falls below
+//      tol times the total norm.  Padded indices have exactly zero rows and
+//      columns, so they are never rotated and stay out of the real eigenvectors.
 //   3. The eigenvectors are re-orthonormalised by two Newton-Schulz steps.
 //   4. P = M V (or M^T U); s_i = |P e_i| sorted descending, d_i = s_i/(s_i+tau_p),
 //      and the long-side factor is P diag(1/s), zero columns where s_i = 0.
@@ -23,6 +23,7 @@
 // enters G_filt multiplied by d_i).
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "gemm.cuh"
@@ -96,129 +97,163 @@ __device__ __forceinline__ int pair_index(int nb, int round, int p, int l) {
     return (l < kB ? a : b) * kB + (l & (kB - 1));
 }
 
-constexpr int kSolveThreads = 512;
-constexpr int kSP = kP + 1;  // padded pitch of the subproblem tiles
+constexpr int kSolveThreads = 256;
+constexpr int kSP = kP + 2;  // pitch of S (66 spreads every access pattern below over the banks)
+constexpr int kRP = kP;      // pitch of the rotation accumulator
 
-// One CTA per pair: load the 64 x 64 subproblem, run up to `inner_sweeps`
-// cyclic Jacobi sweeps in parallel order (32 disjoint rotations per step), and
-// write the accumulated rotation R (64 x 64).  Each step has two phases: 32
-// threads compute the rotations; then every 2 x 2 block (p_a, q_a) x (p_b, q_b)
-// of S receives the row rotation of pair a and the column rotation of pair b
-// at once, and Q's columns p_b, q_b the rotation of pair b.
-constexpr size_t kSolveSmem = 2 * kP * kSP * 4 + kB * 2 * 4 + kB * 2 * 4 + 16;
+// Rotation (c, s) of one pair with fast reciprocal / square-root intrinsics:
+// c^2 + s^2 = 1 to a few ulp, the same order as the correctly rounded form.
+__device__ __forceinline__ void jacobi_cs_fast(float app, float aqq, float apq, float &c, float &s) {
+    const float theta = __fdividef(aqq - app, 2.f * apq);
+    // |theta| beyond 2^64 overflows theta^2 to inf and gives t = 0: the rotation is below fp32 resolution
+    float t = __frcp_rn(fabsf(theta) + sqrtf(fmaf(theta, theta, 1.f)));
+    t = copysignf(t, theta);
+    c = rsqrtf(fmaf(t, t, 1.f));
+    s = t * c;
+    if (apq == 0.f) {
+        c = 1.f;
+        s = 0.f;
+    }
+}
+
+// One CTA (8 warps) per pair: load the 64 x 64 subproblem S, run up to
+// `inner_sweeps` cyclic Jacobi sweeps in parallel order (32 disjoint rotations
+// per step), and write the accumulated rotation R (64 x 64).
+//  * Every warp computes all 32 rotations of a step itself (lane l owns pair
+//    l), so there is no shared rotation table and no barrier before the updates.
+//  * S and R are double buffered (a step reads one copy and writes the other):
+//    one barrier per step.
+//  * S stays symmetric, so only the 2 x 2 blocks (pair ka, pair kb), ka < kb,
+//    are computed; each is written with its transpose.  Warp w takes the block
+//    rows r = w and r = w + 8 together with their partners 31 - r (31 blocks
+//    per row couple, one per lane 0..30).  The 32 diagonal blocks come from the
+//    rotations themselves (warp 0 writes them).
+//  * Lane l applies its own rotation to columns p_l, q_l of R in rows 8w .. 8w+7.
+constexpr size_t kSolveSmem = (2 * (size_t)kP * kSP + 2 * (size_t)kP * kRP) * 4 + 16;
 
 __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsigned char *smem) {
     float *S = reinterpret_cast<float *>(smem);
-    float *Q = S + kP * kSP;
-    float(*cs)[2] = reinterpret_cast<float(*)[2]>(Q + kP * kSP);
-    int(*pq)[2] = reinterpret_cast<int(*)[2]>(cs + kB);
-    float *red = reinterpret_cast<float *>(pq + kB);
+    float *Sn = S + kP * kSP;
+    float *Q = Sn + kP * kSP;
+    float *Qn = Q + kP * kRP;
+    float *red = Qn + kP * kRP;
     const int job = find_job(jb.pair_off, jb.count, item);
     if (!jb.active[job]) return;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
     const int pair = item - jb.pair_off[job];
     const float *A = jb.A[job];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // 64 rows x 16 float4 (each row of the subproblem is two runs of 32 floats)
     for (int e = tid; e < kP * (kP / 4); e += kSolveThreads) {
         const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
         const float4 v = *reinterpret_cast<const float4 *>(
             &A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j4)]);
-        S[i * kSP + j4] = v.x;
-        S[i * kSP + j4 + 1] = v.y;
-        S[i * kSP + j4 + 2] = v.z;
-        S[i * kSP + j4 + 3] = v.w;
+        *reinterpret_cast<float2 *>(&S[i * kSP + j4]) = make_float2(v.x, v.y);
+        *reinterpret_cast<float2 *>(&S[i * kSP + j4 + 2]) = make_float2(v.z, v.w);
     }
-    for (int e = tid; e < kP * kP; e += kSolveThreads) Q[(e / kP) * kSP + e % kP] = (e / kP == e % kP) ? 1.f : 0.f;
+    for (int e = tid; e < kP * kP; e += kSolveThreads) Q[(e / kP) * kRP + e % kP] = (e / kP == e % kP) ? 1.f : 0.f;
     __syncthreads();
+    // this lane's two blocks: (ka[u], kb[u]) for the row couples r = warp + 8u
+    int ka[2], kb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int r = warp + 8 * u;
+        if (lane < 31 - r) {
+            ka[u] = r;
+            kb[u] = r + 1 + lane;
+        } else {
+            ka[u] = 31 - r;
+            kb[u] = lane + 1;  // lane 31 gives kb = 32: no block
+        }
+    }
     for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
         float offmax = 0.f, dmax = 0.f;
         for (int step = 0; step < kP - 1; ++step) {
-            if (tid < kB) {
-                int p, q;
-                rr_pair(kP, step, tid, p, q);
+            // pair `lane` of this step (round-robin over 64 indices)
+            int p, q;
+            if (lane == 0) {
+                p = kP - 1;
+                q = step;
+            } else {
+                p = step + lane;
+                p = p >= kP - 1 ? p - (kP - 1) : p;
+                q = step - lane;
+                q = q < 0 ? q + (kP - 1) : q;
+            }
+            float c, sn;
+            {
                 const float app = S[p * kSP + p], aqq = S[q * kSP + q], apq = S[p * kSP + q];
-                float c, sn;
-                jacobi_cs(app, aqq, apq, c, sn);
-                cs[tid][0] = c;
-                cs[tid][1] = sn;
-                pq[tid][0] = p;
-                pq[tid][1] = q;
+                jacobi_cs_fast(app, aqq, apq, c, sn);
                 offmax = fmaxf(offmax, fabsf(apq));
                 dmax = fmaxf(dmax, fmaxf(fabsf(app), fabsf(aqq)));
+                if (warp == 0) {  // diagonal block of this pair: diag(J^T S J), decoupled
+                    const float cc = c * c, ss = sn * sn, cs2 = 2.f * c * sn * apq;
+                    Sn[p * kSP + p] = cc * app - cs2 + ss * aqq;
+                    Sn[q * kSP + q] = ss * app + cs2 + cc * aqq;
+                    Sn[p * kSP + q] = 0.f;
+                    Sn[q * kSP + p] = 0.f;
+                }
             }
-            __syncthreads();
-            // S: 32 x 32 blocks of 2 x 2, two per thread
-            float z[2][4];
-            int addr[2][4];
+            const int pq = p | (q << 8);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int b = tid + u * kSolveThreads;
-                const int ka = b / kB, kb = b % kB;
-                const int pa = pq[ka][0], qa = pq[ka][1], pb = pq[kb][0], qb = pq[kb][1];
-                const float ca = cs[ka][0], sa = cs[ka][1], cb = cs[kb][0], sb = cs[kb][1];
-                addr[u][0] = pa * kSP + pb;
-                addr[u][1] = pa * kSP + qb;
-                addr[u][2] = qa * kSP + pb;
-                addr[u][3] = qa * kSP + qb;
-                const float x11 = S[addr[u][0]], x12 = S[addr[u][1]], x21 = S[addr[u][2]], x22 = S[addr[u][3]];
-                const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
-                const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
-                z[u][0] = cb * y11 - sb * y12;
-                z[u][1] = sb * y11 + cb * y12;
-                z[u][2] = cb * y21 - sb * y22;
-                z[u][3] = sb * y21 + cb * y22;
-                if (ka == kb) z[u][1] = z[u][2] = 0.f;  // the rotated pair is now decoupled
+                const int a = ka[u], b = kb[u] & 31;
+                const int pqa = __shfl_sync(0xffffffffu, pq, a), pqb = __shfl_sync(0xffffffffu, pq, b);
+                const float ca = __shfl_sync(0xffffffffu, c, a), sa = __shfl_sync(0xffffffffu, sn, a);
+                const float cb = __shfl_sync(0xffffffffu, c, b), sb = __shfl_sync(0xffffffffu, sn, b);
+                if (kb[u] < 32) {
+                    const int pa = pqa & 0xff, qa = pqa >> 8, pb = pqb & 0xff, qb = pqb >> 8;
+                    const float x11 = S[pa * kSP + pb], x12 = S[pa * kSP + qb];
+                    const float x21 = S[qa * kSP + pb], x22 = S[qa * kSP + qb];
+                    // rows: J_a^T X, then columns: (J_a^T X) J_b
+                    const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
+                    const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
+                    const float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
+                    const float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
+                    Sn[pa * kSP + pb] = z11;
+                    Sn[pa * kSP + qb] = z12;
+                    Sn[qa * kSP + pb] = z21;
+                    Sn[qa * kSP + qb] = z22;
+                    Sn[pb * kSP + pa] = z11;
+                    Sn[qb * kSP + pa] = z12;
+                    Sn[pb * kSP + qa] = z21;
+                    Sn[qb * kSP + qa] = z22;
+                }
             }
-            // Q: columns p_b, q_b of 64 rows, four element pairs per thread
-            float qv[4][2];
-            int qa_[4][2];
+            // accumulator: columns p, q of rows 8 warp .. 8 warp + 7
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + u * kSolveThreads;
-                const int kb = e / kP, i = e % kP;
-                const int pb = pq[kb][0], qb = pq[kb][1];
-                const float cb = cs[kb][0], sb = cs[kb][1];
-                qa_[u][0] = i * kSP + pb;
-                qa_[u][1] = i * kSP + qb;
-                const float x = Q[qa_[u][0]], y = Q[qa_[u][1]];
-                qv[u][0] = cb * x - sb * y;
-                qv[u][1] = sb * x + cb * y;
-            }
-            __syncthreads();  // every read of this step is done before any write
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int t = 0; t < 4; ++t) S[addr[u][t]] = z[u][t];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                Q[qa_[u][0]] = qv[u][0];
-                Q[qa_[u][1]] = qv[u][1];
+            for (int t = 0; t < 8; ++t) {
+                const int i = 8 * warp + t;
+                const float x = Q[i * kRP + p], y = Q[i * kRP + q];
+                Qn[i * kRP + p] = c * x - sn * y;
+                Qn[i * kRP + q] = sn * x + c * y;
             }
             __syncthreads();
+            float *t1 = S;
+            S = Sn;
+            Sn = t1;
+            float *t2 = Q;
+            Q = Qn;
+            Qn = t2;
         }
         // stop once no off-diagonal entry rotated in this sweep was above fp32 noise
-        if (tid < 32) {
+        if (warp == 0) {
             for (int o = 16; o > 0; o >>= 1) {
                 offmax = fmaxf(offmax, __shfl_xor_sync(0xffffffffu, offmax, o));
                 dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
             }
-            if (tid == 0) {
+            if (lane == 0) {
                 red[0] = offmax;
                 red[1] = dmax;
             }
         }
         __syncthreads();
-        const bool done = red[0] <= 1e-7f * red[1];
-        __syncthreads();
-        if (done) break;
+        // red is rewritten only after the next sweep's barriers
+        if (red[0] <= 1e-7f * red[1]) break;
     }
     float *Rp = jb.R[job] + (size_t)pair * kP * kP;
-    for (int e = tid; e < kP * kP / 4; e += kSolveThreads) {
-        const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
-        *reinterpret_cast<float4 *>(&Rp[i * kP + j4]) =
-            make_float4(Q[i * kSP + j4], Q[i * kSP + j4 + 1], Q[i * kSP + j4 + 2], Q[i * kSP + j4 + 3]);
-    }
+    for (int e = tid; e < kP * kP / 4; e += kSolveThreads)
+        *reinterpret_cast<float4 *>(&Rp[4 * e]) = *reinterpret_cast<const float4 *>(&Q[4 * e]);
 }
 
 // 64 x 64 x 64 product of two shared tiles into registers, 4 x 4 outputs per
@@ -352,26 +387,23 @@ __device__ void q_slab(const JacBatch &jb, int item, int tid, int bar, float *T1
             make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
 }
 
-constexpr size_t kQSolveSmem = 4 * (size_t)kP * kQ * 4;  // two Q slabs of two tiles (>= kSolveSmem)
-static_assert(kQSolveSmem >= kSolveSmem, "q_solve shared memory");
+constexpr size_t kQSolveSmem = kSolveSmem > 2 * (size_t)kP * kQ * 4 ? kSolveSmem : 2 * (size_t)kP * kQ * 4;
 
-// The subproblem solves of round k+1 (first ns CTAs, dispatched first so that
-// their long sequential work starts at once) and the Q accumulation of round k
-// (remaining CTAs, two slabs each) in one launch: the solve of round k+1
-// depends only on A after round k, the Q update only on round k's R, and the
-// two rounds use different R buffers.
+// One launch per round boundary: the subproblem solves of round k+1 (CTAs
+// 0 .. solve_grid-1, dispatched first: they are the critical path) and the Q
+// slabs of round k (the remaining CTAs) fill the machine together.  Both read
+// the A that round k's apply left; the solves write the other rotation buffer.
+static_assert(kSolveThreads == 256, "one Q slab per CTA");
 __global__ void __launch_bounds__(kSolveThreads)
-jacobi_q_solve_kernel(const JacBatch jq, const JacBatch js, int ns, int inner_sweeps) {
+jacobi_q_solve_kernel(const JacBatch jq, const JacBatch js, int solve_grid, int inner_sweeps) {
     extern __shared__ __align__(16) unsigned char qs_smem[];
-    if ((int)blockIdx.x < ns) {
+    if ((int)blockIdx.x < solve_grid) {
         solve_pair(js, blockIdx.x, inner_sweeps, qs_smem);
-        return;
+    } else {
+        float *T1 = reinterpret_cast<float *>(qs_smem);
+        float *T2 = T1 + kP * kQ;
+        q_slab(jq, blockIdx.x - solve_grid, threadIdx.x, 1, T1, T2);
     }
-    const int half = threadIdx.x / 256;
-    float *T1 = reinterpret_cast<float *>(qs_smem) + half * 2 * kP * kQ;
-    float *T2 = T1 + kP * kQ;
-    const int item = 2 * (blockIdx.x - ns) + half;
-    if (item < jq.q_off[jq.count]) q_slab(jq, item, threadIdx.x % 256, 1 + half, T1, T2);
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -513,7 +545,7 @@ struct JobBufs {
     int r, Np, nb;
     int64_t L;
     bool tall;
-    float *A, *Qacc, *R, *R2, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    float *A, *Qacc, *R, *Sf, *Tmp, *P, *s_raw, *inv_s;
     int *order;
     double *norms;
 };
@@ -528,8 +560,7 @@ JobBufs carve(const SvdJob &a) {
     b.A = a.work;
     b.Qacc = b.A + (size_t)b.Np * b.Np;
     b.R = b.Qacc + (size_t)b.Np * b.Np;
-    b.R2 = b.R + (size_t)b.Np * kP;
-    b.Sf = b.R2 + (size_t)b.Np * kP;
+    b.Sf = b.R + (size_t)2 * b.Np * kP;
     b.Tmp = b.Sf + (size_t)b.r * b.r;
     b.P = b.Tmp + (size_t)b.r * b.r;
     b.s_raw = b.P + (size_t)b.L * b.r;
@@ -625,6 +656,22 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
 
 }  // namespace
 
+int set_solve_attributes() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {false};
+    int dev = 0;
+    SPECOPTIM_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: device ordinal out of range");
+    std::lock_guard<std::mutex> lk(mu);
+    if (!done[dev]) {
+        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_q_solve_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSolveSmem));
+        done[dev] = true;
+    }
+    return SPECOPTIM_OK;
+}
+
 int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     if (count < 1 || count > kMaxBatch)
         return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: 1 to 16 matrices per batch");
@@ -655,35 +702,34 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     }
     const int solve_grid = jb.pair_off[count];
     const int apply_grid = jb.row_off[count];
-    const int nq = (jb.q_off[count] + 1) / 2;
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
-    static bool attr = false;
-    if (!attr) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_q_solve_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSolveSmem));
-        attr = true;
-    }
-    // rounds of matrix i at global round g: g mod (nb_i - 1); rotations of round g in R[g % 2]
+    int rc2 = set_solve_attributes();
+    if (rc2) return rc2;
+    // rotations of round g live in buffer g % 2
     auto set_round = [&](JacBatch &x, long g) {
         for (int i = 0; i < count; ++i) {
             x.round[i] = (int)(g % (b[i].nb - 1));
-            x.R[i] = (g % 2) ? b[i].R2 : b[i].R;
+            x.R[i] = b[i].R + (size_t)(g % 2) * b[i].Np * kP;
         }
     };
     JacBatch js = jb, jq = jb;
-    set_round(js, 0);
-    SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
     std::vector<double> host(2 * count);
     int active = count;
     long g = 0;
+    // round 0's solves alone (no Q slabs yet)
+    set_round(js, 0);
+    SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(jb, g);
             SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(jb));
-            jq = jb;
+            // Q with round g's rotations, with the active set of this apply
+            set_round(jq, g);
             set_round(js, g + 1);
-            SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid + nq, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
+            SPCO_LAUNCH("svd_jacobi_q_solve", st,
+                        jacobi_q_solve_kernel<<<solve_grid + jq.q_off[count], kSolveThreads, kQSolveSmem, st>>>(
+                            jq, js, solve_grid, inner));
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {
