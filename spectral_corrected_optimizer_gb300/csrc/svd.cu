@@ -10,10 +10,12 @@
 //      blocks of 32 indices meet in round-robin order; in each round every
 //      pair of blocks forms a 64 x 64 subproblem that one CTA sweeps in shared
 //      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
-//      per pair.  The rotations are then applied: every 64 x 64 tile (pair p1,
-//      pair p2) of A becomes R_p1^T A R_p2 and every 64-row slab of Q becomes
-//      Q R_p.  Sweeps repeat until the off-diagonal Frobenius norm falls below
-//      tol times the total norm.  Padded indices have exactly zero rows and
+//      per pair (R = the block-diagonal of all R_p in the round's order).  The
+//      rotations are applied on the tensor cores (jacobi_tc.cu, 3xTF32):
+//      B^T = (A R)^T, then A <- B^T R = R^T A R, and Q <- Q R on a second,
+//      low-priority stream that trails the A chain by up to three rounds.
+//      Sweeps repeat until the off-diagonal Frobenius norm falls below tol
+//      times the total norm.  Padded indices have exactly zero rows and
 //      columns, so they are never rotated and stay out of the real eigenvectors.
 //   3. The eigenvectors are re-orthonormalised by two Newton-Schulz steps.
 //   4. P = M V (or M^T U); s_i = |P e_i| sorted descending, d_i = s_i/(s_i+tau_p),
@@ -27,74 +29,35 @@
 #include <vector>
 
 #include "gemm.cuh"
+#include "jacobi.cuh"
 #include "svd.cuh"
+#include "tc.cuh"
 
 namespace spco {
 namespace {
 
-constexpr int kB = 32;      // block size of the block-Jacobi
-constexpr int kP = 2 * kB;  // subproblem size (one CTA)
 constexpr int kMaxBatch = 16;
-
-// round-robin schedule over `players` (even): pair i of round k
-__host__ __device__ __forceinline__ void rr_pair(int players, int round, int i, int &a, int &b) {
-    const int n1 = players - 1;
-    if (i == 0) {
-        a = n1;
-        b = round;
-    } else {
-        a = (round + i) % n1;
-        b = (round - i + n1) % n1;
-    }
-}
-
-// Jacobi rotation (c, s) that zeroes the (p,q) entry of [[app, apq], [apq, aqq]]
-__device__ __forceinline__ void jacobi_cs(float app, float aqq, float apq, float &c, float &s) {
-    if (apq == 0.f) {
-        c = 1.f;
-        s = 0.f;
-        return;
-    }
-    const float theta = (aqq - app) / (2.f * apq);
-    float t;
-    if (fabsf(theta) > 1e18f) {
-        t = 0.5f / theta;
-    } else {
-        t = 1.f / (fabsf(theta) + sqrtf(1.f + theta * theta));
-        if (theta < 0.f) t = -t;
-    }
-    c = 1.f / sqrtf(1.f + t * t);
-    s = t * c;
-}
+constexpr int kRing = 4;  // rotation slots: the Q chain may lag the A chain by kRing - 1 rounds
 
 // All matrices of one batched refresh.  Each matrix i has Np[i] (a multiple of
-// 64) padded indices in nb = Np/32 blocks; in its round `round[i]` the blocks
-// meet in Np/64 pairs.  Work items of every kernel are numbered over the whole
-// batch through the prefix arrays.
+// 128) padded indices in nb = Np/32 blocks; in its round `round[i]` the blocks
+// meet in Np/64 pairs.  The solve kernel takes one CTA per pair, numbered over
+// the whole batch through pair_off.  R[i] points at the rotation slot of the
+// round: per pair, R_p^T split for 3xTF32 (hi block, then lo block, 64 x 64 each).
 struct JacBatch {
     int count;
     float *A[kMaxBatch];
-    float *Q[kMaxBatch];
     float *R[kMaxBatch];
     int Np[kMaxBatch];
     int round[kMaxBatch];
     int active[kMaxBatch];
-    int pair_off[kMaxBatch + 1];   // solve: one CTA per pair
-    int row_off[kMaxBatch + 1];    // apply: upper-triangle A tiles (pair p1 <= pair p2)
-    int q_off[kMaxBatch + 1];      // apply: Q slabs, (Np/64) row chunks x pairs
+    int pair_off[kMaxBatch + 1];
 };
 
 __device__ __forceinline__ int find_job(const int *off, int count, int item) {
     int i = 0;
     while (i + 1 < count && item >= off[i + 1]) ++i;
     return i;
-}
-
-// global index of local index l (0..63) of pair p of the given round (nb blocks)
-__device__ __forceinline__ int pair_index(int nb, int round, int p, int l) {
-    int a, b;
-    rr_pair(nb, round, p, a, b);
-    return (l < kB ? a : b) * kB + (l & (kB - 1));
 }
 
 constexpr int kSolveThreads = 256;
@@ -251,159 +214,29 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
         // red is rewritten only after the next sweep's barriers
         if (red[0] <= 1e-7f * red[1]) break;
     }
-    float *Rp = jb.R[job] + (size_t)pair * kP * kP;
-    for (int e = tid; e < kP * kP / 4; e += kSolveThreads)
-        *reinterpret_cast<float4 *>(&Rp[4 * e]) = *reinterpret_cast<const float4 *>(&Q[4 * e]);
-}
-
-// 64 x 64 x 64 product of two shared tiles into registers, 4 x 4 outputs per
-// thread (256 threads): acc[a][b] = sum_k L[k][4 ti + a] * Rt[k][4 tj + b]
-// (both tiles stored k-major with pitch kQ, so each k step is two float4 loads).
-constexpr int kQ = kP + 4;
-__device__ __forceinline__ void tile_product_kt(const float *L, const float *Rt, int ti, int tj,
-                                                float (&acc)[4][4]) {
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < kP; ++k) {
-        const float4 l = *reinterpret_cast<const float4 *>(&L[k * kQ + 4 * ti]);
-        const float4 r = *reinterpret_cast<const float4 *>(&Rt[k * kQ + 4 * tj]);
-        const float lv[4] = {l.x, l.y, l.z, l.w}, rv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(lv[a], rv[b], acc[a][b]);
+    // R_p^T = hi + lo for the tensor-core rotation: R^T[j][k] = R[k][j] (Q holds R
+    // row-major); transposed through the free S buffer, then written row by row
+    for (int e = tid; e < kP * kP; e += kSolveThreads) {
+        const int jj = e % kP, k = e / kP;
+        Sn[jj * kSP + k] = Q[k * kRP + jj];
+    }
+    __syncthreads();
+    float *Rp = jb.R[job] + (size_t)pair * 2 * kP * kP;
+    for (int e = tid; e < kP * kP / 2; e += kSolveThreads) {
+        const int jj = e / (kP / 2), k2 = (e % (kP / 2)) * 2;
+        const float2 x = *reinterpret_cast<const float2 *>(&Sn[jj * kSP + k2]);
+        const float h0 = round_to_tf32(x.x), h1 = round_to_tf32(x.y);
+        *reinterpret_cast<float2 *>(&Rp[jj * kP + k2]) = make_float2(h0, h1);
+        *reinterpret_cast<float2 *>(&Rp[kP * kP + jj * kP + k2]) =
+            make_float2(round_to_tf32(x.x - h0), round_to_tf32(x.y - h1));
     }
 }
 
-// load a 64 x 64 fp32 tile (row-major, pitch 64) into shared memory with pitch kQ
-__device__ __forceinline__ void load_tile64(float *dst, const float *src, int tid) {
-    for (int e = tid; e < kP * kP / 4; e += 256) {
-        const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
-        *reinterpret_cast<float4 *>(&dst[i * kQ + j4]) = *reinterpret_cast<const float4 *>(&src[i * kP + j4]);
-    }
-}
-
-// One round's rotations, applied in one pass:
-//  * A tiles (p1 <= p2): A'[p1,p2] = R1^T A[p1,p2] R2, also written transposed
-//    into [p2,p1] (A stays symmetric, so only the upper triangle is computed);
-//  * Q slabs (64 rows x pair p): Q' = Q R_p.
-// Every item reads only what the previous round left and writes disjoint elements.
-__global__ void __launch_bounds__(256)
-jacobi_apply_kernel(const JacBatch jb) {
-    __shared__ __align__(16) float T0[kP * kQ];
-    __shared__ __align__(16) float T1[kP * kQ];
-    __shared__ __align__(16) float T2[kP * kQ];
-    const int tid = threadIdx.x, ti = tid / 16, tj = tid % 16;
-    const int total_a = jb.row_off[jb.count];
-    int item = blockIdx.x;
-    {
-        const int job = find_job(jb.row_off, jb.count, item);
-        if (!jb.active[job]) return;
-        const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
-        int local = item - jb.row_off[job];
-        // local -> (p1, p2) with p1 <= p2, row by row of the upper triangle
-        int p1 = 0;
-        while (local >= np - p1) {
-            local -= np - p1;
-            ++p1;
-        }
-        const int p2 = p1 + local;
-        float *A = jb.A[job];
-        const float *R1 = jb.R[job] + (size_t)p1 * kP * kP;
-        const float *R2 = jb.R[job] + (size_t)p2 * kP * kP;
-        load_tile64(T0, R1, tid);  // T0[k][i] = R1[k][i]
-        // T1[k][j] = A[g1(k)][g2(j)] (rows of pair p1, columns of pair p2)
-        for (int e = tid; e < kP * kP / 4; e += 256) {
-            const int k = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
-            *reinterpret_cast<float4 *>(&T1[k * kQ + j4]) = *reinterpret_cast<const float4 *>(
-                &A[(size_t)pair_index(nb, round, p1, k) * Np + pair_index(nb, round, p2, j4)]);
-        }
-        __syncthreads();
-        float acc[4][4];
-        tile_product_kt(T0, T1, ti, tj, acc);  // Y = R1^T X  (Y[i][j])
-        __syncthreads();
-        // store Y transposed: T1[j][i] = Y[i][j]  (so the next product is k-major in j)
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) T1[(4 * tj + b) * kQ + 4 * ti + a] = acc[a][b];
-        load_tile64(T2, R2, tid);  // T2[k][j] = R2[k][j]
-        __syncthreads();
-        // Z[i][j] = sum_k Y[i][k] R2[k][j] = sum_k T1[k][i] T2[k][j]
-        tile_product_kt(T1, T2, ti, tj, acc);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int gi = pair_index(nb, round, p1, 4 * ti + a);
-            *reinterpret_cast<float4 *>(&A[(size_t)gi * Np + pair_index(nb, round, p2, 4 * tj)]) =
-                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        }
-        if (p1 != p2) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int gj = pair_index(nb, round, p2, 4 * tj + b);
-                *reinterpret_cast<float4 *>(&A[(size_t)gj * Np + pair_index(nb, round, p1, 4 * ti)]) =
-                    make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
-            }
-        }
-    }
-}
-
-// Q slab of round k (64 rows x pair p, Q' = Q R_p) computed by 256 threads
-// (`tid` in 0..255) that synchronise on their own named barrier `bar`.
-__device__ void q_slab(const JacBatch &jb, int item, int tid, int bar, float *T1, float *T2) {
-    const int ti = tid / 16, tj = tid % 16;
-    const int job = find_job(jb.q_off, jb.count, item);
-    const bool live = jb.active[job] != 0;
-    const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job], np = Np / kP;
-    const int local = item - jb.q_off[job];
-    const int r0 = (local / np) * kP, pair = local % np;
-    float *Qm = jb.Q[job];
-    if (live) {
-        const float *R = jb.R[job] + (size_t)pair * kP * kP;
-        for (int e = tid; e < kP * kP / 4; e += 256) {
-            const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
-            *reinterpret_cast<float4 *>(&T2[i * kQ + j4]) = *reinterpret_cast<const float4 *>(&R[i * kP + j4]);
-        }
-        // T1[l][rr] = Q[r0 + rr][g(l)]  (transposed so the product is k-major in rr)
-        for (int e = tid; e < kP * kP / 4; e += 256) {
-            const int rr = e % kP, l4 = (e / kP) * 4;
-            const float4 v = *reinterpret_cast<const float4 *>(&Qm[(size_t)(r0 + rr) * Np + pair_index(nb, round, pair, l4)]);
-            T1[(l4 + 0) * kQ + rr] = v.x;
-            T1[(l4 + 1) * kQ + rr] = v.y;
-            T1[(l4 + 2) * kQ + rr] = v.z;
-            T1[(l4 + 3) * kQ + rr] = v.w;
-        }
-    }
-    asm volatile("bar.sync %0, 256;" ::"r"(bar) : "memory");
-    if (!live) return;
-    float acc[4][4];
-    tile_product_kt(T1, T2, ti, tj, acc);  // (Q R)[rr][j]
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-        *reinterpret_cast<float4 *>(&Qm[(size_t)(r0 + 4 * ti + a) * Np + pair_index(nb, round, pair, 4 * tj)]) =
-            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-}
-
-constexpr size_t kQSolveSmem = kSolveSmem > 2 * (size_t)kP * kQ * 4 ? kSolveSmem : 2 * (size_t)kP * kQ * 4;
-
-// One launch per round boundary: the subproblem solves of round k+1 (CTAs
-// 0 .. solve_grid-1, dispatched first: they are the critical path) and the Q
-// slabs of round k (the remaining CTAs) fill the machine together.  Both read
-// the A that round k's apply left; the solves write the other rotation buffer.
-static_assert(kSolveThreads == 256, "one Q slab per CTA");
+// Subproblem solves of one round: one CTA per pair.
 __global__ void __launch_bounds__(kSolveThreads)
-jacobi_q_solve_kernel(const JacBatch jq, const JacBatch js, int solve_grid, int inner_sweeps) {
-    extern __shared__ __align__(16) unsigned char qs_smem[];
-    if ((int)blockIdx.x < solve_grid) {
-        solve_pair(js, blockIdx.x, inner_sweeps, qs_smem);
-    } else {
-        float *T1 = reinterpret_cast<float *>(qs_smem);
-        float *T2 = T1 + kP * kQ;
-        q_slab(jq, blockIdx.x - solve_grid, threadIdx.x, 1, T1, T2);
-    }
+jacobi_solve_kernel(const JacBatch js, int inner_sweeps) {
+    extern __shared__ __align__(16) unsigned char solve_smem[];
+    solve_pair(js, blockIdx.x, inner_sweeps, solve_smem);
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -531,12 +364,23 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
+namespace {
+
+int64_t padded_order(int r) { return ((int64_t)(r + kNpAlign - 1) / kNpAlign) * kNpAlign; }
+
+constexpr int kMaps = 5;                         // A, B^T (two boxes), Q, rotations
+constexpr int64_t kMapFloats = kMaps * 32 + 32;  // 128-byte maps + 128-byte alignment slack
+
+}  // namespace
+
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
-    const int64_t Np = ((r + kP - 1) / kP) * kP;
-    // A, Qacc, two rotation buffers (Np/64 x 64 x 64 each), short factor + scratch (2 r^2), long factor P
-    // (L r), s_raw, inv_s, order (int), 2 doubles
-    return (size_t)(2 * Np * Np + 2 * Np * kP + 2 * (int64_t)r * r + (int64_t)L * r + 3 * r + 8);
+    const int64_t Np = padded_order(r);
+    // A, Qacc, B^T (Np^2 each), kRing rotation slots (Np/64 pairs x R^T hi/lo, 64 x 64 each),
+    // TMA maps, short factor + scratch (2 r^2), long factor P (L r), s_raw, inv_s,
+    // order (int), 2 doubles
+    return (size_t)(3 * Np * Np + kRing * (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
+                    (int64_t)L * r + 3 * r + 8);
 }
 
 namespace {
@@ -545,7 +389,8 @@ struct JobBufs {
     int r, Np, nb;
     int64_t L;
     bool tall;
-    float *A, *Qacc, *R, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    float *A, *Qacc, *BT, *Rt, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    CUtensorMap *maps;  // device: A, B^T (32 x 128 box), B^T (32 x 32 box), Q, R^T
     int *order;
     double *norms;
 };
@@ -555,12 +400,16 @@ JobBufs carve(const SvdJob &a) {
     b.tall = a.m >= a.n;
     b.r = b.tall ? a.n : a.m;
     b.L = b.tall ? a.m : a.n;
-    b.Np = ((b.r + kP - 1) / kP) * kP;
+    b.Np = (int)padded_order(b.r);
     b.nb = b.Np / kB;
+    const size_t NN = (size_t)b.Np * b.Np;
     b.A = a.work;
-    b.Qacc = b.A + (size_t)b.Np * b.Np;
-    b.R = b.Qacc + (size_t)b.Np * b.Np;
-    b.Sf = b.R + (size_t)2 * b.Np * kP;
+    b.Qacc = b.A + NN;
+    b.BT = b.Qacc + NN;
+    b.Rt = b.BT + NN;
+    float *mp = b.Rt + (size_t)kRing * (b.Np / kP) * 2 * kP * kP;
+    b.maps = reinterpret_cast<CUtensorMap *>((reinterpret_cast<uintptr_t>(mp) + 127) & ~uintptr_t(127));
+    b.Sf = mp + kMapFloats;
     b.Tmp = b.Sf + (size_t)b.r * b.r;
     b.P = b.Tmp + (size_t)b.r * b.r;
     b.s_raw = b.P + (size_t)b.L * b.r;
@@ -568,6 +417,21 @@ JobBufs carve(const SvdJob &a) {
     b.order = reinterpret_cast<int *>(b.inv_s + b.r);
     b.norms = reinterpret_cast<double *>((reinterpret_cast<uintptr_t>(b.order + b.r) + 15) & ~uintptr_t(15));
     return b;
+}
+
+// TMA maps of one matrix's Jacobi tensors, encoded on the host and copied to
+// the workspace (the rotation kernel reads them from device memory)
+int upload_maps(const JobBufs &b, cudaStream_t st) {
+    CUtensorMap h[kMaps];
+    int rc;
+    const int64_t rot_rows = (int64_t)kRing * (b.Np / kP) * 2 * kP;
+    if ((rc = make_tmap_2d(&h[0], b.A, b.Np, b.Np, b.Np, kB, 128))) return rc;
+    if ((rc = make_tmap_2d(&h[1], b.BT, b.Np, b.Np, b.Np, kB, 128))) return rc;
+    if ((rc = make_tmap_2d(&h[2], b.BT, b.Np, b.Np, b.Np, kB, 32))) return rc;
+    if ((rc = make_tmap_2d(&h[3], b.Qacc, b.Np, b.Np, b.Np, kB, 128))) return rc;
+    if ((rc = make_tmap_2d(&h[4], b.Rt, rot_rows, kP, kP, kB, kP))) return rc;
+    SPECOPTIM_CUDA(cudaMemcpyAsync(b.maps, h, sizeof(h), cudaMemcpyHostToDevice, st));
+    return SPECOPTIM_OK;
 }
 
 // Gram matrix of the short side into the padded A, and the starting basis:
@@ -656,21 +520,46 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
 
 }  // namespace
 
-int set_solve_attributes() {
-    constexpr int kMaxDevices = 64;
-    static std::mutex mu;
-    static bool done[kMaxDevices] = {false};
-    int dev = 0;
-    SPECOPTIM_CUDA(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= kMaxDevices) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: device ordinal out of range");
-    std::lock_guard<std::mutex> lk(mu);
-    if (!done[dev]) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_q_solve_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSolveSmem));
-        done[dev] = true;
+// Streams and events of one refresh call's Jacobi loop: `hi` carries the
+// critical chain (rotation of A, subproblem solves, convergence checks) at the
+// highest stream priority, `lo` the accumulation of Q at the lowest.  The
+// rotation slot of round g is g % kRing; solved / consumed mark when the
+// solves wrote a slot and when the Q update has read it.  Created per call (a
+// few tens of microseconds against a refresh of many milliseconds), so
+// concurrent refreshes on different streams stay independent; destroyed when
+// the call returns (the driver releases them once their work completes).
+struct JacStreams {
+    cudaStream_t hi = nullptr, lo = nullptr;
+    cudaEvent_t solved[kRing] = {}, consumed[kRing] = {}, sync_ev = nullptr;
+    ~JacStreams() {
+        for (int k = 0; k < kRing; ++k) {
+            if (solved[k]) cudaEventDestroy(solved[k]);
+            if (consumed[k]) cudaEventDestroy(consumed[k]);
+        }
+        if (sync_ev) cudaEventDestroy(sync_ev);
+        if (hi) cudaStreamDestroy(hi);
+        if (lo) cudaStreamDestroy(lo);
     }
-    return SPECOPTIM_OK;
-}
+    int create() {
+        static std::once_flag attr_once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(attr_once, [] {
+            attr_err = cudaFuncSetAttribute(jacobi_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kSolveSmem);
+        });
+        SPECOPTIM_CUDA(attr_err);
+        int least = 0, greatest = 0;
+        SPECOPTIM_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+        for (int k = 0; k < kRing; ++k) {
+            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&solved[k], cudaEventDisableTiming));
+            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&consumed[k], cudaEventDisableTiming));
+        }
+        SPECOPTIM_CUDA(cudaEventCreateWithFlags(&sync_ev, cudaEventDisableTiming));
+        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least));
+        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest));
+        return SPECOPTIM_OK;
+    }
+};
 
 int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     if (count < 1 || count > kMaxBatch)
@@ -687,62 +576,82 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     std::memset(&jb, 0, sizeof(jb));
     jb.count = count;
     int max_sweeps = 1, rounds = 1;
+    CtJob pass1[kMaxBatch], pass2[kMaxBatch], qjob[kMaxBatch];
     for (int i = 0; i < count; ++i) {
+        if ((rc = upload_maps(b[i], st))) return rc;
         jb.A[i] = b[i].A;
-        jb.Q[i] = b[i].Qacc;
-        jb.R[i] = b[i].R;
         jb.Np[i] = b[i].Np;
         jb.active[i] = 1;
-        const int pairs = b[i].Np / kP;
-        jb.pair_off[i + 1] = jb.pair_off[i] + pairs;
-        jb.row_off[i + 1] = jb.row_off[i] + pairs * (pairs + 1) / 2;  // A tiles p1 <= p2
-        jb.q_off[i + 1] = jb.q_off[i] + pairs * pairs;                // Q slabs
+        jb.pair_off[i + 1] = jb.pair_off[i] + b[i].Np / kP;
         max_sweeps = std::max(max_sweeps, jobs[i].max_sweeps);
         rounds = std::max(rounds, b[i].nb - 1);
+        const CUtensorMap *m = b[i].maps;
+        // B^T = (A R)^T, then A' = B^T R = R^T A R (A symmetric) and Q' = Q R
+        pass1[i] = CtJob{&m[0], &m[2], &m[4], b[i].Np, 0, 0, 1, 1};
+        pass2[i] = CtJob{&m[1], &m[0], &m[4], b[i].Np, 0, 0, 0, 1};
+        qjob[i] = CtJob{&m[3], &m[3], &m[4], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
-    const int apply_grid = jb.row_off[count];
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
-    int rc2 = set_solve_attributes();
+    JacStreams streams;
+    JacStreams *jst = &streams;
+    int rc2 = streams.create();
     if (rc2) return rc2;
-    // rotations of round g live in buffer g % 2
-    auto set_round = [&](JacBatch &x, long g) {
+    cudaStream_t hi = jst->hi, lo = jst->lo;
+    auto set_round = [&](long g) {
         for (int i = 0; i < count; ++i) {
-            x.round[i] = (int)(g % (b[i].nb - 1));
-            x.R[i] = b[i].R + (size_t)(g % 2) * b[i].Np * kP;
+            const int round = (int)(g % (b[i].nb - 1)), slot = (int)(g % kRing);
+            jb.round[i] = round;
+            jb.R[i] = b[i].Rt + (size_t)slot * (b[i].Np / kP) * 2 * kP * kP;
+            for (CtJob *c : {&pass1[i], &pass2[i], &qjob[i]}) {
+                c->round = round;
+                c->slot = slot;
+                c->active = jb.active[i];
+            }
         }
     };
-    JacBatch js = jb, jq = jb;
+    // both chains start after the caller's stream (Gram, start basis, maps)
+    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, st));
+    SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, jst->sync_ev, 0));
+    SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, jst->sync_ev, 0));
+    for (int k = 0; k < kRing; ++k) SPECOPTIM_CUDA(cudaEventRecord(jst->consumed[k], lo));
+    // solves of round gg write slot gg % kRing once Q of round gg - kRing has read it
+    auto solve = [&](long gg) -> int {
+        set_round(gg);
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, jst->consumed[gg % kRing], 0));
+        SPCO_LAUNCH("svd_jacobi_solve", hi, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, hi>>>(jb, inner));
+        SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
+        SPECOPTIM_CUDA(cudaEventRecord(jst->solved[gg % kRing], hi));
+        return SPECOPTIM_OK;
+    };
     std::vector<double> host(2 * count);
     int active = count;
     long g = 0;
-    // round 0's solves alone (no Q slabs yet)
-    set_round(js, 0);
-    SPCO_LAUNCH("svd_jacobi_q_solve", st, jacobi_q_solve_kernel<<<solve_grid, kSolveThreads, kQSolveSmem, st>>>(jq, js, solve_grid, inner));
+    if ((rc2 = solve(0))) return rc2;
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
-            set_round(jb, g);
-            SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<apply_grid, 256, 0, st>>>(jb));
-            // Q with round g's rotations, with the active set of this apply
-            set_round(jq, g);
-            set_round(js, g + 1);
-            SPCO_LAUNCH("svd_jacobi_q_solve", st,
-                        jacobi_q_solve_kernel<<<solve_grid + jq.q_off[count], kSolveThreads, kQSolveSmem, st>>>(
-                            jq, js, solve_grid, inner));
+            set_round(g);
+            if ((rc2 = jacobi_rotate(pass1, count, hi))) return rc2;
+            if ((rc2 = jacobi_rotate(pass2, count, hi))) return rc2;
+            // Q of round g, with the same active set, beside the next solves
+            SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, jst->solved[g % kRing], 0));
+            if ((rc2 = jacobi_rotate(qjob, count, lo))) return rc2;
+            SPECOPTIM_CUDA(cudaEventRecord(jst->consumed[g % kRing], lo));
+            if ((rc2 = solve(g + 1))) return rc2;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             jobs[i].sweeps = sweep + 1;
-            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), st));
+            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), hi));
             const int64_t NN = (int64_t)b[i].Np * b[i].Np;
-            SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b[i].A, b[i].Np, b[i].norms));
+            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<grid_for(NN, 256), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
             SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
-                                           cudaMemcpyDeviceToHost, st));
+                                           cudaMemcpyDeviceToHost, hi));
         }
         SPECOPTIM_LAUNCHED("offnorm_kernel");
-        SPECOPTIM_CUDA(cudaStreamSynchronize(st));
+        SPECOPTIM_CUDA(cudaStreamSynchronize(hi));
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             const double tol = jobs[i].tol;
@@ -754,11 +663,16 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
                 jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
             }
             if (!now_active) {
-                jb.active[i] = js.active[i] = jq.active[i] = 0;
+                jb.active[i] = 0;
                 --active;
             }
         }
     }
+    // the caller's stream resumes once both chains are done
+    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, lo));
+    SPECOPTIM_CUDA(cudaStreamWaitEvent(st, jst->sync_ev, 0));
+    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, hi));
+    SPECOPTIM_CUDA(cudaStreamWaitEvent(st, jst->sync_ev, 0));
     int first_bad = SPECOPTIM_OK;
     for (int i = 0; i < count; ++i) {
         if (jb.active[i]) jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
