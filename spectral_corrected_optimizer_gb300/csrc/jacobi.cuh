@@ -43,7 +43,8 @@ __host__ __device__ __forceinline__ int pair_index(int nb, int round, int p, int
 // row-major fp32 blocks, hi then lo) at row ((slot * Np/64 + p) * 2) * 64 of
 // the rotation tensor.  All three tensors are reached through TMA maps that
 // live in device memory: `in` and `out` with boxes of 32 columns x 128 rows
-// (transposed output: 32 x 32), `rot` with 32 x 64.
+// (transposed output: 32 x 32), `rot` with 32 x 64.  OUT may be IN itself
+// (every task reads and writes only its own slab and pair).
 struct CtJob {
     const CUtensorMap *in, *out, *rot;
     int Np, round, slot, transposed, active;

@@ -1,18 +1,22 @@
 // Rotation kernel of the block-Jacobi eigen-solver on the tcgen05 tensor cores.
 //
-// One CTA (4 warps) per task = (matrix, 128-row slab, pair p):
+// Task = (matrix, 128-row slab, pair p):
 //   X (128 x 64)  = IN[slab rows, cols(p)]        two TMA boxes of 32 columns
 //   R_p^T hi / lo (64 x 64 each)                  four TMA boxes
 //   X is split in shared memory into hi = rna_tf32(x) and lo = rna_tf32(x - hi)
 //   (element-wise, so the 128-byte swizzle of the TMA layout is kept), then one
 //   thread issues 24 tcgen05.mma (M = 128, N = 64, K = 8) into a 64-column TMEM
 //   accumulator:  D = Xhi.Rhi + Xhi.Rlo + Xlo.Rhi  (3xTF32, fp32-accurate, the
-//   lo.lo term is below fp32 rounding).
-//   The 4 warps read D back (tcgen05.ld, one row per thread), stage it in the
-//   shared memory of X in the swizzled box layout (as is, or transposed), and
-//   one thread stores it with TMA.
-// Every mbarrier wait is bounded; a wait that gives up records a code in the
-// library's device flag and the CTA skips the rest of its work (TMEM is freed).
+//   lo.lo term is below fp32 rounding).  D is staged in shared memory in the
+//   box layout of the output (as is, or transposed) and stored with TMA.
+// One persistent CTA per SM takes a contiguous range of tasks, with warp roles:
+//   warp 0      TMA producer into a two-stage ring (X, R hi, R lo, X lo per stage)
+//   warp 1      TMEM (two 64-column accumulators) and the MMA issuer
+//   warps 2-5   split X of the next stage into hi / lo
+//   warps 6-9   epilogue: tcgen05.ld of their lane quarter, staging, TMA store
+// so the loads of task i+1, the split of task i+1, the MMAs of task i and the
+// stores of task i-1 overlap.  Every mbarrier wait is bounded; a wait that
+// gives up records a code in the library's device flag and the role stops.
 #include <algorithm>
 #include <cstring>
 
@@ -24,20 +28,61 @@ namespace spco {
 namespace {
 
 constexpr int kCtRows = 128;                    // slab rows = MMA M
-constexpr int kCtThreads = 128;
+constexpr int kCtThreads = 320;
+constexpr int kStages = 2;
 constexpr uint32_t kXAtom = kCtRows * 128;      // 32 columns x 128 rows of fp32: 16 KB
 constexpr uint32_t kXBytes = 2 * kXAtom;        // the 64 columns of a pair
 constexpr uint32_t kRAtom = kP * 128;           // 32 columns x 64 rows: 8 KB
 constexpr uint32_t kRBytes = 2 * kRAtom;        // one part (hi or lo) of R_p^T
-constexpr uint32_t kTmemCols = 64;
-constexpr size_t kCtSmem = 2 * (size_t)kXBytes + 2 * (size_t)kRBytes + 1024 /*align*/ + 64;
+constexpr uint32_t kLoadBytes = kXBytes + 2 * kRBytes;   // X raw + R hi + R lo
+constexpr uint32_t kStageBytes = kLoadBytes + kXBytes;   // + X lo
+constexpr uint32_t kTmemCols = 128;                      // two accumulators
+// stages, output staging (one 128 x 64 tile), barriers
+constexpr size_t kCtSmem = (size_t)kStages * kStageBytes + kXBytes + 1024 /*align*/ + 128;
+static_assert(kCtSmem <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kCtIdesc = tf32_idesc(kCtRows, kP);
 
 struct CtBatch {
     int count;
+    int total;
     CtJob job[kCtMaxJobs];
     int task_off[kCtMaxJobs + 1];
 };
+
+// task t of the batch: matrix j, then pair-major with the slab fastest, so a
+// CTA's contiguous range reuses one R_p (L2-hot) across consecutive tasks
+struct CtTask {
+    const CtJob *job;
+    int slab, blk_a, blk_b, rrow;
+};
+
+__device__ __forceinline__ CtTask ct_task(const CtBatch &cb, int t) {
+    int j = 0;
+    while (j + 1 < cb.count && t >= cb.task_off[j + 1]) ++j;
+    CtTask k;
+    k.job = &cb.job[j];
+    const int np = k.job->Np / kP, nb = k.job->Np / kB, ns = k.job->Np / kCtRows;
+    const int local = t - cb.task_off[j];
+    k.slab = local % ns;
+    const int pair = local / ns;
+    rr_pair(nb, k.job->round, pair, k.blk_a, k.blk_b);
+    k.rrow = (k.job->slot * np + pair) * 2 * kP;
+    return k;
+}
+
+// loads X of task k into `stage`, and R_p^T hi / lo unless the stage already
+// holds them (same rotation tensor and row)
+__device__ __forceinline__ void ct_load(const CtTask &k, unsigned char *stage, uint64_t *bar, bool with_r) {
+    unsigned char *x = stage, *rh = stage + kXBytes, *rl = rh + kRBytes;
+    mbar_arrive_expect_tx(bar, with_r ? kLoadBytes : kXBytes);
+    tma_load_2d(x, k.job->in, k.blk_a * kB, k.slab * kCtRows, bar);
+    tma_load_2d(x + kXAtom, k.job->in, k.blk_b * kB, k.slab * kCtRows, bar);
+    if (!with_r) return;
+    tma_load_2d(rh, k.job->rot, 0, k.rrow, bar);
+    tma_load_2d(rh + kRAtom, k.job->rot, kB, k.rrow, bar);
+    tma_load_2d(rl, k.job->rot, 0, k.rrow + kP, bar);
+    tma_load_2d(rl + kRAtom, k.job->rot, kB, k.rrow + kP, bar);
+}
 
 __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo) {
     float4 h;
@@ -52,34 +97,38 @@ __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo) {
     return h;
 }
 
-__global__ void __launch_bounds__(kCtThreads)
+__global__ void __launch_bounds__(kCtThreads, 1)
 jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char ct_smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(ct_smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *xh = smem, *xl = smem + kXBytes;
-    unsigned char *rh = smem + 2 * kXBytes, *rl = rh + kRBytes;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(rl + kRBytes);  // [0] loads, [1] MMAs
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *full = bars;                 // [kStages] TMA landed
+    uint64_t *split = full + kStages;      // [kStages] X split (128 arrivals)
+    uint64_t *empty = split + kStages;     // [kStages] MMAs done with the stage
+    uint64_t *tfull = empty + kStages;     // [2] accumulator ready
+    uint64_t *tempty = tfull + 2;          // [2] accumulator read (128 arrivals)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
 
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    int j = 0;
-    while (j + 1 < cb.count && (int)blockIdx.x >= cb.task_off[j + 1]) ++j;
-    const CtJob &job = cb.job[j];
-    if (!job.active) return;  // whole CTA
-    const int np = job.Np / kP, nb = job.Np / kB;
-    const int local = (int)blockIdx.x - cb.task_off[j];
-    const int slab = local / np, pair = local % np;
-    int blk_a, blk_b;
-    rr_pair(nb, job.round, pair, blk_a, blk_b);
-    const int row0 = slab * kCtRows;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // this CTA's contiguous task range
+    const int per = cb.total / (int)gridDim.x, extra = cb.total % (int)gridDim.x;
+    const int t0 = (int)blockIdx.x * per + min((int)blockIdx.x, extra);
+    const int n = per + ((int)blockIdx.x < extra ? 1 : 0);
 
-    if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&split[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(tslot, kTmemCols);
         tmem_relinquish();
     }
@@ -88,96 +137,136 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[0], kXBytes + 2 * kRBytes);
-        tma_load_2d(xh, job.in, blk_a * kB, row0, &bar[0]);
-        tma_load_2d(xh + kXAtom, job.in, blk_b * kB, row0, &bar[0]);
-        const int rrow = (job.slot * np + pair) * 2 * kP;
-        tma_load_2d(rh, job.rot, 0, rrow, &bar[0]);
-        tma_load_2d(rh + kRAtom, job.rot, kB, rrow, &bar[0]);
-        tma_load_2d(rl, job.rot, 0, rrow + kP, &bar[0]);
-        tma_load_2d(rl + kRAtom, job.rot, kB, rrow + kP, &bar[0]);
-    }
-    bool ok = mbar_wait_bounded(&bar[0], 0, flag, 0x201u);
-    ok = __syncthreads_and(ok) != 0;
-    if (ok) {
-        float4 *h4 = reinterpret_cast<float4 *>(xh), *l4 = reinterpret_cast<float4 *>(xl);
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int i = 0;
+            const CUtensorMap *held_map[kStages] = {nullptr, nullptr};
+            int held_row[kStages] = {-1, -1};
+            for (; i < n; ++i) {
+                const int s = i % kStages;
+                if (!mbar_wait_bounded(&empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, flag, 0x201u)) break;
+                const CtTask k = ct_task(cb, t0 + i);
+                const bool with_r = held_map[s] != k.job->rot || held_row[s] != k.rrow;
+                held_map[s] = k.job->rot;
+                held_row[s] = k.rrow;
+                ct_load(k, smem + s * kStageBytes, &full[s], with_r);
+            }
+            if (i < n)  // gave up: let the loads already issued land before the CTA exits
+                for (int q = (i > kStages ? i - kStages : 0); q < i; ++q)
+                    mbar_wait_bounded(&full[q % kStages], (uint32_t)(q / kStages) & 1u, flag, 0x205u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int i = 0;
+            for (; i < n; ++i) {
+                const int s = i % kStages, a = i & 1;
+                if (!mbar_wait_bounded(&split[s], (uint32_t)(i / kStages) & 1u, flag, 0x202u)) break;
+                if (!mbar_wait_bounded(&tempty[a], ((uint32_t)(i >> 1) & 1u) ^ 1u, flag, 0x203u)) break;
+                tc_fence_after();
+                unsigned char *st = smem + s * kStageBytes;
+                const uint32_t a_hi = smem_u32(st), b_hi = a_hi + kXBytes, b_lo = b_hi + kRBytes,
+                               a_lo = a_hi + kLoadBytes;
+                const uint32_t as[3] = {a_hi, a_hi, a_lo}, bs[3] = {b_hi, b_lo, b_hi};
+                const uint32_t d = tmem + (uint32_t)(a * kP);
+                uint32_t acc = 0;
+#pragma unroll
+                for (int u = 0; u < 3; ++u)
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            mma_tf32(d, smem_desc_sw128(as[u] + kk * kXAtom + q * 32),
+                                     smem_desc_sw128(bs[u] + kk * kRAtom + q * 32), kCtIdesc, acc);
+                            acc = 1;
+                        }
+                mma_commit(&empty[s]);  // stage free once these MMAs have read it
+                mma_commit(&tfull[a]);  // accumulator ready once they completed
+            }
+            if (i < n && i > 0)  // gave up: the last MMAs issued finish before TMEM is freed
+                mbar_wait_bounded(&tfull[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u, flag, 0x206u);
+        }
+    } else if (warp < 6) {
+        // ---------------- split X into hi (in place) and lo
+        const int tid = threadIdx.x - 64;
+        for (int i = 0; i < n; ++i) {
+            const int s = i % kStages;
+            if (!mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, flag, 0x204u)) break;
+            unsigned char *st = smem + s * kStageBytes;
+            float4 *h4 = reinterpret_cast<float4 *>(st), *l4 = reinterpret_cast<float4 *>(st + kLoadBytes);
 #pragma unroll 4
-        for (int e = tid; e < (int)(kXBytes / 16); e += kCtThreads) {
-            float4 lo;
-            h4[e] = split_hi(h4[e], lo);
-            l4[e] = lo;
+            for (int e = tid; e < (int)(kXBytes / 16); e += 128) {
+                float4 lo;
+                h4[e] = split_hi(h4[e], lo);
+                l4[e] = lo;
+            }
+            fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+            mbar_arrive(&split[s]);
         }
-    }
-    fence_proxy_async_smem();  // the tensor core reads what these threads wrote
-    __syncthreads();
-    if (ok && tid == 0) {
-        tc_fence_after();
-        const uint32_t a_hi = smem_u32(xh), a_lo = smem_u32(xl), b_hi = smem_u32(rh), b_lo = smem_u32(rl);
-        const uint32_t as[3] = {a_hi, a_hi, a_lo}, bs[3] = {b_hi, b_lo, b_hi};
-        uint32_t acc = 0;
+    } else {
+        // ---------------- epilogue: TMEM lane quarter q = rows 32q .. 32q+31 of the slab,
+        // staged in the box layout of the output map, stored by TMA
+        const int q = warp % 4;
+        const bool leader = warp == 6 && lane == 0;
+        unsigned char *out = smem + kStages * kStageBytes;
+        for (int i = 0; i < n; ++i) {
+            const int a = i & 1;
+            if (!mbar_wait_bounded(&tfull[a], (uint32_t)(i >> 1) & 1u, flag, 0x207u)) break;
+            tc_fence_after();
+            float v[2][32];
+            const uint32_t taddr = tmem + (uint32_t)(a * kP) + ((uint32_t)(q * 32) << 16);
+            tmem_ld32(taddr, v[0]);
+            tmem_ld32(taddr + 32, v[1]);
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+            const CtTask k = ct_task(cb, t0 + i);
+            // the previous task's TMA store has finished reading the staging tile
+            if (leader) bulk_wait_read<0>();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const int r = q * 32 + lane;  // row within the slab
+            if (!k.job->transposed) {
+                // atom kk (32 columns), row r, 16-byte chunk c at c ^ (r % 8)
 #pragma unroll
-        for (int t = 0; t < 3; ++t)
+                for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4 *>(out + kk * kXAtom + r * 128 + ((c ^ (r & 7)) << 4)) =
+                            make_float4(v[kk][4 * c], v[kk][4 * c + 1], v[kk][4 * c + 2], v[kk][4 * c + 3]);
+            } else {
+                // output row jj (pair index), output column r: 32 x 32 boxes, box (q, jj / 32)
+                // at q * 8 KB + (jj / 32) * 4 KB
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    mma_tf32(tmem, smem_desc_sw128(as[t] + kk * kXAtom + s * 32),
-                             smem_desc_sw128(bs[t] + kk * kRAtom + s * 32), kCtIdesc, acc);
-                    acc = 1;
+                for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int jj = kk * 32 + c;
+                        *reinterpret_cast<float *>(out + q * (kP * 128) + jj * 128 +
+                                                   (((lane >> 2) ^ (jj & 7)) << 4) + (lane & 3) * 4) = v[kk][c];
+                    }
+            }
+            fence_proxy_async_smem();  // the TMA engine reads what these threads wrote
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (leader) {
+                const int row0 = k.slab * kCtRows;
+                if (!k.job->transposed) {
+                    tma_store_2d(k.job->out, out, k.blk_a * kB, row0);
+                    tma_store_2d(k.job->out, out + kXAtom, k.blk_b * kB, row0);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        tma_store_2d(k.job->out, out + w * (kP * 128), row0 + w * 32, k.blk_a * kB);
+                        tma_store_2d(k.job->out, out + w * (kP * 128) + 32 * 128, row0 + w * 32, k.blk_b * kB);
+                    }
                 }
-        mma_commit(&bar[1]);
-    }
-    if (ok) ok = mbar_wait_bounded(&bar[1], 0, flag, 0x202u);
-    ok = __syncthreads_and(ok) != 0;
-    tc_fence_after();
-    if (ok) {
-        // this thread's accumulator row: slab row `r`, 64 columns
-        const int r = warp * 32 + lane;
-        float v[2][32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), v[0]);
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32, v[1]);
-        // X's buffer is free (the MMAs completed): stage the result there
-        if (!job.transposed) {
-            // box layout of the load: atom kk, row r, 16-byte chunk c at c ^ (r % 8)
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(xh + kk * kXAtom + r * 128 + ((c ^ (r & 7)) << 4)) =
-                        make_float4(v[kk][4 * c], v[kk][4 * c + 1], v[kk][4 * c + 2], v[kk][4 * c + 3]);
-        } else {
-            // transposed: output row jj (0..63) = column jj of the pair, output
-            // column r; 32-row boxes, box (warp, jj / 32) at warp * 8 KB + (jj / 32) * 4 KB
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int jj = kk * 32 + i;
-                    *reinterpret_cast<float *>(xh + warp * (kP * 128) + jj * 128 +
-                                               (((lane >> 2) ^ (jj & 7)) << 4) + (lane & 3) * 4) = v[kk][i];
-                }
-        }
-    }
-    fence_proxy_async_smem();  // the TMA engine reads what these threads wrote
-    __syncthreads();
-    if (ok && tid == 0) {
-        if (!job.transposed) {
-            tma_store_2d(job.out, xh, blk_a * kB, row0);
-            tma_store_2d(job.out, xh + kXAtom, blk_b * kB, row0);
-        } else {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                tma_store_2d(job.out, xh + w * (kP * 128), row0 + w * 32, blk_a * kB);
-                tma_store_2d(job.out, xh + w * (kP * 128) + 32 * 128, row0 + w * 32, blk_b * kB);
+                bulk_commit();
             }
         }
-        bulk_commit();
-        bulk_wait_all();
+        if (leader) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -189,21 +278,26 @@ int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st) {
     if (count < 1 || count > kCtMaxJobs) return fail(SPECOPTIM_ERR_INVALID_ARG, "jacobi_rotate: 1 to 32 matrices");
     CtBatch cb;
     std::memset(&cb, 0, sizeof(cb));
-    cb.count = count;
     for (int i = 0; i < count; ++i) {
         if (jobs[i].Np % kNpAlign != 0 || jobs[i].Np < kNpAlign)
             return fail(SPECOPTIM_ERR_INVALID_ARG, "jacobi_rotate: Np must be a positive multiple of 128");
-        cb.job[i] = jobs[i];
-        cb.task_off[i + 1] = cb.task_off[i] + (jobs[i].Np / kCtRows) * (jobs[i].Np / kP);
+        if (!jobs[i].active) continue;  // converged matrices drop out of the task list
+        cb.job[cb.count] = jobs[i];
+        cb.task_off[cb.count + 1] = cb.task_off[cb.count] + (jobs[i].Np / kCtRows) * (jobs[i].Np / kP);
+        ++cb.count;
     }
+    if (cb.count == 0) return SPECOPTIM_OK;
+    cb.total = cb.task_off[cb.count];
     static bool attr = false;
     if (!attr) {
         SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_rotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)kCtSmem));
         attr = true;
     }
+    // one CTA per SM with at least two tasks each (the pipeline needs a few to fill)
+    const int grid = std::max(1, std::min(num_sms(), cb.total / 2));
     SPCO_LAUNCH("svd_jacobi_rotate", st,
-                jacobi_rotate_kernel<<<cb.task_off[count], kCtThreads, kCtSmem, st>>>(cb, device_flag_ptr()));
+                jacobi_rotate_kernel<<<grid, kCtThreads, kCtSmem, st>>>(cb, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("jacobi_rotate_kernel");
     return SPECOPTIM_OK;
 }
