@@ -61,8 +61,6 @@ __device__ __forceinline__ int find_job(const int *off, int count, int item) {
 }
 
 constexpr int kSolveThreads = 256;
-constexpr int kSP = kP + 2;  // pitch of S (66 spreads every access pattern below over the banks)
-constexpr int kRP = kP;      // pitch of the rotation accumulator
 
 // Rotation (c, s) of one pair with fast reciprocal / square-root intrinsics:
 // c^2 + s^2 = 1 to a few ulp, the same order as the correctly rounded form.
@@ -79,125 +77,145 @@ __device__ __forceinline__ void jacobi_cs_fast(float app, float aqq, float apq, 
     }
 }
 
+// The subproblem is kept in "position" order (the circle method of the
+// round-robin, with the data moving instead of the indices): positions k (top)
+// and 32 + k (bottom) form pair k in every step, and after a step the element
+// at position p moves to cat_next(p): top 0 stays, top k -> k + 1, top 31 ->
+// bottom 31, bottom k -> k - 1, bottom 0 -> top 1.  The other 63 positions form
+// one cycle, so any two indices meet exactly once in the 63 steps of a sweep
+// and a sweep ends in the order it started from.
+__host__ __device__ __forceinline__ int cat_next(int p) {
+    if (p == 0) return 0;
+    if (p < kB - 1) return p + 1;
+    if (p == kB - 1) return kP - 1;
+    if (p == kB) return 1;
+    return p - 1;
+}
+
+// Physical column of position c in a row of S: bottom positions are rotated by
+// two banks, so that for a fixed row the 32 lanes of a warp reading columns l
+// or 32 + l, or writing the moved columns cat_next(l) or cat_next(32 + l),
+// each touch 32 distinct banks (and so do the reads of the pair entries).
+__device__ __forceinline__ int sphys(int c) { return c < kB ? c : kB + ((c - kB + 2) & (kB - 1)); }
+
+constexpr int kSP = kP;  // row pitch of S (every row starts at bank 0)
+
 // One CTA (8 warps) per pair: load the 64 x 64 subproblem S, run up to
-// `inner_sweeps` cyclic Jacobi sweeps in parallel order (32 disjoint rotations
-// per step), and write the accumulated rotation R (64 x 64).
+// `inner_sweeps` cyclic Jacobi sweeps (32 disjoint rotations per step) and
+// write the accumulated rotation R (64 x 64), split for 3xTF32.
 //  * Every warp computes all 32 rotations of a step itself (lane l owns pair
-//    l), so there is no shared rotation table and no barrier before the updates.
-//  * S and R are double buffered (a step reads one copy and writes the other):
-//    one barrier per step.
-//  * S stays symmetric, so only the 2 x 2 blocks (pair ka, pair kb), ka < kb,
-//    are computed; each is written with its transpose.  Warp w takes the block
-//    rows r = w and r = w + 8 together with their partners 31 - r (31 blocks
-//    per row couple, one per lane 0..30).  The 32 diagonal blocks come from the
-//    rotations themselves (warp 0 writes them).
-//  * Lane l applies its own rotation to columns p_l, q_l of R in rows 8w .. 8w+7.
-constexpr size_t kSolveSmem = (2 * (size_t)kP * kSP + 2 * (size_t)kP * kRP) * 4 + 16;
+//    l), so the block updates need no barrier and no shared rotation table.
+//  * S is double buffered: a step reads one copy and writes the moved blocks
+//    into the other, so one barrier per step separates the steps.  Thread
+//    (warp w, lane l) updates the 2 x 2 blocks (pair w + 8u rows, pair l
+//    columns), u = 0..3, at loop-invariant addresses.
+//  * R lives in registers: thread (w, l) holds row 8w + l/4 of R, positions of
+//    pairs 8m .. 8m+7 (m = l % 4).  After the barrier of step t it applies the
+//    step's rotations (read from a two-slot table that warp 0 fills) and moves
+//    its values to the next positions, exchanging one value with each
+//    neighbouring quarter by shuffles.
+constexpr size_t kSolveSmem = (2 * (size_t)kP * kSP + 2 * 2 * (size_t)kB) * 4 + 16;
 
 __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsigned char *smem) {
     float *S = reinterpret_cast<float *>(smem);
     float *Sn = S + kP * kSP;
-    float *Q = Sn + kP * kSP;
-    float *Qn = Q + kP * kRP;
-    float *red = Qn + kP * kRP;
+    float2 *csb = reinterpret_cast<float2 *>(Sn + kP * kSP);  // [2][32] (c, s) of a step
+    float *red = reinterpret_cast<float *>(csb + 2 * kB);
     const int job = find_job(jb.pair_off, jb.count, item);
     if (!jb.active[job]) return;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
     const int pair = item - jb.pair_off[job];
     const float *A = jb.A[job];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // 64 rows x 16 float4 (each row of the subproblem is two runs of 32 floats)
+    // the subproblem in its start order (position = local index)
     for (int e = tid; e < kP * (kP / 4); e += kSolveThreads) {
         const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
         const float4 v = *reinterpret_cast<const float4 *>(
             &A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j4)]);
-        *reinterpret_cast<float2 *>(&S[i * kSP + j4]) = make_float2(v.x, v.y);
-        *reinterpret_cast<float2 *>(&S[i * kSP + j4 + 2]) = make_float2(v.z, v.w);
+        S[i * kSP + sphys(j4)] = v.x;
+        S[i * kSP + sphys(j4 + 1)] = v.y;
+        S[i * kSP + sphys(j4 + 2)] = v.z;
+        S[i * kSP + sphys(j4 + 3)] = v.w;
     }
-    for (int e = tid; e < kP * kP; e += kSolveThreads) Q[(e / kP) * kRP + e % kP] = (e / kP == e % kP) ? 1.f : 0.f;
-    __syncthreads();
-    // this lane's two blocks: (ka[u], kb[u]) for the row couples r = warp + 8u
-    int ka[2], kb[2];
+    // R = I in registers
+    const int ri = warp * 8 + (lane >> 2), m = lane & 3;
+    float rt[8], rb[8];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int r = warp + 8 * u;
-        if (lane < 31 - r) {
-            ka[u] = r;
-            kb[u] = r + 1 + lane;
-        } else {
-            ka[u] = 31 - r;
-            kb[u] = lane + 1;  // lane 31 gives kb = 32: no block
-        }
+    for (int q = 0; q < 8; ++q) {
+        rt[q] = ri == 8 * m + q ? 1.f : 0.f;
+        rb[q] = ri == kB + 8 * m + q ? 1.f : 0.f;
     }
+    // loop-invariant addresses: pair entries of pair `lane`, and this thread's blocks
+    const int cbot = sphys(kB + lane);
+    const int a_pp = lane * kSP + lane, a_qq = (kB + lane) * kSP + cbot, a_pq = lane * kSP + cbot;
+    const int wct = sphys(cat_next(lane)), wcb = sphys(cat_next(kB + lane));
+    int rd_t[4], rd_b[4], wr_t[4], wr_b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ka = warp + 8 * u;
+        rd_t[u] = ka * kSP;
+        rd_b[u] = (kB + ka) * kSP;
+        wr_t[u] = cat_next(ka) * kSP;
+        wr_b[u] = cat_next(kB + ka) * kSP;
+    }
+    __syncthreads();
     for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
         float offmax = 0.f, dmax = 0.f;
         for (int step = 0; step < kP - 1; ++step) {
-            // pair `lane` of this step (round-robin over 64 indices)
-            int p, q;
-            if (lane == 0) {
-                p = kP - 1;
-                q = step;
-            } else {
-                p = step + lane;
-                p = p >= kP - 1 ? p - (kP - 1) : p;
-                q = step - lane;
-                q = q < 0 ? q + (kP - 1) : q;
-            }
             float c, sn;
             {
-                const float app = S[p * kSP + p], aqq = S[q * kSP + q], apq = S[p * kSP + q];
+                const float app = S[a_pp], aqq = S[a_qq], apq = S[a_pq];
                 jacobi_cs_fast(app, aqq, apq, c, sn);
                 offmax = fmaxf(offmax, fabsf(apq));
                 dmax = fmaxf(dmax, fmaxf(fabsf(app), fabsf(aqq)));
-                if (warp == 0) {  // diagonal block of this pair: diag(J^T S J), decoupled
-                    const float cc = c * c, ss = sn * sn, cs2 = 2.f * c * sn * apq;
-                    Sn[p * kSP + p] = cc * app - cs2 + ss * aqq;
-                    Sn[q * kSP + q] = ss * app + cs2 + cc * aqq;
-                    Sn[p * kSP + q] = 0.f;
-                    Sn[q * kSP + p] = 0.f;
-                }
             }
-            const int pq = p | (q << 8);
+            if (warp == 0) csb[(step & 1) * kB + lane] = make_float2(c, sn);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int a = ka[u], b = kb[u] & 31;
-                const int pqa = __shfl_sync(0xffffffffu, pq, a), pqb = __shfl_sync(0xffffffffu, pq, b);
-                const float ca = __shfl_sync(0xffffffffu, c, a), sa = __shfl_sync(0xffffffffu, sn, a);
-                const float cb = __shfl_sync(0xffffffffu, c, b), sb = __shfl_sync(0xffffffffu, sn, b);
-                if (kb[u] < 32) {
-                    const int pa = pqa & 0xff, qa = pqa >> 8, pb = pqb & 0xff, qb = pqb >> 8;
-                    const float x11 = S[pa * kSP + pb], x12 = S[pa * kSP + qb];
-                    const float x21 = S[qa * kSP + pb], x22 = S[qa * kSP + qb];
-                    // rows: J_a^T X, then columns: (J_a^T X) J_b
-                    const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
-                    const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
-                    const float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
-                    const float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
-                    Sn[pa * kSP + pb] = z11;
-                    Sn[pa * kSP + qb] = z12;
-                    Sn[qa * kSP + pb] = z21;
-                    Sn[qa * kSP + qb] = z22;
-                    Sn[pb * kSP + pa] = z11;
-                    Sn[qb * kSP + pa] = z12;
-                    Sn[pb * kSP + qa] = z21;
-                    Sn[qb * kSP + qa] = z22;
-                }
-            }
-            // accumulator: columns p, q of rows 8 warp .. 8 warp + 7
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int i = 8 * warp + t;
-                const float x = Q[i * kRP + p], y = Q[i * kRP + q];
-                Qn[i * kRP + p] = c * x - sn * y;
-                Qn[i * kRP + q] = sn * x + c * y;
+            for (int u = 0; u < 4; ++u) {
+                const int ka = warp + 8 * u;
+                const float ca = __shfl_sync(0xffffffffu, c, ka), sa = __shfl_sync(0xffffffffu, sn, ka);
+                const float x11 = S[rd_t[u] + lane], x12 = S[rd_t[u] + cbot];
+                const float x21 = S[rd_b[u] + lane], x22 = S[rd_b[u] + cbot];
+                // rows: J_a^T X, then columns: (J_a^T X) J_b
+                const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
+                const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
+                float z12 = sn * y11 + c * y12, z21 = c * y21 - sn * y22;
+                if (ka == lane) z12 = z21 = 0.f;  // the rotated pair is now decoupled
+                Sn[wr_t[u] + wct] = c * y11 - sn * y12;
+                Sn[wr_t[u] + wcb] = z12;
+                Sn[wr_b[u] + wct] = z21;
+                Sn[wr_b[u] + wcb] = sn * y21 + c * y22;
             }
             __syncthreads();
             float *t1 = S;
             S = Sn;
             Sn = t1;
-            float *t2 = Q;
-            Q = Qn;
-            Qn = t2;
+            // R <- R J_step on this thread's pairs, then the positions move on
+            const float4 *cs4 = reinterpret_cast<const float4 *>(csb + (step & 1) * kB + 8 * m);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 w = cs4[h];
+                float x = rt[2 * h], y = rb[2 * h];
+                rt[2 * h] = w.x * x - w.y * y;
+                rb[2 * h] = w.y * x + w.x * y;
+                x = rt[2 * h + 1];
+                y = rb[2 * h + 1];
+                rt[2 * h + 1] = w.z * x - w.w * y;
+                rb[2 * h + 1] = w.w * x + w.z * y;
+            }
+            const float top_last = rt[7], bot_first = rb[0];
+            const float top_in = __shfl_up_sync(0xffffffffu, top_last, 1);     // quarter m-1, same row
+            const float bot_in = __shfl_down_sync(0xffffffffu, bot_first, 1);  // quarter m+1, same row
+#pragma unroll
+            for (int q = 7; q >= 1; --q) rt[q] = rt[q - 1];
+            if (m == 0) {
+                rt[1] = bot_first;  // bottom 0 -> top 1; top 0 stays (rt[0] unchanged)
+            } else {
+                rt[0] = top_in;
+            }
+#pragma unroll
+            for (int q = 0; q < 7; ++q) rb[q] = rb[q + 1];
+            rb[7] = m == 3 ? top_last : bot_in;  // top 31 -> bottom 31
         }
         // stop once no off-diagonal entry rotated in this sweep was above fp32 noise
         if (warp == 0) {
@@ -214,21 +232,25 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
         // red is rewritten only after the next sweep's barriers
         if (red[0] <= 1e-7f * red[1]) break;
     }
-    // R_p^T = hi + lo for the tensor-core rotation: R^T[j][k] = R[k][j] (Q holds R
-    // row-major); transposed through the free S buffer, then written row by row
-    for (int e = tid; e < kP * kP; e += kSolveThreads) {
-        const int jj = e % kP, k = e / kP;
-        Sn[jj * kSP + k] = Q[k * kRP + jj];
+    // R_p^T = hi + lo for the tensor-core rotation: R^T[j][k] = R[k][j].  R goes
+    // through shared memory (pitch 65, S is no longer read) so that both the
+    // staging and the row-wise writes of R^T are conflict-free and coalesced.
+    constexpr int kTP = kP + 1;
+    float *Rs = reinterpret_cast<float *>(smem);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        Rs[ri * kTP + 8 * m + q] = rt[q];
+        Rs[ri * kTP + kB + 8 * m + q] = rb[q];
     }
     __syncthreads();
     float *Rp = jb.R[job] + (size_t)pair * 2 * kP * kP;
     for (int e = tid; e < kP * kP / 2; e += kSolveThreads) {
         const int jj = e / (kP / 2), k2 = (e % (kP / 2)) * 2;
-        const float2 x = *reinterpret_cast<const float2 *>(&Sn[jj * kSP + k2]);
-        const float h0 = round_to_tf32(x.x), h1 = round_to_tf32(x.y);
+        const float x0 = Rs[k2 * kTP + jj], x1 = Rs[(k2 + 1) * kTP + jj];
+        const float h0 = round_to_tf32(x0), h1 = round_to_tf32(x1);
         *reinterpret_cast<float2 *>(&Rp[jj * kP + k2]) = make_float2(h0, h1);
         *reinterpret_cast<float2 *>(&Rp[kP * kP + jj * kP + k2]) =
-            make_float2(round_to_tf32(x.x - h0), round_to_tf32(x.y - h1));
+            make_float2(round_to_tf32(x0 - h0), round_to_tf32(x1 - h1));
     }
 }
 
