@@ -29,7 +29,6 @@ namespace {
 
 constexpr int kCtRows = 128;                    // slab rows = MMA M
 constexpr int kCtThreads = 320;
-constexpr int kStages = 2;
 constexpr uint32_t kXAtom = kCtRows * 128;      // 32 columns x 128 rows of fp32: 16 KB
 constexpr uint32_t kXBytes = 2 * kXAtom;        // the 64 columns of a pair
 constexpr uint32_t kRAtom = kP * 128;           // 32 columns x 64 rows: 8 KB
@@ -38,8 +37,9 @@ constexpr uint32_t kLoadBytes = kXBytes + 2 * kRBytes;   // X raw + R hi + R lo
 constexpr uint32_t kStageBytes = kLoadBytes + kXBytes;   // + X lo
 constexpr uint32_t kTmemCols = 128;                      // two accumulators
 // stages, output staging (one 128 x 64 tile), barriers
-constexpr size_t kCtSmem = (size_t)kStages * kStageBytes + kXBytes + 1024 /*align*/ + 128;
-static_assert(kCtSmem <= 232448, "shared memory budget of one CTA");
+constexpr size_t ct_smem(int stages) { return (size_t)stages * kStageBytes + kXBytes + 1024 /*align*/ + 128; }
+constexpr int kStages = 2;
+static_assert(ct_smem(2) <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kCtIdesc = tf32_idesc(kCtRows, kP);
 
 struct CtBatch {
@@ -97,16 +97,17 @@ __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo) {
     return h;
 }
 
+template <int STAGES>
 __global__ void __launch_bounds__(kCtThreads, 1)
 jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char ct_smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(ct_smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *full = bars;                 // [kStages] TMA landed
-    uint64_t *split = full + kStages;      // [kStages] X split (128 arrivals)
-    uint64_t *empty = split + kStages;     // [kStages] MMAs done with the stage
-    uint64_t *tfull = empty + kStages;     // [2] accumulator ready
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes);
+    uint64_t *full = bars;                 // [STAGES] TMA landed
+    uint64_t *split = full + STAGES;      // [STAGES] X split (128 arrivals)
+    uint64_t *empty = split + STAGES;     // [STAGES] MMAs done with the stage
+    uint64_t *tfull = empty + STAGES;     // [2] accumulator ready
     uint64_t *tempty = tfull + 2;          // [2] accumulator read (128 arrivals)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
 
@@ -117,7 +118,7 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
     const int n = per + ((int)blockIdx.x < extra ? 1 : 0);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&split[s], 128);
             mbar_init(&empty[s], 1);
@@ -141,11 +142,16 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
         if (lane == 0) {
             // ---------------- TMA producer
             int i = 0;
-            const CUtensorMap *held_map[kStages] = {nullptr, nullptr};
-            int held_row[kStages] = {-1, -1};
+            const CUtensorMap *held_map[STAGES];
+            int held_row[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) {
+                held_map[s] = nullptr;
+                held_row[s] = -1;
+            }
             for (; i < n; ++i) {
-                const int s = i % kStages;
-                if (!mbar_wait_bounded(&empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, flag, 0x201u)) break;
+                const int s = i % STAGES;
+                if (!mbar_wait_bounded(&empty[s], ((uint32_t)(i / STAGES) & 1u) ^ 1u, flag, 0x201u)) break;
                 const CtTask k = ct_task(cb, t0 + i);
                 const bool with_r = held_map[s] != k.job->rot || held_row[s] != k.rrow;
                 held_map[s] = k.job->rot;
@@ -153,16 +159,16 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
                 ct_load(k, smem + s * kStageBytes, &full[s], with_r);
             }
             if (i < n)  // gave up: let the loads already issued land before the CTA exits
-                for (int q = (i > kStages ? i - kStages : 0); q < i; ++q)
-                    mbar_wait_bounded(&full[q % kStages], (uint32_t)(q / kStages) & 1u, flag, 0x205u);
+                for (int q = (i > STAGES ? i - STAGES : 0); q < i; ++q)
+                    mbar_wait_bounded(&full[q % STAGES], (uint32_t)(q / STAGES) & 1u, flag, 0x205u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
             int i = 0;
             for (; i < n; ++i) {
-                const int s = i % kStages, a = i & 1;
-                if (!mbar_wait_bounded(&split[s], (uint32_t)(i / kStages) & 1u, flag, 0x202u)) break;
+                const int s = i % STAGES, a = i & 1;
+                if (!mbar_wait_bounded(&split[s], (uint32_t)(i / STAGES) & 1u, flag, 0x202u)) break;
                 if (!mbar_wait_bounded(&tempty[a], ((uint32_t)(i >> 1) & 1u) ^ 1u, flag, 0x203u)) break;
                 tc_fence_after();
                 unsigned char *st = smem + s * kStageBytes;
@@ -191,8 +197,8 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
         // ---------------- split X into hi (in place) and lo
         const int tid = threadIdx.x - 64;
         for (int i = 0; i < n; ++i) {
-            const int s = i % kStages;
-            if (!mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, flag, 0x204u)) break;
+            const int s = i % STAGES;
+            if (!mbar_wait_bounded(&full[s], (uint32_t)(i / STAGES) & 1u, flag, 0x204u)) break;
             unsigned char *st = smem + s * kStageBytes;
             float4 *h4 = reinterpret_cast<float4 *>(st), *l4 = reinterpret_cast<float4 *>(st + kLoadBytes);
 #pragma unroll 4
@@ -209,7 +215,7 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
         // staged in the box layout of the output map, stored by TMA
         const int q = warp % 4;
         const bool leader = warp == 6 && lane == 0;
-        unsigned char *out = smem + kStages * kStageBytes;
+        unsigned char *out = smem + STAGES * kStageBytes;
         for (int i = 0; i < n; ++i) {
             const int a = i & 1;
             if (!mbar_wait_bounded(&tfull[a], (uint32_t)(i >> 1) & 1u, flag, 0x207u)) break;
@@ -290,14 +296,14 @@ int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st) {
     cb.total = cb.task_off[cb.count];
     static bool attr = false;
     if (!attr) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_rotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kCtSmem));
+        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_rotate_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)ct_smem(kStages)));
         attr = true;
     }
     // one CTA per SM with at least two tasks each (the pipeline needs a few to fill)
     const int grid = std::max(1, std::min(num_sms(), cb.total / 2));
     SPCO_LAUNCH("svd_jacobi_rotate", st,
-                jacobi_rotate_kernel<<<grid, kCtThreads, kCtSmem, st>>>(cb, device_flag_ptr()));
+                jacobi_rotate_kernel<kStages><<<grid, kCtThreads, ct_smem(kStages), st>>>(cb, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("jacobi_rotate_kernel");
     return SPECOPTIM_OK;
 }

@@ -12,8 +12,7 @@
 //      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
 //      per pair (R = the block-diagonal of all R_p in the round's order).  The
 //      rotations are applied on the tensor cores (jacobi_tc.cu, 3xTF32):
-//      B^T = (A R)^T, then A <- B^T R = R^T A R, and Q <- Q R on a second,
-//      low-priority stream that trails the A chain by up to three rounds.
+//      B^T = (A R)^T, then A <- B^T R = R^T A R and Q <- Q R in one launch.
 //      Sweeps repeat until the off-diagonal Frobenius norm falls below tol
 //      times the total norm.  Padded indices have exactly zero rows and
 //      columns, so they are never rotated and stay out of the real eigenvectors.
@@ -37,7 +36,6 @@ namespace spco {
 namespace {
 
 constexpr int kMaxBatch = 16;
-constexpr int kRing = 4;  // rotation slots: the Q chain may lag the A chain by kRing - 1 rounds
 
 // All matrices of one batched refresh.  Each matrix i has Np[i] (a multiple of
 // 128) padded indices in nb = Np/32 blocks; in its round `round[i]` the blocks
@@ -398,10 +396,10 @@ constexpr int64_t kMapFloats = kMaps * 32 + 32;  // 128-byte maps + 128-byte ali
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = padded_order(r);
-    // A, Qacc, B^T (Np^2 each), kRing rotation slots (Np/64 pairs x R^T hi/lo, 64 x 64 each),
+    // A, Qacc, B^T (Np^2 each), the rotations of a round (Np/64 pairs x R^T hi/lo, 64 x 64 each),
     // TMA maps, short factor + scratch (2 r^2), long factor P (L r), s_raw, inv_s,
     // order (int), 2 doubles
-    return (size_t)(3 * Np * Np + kRing * (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
+    return (size_t)(3 * Np * Np + (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
                     (int64_t)L * r + 3 * r + 8);
 }
 
@@ -429,7 +427,7 @@ JobBufs carve(const SvdJob &a) {
     b.Qacc = b.A + NN;
     b.BT = b.Qacc + NN;
     b.Rt = b.BT + NN;
-    float *mp = b.Rt + (size_t)kRing * (b.Np / kP) * 2 * kP * kP;
+    float *mp = b.Rt + (size_t)(b.Np / kP) * 2 * kP * kP;
     b.maps = reinterpret_cast<CUtensorMap *>((reinterpret_cast<uintptr_t>(mp) + 127) & ~uintptr_t(127));
     b.Sf = mp + kMapFloats;
     b.Tmp = b.Sf + (size_t)b.r * b.r;
@@ -446,7 +444,7 @@ JobBufs carve(const SvdJob &a) {
 int upload_maps(const JobBufs &b, cudaStream_t st) {
     CUtensorMap h[kMaps];
     int rc;
-    const int64_t rot_rows = (int64_t)kRing * (b.Np / kP) * 2 * kP;
+    const int64_t rot_rows = (int64_t)(b.Np / kP) * 2 * kP;
     if ((rc = make_tmap_2d(&h[0], b.A, b.Np, b.Np, b.Np, kB, 128))) return rc;
     if ((rc = make_tmap_2d(&h[1], b.BT, b.Np, b.Np, b.Np, kB, 128))) return rc;
     if ((rc = make_tmap_2d(&h[2], b.BT, b.Np, b.Np, b.Np, kB, 32))) return rc;
@@ -542,46 +540,15 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
 
 }  // namespace
 
-// Streams and events of one refresh call's Jacobi loop: `hi` carries the
-// critical chain (rotation of A, subproblem solves, convergence checks) at the
-// highest stream priority, `lo` the accumulation of Q at the lowest.  The
-// rotation slot of round g is g % kRing; solved / consumed mark when the
-// solves wrote a slot and when the Q update has read it.  Created per call (a
-// few tens of microseconds against a refresh of many milliseconds), so
-// concurrent refreshes on different streams stay independent; destroyed when
-// the call returns (the driver releases them once their work completes).
-struct JacStreams {
-    cudaStream_t hi = nullptr, lo = nullptr;
-    cudaEvent_t solved[kRing] = {}, consumed[kRing] = {}, sync_ev = nullptr;
-    ~JacStreams() {
-        for (int k = 0; k < kRing; ++k) {
-            if (solved[k]) cudaEventDestroy(solved[k]);
-            if (consumed[k]) cudaEventDestroy(consumed[k]);
-        }
-        if (sync_ev) cudaEventDestroy(sync_ev);
-        if (hi) cudaStreamDestroy(hi);
-        if (lo) cudaStreamDestroy(lo);
-    }
-    int create() {
-        static std::once_flag attr_once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(attr_once, [] {
-            attr_err = cudaFuncSetAttribute(jacobi_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kSolveSmem);
-        });
-        SPECOPTIM_CUDA(attr_err);
-        int least = 0, greatest = 0;
-        SPECOPTIM_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest));
-        for (int k = 0; k < kRing; ++k) {
-            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&solved[k], cudaEventDisableTiming));
-            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&consumed[k], cudaEventDisableTiming));
-        }
-        SPECOPTIM_CUDA(cudaEventCreateWithFlags(&sync_ev, cudaEventDisableTiming));
-        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least));
-        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest));
-        return SPECOPTIM_OK;
-    }
-};
+int set_solve_attributes() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(jacobi_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSolveSmem);
+    });
+    SPECOPTIM_CUDA(err);
+    return SPECOPTIM_OK;
+}
 
 int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     if (count < 1 || count > kMaxBatch)
@@ -598,7 +565,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     std::memset(&jb, 0, sizeof(jb));
     jb.count = count;
     int max_sweeps = 1, rounds = 1;
-    CtJob pass1[kMaxBatch], pass2[kMaxBatch], qjob[kMaxBatch];
+    CtJob pass1[kMaxBatch], pass2[2 * kMaxBatch];
     for (int i = 0; i < count; ++i) {
         if ((rc = upload_maps(b[i], st))) return rc;
         jb.A[i] = b[i].A;
@@ -611,40 +578,32 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         // B^T = (A R)^T, then A' = B^T R = R^T A R (A symmetric) and Q' = Q R
         pass1[i] = CtJob{&m[0], &m[2], &m[4], b[i].Np, 0, 0, 1, 1};
         pass2[i] = CtJob{&m[1], &m[0], &m[4], b[i].Np, 0, 0, 0, 1};
-        qjob[i] = CtJob{&m[3], &m[3], &m[4], b[i].Np, 0, 0, 0, 1};
+        pass2[count + i] = CtJob{&m[3], &m[3], &m[4], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
-    JacStreams streams;
-    JacStreams *jst = &streams;
-    int rc2 = streams.create();
+    int rc2 = set_solve_attributes();
     if (rc2) return rc2;
-    cudaStream_t hi = jst->hi, lo = jst->lo;
     auto set_round = [&](long g) {
         for (int i = 0; i < count; ++i) {
-            const int round = (int)(g % (b[i].nb - 1)), slot = (int)(g % kRing);
+            const int round = (int)(g % (b[i].nb - 1));
             jb.round[i] = round;
-            jb.R[i] = b[i].Rt + (size_t)slot * (b[i].Np / kP) * 2 * kP * kP;
-            for (CtJob *c : {&pass1[i], &pass2[i], &qjob[i]}) {
+            jb.R[i] = b[i].Rt;
+            for (CtJob *c : {&pass1[i], &pass2[i], &pass2[count + i]}) {
                 c->round = round;
-                c->slot = slot;
+                c->slot = 0;
                 c->active = jb.active[i];
             }
         }
     };
-    // both chains start after the caller's stream (Gram, start basis, maps)
-    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, st));
-    SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, jst->sync_ev, 0));
-    SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, jst->sync_ev, 0));
-    for (int k = 0; k < kRing; ++k) SPECOPTIM_CUDA(cudaEventRecord(jst->consumed[k], lo));
-    // solves of round gg write slot gg % kRing once Q of round gg - kRing has read it
+    // One stream: solve(g) -> B^T = (A R)^T -> [A <- B^T R, Q <- Q R] -> solve(g+1);
+    // the solves of round g+1 overwrite the rotations of round g only after
+    // the launch that read them completed.
     auto solve = [&](long gg) -> int {
         set_round(gg);
-        SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, jst->consumed[gg % kRing], 0));
-        SPCO_LAUNCH("svd_jacobi_solve", hi, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, hi>>>(jb, inner));
+        SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, st>>>(jb, inner));
         SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
-        SPECOPTIM_CUDA(cudaEventRecord(jst->solved[gg % kRing], hi));
         return SPECOPTIM_OK;
     };
     std::vector<double> host(2 * count);
@@ -654,26 +613,22 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(g);
-            if ((rc2 = jacobi_rotate(pass1, count, hi))) return rc2;
-            if ((rc2 = jacobi_rotate(pass2, count, hi))) return rc2;
-            // Q of round g, with the same active set, beside the next solves
-            SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, jst->solved[g % kRing], 0));
-            if ((rc2 = jacobi_rotate(qjob, count, lo))) return rc2;
-            SPECOPTIM_CUDA(cudaEventRecord(jst->consumed[g % kRing], lo));
+            if ((rc2 = jacobi_rotate(pass1, count, st))) return rc2;
+            if ((rc2 = jacobi_rotate(pass2, 2 * count, st))) return rc2;
             if ((rc2 = solve(g + 1))) return rc2;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             jobs[i].sweeps = sweep + 1;
-            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), hi));
+            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), st));
             const int64_t NN = (int64_t)b[i].Np * b[i].Np;
-            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<grid_for(NN, 256), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
+            SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b[i].A, b[i].Np, b[i].norms));
             SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
-                                           cudaMemcpyDeviceToHost, hi));
+                                           cudaMemcpyDeviceToHost, st));
         }
         SPECOPTIM_LAUNCHED("offnorm_kernel");
-        SPECOPTIM_CUDA(cudaStreamSynchronize(hi));
+        SPECOPTIM_CUDA(cudaStreamSynchronize(st));
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             const double tol = jobs[i].tol;
@@ -690,11 +645,6 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             }
         }
     }
-    // the caller's stream resumes once both chains are done
-    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, lo));
-    SPECOPTIM_CUDA(cudaStreamWaitEvent(st, jst->sync_ev, 0));
-    SPECOPTIM_CUDA(cudaEventRecord(jst->sync_ev, hi));
-    SPECOPTIM_CUDA(cudaStreamWaitEvent(st, jst->sync_ev, 0));
     int first_bad = SPECOPTIM_OK;
     for (int i = 0; i < count; ++i) {
         if (jb.active[i]) jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
