@@ -44,7 +44,6 @@ MASK_ROWS, MASK_H, MASK_P = 32 * 2048, 2048, 0.95
 MASK_BOUNDARIES = 15
 POOL = 4               # distinct masked-gradient sets kept resident in HBM
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor throughput ratio
-FP32_FMA_PEAK_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s, SIMT fp32
 
 WORKLOAD = ("llama-3.2-1b decoder layer (q,o 2048x2048; k,v 512x2048; gate,up 8192x2048; "
             "down 2048x8192), rank-32 anchor signal, SVD refresh every 20 steps, "
@@ -58,18 +57,18 @@ def env_int(name, default):
         return default
 
 
-def gemm_traffic_per_launch():
-    """DRAM bytes per grouped gemm_tf32 launch from the committed ncu summary, or None
-    when the kernel or its orchestration changed since the counters were taken."""
+def profiled_traffic(profile: str, sources):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, or None
+    when one of the kernel's sources changed since the counters were taken."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "spectral_corrected_optimizer_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("gemm_tc.cu", "gemm.cuh", "specoptim.cu"):
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     try:
-        with open(os.path.join(ROOT, "profiles", "gemm_tf32_layer_step.md")) as f:
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
             text = f.read()
     except OSError:
         return None
@@ -77,6 +76,20 @@ def gemm_traffic_per_launch():
     if not m or m.group(2) != h.hexdigest()[:16]:
         return None
     return float(m.group(1))
+
+
+GEMM_PROFILE = ("gemm_tf32_layer_step.md", ("gemm_tc.cu", "gemm.cuh", "tc.cuh", "specoptim.cu"))
+ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh", "svd.cu"))
+
+
+def padded_order(r: int) -> int:
+    return (r + 127) // 128 * 128
+
+
+def rotate_bytes(Np: int) -> float:
+    """Algorithmic bytes of one matrix in one rotation pass: the Np x Np fp32
+    operand read and written once, and its Np/64 rotations (R^T hi and lo) read once."""
+    return 8.0 * Np * Np + 512.0 * Np
 
 
 def read_peaks():
@@ -335,34 +348,46 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
     mask_frac = mask["p0.95"]["effective_GBps"] / peaks["hbm_gbs"]
 
-    # roofline of the dominant kernel of the steady step (the three epilogue
-    # variants of the tensor-core GEMM are one kernel)
+    # rooflines of the two heaviest kernels: the tensor-core GEMM of the steady
+    # step (its three epilogue variants are one kernel) and the Jacobi rotation
+    # of the refresh; the primary one is the kernel with more device time per
+    # refresh period (REFRESH_EVERY steady steps + one refresh)
     fam = {}
     for k, (n, t) in rep.items():
         key = "gemm_tf32" if k.startswith("gemm_tf32") else k
         a = fam.setdefault(key, [0, 0.0])
         a[0] += n
         a[1] += t
-    name, (n_launch, t_ms) = max(fam.items(), key=lambda kv: kv[1][1])
     total_ms = sum(v[1] for v in rep.values())
     tf32_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
-    if name == "gemm_tf32":
-        achieved = layer.flops * steady_n / (t_ms * 1e-3) / 1e12
-        roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": tf32_peak,
-                "unit": "TFLOP/s", "frac": achieved / tf32_peak,
-                "peak_source": "%s bf16 sustained x nominal tf32/bf16 %.3f" % (peak_src, TF32_OVER_BF16)}
-    elif name == "gemm_simt":
-        achieved = layer.flops * steady_n / (t_ms * 1e-3) / 1e12
-        roof = {"kernel": name, "bound": "alu", "achieved": achieved, "peak": FP32_FMA_PEAK_NOMINAL,
-                "unit": "TFLOP/s", "frac": achieved / FP32_FMA_PEAK_NOMINAL,
-                "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x 2.07 GHz"}
-    else:
-        roof = {"kernel": name, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": None}
-    roof.update({"launches_per_step": n_launch / steady_n, "avg_launch_ms": t_ms / n_launch,
-                 "share_of_step": t_ms / total_ms,
-                 "traffic": gemm_traffic_per_launch() if name == "gemm_tf32" else None,
-                 "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"})
+    g_launch, g_ms = fam.get("gemm_tf32", [0, 0.0])
+    g_ach = layer.flops * steady_n / (g_ms * 1e-3) / 1e12 if g_ms > 0 else None
+    roof_steady = {"kernel": "gemm_tf32", "bound": "tensor", "achieved": g_ach, "peak": tf32_peak,
+                   "unit": "TFLOP/s", "frac": g_ach / tf32_peak if g_ach else None,
+                   "peak_source": "%s bf16 sustained x nominal tf32/bf16 %.3f" % (peak_src, TF32_OVER_BF16),
+                   "launches_per_step": g_launch / steady_n, "avg_launch_ms": g_ms / max(g_launch, 1),
+                   "share_of_step": g_ms / total_ms, "traffic": profiled_traffic(*GEMM_PROFILE),
+                   "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"}
+    r_launch, r_ms = refresh_rep.get("svd_jacobi_rotate", (0, 0.0))
+    nps = [padded_order(min(i.m, i.n)) for i in layer.inputs.values()]
+    rounds = max(n // 32 for n in nps) - 1
+    r_bytes = sum(sw * rounds * 3 * rotate_bytes(n) for sw, n in zip(sweeps[0], nps))
+    r_ach = r_bytes / (r_ms * 1e-3) / 1e9 if r_ms > 0 else None
+    roof_refresh = {"kernel": "jacobi_rotate", "bound": "hbm", "achieved": r_ach, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": r_ach / peaks["hbm_gbs"] if r_ach else None,
+                    "peak_source": "%s HBM copy bandwidth" % peak_src,
+                    "launches_per_refresh": r_launch, "avg_launch_ms": r_ms / max(r_launch, 1),
+                    "algorithmic_bytes_per_refresh": r_bytes,
+                    "algorithmic_bytes_per_launch_all_active": 1.5 * sum(rotate_bytes(n) for n in nps),
+                    "traffic": profiled_traffic(*ROTATE_PROFILE),
+                    "traffic_note": "ncu DRAM bytes per launch, mean of the launches of one round with all "
+                                    "7 matrices active (compare with algorithmic_bytes_per_launch_all_active)",
+                    "traffic_source": "profiles/jacobi_rotate_layer_refresh.md"}
+    share_refresh = r_ms / (REFRESH_EVERY * steady_ms + refresh_ms)
+    share_steady = REFRESH_EVERY * g_ms / steady_n / (REFRESH_EVERY * steady_ms + refresh_ms)
+    roof_refresh["share_of_period"] = share_refresh
+    roof_steady["share_of_period"] = share_steady
+    roof = roof_refresh if share_refresh > share_steady else roof_steady
     step_bound_ms = 1e3 * max(layer.flops / (tf32_peak * 1e12), layer.bytes / (peaks["hbm_gbs"] * 1e9))
 
     result = {
@@ -376,7 +401,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "roofline": roof,
-        "breakdown": {"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
+        "breakdown": {"roofline_steady_gemm": roof_steady, "roofline_refresh_rotate": roof_refresh,"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
                       "step_roofline_ms": step_bound_ms, "step_frac": step_bound_ms / steady_ms,
                       "refresh_ms": refresh_ms, "refresh_sweeps": sweeps[0],
                       "refresh_note": "traced; one more refresh of the same layer (the Jacobi sweep count "

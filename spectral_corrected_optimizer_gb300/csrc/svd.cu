@@ -60,12 +60,17 @@ __device__ __forceinline__ int find_job(const int *off, int count, int item) {
 
 constexpr int kSolveThreads = 256;
 
-// Rotation (c, s) of one pair with fast reciprocal / square-root intrinsics:
-// c^2 + s^2 = 1 to a few ulp, the same order as the correctly rounded form.
+// Rotation (c, s) of one pair from approximate reciprocal / square-root
+// intrinsics (a few ulp each): c^2 + s^2 = 1 to a few ulp, the same order as
+// with correctly rounded operations; the rotation only has to be orthogonal to
+// fp32 accuracy and close to the exact Jacobi angle.
 __device__ __forceinline__ void jacobi_cs_fast(float app, float aqq, float apq, float &c, float &s) {
     const float theta = __fdividef(aqq - app, 2.f * apq);
-    // |theta| beyond 2^64 overflows theta^2 to inf and gives t = 0: the rotation is below fp32 resolution
-    float t = __frcp_rn(fabsf(theta) + sqrtf(fmaf(theta, theta, 1.f)));
+    const float at = fabsf(theta);
+    const float x = fmaf(theta, theta, 1.f);
+    // t = 1 / (|theta| + sqrt(1 + theta^2)); beyond |theta| = 1e18 the square
+    // would overflow and t = 1 / (2 |theta|) to fp32 accuracy
+    float t = at > 1e18f ? __fdividef(0.5f, at) : __fdividef(1.f, at + x * rsqrtf(x));
     t = copysignf(t, theta);
     c = rsqrtf(fmaf(t, t, 1.f));
     s = t * c;
@@ -97,6 +102,14 @@ __host__ __device__ __forceinline__ int cat_next(int p) {
 __device__ __forceinline__ int sphys(int c) { return c < kB ? c : kB + ((c - kB + 2) & (kB - 1)); }
 
 constexpr int kSP = kP;  // row pitch of S (every row starts at bank 0)
+constexpr int kSBuf = kP * kSP;  // floats per copy of S
+
+// Rotation table of a step: (c, s) of pair k at float2 index cs_index(k).  The
+// thread that owns pairs 8m .. 8m+7 reads them as four 16-byte loads; group m
+// starts at 64 m + 16 (m / 2) bytes, so the four groups read in one phase of a
+// 16-byte load fall in four different bank quads.
+constexpr int kCsSlot = 36;  // float2 per slot (4 x 8 entries + skew, 16-byte multiple)
+__device__ __forceinline__ int cs_index(int k) { return (k >> 3) * 8 + (k & 7) + ((k >> 4) << 1); }
 
 // One CTA (8 warps) per pair: load the 64 x 64 subproblem S, run up to
 // `inner_sweeps` cyclic Jacobi sweeps (32 disjoint rotations per step) and
@@ -106,124 +119,161 @@ constexpr int kSP = kP;  // row pitch of S (every row starts at bank 0)
 //  * S is double buffered: a step reads one copy and writes the moved blocks
 //    into the other, so one barrier per step separates the steps.  Thread
 //    (warp w, lane l) updates the 2 x 2 blocks (pair w + 8u rows, pair l
-//    columns), u = 0..3, at loop-invariant addresses.
+//    columns), u = 0..3, at loop-invariant addresses (the copy a step reads is
+//    a template argument, so every access is register + immediate).
 //  * R lives in registers: thread (w, l) holds row 8w + l/4 of R, positions of
-//    pairs 8m .. 8m+7 (m = l % 4).  After the barrier of step t it applies the
-//    step's rotations (read from a two-slot table that warp 0 fills) and moves
-//    its values to the next positions, exchanging one value with each
+//    pairs 8m .. 8m+7 (m = l % 4).  After the barrier of a step it applies the
+//    step's rotations (from a two-slot table that warp 0 fills) and moves its
+//    values to the next positions, exchanging one value with each
 //    neighbouring quarter by shuffles.
-constexpr size_t kSolveSmem = (2 * (size_t)kP * kSP + 2 * 2 * (size_t)kB) * 4 + 16;
+constexpr size_t kSolveSmem = (2 * (size_t)kSBuf + 2 * 2 * (size_t)kCsSlot) * 4 + 16;
+
+struct SolveState {
+    float rt[8], rb[8];       // this thread's part of R (top / bottom positions of 8 pairs)
+    int rd_t[4], rd_b[4];     // row offsets of the blocks read (pair rows ka, 32 + ka)
+    int wr_t[4], wr_b[4];     // row offsets after the move
+    int a_pp, a_qq, a_pq;     // pair `lane`'s entries
+    int cbot, wct, wcb;       // columns: bottom of `lane`, and both after the move
+    int m;
+    float offmax, dmax;
+};
+
+// One Jacobi step reading copy FROM of S and writing copy 1 - FROM; its
+// rotations go to table slot FROM (consecutive steps alternate).
+template <int FROM>
+__device__ __forceinline__ void solve_step(float *S0, float2 *csb, SolveState &st, int lane, int warp,
+                                           bool track) {
+    const float *S = S0 + FROM * kSBuf;
+    float *Sn = S0 + (1 - FROM) * kSBuf;
+    float c, sn;
+    {
+        const float app = S[st.a_pp], aqq = S[st.a_qq], apq = S[st.a_pq];
+        jacobi_cs_fast(app, aqq, apq, c, sn);
+        if (track) {
+            st.offmax = fmaxf(st.offmax, fabsf(apq));
+            st.dmax = fmaxf(st.dmax, fmaxf(fabsf(app), fabsf(aqq)));
+        }
+    }
+    if (warp == 0) csb[FROM * kCsSlot + cs_index(lane)] = make_float2(c, sn);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ka = warp + 8 * u;
+        const float ca = __shfl_sync(0xffffffffu, c, ka), sa = __shfl_sync(0xffffffffu, sn, ka);
+        const float x11 = S[st.rd_t[u] + lane], x12 = S[st.rd_t[u] + st.cbot];
+        const float x21 = S[st.rd_b[u] + lane], x22 = S[st.rd_b[u] + st.cbot];
+        // rows: J_a^T X, then columns: (J_a^T X) J_b
+        const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
+        const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
+        float z12 = sn * y11 + c * y12, z21 = c * y21 - sn * y22;
+        if (ka == lane) z12 = z21 = 0.f;  // the rotated pair is now decoupled
+        Sn[st.wr_t[u] + st.wct] = c * y11 - sn * y12;
+        Sn[st.wr_t[u] + st.wcb] = z12;
+        Sn[st.wr_b[u] + st.wct] = z21;
+        Sn[st.wr_b[u] + st.wcb] = sn * y21 + c * y22;
+    }
+    __syncthreads();
+    // R <- R J_step on this thread's pairs, then the positions move on
+    const float4 *cs4 = reinterpret_cast<const float4 *>(csb + FROM * kCsSlot + 8 * st.m + 2 * (st.m >> 1));
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float4 w = cs4[h];
+        float x = st.rt[2 * h], y = st.rb[2 * h];
+        st.rt[2 * h] = w.x * x - w.y * y;
+        st.rb[2 * h] = w.y * x + w.x * y;
+        x = st.rt[2 * h + 1];
+        y = st.rb[2 * h + 1];
+        st.rt[2 * h + 1] = w.z * x - w.w * y;
+        st.rb[2 * h + 1] = w.w * x + w.z * y;
+    }
+    const float top_last = st.rt[7], bot_first = st.rb[0];
+    const float top_in = __shfl_up_sync(0xffffffffu, top_last, 1);     // quarter m-1, same row
+    const float bot_in = __shfl_down_sync(0xffffffffu, bot_first, 1);  // quarter m+1, same row
+#pragma unroll
+    for (int q = 7; q >= 1; --q) st.rt[q] = st.rt[q - 1];
+    if (st.m == 0) {
+        st.rt[1] = bot_first;  // bottom 0 -> top 1; top 0 stays (rt[0] unchanged)
+    } else {
+        st.rt[0] = top_in;
+    }
+#pragma unroll
+    for (int q = 0; q < 7; ++q) st.rb[q] = st.rb[q + 1];
+    st.rb[7] = st.m == 3 ? top_last : bot_in;  // top 31 -> bottom 31
+}
 
 __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsigned char *smem) {
-    float *S = reinterpret_cast<float *>(smem);
-    float *Sn = S + kP * kSP;
-    float2 *csb = reinterpret_cast<float2 *>(Sn + kP * kSP);  // [2][32] (c, s) of a step
-    float *red = reinterpret_cast<float *>(csb + 2 * kB);
+    float *S0 = reinterpret_cast<float *>(smem);
+    float2 *csb = reinterpret_cast<float2 *>(S0 + 2 * kSBuf);  // [2][kCsSlot] (c, s) of a step
+    float *red = reinterpret_cast<float *>(csb + 2 * kCsSlot);
     const int job = find_job(jb.pair_off, jb.count, item);
     if (!jb.active[job]) return;
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
     const int pair = item - jb.pair_off[job];
     const float *A = jb.A[job];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // the subproblem in its start order (position = local index)
+    // the subproblem in its start order (position = local index), copy 0
     for (int e = tid; e < kP * (kP / 4); e += kSolveThreads) {
         const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
         const float4 v = *reinterpret_cast<const float4 *>(
             &A[(size_t)pair_index(nb, round, pair, i) * Np + pair_index(nb, round, pair, j4)]);
-        S[i * kSP + sphys(j4)] = v.x;
-        S[i * kSP + sphys(j4 + 1)] = v.y;
-        S[i * kSP + sphys(j4 + 2)] = v.z;
-        S[i * kSP + sphys(j4 + 3)] = v.w;
+        S0[i * kSP + sphys(j4)] = v.x;
+        S0[i * kSP + sphys(j4 + 1)] = v.y;
+        S0[i * kSP + sphys(j4 + 2)] = v.z;
+        S0[i * kSP + sphys(j4 + 3)] = v.w;
     }
-    // R = I in registers
-    const int ri = warp * 8 + (lane >> 2), m = lane & 3;
-    float rt[8], rb[8];
+    SolveState st;
+    const int ri = warp * 8 + (lane >> 2);
+    st.m = lane & 3;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        rt[q] = ri == 8 * m + q ? 1.f : 0.f;
-        rb[q] = ri == kB + 8 * m + q ? 1.f : 0.f;
+    for (int q = 0; q < 8; ++q) {  // R = I
+        st.rt[q] = ri == 8 * st.m + q ? 1.f : 0.f;
+        st.rb[q] = ri == kB + 8 * st.m + q ? 1.f : 0.f;
     }
-    // loop-invariant addresses: pair entries of pair `lane`, and this thread's blocks
-    const int cbot = sphys(kB + lane);
-    const int a_pp = lane * kSP + lane, a_qq = (kB + lane) * kSP + cbot, a_pq = lane * kSP + cbot;
-    const int wct = sphys(cat_next(lane)), wcb = sphys(cat_next(kB + lane));
-    int rd_t[4], rd_b[4], wr_t[4], wr_b[4];
+    st.cbot = sphys(kB + lane);
+    st.a_pp = lane * kSP + lane;
+    st.a_qq = (kB + lane) * kSP + st.cbot;
+    st.a_pq = lane * kSP + st.cbot;
+    st.wct = sphys(cat_next(lane));
+    st.wcb = sphys(cat_next(kB + lane));
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int ka = warp + 8 * u;
-        rd_t[u] = ka * kSP;
-        rd_b[u] = (kB + ka) * kSP;
-        wr_t[u] = cat_next(ka) * kSP;
-        wr_b[u] = cat_next(kB + ka) * kSP;
+        st.rd_t[u] = ka * kSP;
+        st.rd_b[u] = (kB + ka) * kSP;
+        st.wr_t[u] = cat_next(ka) * kSP;
+        st.wr_b[u] = cat_next(kB + ka) * kSP;
     }
     __syncthreads();
+    // A sweep has an odd number of steps (63): the copy holding S alternates
+    // between sweeps.  The convergence test only matters with more than one sweep.
+    const bool track = inner_sweeps > 1;
+    int from = 0;
     for (int sweep = 0; sweep < inner_sweeps; ++sweep) {
-        float offmax = 0.f, dmax = 0.f;
-        for (int step = 0; step < kP - 1; ++step) {
-            float c, sn;
-            {
-                const float app = S[a_pp], aqq = S[a_qq], apq = S[a_pq];
-                jacobi_cs_fast(app, aqq, apq, c, sn);
-                offmax = fmaxf(offmax, fabsf(apq));
-                dmax = fmaxf(dmax, fmaxf(fabsf(app), fabsf(aqq)));
+        st.offmax = 0.f;
+        st.dmax = 0.f;
+        if (from == 0) {
+            for (int step = 0; step + 1 < kP - 1; step += 2) {
+                solve_step<0>(S0, csb, st, lane, warp, track);
+                solve_step<1>(S0, csb, st, lane, warp, track);
             }
-            if (warp == 0) csb[(step & 1) * kB + lane] = make_float2(c, sn);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int ka = warp + 8 * u;
-                const float ca = __shfl_sync(0xffffffffu, c, ka), sa = __shfl_sync(0xffffffffu, sn, ka);
-                const float x11 = S[rd_t[u] + lane], x12 = S[rd_t[u] + cbot];
-                const float x21 = S[rd_b[u] + lane], x22 = S[rd_b[u] + cbot];
-                // rows: J_a^T X, then columns: (J_a^T X) J_b
-                const float y11 = ca * x11 - sa * x21, y21 = sa * x11 + ca * x21;
-                const float y12 = ca * x12 - sa * x22, y22 = sa * x12 + ca * x22;
-                float z12 = sn * y11 + c * y12, z21 = c * y21 - sn * y22;
-                if (ka == lane) z12 = z21 = 0.f;  // the rotated pair is now decoupled
-                Sn[wr_t[u] + wct] = c * y11 - sn * y12;
-                Sn[wr_t[u] + wcb] = z12;
-                Sn[wr_b[u] + wct] = z21;
-                Sn[wr_b[u] + wcb] = sn * y21 + c * y22;
+            solve_step<0>(S0, csb, st, lane, warp, track);
+        } else {
+            for (int step = 0; step + 1 < kP - 1; step += 2) {
+                solve_step<1>(S0, csb, st, lane, warp, track);
+                solve_step<0>(S0, csb, st, lane, warp, track);
             }
-            __syncthreads();
-            float *t1 = S;
-            S = Sn;
-            Sn = t1;
-            // R <- R J_step on this thread's pairs, then the positions move on
-            const float4 *cs4 = reinterpret_cast<const float4 *>(csb + (step & 1) * kB + 8 * m);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float4 w = cs4[h];
-                float x = rt[2 * h], y = rb[2 * h];
-                rt[2 * h] = w.x * x - w.y * y;
-                rb[2 * h] = w.y * x + w.x * y;
-                x = rt[2 * h + 1];
-                y = rb[2 * h + 1];
-                rt[2 * h + 1] = w.z * x - w.w * y;
-                rb[2 * h + 1] = w.w * x + w.z * y;
-            }
-            const float top_last = rt[7], bot_first = rb[0];
-            const float top_in = __shfl_up_sync(0xffffffffu, top_last, 1);     // quarter m-1, same row
-            const float bot_in = __shfl_down_sync(0xffffffffu, bot_first, 1);  // quarter m+1, same row
-#pragma unroll
-            for (int q = 7; q >= 1; --q) rt[q] = rt[q - 1];
-            if (m == 0) {
-                rt[1] = bot_first;  // bottom 0 -> top 1; top 0 stays (rt[0] unchanged)
-            } else {
-                rt[0] = top_in;
-            }
-#pragma unroll
-            for (int q = 0; q < 7; ++q) rb[q] = rb[q + 1];
-            rb[7] = m == 3 ? top_last : bot_in;  // top 31 -> bottom 31
+            solve_step<1>(S0, csb, st, lane, warp, track);
         }
+        from ^= 1;
+        if (!track) break;
         // stop once no off-diagonal entry rotated in this sweep was above fp32 noise
         if (warp == 0) {
             for (int o = 16; o > 0; o >>= 1) {
-                offmax = fmaxf(offmax, __shfl_xor_sync(0xffffffffu, offmax, o));
-                dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+                st.offmax = fmaxf(st.offmax, __shfl_xor_sync(0xffffffffu, st.offmax, o));
+                st.dmax = fmaxf(st.dmax, __shfl_xor_sync(0xffffffffu, st.dmax, o));
             }
             if (lane == 0) {
-                red[0] = offmax;
-                red[1] = dmax;
+                red[0] = st.offmax;
+                red[1] = st.dmax;
             }
         }
         __syncthreads();
@@ -232,13 +282,13 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
     }
     // R_p^T = hi + lo for the tensor-core rotation: R^T[j][k] = R[k][j].  R goes
     // through shared memory (pitch 65, S is no longer read) so that both the
-    // staging and the row-wise writes of R^T are conflict-free and coalesced.
+    // staging and the row-wise writes of R^T are coalesced.
     constexpr int kTP = kP + 1;
-    float *Rs = reinterpret_cast<float *>(smem);
+    float *Rs = S0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        Rs[ri * kTP + 8 * m + q] = rt[q];
-        Rs[ri * kTP + kB + 8 * m + q] = rb[q];
+        Rs[ri * kTP + 8 * st.m + q] = st.rt[q];
+        Rs[ri * kTP + kB + 8 * st.m + q] = st.rb[q];
     }
     __syncthreads();
     float *Rp = jb.R[job] + (size_t)pair * 2 * kP * kP;
