@@ -79,7 +79,7 @@ def profiled_traffic(profile: str, sources):
 
 
 GEMM_PROFILE = ("gemm_tf32_layer_step.md", ("gemm_tc.cu", "gemm.cuh", "tc.cuh", "specoptim.cu"))
-ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh", "svd.cu"))
+ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh"))
 
 
 def padded_order(r: int) -> int:
