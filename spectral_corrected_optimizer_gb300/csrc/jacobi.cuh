@@ -52,6 +52,19 @@ struct CtJob {
 
 constexpr int kCtMaxJobs = 32;
 
+// One matrix of a two-sided rotation launch (jacobi_apply_tc.cu): A <- R^T A R
+// in place for round `round`, A symmetric Np x Np.  `a32` is a TMA map of A
+// with 32 x 32 boxes, `rot` the rotation tensor's map (as for CtJob, slot 0).
+struct ApJob {
+    const CUtensorMap *a32, *rot;
+    int Np, round, active;
+};
+
+constexpr int kApMaxJobs = 16;
+
+// Launches the two-sided rotation of `count` (<= 16) matrices in one kernel.
+int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st);
+
 // Launches the rotation of `count` (<= 32) matrices in one kernel.
 int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st);
 

@@ -11,8 +11,9 @@
 //      pair of blocks forms a 64 x 64 subproblem that one CTA sweeps in shared
 //      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
 //      per pair (R = the block-diagonal of all R_p in the round's order).  The
-//      rotations are applied on the tensor cores (jacobi_tc.cu, 3xTF32):
-//      B^T = (A R)^T, then A <- B^T R = R^T A R and Q <- Q R in one launch.
+//      rotations are applied on the tensor cores (3xTF32): A <- R^T A R in one
+//      pass over its upper 128 x 128 super-tiles (jacobi_apply_tc.cu), then
+//      Q <- Q R (jacobi_tc.cu).
 //      Sweeps repeat until the off-diagonal Frobenius norm falls below tol
 //      times the total norm.  Padded indices have exactly zero rows and
 //      columns, so they are never rotated and stay out of the real eigenvectors.
@@ -438,7 +439,7 @@ namespace {
 
 int64_t padded_order(int r) { return ((int64_t)(r + kNpAlign - 1) / kNpAlign) * kNpAlign; }
 
-constexpr int kMaps = 5;                         // A, B^T (two boxes), Q, rotations
+constexpr int kMaps = 3;                         // A (32 x 32 boxes), Q (32 x 128), rotations (32 x 64)
 constexpr int64_t kMapFloats = kMaps * 32 + 32;  // 128-byte maps + 128-byte alignment slack
 
 }  // namespace
@@ -446,10 +447,10 @@ constexpr int64_t kMapFloats = kMaps * 32 + 32;  // 128-byte maps + 128-byte ali
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = padded_order(r);
-    // A, Qacc, B^T (Np^2 each), the rotations of a round (Np/64 pairs x R^T hi/lo, 64 x 64 each),
+    // A, Qacc (Np^2 each), the rotations of a round (Np/64 pairs x R^T hi/lo, 64 x 64 each),
     // TMA maps, short factor + scratch (2 r^2), long factor P (L r), s_raw, inv_s,
     // order (int), 2 doubles
-    return (size_t)(3 * Np * Np + (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
+    return (size_t)(2 * Np * Np + (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
                     (int64_t)L * r + 3 * r + 8);
 }
 
@@ -459,8 +460,8 @@ struct JobBufs {
     int r, Np, nb;
     int64_t L;
     bool tall;
-    float *A, *Qacc, *BT, *Rt, *Sf, *Tmp, *P, *s_raw, *inv_s;
-    CUtensorMap *maps;  // device: A, B^T (32 x 128 box), B^T (32 x 32 box), Q, R^T
+    float *A, *Qacc, *Rt, *Sf, *Tmp, *P, *s_raw, *inv_s;
+    CUtensorMap *maps;  // device: A (32 x 32 boxes), Q (32 x 128), R^T (32 x 64)
     int *order;
     double *norms;
 };
@@ -475,8 +476,7 @@ JobBufs carve(const SvdJob &a) {
     const size_t NN = (size_t)b.Np * b.Np;
     b.A = a.work;
     b.Qacc = b.A + NN;
-    b.BT = b.Qacc + NN;
-    b.Rt = b.BT + NN;
+    b.Rt = b.Qacc + NN;
     float *mp = b.Rt + (size_t)(b.Np / kP) * 2 * kP * kP;
     b.maps = reinterpret_cast<CUtensorMap *>((reinterpret_cast<uintptr_t>(mp) + 127) & ~uintptr_t(127));
     b.Sf = mp + kMapFloats;
@@ -495,11 +495,9 @@ int upload_maps(const JobBufs &b, cudaStream_t st) {
     CUtensorMap h[kMaps];
     int rc;
     const int64_t rot_rows = (int64_t)(b.Np / kP) * 2 * kP;
-    if ((rc = make_tmap_2d(&h[0], b.A, b.Np, b.Np, b.Np, kB, 128))) return rc;
-    if ((rc = make_tmap_2d(&h[1], b.BT, b.Np, b.Np, b.Np, kB, 128))) return rc;
-    if ((rc = make_tmap_2d(&h[2], b.BT, b.Np, b.Np, b.Np, kB, 32))) return rc;
-    if ((rc = make_tmap_2d(&h[3], b.Qacc, b.Np, b.Np, b.Np, kB, 128))) return rc;
-    if ((rc = make_tmap_2d(&h[4], b.Rt, rot_rows, kP, kP, kB, kP))) return rc;
+    if ((rc = make_tmap_2d(&h[0], b.A, b.Np, b.Np, b.Np, kB, kB))) return rc;
+    if ((rc = make_tmap_2d(&h[1], b.Qacc, b.Np, b.Np, b.Np, kB, 128))) return rc;
+    if ((rc = make_tmap_2d(&h[2], b.Rt, rot_rows, kP, kP, kB, kP))) return rc;
     SPECOPTIM_CUDA(cudaMemcpyAsync(b.maps, h, sizeof(h), cudaMemcpyHostToDevice, st));
     return SPECOPTIM_OK;
 }
@@ -615,7 +613,8 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     std::memset(&jb, 0, sizeof(jb));
     jb.count = count;
     int max_sweeps = 1, rounds = 1;
-    CtJob pass1[kMaxBatch], pass2[2 * kMaxBatch];
+    ApJob ajob[kMaxBatch];
+    CtJob qjob[kMaxBatch];
     for (int i = 0; i < count; ++i) {
         if ((rc = upload_maps(b[i], st))) return rc;
         jb.A[i] = b[i].A;
@@ -625,10 +624,9 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         max_sweeps = std::max(max_sweeps, jobs[i].max_sweeps);
         rounds = std::max(rounds, b[i].nb - 1);
         const CUtensorMap *m = b[i].maps;
-        // B^T = (A R)^T, then A' = B^T R = R^T A R (A symmetric) and Q' = Q R
-        pass1[i] = CtJob{&m[0], &m[2], &m[4], b[i].Np, 0, 0, 1, 1};
-        pass2[i] = CtJob{&m[1], &m[0], &m[4], b[i].Np, 0, 0, 0, 1};
-        pass2[count + i] = CtJob{&m[3], &m[3], &m[4], b[i].Np, 0, 0, 0, 1};
+        // A <- R^T A R (two-sided, upper super-tiles) and Q <- Q R
+        ajob[i] = ApJob{&m[0], &m[2], b[i].Np, 0, 1};
+        qjob[i] = CtJob{&m[1], &m[1], &m[2], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
     int inner = 1;
@@ -640,14 +638,11 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             const int round = (int)(g % (b[i].nb - 1));
             jb.round[i] = round;
             jb.R[i] = b[i].Rt;
-            for (CtJob *c : {&pass1[i], &pass2[i], &pass2[count + i]}) {
-                c->round = round;
-                c->slot = 0;
-                c->active = jb.active[i];
-            }
+            ajob[i].round = qjob[i].round = round;
+            ajob[i].active = qjob[i].active = jb.active[i];
         }
     };
-    // One stream: solve(g) -> B^T = (A R)^T -> [A <- B^T R, Q <- Q R] -> solve(g+1);
+    // One stream: solve(g) -> A <- R^T A R -> Q <- Q R -> solve(g+1);
     // the solves of round g+1 overwrite the rotations of round g only after
     // the launch that read them completed.
     auto solve = [&](long gg) -> int {
@@ -663,8 +658,8 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(g);
-            if ((rc2 = jacobi_rotate(pass1, count, st))) return rc2;
-            if ((rc2 = jacobi_rotate(pass2, 2 * count, st))) return rc2;
+            if ((rc2 = jacobi_apply(ajob, count, st))) return rc2;
+            if ((rc2 = jacobi_rotate(qjob, count, st))) return rc2;
             if ((rc2 = solve(g + 1))) return rc2;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
