@@ -17,6 +17,20 @@ constexpr int kB = 32;      // block size of the block-Jacobi
 constexpr int kP = 2 * kB;  // subproblem size (one pair of blocks)
 constexpr int kNpAlign = 128;  // Np granularity: whole 128-row slabs for the rotation kernel
 
+// 3xTF32 operand split x = hi + lo: hi is x rounded to the 10 explicit mantissa
+// bits of TF32, to nearest with ties away from zero (half a unit of the 13
+// dropped bits is added to the magnitude, then they are cleared; for finite x
+// below the largest float), and lo = x - hi (exact) rounded the same way.  The
+// tensor core reads the top 19 bits of each.  Integer operations only.
+__device__ __forceinline__ float tf32_round(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+__device__ __forceinline__ float tf32_split(float x, float &lo) {
+    const float hi = tf32_round(x);
+    lo = tf32_round(x - hi);
+    return hi;
+}
+
 // round-robin schedule over `players` (even): pair i of round k
 __host__ __device__ __forceinline__ void rr_pair(int players, int round, int i, int &a, int &b) {
     const int n1 = players - 1;
@@ -53,10 +67,12 @@ struct CtJob {
 constexpr int kCtMaxJobs = 32;
 
 // One matrix of a two-sided rotation launch (jacobi_apply_tc.cu): A <- R^T A R
-// in place for round `round`, A symmetric Np x Np.  `a32` is a TMA map of A
-// with 32 x 32 boxes, `rot` the rotation tensor's map (as for CtJob, slot 0).
+// in place for round `round`, A symmetric Np x Np (row-major, leading
+// dimension Np).  `a32` is a TMA map of A with 32 x 32 boxes, `rot` the
+// rotation tensor's map (as for CtJob, slot 0).
 struct ApJob {
     const CUtensorMap *a32, *rot;
+    float *A;
     int Np, round, active;
 };
 

@@ -86,14 +86,10 @@ __device__ __forceinline__ void ct_load(const CtTask &k, unsigned char *stage, u
 
 __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo) {
     float4 h;
-    h.x = round_to_tf32(v.x);
-    h.y = round_to_tf32(v.y);
-    h.z = round_to_tf32(v.z);
-    h.w = round_to_tf32(v.w);
-    lo.x = round_to_tf32(v.x - h.x);
-    lo.y = round_to_tf32(v.y - h.y);
-    lo.z = round_to_tf32(v.z - h.z);
-    lo.w = round_to_tf32(v.w - h.w);
+    h.x = tf32_split(v.x, lo.x);
+    h.y = tf32_split(v.y, lo.y);
+    h.z = tf32_split(v.z, lo.z);
+    h.w = tf32_split(v.w, lo.w);
     return h;
 }
 

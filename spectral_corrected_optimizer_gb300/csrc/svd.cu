@@ -296,10 +296,10 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
     for (int e = tid; e < kP * kP / 2; e += kSolveThreads) {
         const int jj = e / (kP / 2), k2 = (e % (kP / 2)) * 2;
         const float x0 = Rs[k2 * kTP + jj], x1 = Rs[(k2 + 1) * kTP + jj];
-        const float h0 = round_to_tf32(x0), h1 = round_to_tf32(x1);
+        float l0, l1;
+        const float h0 = tf32_split(x0, l0), h1 = tf32_split(x1, l1);
         *reinterpret_cast<float2 *>(&Rp[jj * kP + k2]) = make_float2(h0, h1);
-        *reinterpret_cast<float2 *>(&Rp[kP * kP + jj * kP + k2]) =
-            make_float2(round_to_tf32(x0 - h0), round_to_tf32(x1 - h1));
+        *reinterpret_cast<float2 *>(&Rp[kP * kP + jj * kP + k2]) = make_float2(l0, l1);
     }
 }
 
@@ -625,7 +625,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         rounds = std::max(rounds, b[i].nb - 1);
         const CUtensorMap *m = b[i].maps;
         // A <- R^T A R (two-sided, upper super-tiles) and Q <- Q R
-        ajob[i] = ApJob{&m[0], &m[2], b[i].Np, 0, 1};
+        ajob[i] = ApJob{&m[0], &m[2], b[i].A, b[i].Np, 0, 1};
         qjob[i] = CtJob{&m[1], &m[1], &m[2], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
