@@ -16,13 +16,18 @@
 // first.  Every block pair of A is read and written by exactly one task, so
 // the update is in place.
 //
-// One CTA (8 warps) per SM walks its super-tiles; the phases of a task run one
-// after the other (split, MMAs, TMEM -> shared, MMAs, staging, stores) inside
-// 192 KB of shared memory and 256 TMEM columns, with the loads in flight
-// behind other work: the next task's X (both column pairs) while this one
-// writes its result, the stage-2 rotations during the TMEM -> shared copy.  Every mbarrier wait is
-// bounded; a wait that gives up records a code in the library's device flag and
-// the CTA stops after letting its copies land.
+// One CTA per SM walks its super-tiles with warp roles, so that the epilogue of
+// one super-tile overlaps the loads, split and stage-1 MMAs of the next:
+//   warp 0      TMA producer (X of both column pairs, then the stage-2 rotations)
+//   warp 1      TMEM (256 columns: D1 of both column pairs, D2 of both row pairs)
+//               and the MMA issuer
+//   warps 2-5   transform: split X into hi / lo; build A2 from D1
+//   warps 6-9   epilogue: D2 -> both orientations, straight from registers
+//               (the transposed copy in 128-byte lines, the mirror rows in
+//               16-byte pieces that L2 merges into lines)
+// Every mbarrier wait is bounded; a wait that gives up records a code in the
+// library's device flag and that role stops (the producer and the MMA issuer
+// first let their last copies and MMAs land).
 #include <algorithm>
 #include <cstring>
 
@@ -33,17 +38,15 @@
 namespace spco {
 namespace {
 
-constexpr int kApThreads = 256;
+constexpr int kApThreads = 320;  // producer, MMA, 4 transform and 4 epilogue warps
 constexpr uint32_t kKB = 1024;
-// Shared memory (192 KB) in three 64 KB regions, the same roles in every task:
+// Shared memory (192 KB) in three 64 KB regions:
 //   P0 = [0, 64) KB     X_0 (32 KB, raw then hi) + R^T hi / lo of column pair 0
 //   P1 = [64, 128) KB   X_1 + R^T of column pair 1
 //   LO = [128, 192) KB  X_0 lo, X_1 lo
-// After stage 1: A2_r hi + lo (64 KB per row pair r) in P0 and P1, the row
-// pairs' R^T hi / lo in LO.  After stage 2: P0 and P1 take the next task's
-// loads while LO stages the mirror super-tile for its TMA stores; the
-// transposed copy goes to global memory straight from registers (each store
-// of a warp is one 128-byte line).
+// After the stage-1 MMAs: A2_r hi + lo (64 KB per row pair r) in P0 and P1, the
+// row pairs' R^T hi / lo in LO.  After the stage-2 MMAs all three regions take
+// the next super-tile.
 constexpr uint32_t kLO = 128 * kKB;
 constexpr size_t kApSmem = 192 * (size_t)kKB + 1024 /*align*/ + 128;
 static_assert(kApSmem <= 232448, "shared memory budget of one CTA");
@@ -141,29 +144,33 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char ap_smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(ap_smem_raw) + 1023) & ~uintptr_t(1023));
-    // [0] X_0, [1] X_1, [2] stage-2 rotations, [3] stage-1 MMAs, [4] stage-2 MMAs; each
-    // completes once per task, so a task's waits use parity (task index & 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 192 * kKB);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int q = warp & 3, h = warp >> 2;  // TMEM lane quarter, column half
+    uint64_t *xfull = bar;        // [2] X_c and R_c^T landed (producer, tx bytes)
+    uint64_t *xsplit = bar + 2;   // [2] X_c split into hi / lo (128 transform threads)
+    uint64_t *s1done = bar + 4;   // stage-1 MMAs complete (commit)
+    uint64_t *r2full = bar + 5;   // stage-2 rotations landed (producer, tx bytes)
+    uint64_t *a2ready = bar + 6;  // A2 built, D1 read (128 transform threads)
+    uint64_t *s2done = bar + 7;   // stage-2 MMAs complete (commit)
+    uint64_t *d2free = bar + 8;   // D2 read by the epilogue (128 epilogue threads)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 9);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned char *LO = smem + kLO;
-    // thread 0: operations issued / seen complete per barrier (a clean stop after a timeout)
-    int iss[5] = {0, 0, 0, 0, 0}, seen[5] = {0, 0, 0, 0, 0};
-    auto load_x = [&](const ApTask &k) {  // both column pairs of a task into P0, P1
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            unsigned char *p = smem + c * 64 * kKB;
-            load_stage1(k, c, p, p + 32 * kKB, &bar[c]);
-            ++iss[c];
+    // this CTA's tasks: t = blockIdx.x + i * gridDim.x, i < n
+    const int n = ab.total > (int)blockIdx.x ? (ab.total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&xfull[b], 1);
+            mbar_init(&xsplit[b], 128);
         }
-    };
-    if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
+        mbar_init(s1done, 1);
+        mbar_init(r2full, 1);
+        mbar_init(a2ready, 128);
+        mbar_init(s2done, 1);
+        mbar_init(d2free, 128);
         fence_mbar_init();
-        if ((int)blockIdx.x < ab.total) load_x(ap_task(ab, blockIdx.x));
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(tslot, kApTmemCols);
         tmem_relinquish();
     }
@@ -171,136 +178,158 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tq = (uint32_t)(32 * q) << 16;  // this warp's TMEM lanes
 
-    // all threads wait; thread 0 counts; the result is made uniform over the CTA
-    auto wait_all = [&](int b, uint32_t par, unsigned code) -> bool {
-        const bool w = mbar_wait_bounded(&bar[b], par, flag, code);
-        if (w && tid == 0) ++seen[b];
-        return __syncthreads_and(w) != 0;
-    };
-
-    bool ok = true;
-    int it = 0;
-    for (int t = blockIdx.x; t < ab.total && ok; t += gridDim.x, ++it) {
-        const ApTask k = ap_task(ab, t);
-        const uint32_t par = (uint32_t)it & 1u;
-        if (tid == 0) bulk_wait_read<0>();  // the previous task's stores have read LO
-        // ---- stage 1: Y_c = X_c R_c into TMEM columns 64 c
-        for (int c = 0; c < 2; ++c) {
-            unsigned char *x = smem + c * 64 * kKB, *xl = LO + c * 32 * kKB, *r = x + 32 * kKB;
-            if (!(ok = wait_all(c, par, 0x301u + c))) break;
-            float4 *h4 = reinterpret_cast<float4 *>(x), *l4 = reinterpret_cast<float4 *>(xl);
-#pragma unroll 4
-            for (int e = tid; e < (int)(32 * kKB / 16); e += kApThreads) split4(h4, l4, e);
-            fence_proxy_async_smem();  // the tensor core reads what these threads wrote
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                mma_3xtf32(tmem + 64u * c, smem_u32(x), smem_u32(xl), smem_u32(r), smem_u32(r) + 16 * kKB);
-                if (c == 1) {
-                    mma_commit(&bar[3]);
-                    ++iss[3];
-                }
-            }
-        }
-        if (!ok || !(ok = wait_all(3, par, 0x303u))) break;
-        tc_fence_after();
-        float v[2][32];
-        tmem_ld32(tmem + 32u * h + tq, v[0]);       // Y_0[rho][32 h ..], rho = 32 q + lane
-        tmem_ld32(tmem + 64u + 32u * h + tq, v[1]);  // Y_1[rho][32 h ..]
-        // the stage-1 buffers are free: rotations of the row pairs for stage 2 into LO
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar[2], 64 * kKB);
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int i = 0, x_iss = 0, r_iss = 0;
+            for (; i < n; ++i) {
+                const ApTask k = ap_task(ab, blockIdx.x + i * gridDim.x);
+                const uint32_t par = (uint32_t)i & 1u;
+                // P0 / P1 held the previous task's A2 until its stage-2 MMAs completed
+                if (!mbar_wait_bounded(s2done, par ^ 1u, flag, 0x311u)) break;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                unsigned char *rr = LO + r * 32 * kKB;
-                tma_load_2d(rr, k.job->rot, 0, k.rrow[r], &bar[2]);
-                tma_load_2d(rr + 8 * kKB, k.job->rot, kB, k.rrow[r], &bar[2]);
-                tma_load_2d(rr + 16 * kKB, k.job->rot, 0, k.rrow[r] + kP, &bar[2]);
-                tma_load_2d(rr + 24 * kKB, k.job->rot, kB, k.rrow[r] + kP, &bar[2]);
+                for (int c = 0; c < 2; ++c) {
+                    unsigned char *p = smem + c * 64 * kKB;
+                    load_stage1(k, c, p, p + 32 * kKB, &xfull[c]);
+                }
+                ++x_iss;
+                // LO holds this task's X lo until its stage-1 MMAs completed
+                if (!mbar_wait_bounded(s1done, par, flag, 0x312u)) break;
+                mbar_arrive_expect_tx(r2full, 64 * kKB);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    unsigned char *rr = LO + r * 32 * kKB;
+                    tma_load_2d(rr, k.job->rot, 0, k.rrow[r], r2full);
+                    tma_load_2d(rr + 8 * kKB, k.job->rot, kB, k.rrow[r], r2full);
+                    tma_load_2d(rr + 16 * kKB, k.job->rot, 0, k.rrow[r] + kP, r2full);
+                    tma_load_2d(rr + 24 * kKB, k.job->rot, kB, k.rrow[r] + kP, r2full);
+                }
+                ++r_iss;
             }
-            ++iss[2];
+            if (i < n) {  // gave up: let the last loads issued land before the CTA exits
+                if (x_iss > 0)
+                    for (int c = 0; c < 2; ++c)
+                        mbar_wait_bounded(&xfull[c], (uint32_t)(x_iss - 1) & 1u, flag, 0x313u);
+                if (r_iss > 0) mbar_wait_bounded(r2full, (uint32_t)(r_iss - 1) & 1u, flag, 0x313u);
+            }
         }
-        // A2_r[c*64 + j][k] = Y_c[r*64 + k][j]: row rho = 32 q + lane is k = 32 (q & 1) + lane of
-        // row pair r = q / 2, i.e. column `lane` of K-atom (q & 1); 128-byte swizzled rows
-        {
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int i = 0;
+            bool pending = false;
+            uint64_t *last = nullptr;
+            uint32_t last_par = 0;
+            for (; i < n; ++i) {
+                const uint32_t par = (uint32_t)i & 1u;
+                bool ok = true;
+                for (int c = 0; c < 2 && ok; ++c) {
+                    if (!(ok = mbar_wait_bounded(&xsplit[c], par, flag, 0x321u))) break;
+                    tc_fence_after();
+                    const uint32_t x = smem_u32(smem + c * 64 * kKB), xl = smem_u32(LO + c * 32 * kKB);
+                    mma_3xtf32(tmem + 64u * c, x, xl, x + 32 * kKB, x + 48 * kKB);
+                }
+                if (!ok) break;
+                mma_commit(s1done);
+                pending = true;
+                last = s1done;
+                last_par = par;
+                if (!mbar_wait_bounded(a2ready, par, flag, 0x322u)) break;
+                if (!mbar_wait_bounded(r2full, par, flag, 0x323u)) break;
+                if (!mbar_wait_bounded(d2free, par ^ 1u, flag, 0x324u)) break;  // D2 of the previous task read
+                tc_fence_after();
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t a = smem_u32(smem + r * 64 * kKB), b = smem_u32(LO + r * 32 * kKB);
+                    mma_3xtf32(tmem + 128u + 64u * r, a, a + 32 * kKB, b, b + 16 * kKB);
+                }
+                mma_commit(s2done);
+                last = s2done;
+            }
+            if (i < n && pending) mbar_wait_bounded(last, last_par, flag, 0x325u);
+        }
+    } else if (warp < 6) {
+        // ---------------- transform: split X, then A2 from the stage-1 accumulators
+        const int tid = threadIdx.x - 64, q = warp & 3;
+        const uint32_t tq = (uint32_t)(32 * q) << 16;
+        for (int i = 0; i < n; ++i) {
+            const uint32_t par = (uint32_t)i & 1u;
+            bool ok = true;
+            for (int c = 0; c < 2; ++c) {
+                if (!(ok = mbar_wait_bounded(&xfull[c], par, flag, 0x331u))) break;
+                float4 *h4 = reinterpret_cast<float4 *>(smem + c * 64 * kKB);
+                float4 *l4 = reinterpret_cast<float4 *>(LO + c * 32 * kKB);
+#pragma unroll 4
+                for (int e = tid; e < (int)(32 * kKB / 16); e += 128) split4(h4, l4, e);
+                fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+                mbar_arrive(&xsplit[c]);
+            }
+            if (!ok || !mbar_wait_bounded(s1done, par, flag, 0x332u)) break;
+            tc_fence_after();
+            // A2_r[c*64 + j][k] = Y_c[r*64 + k][j]: row rho = 32 q + lane is k = 32 (q & 1) + lane of
+            // row pair r = q / 2, i.e. column `lane` of K-atom (q & 1); 128-byte swizzled rows
             unsigned char *a2h = smem + (q >> 1) * 64 * kKB + (q & 1) * 16 * kKB, *a2l = a2h + 32 * kKB;
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int row = c * 64 + 32 * h + jj;
-                    const uint32_t off = row * 128 + ((((uint32_t)lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4;
-                    float lo;
-                    *reinterpret_cast<float *>(a2h + off) = tf32_split(v[c][jj], lo);
-                    *reinterpret_cast<float *>(a2l + off) = lo;
+                for (int hh = 0; hh < 2; ++hh) {
+                    float v[32];
+                    tmem_ld32(tmem + 64u * c + 32u * hh + tq, v);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int row = c * 64 + 32 * hh + jj;
+                        const uint32_t off = row * 128 + ((((uint32_t)lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4;
+                        float lo;
+                        *reinterpret_cast<float *>(a2h + off) = tf32_split(v[jj], lo);
+                        *reinterpret_cast<float *>(a2l + off) = lo;
+                    }
                 }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(a2ready);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (!(ok = wait_all(2, par, 0x304u))) break;
-        // ---- stage 2: Z^T rows of row pair r into TMEM columns 128 + 64 r
-        if (tid == 0) {
+    } else {
+        // ---------------- epilogue: D2 rows -> both orientations in global memory
+        const int q = warp & 3;
+        const uint32_t tq = (uint32_t)(32 * q) << 16;
+        for (int i = 0; i < n; ++i) {
+            const ApTask k = ap_task(ab, blockIdx.x + i * gridDim.x);
+            const uint32_t par = (uint32_t)i & 1u;
+            if (!mbar_wait_bounded(s2done, par, flag, 0x341u)) break;
             tc_fence_after();
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const uint32_t a = smem_u32(smem + r * 64 * kKB), b = smem_u32(LO + r * 32 * kKB);
-                mma_3xtf32(tmem + 128u + 64u * r, a, a + 32 * kKB, b, b + 16 * kKB);
-            }
-            mma_commit(&bar[4]);
-            ++iss[4];
-        }
-        if (!(ok = wait_all(4, par, 0x305u))) break;
-        tc_fence_after();
-        // P0, P1 and LO are free: the next task's loads go out now
-        if (tid == 0 && t + (int)gridDim.x < ab.total) load_x(ap_task(ab, t + gridDim.x));
-        tmem_ld32(tmem + 128u + 32u * h + tq, v[0]);  // D2_0[L][32 h ..], L = 32 q + lane
-        tmem_ld32(tmem + 192u + 32u * h + tq, v[1]);  // D2_1[L][32 h ..]
-        tc_fence_before();
-        // row L = c*64 + j of D2_r is row colidx(c, j) of the mirror super-tile and
-        // column colidx(c, j) of the super-tile itself
-        const int L = 32 * q + lane;
-        const int gcol = k.colblk[q] * kB + lane;
-        float *A = k.job->A;
-        const int64_t ld = k.job->Np;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            unsigned char *mir = LO + r * 32 * kKB + h * 16 * kKB + L * 128;
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                *reinterpret_cast<float4 *>(mir + ((c4 ^ (L & 7)) << 4)) =
-                    make_float4(v[r][4 * c4], v[r][4 * c4 + 1], v[r][4 * c4 + 2], v[r][4 * c4 + 3]);
-            if (!k.diag) {
-                float *dst = A + (int64_t)(k.rowblk[2 * r + h] * kB) * ld + gcol;
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) dst[ii * ld] = v[r][ii];
-            }
-        }
-        fence_proxy_async_smem();  // the TMA engine reads what these threads wrote
-        __syncthreads();
-        if (tid == 0) {
+            float v[2][2][32];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int qb = 0; qb < 4; ++qb)
+                for (int hh = 0; hh < 2; ++hh) tmem_ld32(tmem + 128u + 64u * r + 32u * hh + tq, v[r][hh]);
+            tc_fence_before();
+            mbar_arrive(d2free);
+            // row L = c*64 + j of D2_r is row colidx(c, j) of the mirror super-tile
+            // and column colidx(c, j) of the super-tile; i = 32 hh + ii
+            float *A = k.job->A;
+            const int64_t ld = k.job->Np;
+            const int gl = k.colblk[q] * kB + lane;  // colidx(L), L = 32 q + lane
 #pragma unroll
-                    for (int kap = 0; kap < 2; ++kap)
-                        tma_store_2d(k.job->a32, LO + r * 32 * kKB + kap * 16 * kKB + qb * 4 * kKB,
-                                     k.rowblk[2 * r + kap] * kB, k.colblk[qb] * kB);
-            bulk_commit();
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float *mir = A + (int64_t)gl * ld + k.rowblk[2 * r + hh] * kB;
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        *reinterpret_cast<float4 *>(mir + 4 * c4) =
+                            make_float4(v[r][hh][4 * c4], v[r][hh][4 * c4 + 1], v[r][hh][4 * c4 + 2], v[r][hh][4 * c4 + 3]);
+                    if (!k.diag) {
+                        float *dst = A + (int64_t)(k.rowblk[2 * r + hh] * kB) * ld + gl;
+#pragma unroll
+                        for (int ii = 0; ii < 32; ++ii) dst[ii * ld] = v[r][hh][ii];
+                    }
+                }
         }
-    }
-    if (tid == 0) {
-        if (!ok)  // let copies and MMAs still in flight land (bounded) before the CTA exits
-            for (int b = 0; b < 5; ++b)
-                for (int n = seen[b]; n < iss[b]; ++n) mbar_wait_bounded(&bar[b], (uint32_t)n & 1u, flag, 0x306u);
-        bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kApTmemCols);
     }
