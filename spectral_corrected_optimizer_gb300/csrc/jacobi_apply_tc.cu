@@ -22,9 +22,9 @@
 //   warp 1      TMEM (256 columns: D1 of both column pairs, D2 of both row pairs)
 //               and the MMA issuer
 //   warps 2-5   transform: split X into hi / lo; build A2 from D1
-//   warps 6-9   epilogue: D2 -> both orientations, straight from registers
-//               (the transposed copy in 128-byte lines, the mirror rows in
-//               16-byte pieces that L2 merges into lines)
+//   warps 6-9   epilogue: D2 -> both orientations in whole 128-byte lines
+//               (the transposed copy straight from registers, the mirror
+//               through a 32 x 33 shared tile per warp)
 // Every mbarrier wait is bounded; a wait that gives up records a code in the
 // library's device flag and that role stops (the producer and the MMA issuer
 // first let their last copies and MMAs land).
@@ -48,7 +48,7 @@ constexpr uint32_t kKB = 1024;
 // row pairs' R^T hi / lo in LO.  After the stage-2 MMAs all three regions take
 // the next super-tile.
 constexpr uint32_t kLO = 128 * kKB;
-constexpr size_t kApSmem = 192 * (size_t)kKB + 1024 /*align*/ + 128;
+constexpr size_t kApSmem = 192 * (size_t)kKB + 128 /*barriers*/ + 4 * 32 * 33 * 4 /*epilogue tiles*/ + 1024 /*align*/;
 static_assert(kApSmem <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kApTmemCols = 256;  // D1_0, D1_1, D2_0, D2_1 (64 columns each)
 constexpr uint32_t kApIdesc = tf32_idesc(128, kP);
@@ -153,6 +153,7 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     uint64_t *s2done = bar + 7;   // stage-2 MMAs complete (commit)
     uint64_t *d2free = bar + 8;   // D2 read by the epilogue (128 epilogue threads)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 9);
+    float *etile = reinterpret_cast<float *>(smem + 192 * kKB + 128);  // 4 epilogue warps x 32 x 33
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned char *LO = smem + kLO;
     // this CTA's tasks: t = blockIdx.x + i * gridDim.x, i < n
@@ -306,24 +307,31 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
             tc_fence_before();
             mbar_arrive(d2free);
             // row L = c*64 + j of D2_r is row colidx(c, j) of the mirror super-tile
-            // and column colidx(c, j) of the super-tile; i = 32 hh + ii
+            // and column colidx(c, j) of the super-tile; i = 32 hh + ii.  The
+            // transposed copy is written column by column (each store of the warp
+            // is one 128-byte line); the mirror goes through a 32 x 33 tile of
+            // this warp so that it, too, leaves in whole lines.
             float *A = k.job->A;
             const int64_t ld = k.job->Np;
             const int gl = k.colblk[q] * kB + lane;  // colidx(L), L = 32 q + lane
+            float *tile = etile + (warp - 6) * 32 * 33;
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float *mir = A + (int64_t)gl * ld + k.rowblk[2 * r + hh] * kB;
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        *reinterpret_cast<float4 *>(mir + 4 * c4) =
-                            make_float4(v[r][hh][4 * c4], v[r][hh][4 * c4 + 1], v[r][hh][4 * c4 + 2], v[r][hh][4 * c4 + 3]);
+                    const int rb = k.rowblk[2 * r + hh] * kB;
                     if (!k.diag) {
-                        float *dst = A + (int64_t)(k.rowblk[2 * r + hh] * kB) * ld + gl;
+                        float *dst = A + (int64_t)rb * ld + gl;
 #pragma unroll
                         for (int ii = 0; ii < 32; ++ii) dst[ii * ld] = v[r][hh][ii];
                     }
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) tile[lane * 33 + ii] = v[r][hh][ii];
+                    __syncwarp();
+                    float *mir = A + (int64_t)(k.colblk[q] * kB) * ld + rb + lane;
+#pragma unroll
+                    for (int row = 0; row < 32; ++row) mir[row * ld] = tile[row * 33 + lane];
+                    __syncwarp();
                 }
         }
     }
