@@ -69,11 +69,11 @@ constexpr int kCtMaxJobs = 32;
 // One matrix of a two-sided rotation launch (jacobi_apply_tc.cu): A <- R^T A R
 // in place for round `round`, A symmetric Np x Np (row-major, leading
 // dimension Np).  `a32` is a TMA map of A with 32 x 32 boxes, `rot` the
-// rotation tensor's map (as for CtJob, slot 0).
+// rotation tensor's map (rotations of the round in slot `slot`, as for CtJob).
 struct ApJob {
     const CUtensorMap *a32, *rot;
     float *A;
-    int Np, round, active;
+    int Np, round, slot, active;
 };
 
 constexpr int kApMaxJobs = 16;

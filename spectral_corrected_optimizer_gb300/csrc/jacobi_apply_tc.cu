@@ -87,8 +87,8 @@ __device__ __forceinline__ ApTask ap_task(const ApBatch &ab, int t) {
     for (int u = 0; u < 2; ++u) {
         rr_pair(nb, k.job->round, 2 * s1 + u, k.rowblk[2 * u], k.rowblk[2 * u + 1]);
         rr_pair(nb, k.job->round, 2 * s2 + u, k.colblk[2 * u], k.colblk[2 * u + 1]);
-        k.rrow[u] = (2 * s1 + u) * 2 * kP;
-        k.crow[u] = (2 * s2 + u) * 2 * kP;
+        k.rrow[u] = (k.job->slot * (k.job->Np / kP) + 2 * s1 + u) * 2 * kP;
+        k.crow[u] = (k.job->slot * (k.job->Np / kP) + 2 * s2 + u) * 2 * kP;
     }
     return k;
 }

@@ -12,8 +12,8 @@
 //      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
 //      per pair (R = the block-diagonal of all R_p in the round's order).  The
 //      rotations are applied on the tensor cores (3xTF32): A <- R^T A R in one
-//      pass over its upper 128 x 128 super-tiles (jacobi_apply_tc.cu), then
-//      Q <- Q R (jacobi_tc.cu).
+//      pass over its upper 128 x 128 super-tiles (jacobi_apply_tc.cu), and
+//      Q <- Q R (jacobi_tc.cu) on a second stream beside the next solves.
 //      Sweeps repeat until the off-diagonal Frobenius norm falls below tol
 //      times the total norm.  Padded indices have exactly zero rows and
 //      columns, so they are never rotated and stay out of the real eigenvectors.
@@ -447,10 +447,10 @@ constexpr int64_t kMapFloats = kMaps * 32 + 32;  // 128-byte maps + 128-byte ali
 size_t svd_workspace_floats(int m, int n) {
     const int r = m < n ? m : n, L = m < n ? n : m;
     const int64_t Np = padded_order(r);
-    // A, Qacc (Np^2 each), the rotations of a round (Np/64 pairs x R^T hi/lo, 64 x 64 each),
+    // A, Qacc (Np^2 each), two rotation slots (Np/64 pairs x R^T hi/lo, 64 x 64 each),
     // TMA maps, short factor + scratch (2 r^2), long factor P (L r), s_raw, inv_s,
     // order (int), 2 doubles
-    return (size_t)(2 * Np * Np + (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
+    return (size_t)(2 * Np * Np + 2 * (Np / kP) * 2 * kP * kP + kMapFloats + 2 * (int64_t)r * r +
                     (int64_t)L * r + 3 * r + 8);
 }
 
@@ -477,7 +477,7 @@ JobBufs carve(const SvdJob &a) {
     b.A = a.work;
     b.Qacc = b.A + NN;
     b.Rt = b.Qacc + NN;
-    float *mp = b.Rt + (size_t)(b.Np / kP) * 2 * kP * kP;
+    float *mp = b.Rt + (size_t)2 * (b.Np / kP) * 2 * kP * kP;
     b.maps = reinterpret_cast<CUtensorMap *>((reinterpret_cast<uintptr_t>(mp) + 127) & ~uintptr_t(127));
     b.Sf = mp + kMapFloats;
     b.Tmp = b.Sf + (size_t)b.r * b.r;
@@ -494,7 +494,7 @@ JobBufs carve(const SvdJob &a) {
 int upload_maps(const JobBufs &b, cudaStream_t st) {
     CUtensorMap h[kMaps];
     int rc;
-    const int64_t rot_rows = (int64_t)(b.Np / kP) * 2 * kP;
+    const int64_t rot_rows = (int64_t)2 * (b.Np / kP) * 2 * kP;
     if ((rc = make_tmap_2d(&h[0], b.A, b.Np, b.Np, b.Np, kB, kB))) return rc;
     if ((rc = make_tmap_2d(&h[1], b.Qacc, b.Np, b.Np, b.Np, kB, 128))) return rc;
     if ((rc = make_tmap_2d(&h[2], b.Rt, rot_rows, kP, kP, kB, kP))) return rc;
@@ -598,6 +598,49 @@ int set_solve_attributes() {
     return SPECOPTIM_OK;
 }
 
+// Streams and events of one refresh call's Jacobi loop (created per call: a few
+// tens of microseconds against a refresh of many milliseconds, and concurrent
+// refreshes on different streams stay independent; released when the call
+// returns, which the driver defers until their work completed).
+struct JacStreams {
+    cudaStream_t hi = nullptr, lo = nullptr;
+    cudaEvent_t a_done[2] = {}, q_done[2] = {}, ev = nullptr;
+    ~JacStreams() {
+        for (int k = 0; k < 2; ++k) {
+            if (a_done[k]) cudaEventDestroy(a_done[k]);
+            if (q_done[k]) cudaEventDestroy(q_done[k]);
+        }
+        if (ev) cudaEventDestroy(ev);
+        if (hi) cudaStreamDestroy(hi);
+        if (lo) cudaStreamDestroy(lo);
+    }
+    // both chains start after the caller's stream's earlier work
+    int create(cudaStream_t st) {
+        int least = 0, greatest = 0;
+        SPECOPTIM_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+        for (int k = 0; k < 2; ++k) {
+            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&a_done[k], cudaEventDisableTiming));
+            SPECOPTIM_CUDA(cudaEventCreateWithFlags(&q_done[k], cudaEventDisableTiming));
+        }
+        SPECOPTIM_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest));
+        SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least));
+        SPECOPTIM_CUDA(cudaEventRecord(ev, st));
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, ev, 0));
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, ev, 0));
+        for (int k = 0; k < 2; ++k) SPECOPTIM_CUDA(cudaEventRecord(q_done[k], lo));
+        return SPECOPTIM_OK;
+    }
+    // the caller's stream resumes once both chains are done
+    int join(cudaStream_t st) {
+        SPECOPTIM_CUDA(cudaEventRecord(ev, lo));
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(st, ev, 0));
+        SPECOPTIM_CUDA(cudaEventRecord(ev, hi));
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(st, ev, 0));
+        return SPECOPTIM_OK;
+    }
+};
+
 int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     if (count < 1 || count > kMaxBatch)
         return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: 1 to 16 matrices per batch");
@@ -625,7 +668,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         rounds = std::max(rounds, b[i].nb - 1);
         const CUtensorMap *m = b[i].maps;
         // A <- R^T A R (two-sided, upper super-tiles) and Q <- Q R
-        ajob[i] = ApJob{&m[0], &m[2], b[i].A, b[i].Np, 0, 1};
+        ajob[i] = ApJob{&m[0], &m[2], b[i].A, b[i].Np, 0, 0, 1};
         qjob[i] = CtJob{&m[1], &m[1], &m[2], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
@@ -637,17 +680,24 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         for (int i = 0; i < count; ++i) {
             const int round = (int)(g % (b[i].nb - 1));
             jb.round[i] = round;
-            jb.R[i] = b[i].Rt;
+            const int slot = (int)(g & 1);
+            jb.R[i] = b[i].Rt + (size_t)slot * (b[i].Np / kP) * 2 * kP * kP;
+            ajob[i].slot = qjob[i].slot = slot;
             ajob[i].round = qjob[i].round = round;
             ajob[i].active = qjob[i].active = jb.active[i];
         }
     };
-    // One stream: solve(g) -> A <- R^T A R -> Q <- Q R -> solve(g+1);
-    // the solves of round g+1 overwrite the rotations of round g only after
-    // the launch that read them completed.
+    // Two chains.  `hi` (highest priority): solve(g) -> A <- R^T A R -> solve(g+1)
+    // ...; `lo`: Q <- Q R for round g, released with solve(g+1) (which does not
+    // need it) so that the two share the SMs.  Rotations of round g live in
+    // slot g % 2; solve(g+1) rewrites the slot of round g-1 once Q(g-1) read it.
+    JacStreams js_;
+    if ((rc2 = js_.create(st))) return rc2;
+    cudaStream_t hi = js_.hi, lo = js_.lo;
     auto solve = [&](long gg) -> int {
         set_round(gg);
-        SPCO_LAUNCH("svd_jacobi_solve", st, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, st>>>(jb, inner));
+        SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, js_.q_done[gg & 1], 0));
+        SPCO_LAUNCH("svd_jacobi_solve", hi, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, hi>>>(jb, inner));
         SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
         return SPECOPTIM_OK;
     };
@@ -658,22 +708,25 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(g);
-            if ((rc2 = jacobi_apply(ajob, count, st))) return rc2;
-            if ((rc2 = jacobi_rotate(qjob, count, st))) return rc2;
+            if ((rc2 = jacobi_apply(ajob, count, hi))) return rc2;
+            SPECOPTIM_CUDA(cudaEventRecord(js_.a_done[g & 1], hi));
+            SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, js_.a_done[g & 1], 0));
+            if ((rc2 = jacobi_rotate(qjob, count, lo))) return rc2;
+            SPECOPTIM_CUDA(cudaEventRecord(js_.q_done[g & 1], lo));
             if ((rc2 = solve(g + 1))) return rc2;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             jobs[i].sweeps = sweep + 1;
-            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), st));
+            SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), hi));
             const int64_t NN = (int64_t)b[i].Np * b[i].Np;
-            SPCO_LAUNCH("svd_offnorm", st, offnorm_kernel<<<grid_for(NN, 256), 256, 0, st>>>(b[i].A, b[i].Np, b[i].norms));
+            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<grid_for(NN, 256), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
             SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
-                                           cudaMemcpyDeviceToHost, st));
+                                           cudaMemcpyDeviceToHost, hi));
         }
         SPECOPTIM_LAUNCHED("offnorm_kernel");
-        SPECOPTIM_CUDA(cudaStreamSynchronize(st));
+        SPECOPTIM_CUDA(cudaStreamSynchronize(hi));
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             const double tol = jobs[i].tol;
@@ -690,6 +743,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             }
         }
     }
+    if ((rc2 = js_.join(st))) return rc2;
     int first_bad = SPECOPTIM_OK;
     for (int i = 0; i < count; ++i) {
         if (jb.active[i]) jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
