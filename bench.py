@@ -80,6 +80,7 @@ def profiled_traffic(profile: str, sources):
 
 GEMM_PROFILE = ("gemm_tf32_layer_step.md", ("gemm_tc.cu", "gemm.cuh", "tc.cuh", "specoptim.cu"))
 ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh"))
+APPLY_PROFILE = ("jacobi_apply_layer_refresh.md", ("jacobi_apply_tc.cu", "jacobi.cuh", "tc.cuh"))
 
 
 def padded_order(r: int) -> int:
@@ -87,9 +88,17 @@ def padded_order(r: int) -> int:
 
 
 def rotate_bytes(Np: int) -> float:
-    """Algorithmic bytes of one matrix in one rotation pass: the Np x Np fp32
-    operand read and written once, and its Np/64 rotations (R^T hi and lo) read once."""
+    """Algorithmic bytes of Q <- Q R for one matrix and round: Q (Np x Np fp32)
+    read and written once, and its Np/64 rotations (R^T hi and lo) read once."""
     return 8.0 * Np * Np + 512.0 * Np
+
+
+def apply_bytes(Np: int) -> float:
+    """Algorithmic bytes of A <- R^T A R for one matrix and round: the upper
+    128 x 128 super-tiles of A read once, all of A written once, the rotations
+    read once."""
+    ns = Np // 128
+    return ns * (ns + 1) / 2 * 128 * 128 * 4 + 4.0 * Np * Np + 512.0 * Np
 
 
 def read_peaks():
@@ -228,6 +237,92 @@ class Layer:
         self.mask_round_trip(i)
 
 
+class ModelWorkload:
+    """`n_layers` decoder layers of the given shapes, each with its own optimizer
+    state, fed with one layer's synthetic inputs (the values do not change the
+    work; generating 16 distinct layers would take minutes of host time), plus
+    plain-AdamW tensors (the full model's embedding and norm vectors)."""
+
+    def __init__(self, shapes: dict, n_layers: int, seed: int, plain=()):
+        import numpy as np
+        import torch
+
+        import spectral_corrected_optimizer_gb300 as so
+        import synthetic
+
+        self.so, self.torch = so, torch
+        self.names = list(shapes)
+        inputs = synthetic.layer_inputs(shapes, seed=seed, rank=32)
+        self.Ganc = {n: [torch.from_numpy(inputs[n].anchor_grad(i)).cuda() for i in range(2)] for n in self.names}
+        self.Gm = {n: [torch.from_numpy(inputs[n].masked_grad(t)).cuda() for t in range(2)] for n in self.names}
+        W0 = {n: torch.from_numpy(inputs[n].weights()).cuda() for n in self.names}
+        self.layers = [{n: so.SpectralOptimizer(*shapes[n]) for n in self.names} for _ in range(n_layers)]
+        self.W = [{n: W0[n].clone() for n in self.names} for _ in range(n_layers)]
+        self.plain = []
+        for i, (rows, cols) in enumerate(plain):
+            w = torch.from_numpy(synthetic.normal_f32(seed, 90, i, (rows, cols), 0.02)).cuda()
+            g = torch.from_numpy(synthetic.normal_f32(seed, 91, i, (rows, cols), 1e-2)).cuda()
+            self.plain.append((w, g, torch.zeros_like(w), torch.zeros_like(w)))
+        self.t = 0
+        self.flops = n_layers * sum(gemm_flops(*shapes[n]) for n in self.names)
+        self.params = n_layers * sum(m * n for m, n in shapes.values()) + sum(r * c for r, c in plain)
+
+    def refresh(self, idx: int):
+        handles = []
+        for layer in self.layers:
+            for n in self.names:
+                layer[n].anchor_update(self.Ganc[n][idx % 2])
+                handles.append(layer[n])
+        sweeps = []
+        for i in range(0, len(handles), 14):  # two layers per batched refresh
+            sweeps += self.so.svd_refresh_many(handles[i:i + 14])
+        return sweeps
+
+    def step(self, i: int):
+        if i % REFRESH_EVERY == 0:
+            self.refresh(i // REFRESH_EVERY)
+        for layer, W in zip(self.layers, self.W):
+            self.so.step_many([layer[n] for n in self.names], [W[n] for n in self.names],
+                              [self.Gm[n][i % 2] for n in self.names], 2e-5)
+        self.t += 1
+        for w, g, m, v in self.plain:
+            self.so.adamw(w, g, m, v, self.t, 2e-5)
+
+
+def run_config(name: str, workload, K: int, W: int, mask_shape=None):
+    """Whole-path steps/s of another configuration: W warm-up steps (the first holds
+    the first refresh), then K timed steps holding one refresh; plus the refresh
+    alone and, where the configuration has one, its mask round trip."""
+    torch = workload.torch
+    for i in range(W):
+        workload.step(i)
+    torch.cuda.synchronize()
+    ms = timed(torch, lambda: [workload.step(W + i) for i in range(K)], False)
+    sweeps = []
+    refresh_ms = timed(torch, lambda: sweeps.append(workload.refresh(7)), False)
+    out = {"workload": name, "steps_per_s": K / (ms * 1e-3), "ms_per_step": ms / K, "steps": K, "warmup": W,
+           "refreshes_in_timed_steps": sum(1 for i in range(W, W + K) if i % REFRESH_EVERY == 0),
+           "refresh_ms": refresh_ms, "refresh_sweeps_max": max(sweeps[0]),
+           "params": workload.params, "gemm_tflop_per_step": workload.flops / 1e12}
+    if mask_shape is not None:
+        so = workload.so
+        rows, H, p = mask_shape
+        Kk = so.mask_keep_count(p, H)
+        h = torch.randn(rows, H, device="cuda").to(torch.bfloat16)
+        hp = torch.empty(rows, Kk, dtype=torch.bfloat16, device="cuda")
+        hd = torch.empty_like(h)
+        for _ in range(3):
+            so.mask_pack(h, Kk, 0, 0, 0, out=hp)
+            so.mask_unpack(hp, H, 0, 0, 0, out=hd)
+        reps = 20
+        t = timed(torch, lambda: [(so.mask_pack(h, Kk, b, 0, 0, out=hp), so.mask_unpack(hp, H, b, 0, 0, out=hd))
+                                  for b in range(reps)], False)
+        op_bytes = rows * (H + Kk) * 2
+        out["mask"] = {"rows": rows, "H": H, "p": p, "K": Kk, "pack_unpack_GBps": 2 * reps * op_bytes / (t * 1e-3) / 1e9,
+                       "timing": "eager, %d pack + unpack pairs" % reps}
+    return out
+
+
 def timed(torch, fn, dist_ok):
     """Device time of fn() with a barrier and a synchronize on both sides (ms)."""
     torch.cuda.synchronize()
@@ -346,6 +441,20 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     refresh_rep = so.trace_report()
     so.trace_enable(False)
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
+    others = {}
+    if not args.no_configs:
+        import synthetic
+        full = ModelWorkload(synthetic.LLAMA_1B_LAYER, synthetic.LLAMA_1B_LAYERS, seed=rank,
+                             plain=[synthetic.LLAMA_1B_EMBED] + [(1, 2048)] * synthetic.LLAMA_1B_NORMS)
+        others["full_1b"] = run_config("llama-3.2-1b full model: 16 layers x 7 matrices spectral-corrected, "
+                                       "embedding 128256x2048 + 33 norm vectors plain AdamW", full, 20, 3)
+        del full
+        torch.cuda.empty_cache()
+        l7 = ModelWorkload(synthetic.LLAMA_7B_LAYER, 1, seed=rank)
+        others["layer_7b"] = run_config("7B-shaped layer: q,o 4096x4096; k,v 1024x4096; gate,up 14336x4096; "
+                                        "down 4096x14336", l7, 20, 3, mask_shape=(8 * 4096, 4096, 0.95))
+        del l7
+        torch.cuda.empty_cache()
     mask_frac = mask["p0.95"]["effective_GBps"] / peaks["hbm_gbs"]
 
     # rooflines of the two heaviest kernels: the tensor-core GEMM of the steady
@@ -368,26 +477,34 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                    "launches_per_step": g_launch / steady_n, "avg_launch_ms": g_ms / max(g_launch, 1),
                    "share_of_step": g_ms / total_ms, "traffic": profiled_traffic(*GEMM_PROFILE),
                    "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"}
-    r_launch, r_ms = refresh_rep.get("svd_jacobi_rotate", (0, 0.0))
+    # the refresh's two tensor-core rotation kernels, both HBM-bound: A <- R^T A R
+    # (jacobi_apply, on the critical chain) and Q <- Q R (jacobi_rotate, on a
+    # second stream beside the solves, so its traced time includes sharing the SMs)
     nps = [padded_order(min(i.m, i.n)) for i in layer.inputs.values()]
     rounds = max(n // 32 for n in nps) - 1
-    r_bytes = sum(sw * rounds * 3 * rotate_bytes(n) for sw, n in zip(sweeps[0], nps))
-    r_ach = r_bytes / (r_ms * 1e-3) / 1e9 if r_ms > 0 else None
-    roof_refresh = {"kernel": "jacobi_rotate", "bound": "hbm", "achieved": r_ach, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": r_ach / peaks["hbm_gbs"] if r_ach else None,
-                    "peak_source": "%s HBM copy bandwidth" % peak_src,
-                    "launches_per_refresh": r_launch, "avg_launch_ms": r_ms / max(r_launch, 1),
-                    "algorithmic_bytes_per_refresh": r_bytes,
-                    "algorithmic_bytes_per_launch_all_active": 1.5 * sum(rotate_bytes(n) for n in nps),
-                    "traffic": profiled_traffic(*ROTATE_PROFILE),
-                    "traffic_note": "ncu DRAM bytes per launch, mean of the launches of one round with all "
-                                    "7 matrices active (compare with algorithmic_bytes_per_launch_all_active)",
-                    "traffic_source": "profiles/jacobi_rotate_layer_refresh.md"}
-    share_refresh = r_ms / (REFRESH_EVERY * steady_ms + refresh_ms)
-    share_steady = REFRESH_EVERY * g_ms / steady_n / (REFRESH_EVERY * steady_ms + refresh_ms)
-    roof_refresh["share_of_period"] = share_refresh
-    roof_steady["share_of_period"] = share_steady
-    roof = roof_refresh if share_refresh > share_steady else roof_steady
+    period_ms = REFRESH_EVERY * steady_ms + refresh_ms
+
+    def hbm_roof(kernel, trace_name, per_matrix, profile):
+        launches, ms = refresh_rep.get(trace_name, (0, 0.0))
+        total = sum(sw * rounds * per_matrix(n) for sw, n in zip(sweeps[0], nps))
+        ach = total / (ms * 1e-3) / 1e9 if ms > 0 else None
+        return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"] if ach else None,
+                "peak_source": "%s HBM copy bandwidth" % peak_src,
+                "launches_per_refresh": launches, "avg_launch_ms": ms / max(launches, 1),
+                "algorithmic_bytes_per_refresh": total,
+                "algorithmic_bytes_per_launch_all_active": sum(per_matrix(n) for n in nps),
+                "traffic": profiled_traffic(*profile),
+                "traffic_note": "ncu DRAM bytes per launch with all 7 matrices active "
+                                "(compare with algorithmic_bytes_per_launch_all_active)",
+                "traffic_source": "profiles/" + profile[0], "share_of_period": ms / period_ms}
+
+    roof_apply = hbm_roof("jacobi_apply", "svd_jacobi_apply", apply_bytes, APPLY_PROFILE)
+    roof_rotate = hbm_roof("jacobi_rotate", "svd_jacobi_rotate", rotate_bytes, ROTATE_PROFILE)
+    roof_rotate["note"] = "runs beside the solves on a second stream; traced time includes that sharing"
+    roof_steady["share_of_period"] = REFRESH_EVERY * g_ms / steady_n / period_ms
+    # primary: the heaviest kernel of the critical chain (the Q update overlaps the solves)
+    roof = max([roof_steady, roof_apply], key=lambda r: r["share_of_period"])
     step_bound_ms = 1e3 * max(layer.flops / (tf32_peak * 1e12), layer.bytes / (peaks["hbm_gbs"] * 1e9))
 
     result = {
@@ -401,7 +518,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "roofline": roof,
-        "breakdown": {"roofline_steady_gemm": roof_steady, "roofline_refresh_rotate": roof_refresh,"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
+        "breakdown": {"roofline_steady_gemm": roof_steady, "roofline_refresh_apply": roof_apply,
+                      "roofline_refresh_q_rotate": roof_rotate,"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
                       "step_roofline_ms": step_bound_ms, "step_frac": step_bound_ms / steady_ms,
                       "refresh_ms": refresh_ms, "refresh_sweeps": sweeps[0],
                       "refresh_note": "traced; one more refresh of the same layer (the Jacobi sweep count "
@@ -409,6 +527,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                       "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()},
                       "refresh_kernels": {k: {"launches": v[0], "ms": round(v[1], 3)} for k, v in refresh_rep.items()}},
         "mask": dict(mask, frac_of_hbm=mask_frac, hbm_peak_GBps=peaks["hbm_gbs"]),
+        "other_configs": others,
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak},
     }
     if not args.no_e2e:
@@ -586,6 +705,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the full-1B and 7B-layer measurements reported beside the headline")
     ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer"], default=None,
                     help="run a small case for ncu captures instead of the benchmark")
     args = ap.parse_args()
