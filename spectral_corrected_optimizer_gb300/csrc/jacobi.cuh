@@ -81,7 +81,8 @@ constexpr int kApMaxJobs = 16;
 // Launches the two-sided rotation of `count` (<= 16) matrices in one kernel.
 int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st);
 
-// Launches the rotation of `count` (<= 32) matrices in one kernel.
-int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st);
+// Launches the rotation of `count` (<= 32) matrices in one kernel on at most
+// `max_ctas` SMs (0: all of them).
+int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st, int max_ctas = 0);
 
 }  // namespace spco

@@ -276,7 +276,7 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
 
 }  // namespace
 
-int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st) {
+int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st, int max_ctas) {
     if (count < 1 || count > kCtMaxJobs) return fail(SPECOPTIM_ERR_INVALID_ARG, "jacobi_rotate: 1 to 32 matrices");
     CtBatch cb;
     std::memset(&cb, 0, sizeof(cb));
@@ -296,8 +296,8 @@ int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st) {
                                             (int)ct_smem(kStages)));
         attr = true;
     }
-    // one CTA per SM with at least two tasks each (the pipeline needs a few to fill)
-    const int grid = std::max(1, std::min(num_sms(), cb.total / 2));
+    // one CTA per SM (or per SM of the share given) with at least two tasks each
+    int grid = std::max(1, std::min(max_ctas > 0 ? max_ctas : num_sms(), cb.total / 2));
     SPCO_LAUNCH("svd_jacobi_rotate", st,
                 jacobi_rotate_kernel<kStages><<<grid, kCtThreads, ct_smem(kStages), st>>>(cb, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("jacobi_rotate_kernel");

@@ -711,7 +711,9 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             if ((rc2 = jacobi_apply(ajob, count, hi))) return rc2;
             SPECOPTIM_CUDA(cudaEventRecord(js_.a_done[g & 1], hi));
             SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, js_.a_done[g & 1], 0));
-            if ((rc2 = jacobi_rotate(qjob, count, lo))) return rc2;
+            // on 3/8 of the SMs: the solves take the rest, and the next round's
+            // rotation of A finds SMs free sooner (measured best among 1/4 .. all)
+            if ((rc2 = jacobi_rotate(qjob, count, lo, num_sms() * 3 / 8))) return rc2;
             SPECOPTIM_CUDA(cudaEventRecord(js_.q_done[g & 1], lo));
             if ((rc2 = solve(g + 1))) return rc2;
         }
