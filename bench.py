@@ -536,44 +536,97 @@ def run_ours(args, rank, world, local_rank, dist_ok):
 
 
 def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
-    """Same steps with host buffers: every step copies its masked gradients and
-    activations host -> device from pinned memory and reads the updated weights
-    back (the parameter snapshot the anchor circuit pulls), inside the timed region."""
+    """Same steps with host buffers, as a training loop would drive them: every
+    step's masked gradients and activations (and, every 20th step, the anchor
+    gradients) come host -> device from pinned memory, and every step's updated
+    weights go device -> host (the parameter snapshot the anchor circuit pulls).
+    The copies run on two more streams (one per direction), double-buffered: step
+    i+1's inputs travel while step i computes, and step i's weights leave from a
+    device-side snapshot while step i+1 computes.  All of it is inside the timed
+    region."""
     torch = layer.torch
-    hostG = {n: [g.cpu().pin_memory() for g in layer.Gpool[n][:2]] for n in layer.names}
-    hostA = {n: [g.cpu().pin_memory() for g in layer.Ganc[n]] for n in layer.names}
-    devG = {n: torch.empty_like(layer.Gpool[n][0]) for n in layer.names}
-    hostW = {n: torch.empty(layer.W[n].shape, dtype=torch.float32).pin_memory() for n in layer.names}
+    names = layer.names
+    hostG = {n: [g.cpu().pin_memory() for g in layer.Gpool[n][:2]] for n in names}
+    hostA = {n: [g.cpu().pin_memory() for g in layer.Ganc[n]] for n in names}
     host_h, host_g = layer.h.cpu().pin_memory(), layer.g.cpu().pin_memory()
-    dev_h, dev_g = torch.empty_like(layer.h), torch.empty_like(layer.g)
+    hostW = {n: torch.empty(layer.W[n].shape, dtype=torch.float32).pin_memory() for n in names}
+    devG = [{n: torch.empty_like(layer.Gpool[n][0]) for n in names} for _ in range(2)]
+    devA = [{n: torch.empty_like(layer.Ganc[n][0]) for n in names} for _ in range(2)]
+    dev_h = [torch.empty_like(layer.h) for _ in range(2)]
+    dev_g = [torch.empty_like(layer.g) for _ in range(2)]
+    snapW = {n: torch.empty_like(layer.W[n]) for n in names}
+    compute, copy, back = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     stats = {"h2d": 0, "d2h": 0}
+    freed = [torch.cuda.Event(), torch.cuda.Event()]  # compute done with input buffer b
+    loaded = [torch.cuda.Event(), torch.cuda.Event()]  # inputs of buffer b landed
+    snapped, sent = torch.cuda.Event(), torch.cuda.Event()
+    for e in freed + [sent]:
+        e.record(compute)
 
-    def one(i):
-        G = None
+    def load(i):  # on the copy stream: step i's inputs into buffer i % 2
+        b = i % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(freed[b])
+            if i % REFRESH_EVERY == 0:
+                for n in names:
+                    devA[b][n].copy_(hostA[n][(i // REFRESH_EVERY) % 2], non_blocking=True)
+                    stats["h2d"] += devA[b][n].numel() * 4
+            for n in names:
+                devG[b][n].copy_(hostG[n][i % 2], non_blocking=True)
+                stats["h2d"] += devG[b][n].numel() * 4
+            dev_h[b].copy_(host_h, non_blocking=True)
+            dev_g[b].copy_(host_g, non_blocking=True)
+            stats["h2d"] += 2 * dev_h[b].numel() * 2
+            loaded[b].record(copy)
+
+    def one(i, last):
+        b = i % 2
+        if not last:
+            load(i + 1)
+        compute.wait_event(loaded[b])
         if i % REFRESH_EVERY == 0:
-            for n in layer.names:
-                devG[n].copy_(hostA[n][(i // REFRESH_EVERY) % 2], non_blocking=True)
-                stats["h2d"] += devG[n].numel() * 4
-            layer.refresh(0, G=devG)
-        for n in layer.names:
-            devG[n].copy_(hostG[n][i % 2], non_blocking=True)
-            stats["h2d"] += devG[n].numel() * 4
-        layer.spectral(i, G=devG)
-        dev_h.copy_(host_h, non_blocking=True)
-        dev_g.copy_(host_g, non_blocking=True)
-        stats["h2d"] += 2 * dev_h.numel() * 2
-        layer.mask_round_trip(i, h=dev_h, g=dev_g)
-        for n in layer.names:
-            hostW[n].copy_(layer.W[n], non_blocking=True)
-            stats["d2h"] += layer.W[n].numel() * 4
+            layer.refresh(0, G=devA[b])
+        layer.spectral(i, G=devG[b])
+        layer.mask_round_trip(i, h=dev_h[b], g=dev_g[b])
+        freed[b].record(compute)
+        compute.wait_event(sent)  # the previous snapshot has left
+        for n in names:
+            snapW[n].copy_(layer.W[n], non_blocking=True)
+        snapped.record(compute)
+        with torch.cuda.stream(back):
+            back.wait_event(snapped)
+            for n in names:
+                hostW[n].copy_(snapW[n], non_blocking=True)
+                stats["d2h"] += snapW[n].numel() * 4
+            sent.record(back)
 
-    for i in range(W):
-        one(10_000 + i)
+    def run(first, count):
+        load(first)
+        for k in range(count):
+            one(first + k, k == count - 1)
+        compute.wait_stream(copy)
+        compute.wait_stream(back)
+
+    run(10_000, W)
     stats["h2d"] = stats["d2h"] = 0
-    ms = timed(torch, lambda: [one(10_000 + W + i) for i in range(K)], dist_ok)
+    ms = timed(torch, lambda: run(10_000 + W, K), dist_ok)
     ms = max_over_ranks(ms, dist_ok)
     return {"value": world * K / (ms * 1e-3), "unit": "steps/s",
-            "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K}
+            "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K,
+            "pipeline": "copies on two more streams (one per direction), double-buffered inputs, weights "
+                        "read back from a device-side snapshot; every copy inside the timed region",
+            "link": link_bandwidth(torch)}
+
+
+def link_bandwidth(torch):
+    """Pinned host <-> device copy bandwidth (GB/s) for 512 MB, each direction alone."""
+    n = 128 << 20
+    h = torch.empty(n, dtype=torch.float32).pin_memory()
+    d = torch.empty(n, dtype=torch.float32, device="cuda")
+    d.copy_(h, non_blocking=True)
+    h2d = timed(torch, lambda: d.copy_(h, non_blocking=True), False)
+    d2h = timed(torch, lambda: h.copy_(d, non_blocking=True), False)
+    return {"h2d_GBps": 4 * n / (h2d * 1e-3) / 1e9, "d2h_GBps": 4 * n / (d2h * 1e-3) / 1e9}
 
 
 # ------------------------------------------------------------------ the oracle on the host
