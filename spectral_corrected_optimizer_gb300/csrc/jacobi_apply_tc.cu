@@ -21,8 +21,9 @@
 //   warp 0      TMA producer (X of both column pairs, then the stage-2 rotations)
 //   warp 1      TMEM (256 columns: D1 of both column pairs, D2 of both row pairs)
 //               and the MMA issuer
-//   warps 2-5   transform: split X into hi / lo; build A2 from D1
-//   warps 6-9   epilogue: D2 -> both orientations in whole 128-byte lines
+//   warps 2-5   transform: split X into hi / lo; build A2 from D1 (first column pair)
+//   warps 6-9   epilogue: build A2 (second column pair); D2 -> both orientations in
+//               whole 128-byte lines
 //               (the transposed copy straight from registers, the mirror
 //               through a 32 x 33 shared tile per warp)
 // Every mbarrier wait is bounded; a wait that gives up records a code in the
@@ -139,6 +140,27 @@ __device__ __forceinline__ void load_stage1(const ApTask &k, int c, unsigned cha
     tma_load_2d(r + 24 * kKB, k.job->rot, kB, k.crow[c] + kP, bar);
 }
 
+// A2_r[c*64 + j][k] = Y_c[r*64 + k][j] for one column pair c: the thread of TMEM lane
+// rho = 32 q + lane holds k = 32 (q & 1) + lane of row pair r = q / 2, i.e. column
+// `lane` of K-atom (q & 1) in every row c*64 + j; 128-byte swizzled rows, hi and lo
+__device__ __forceinline__ void build_a2(unsigned char *smem, uint32_t tmem, int q, int lane, int c) {
+    const uint32_t tq = (uint32_t)(32 * q) << 16;
+    unsigned char *a2h = smem + (q >> 1) * 64 * kKB + (q & 1) * 16 * kKB, *a2l = a2h + 32 * kKB;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+        tmem_ld32(tmem + 64u * c + 32u * hh + tq, v);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int row = c * 64 + 32 * hh + jj;
+            const uint32_t off = row * 128 + ((((uint32_t)lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4;
+            float lo;
+            *reinterpret_cast<float *>(a2h + off) = tf32_split(v[jj], lo);
+            *reinterpret_cast<float *>(a2l + off) = lo;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kApThreads, 1)
 jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char ap_smem_raw[];
@@ -149,10 +171,11 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     uint64_t *xsplit = bar + 2;   // [2] X_c split into hi / lo (128 transform threads)
     uint64_t *s1done = bar + 4;   // stage-1 MMAs complete (commit)
     uint64_t *r2full = bar + 5;   // stage-2 rotations landed (producer, tx bytes)
-    uint64_t *a2ready = bar + 6;  // A2 built, D1 read (128 transform threads)
+    uint64_t *a2ready = bar + 6;  // A2 built, D1 read (128 transform + 128 epilogue threads)
     uint64_t *s2done = bar + 7;   // stage-2 MMAs complete (commit)
     uint64_t *d2free = bar + 8;   // D2 read by the epilogue (128 epilogue threads)
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 9);
+    uint64_t *s2half = bar + 9;   // stage-2 MMAs of row pair 0 complete (P0 and LO[0, 32) free)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 10);
     float *etile = reinterpret_cast<float *>(smem + 192 * kKB + 128);  // 4 epilogue warps x 32 x 33
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned char *LO = smem + kLO;
@@ -166,9 +189,10 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
         }
         mbar_init(s1done, 1);
         mbar_init(r2full, 1);
-        mbar_init(a2ready, 128);
+        mbar_init(a2ready, 256);
         mbar_init(s2done, 1);
         mbar_init(d2free, 128);
+        mbar_init(s2half, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -183,18 +207,21 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int i = 0, x_iss = 0, r_iss = 0;
+            int i = 0, iss[2] = {0, 0}, r_iss = 0;
             for (; i < n; ++i) {
                 const ApTask k = ap_task(ab, blockIdx.x + i * gridDim.x);
                 const uint32_t par = (uint32_t)i & 1u;
-                // P0 / P1 held the previous task's A2 until its stage-2 MMAs completed
-                if (!mbar_wait_bounded(s2done, par ^ 1u, flag, 0x311u)) break;
+                // P_c (and LO's half c) held the previous task's A2 (and R^T) of row pair c until
+                // its stage-2 MMAs of that row pair completed
+                bool ok = true;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
+                    if (!(ok = mbar_wait_bounded(c ? s2done : s2half, par ^ 1u, flag, 0x311u))) break;
                     unsigned char *p = smem + c * 64 * kKB;
                     load_stage1(k, c, p, p + 32 * kKB, &xfull[c]);
+                    ++iss[c];
                 }
-                ++x_iss;
+                if (!ok) break;
                 // LO holds this task's X lo until its stage-1 MMAs completed
                 if (!mbar_wait_bounded(s1done, par, flag, 0x312u)) break;
                 mbar_arrive_expect_tx(r2full, 64 * kKB);
@@ -209,9 +236,8 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
                 ++r_iss;
             }
             if (i < n) {  // gave up: let the last loads issued land before the CTA exits
-                if (x_iss > 0)
-                    for (int c = 0; c < 2; ++c)
-                        mbar_wait_bounded(&xfull[c], (uint32_t)(x_iss - 1) & 1u, flag, 0x313u);
+                for (int c = 0; c < 2; ++c)
+                    if (iss[c] > 0) mbar_wait_bounded(&xfull[c], (uint32_t)(iss[c] - 1) & 1u, flag, 0x313u);
                 if (r_iss > 0) mbar_wait_bounded(r2full, (uint32_t)(r_iss - 1) & 1u, flag, 0x313u);
             }
         }
@@ -244,8 +270,8 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
                 for (int r = 0; r < 2; ++r) {
                     const uint32_t a = smem_u32(smem + r * 64 * kKB), b = smem_u32(LO + r * 32 * kKB);
                     mma_3xtf32(tmem + 128u + 64u * r, a, a + 32 * kKB, b, b + 16 * kKB);
+                    mma_commit(r ? s2done : s2half);
                 }
-                mma_commit(s2done);
                 last = s2done;
             }
             if (i < n && pending) mbar_wait_bounded(last, last_par, flag, 0x325u);
@@ -253,7 +279,6 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     } else if (warp < 6) {
         // ---------------- transform: split X, then A2 from the stage-1 accumulators
         const int tid = threadIdx.x - 64, q = warp & 3;
-        const uint32_t tq = (uint32_t)(32 * q) << 16;
         for (int i = 0; i < n; ++i) {
             const uint32_t par = (uint32_t)i & 1u;
             bool ok = true;
@@ -268,24 +293,7 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
             }
             if (!ok || !mbar_wait_bounded(s1done, par, flag, 0x332u)) break;
             tc_fence_after();
-            // A2_r[c*64 + j][k] = Y_c[r*64 + k][j]: row rho = 32 q + lane is k = 32 (q & 1) + lane of
-            // row pair r = q / 2, i.e. column `lane` of K-atom (q & 1); 128-byte swizzled rows
-            unsigned char *a2h = smem + (q >> 1) * 64 * kKB + (q & 1) * 16 * kKB, *a2l = a2h + 32 * kKB;
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float v[32];
-                    tmem_ld32(tmem + 64u * c + 32u * hh + tq, v);
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int row = c * 64 + 32 * hh + jj;
-                        const uint32_t off = row * 128 + ((((uint32_t)lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4;
-                        float lo;
-                        *reinterpret_cast<float *>(a2h + off) = tf32_split(v[jj], lo);
-                        *reinterpret_cast<float *>(a2l + off) = lo;
-                    }
-                }
+            build_a2(smem, tmem, q, lane, 0);  // rows c = 0 of A2; the epilogue warps build c = 1
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(a2ready);
@@ -297,6 +305,12 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
         for (int i = 0; i < n; ++i) {
             const ApTask k = ap_task(ab, blockIdx.x + i * gridDim.x);
             const uint32_t par = (uint32_t)i & 1u;
+            if (!mbar_wait_bounded(s1done, par, flag, 0x342u)) break;
+            tc_fence_after();
+            build_a2(smem, tmem, q, lane, 1);  // rows c = 1 of A2
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(a2ready);
             if (!mbar_wait_bounded(s2done, par, flag, 0x341u)) break;
             tc_fence_after();
             float v[2][2][32];
