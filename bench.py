@@ -166,20 +166,28 @@ class ClockSampler:
 
 def gemm_flops(m: int, n: int) -> float:
     """Algorithmic flops of one matrix's step in the executed association
-    (4 r^2 max(m,n) + 4 r^3 with r = min(m,n)); equals 2 sum(M N K) of its 4 GEMMs."""
-    r, L = min(m, n), max(m, n)
-    return 4.0 * r * r * L + 4.0 * r ** 3
+    (2 sum(M N K) of its GEMMs): P_R G^T and P_L T for m = n; U^T G, P_R T1^T D,
+    U T2 for m > n; V^T G^T, P_L T1 D, T2 V^T for m < n."""
+    if m == n:
+        return 4.0 * n ** 3
+    if m > n:
+        return 4.0 * m * n * n + 2.0 * n ** 3
+    return 4.0 * m * m * n + 2.0 * m ** 3
 
 
 def step_bytes(m: int, n: int) -> float:
-    """Algorithmic HBM bytes of one matrix's step: G read, W/m/v read+write
-    (28 B per element), U and V read twice, intermediates written and read once,
-    G^T written and read for m > n."""
-    r, mn = min(m, n), m * n
-    b = 28.0 * mn + 8.0 * (m + n) * r + 8.0 * (2 * r * max(m, n) + r * r)
+    """Algorithmic HBM bytes of one matrix's step in the executed association:
+    the fused epilogue's G read and W, m, v read + write (28 B per element), every
+    GEMM operand read once, every intermediate written and read once, and G^T
+    written and read for m > n."""
+    mn = m * n
+    if m == n:
+        return 28.0 * mn + 4.0 * (m * m + n * n) + 4.0 * mn + 8.0 * mn
     if m > n:
-        b += 8.0 * mn
-    return b
+        r = n
+        return 28.0 * mn + 8.0 * mn + 4.0 * mn + 8.0 * m * r + 4.0 * n * n + 16.0 * n * r
+    r = m
+    return 28.0 * mn + 4.0 * mn + 8.0 * n * r + 4.0 * m * m + 16.0 * m * r
 
 
 class Layer:

@@ -166,4 +166,22 @@ int adamw_run(float *W, const float *G, float *m1, float *m2, int64_t n, const A
     return SPECOPTIM_OK;
 }
 
+namespace {
+__global__ void __launch_bounds__(256)
+scale_cols_kernel(const float *__restrict__ X, const float *__restrict__ d, int64_t total, int cols,
+                  float *__restrict__ out) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x)
+        out[e] = X[e] * d[e % cols];
+}
+}  // namespace
+
+int scale_cols_run(const float *X, const float *d, int64_t rows, int cols, float *out, cudaStream_t st) {
+    const int64_t total = rows * cols;
+    if (total == 0) return SPECOPTIM_OK;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 8 * 152);
+    SPCO_LAUNCH("scale_cols", st, scale_cols_kernel<<<blocks, 256, 0, st>>>(X, d, total, cols, out));
+    SPECOPTIM_LAUNCHED("scale_cols_kernel");
+    return SPECOPTIM_OK;
+}
+
 }  // namespace spco

@@ -2,21 +2,24 @@
 // Adaptation over Decentralized GPU Meshes", key designs 2 and 3): handle
 // lifecycle, anchor EMA, SVD refresh, and the step orchestration.
 //
-// Step (key design 3, projection + blend equations, then AdamW), evaluated as
-// four GEMMs whose operands are all stored K-contiguous (the layout the
+// Step (key design 3, projection + blend equations, then AdamW).  The filter
+//   G_filt = U diag(d) U^T G V diag(d) V^T = P_L G P_R,
+//   P_L = U diag(d) U^T (m x m),  P_R = V diag(d) V^T (n x n),
+// is evaluated in the association that needs the fewest flops for the shape;
+// the projectors it uses are formed once per SVD refresh (fp32-accurate
+// 3xTF32 products).  Every operand is stored K-contiguous (the layout the
 // tcgen05 path reads with TMA; the SIMT path reads the same buffers):
-//   m > n (tall, r = n):  G^T = transpose(G)
-//       T1  = U^T G          (r x n, K = m)
-//       Xf  = (T1 V) o dd^T  (r x r, K = n)      diag(d) X diag(d) in the epilogue
-//       Z^T = V Xf^T         (n x r, K = r)
-//       Gf  = U Z            (m x n, K = r)      blend + AdamW in the epilogue
-//   m <= n (wide, r = m):
-//       T^T = V^T G^T        (r x m, K = n)      G read as the K-contiguous operand
-//       Xf^T= (T^T U) o dd^T (r x r, K = m)
-//       Y   = U Xf           (m x r, K = r)
-//       Gf  = Y V^T          (m x n, K = r)      blend + AdamW in the epilogue
-// Both orders cost 4 r^2 max(m,n) + 4 r^3 flops, the cheaper of the two
-// associations of U^T G V and U X V^T for their shape.
+//   m = n:            T^T = P_R G^T     (n x m, K = n)      G read as the K-contiguous operand
+//                     Gf  = P_L T       (m x n, K = m)      blend + AdamW in the epilogue
+//   m > n (r = n):    G^T = transpose(G)
+//                     T1  = U^T G       (r x n, K = m)
+//                     T2^T= P_R T1^T D  (n x r, K = n)      diag(d) on the columns in the epilogue
+//                     Gf  = U T2        (m x n, K = r)      blend + AdamW in the epilogue
+//   m < n (r = m):    T1^T= V^T G^T     (r x m, K = n)
+//                     T2  = P_L T1 D    (m x r, K = m)      diag(d) on the columns in the epilogue
+//                     Gf  = T2 V^T      (m x n, K = r)      blend + AdamW in the epilogue
+// Flops: 4 n^3 (square), 4 m n^2 + 2 n^3 (tall), 4 m^2 n + 2 m^3 (wide), against
+// 8 n^3 and 4 r^2 max(m,n) + 4 r^3 for U^T G V and U X V^T in sequence.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -34,6 +37,7 @@ struct specoptim {
     int64_t t;
     float *M, *U, *s, *V, *d, *m1, *m2;
     float *Uo, *UTo, *Vo, *VTo;  // GEMM operand copies of the factors (TF32-rounded on the TC path)
+    float *PL, *PR;              // projectors U diag(d) U^T (m <= n) and V diag(d) V^T (m >= n)
     float *ws_g, *ws_a, *ws_x;   // step workspace: G^T (tall), T1/Z^T or T^T/Y, Xf
     float *ws_svd;
     bool have_factors;
@@ -108,7 +112,7 @@ int validate_cfg(const specoptim_config *c) {
 
 void free_all(specoptim_t *h) {
     float *bufs[] = {h->M, h->U, h->s, h->V, h->d, h->m1, h->m2, h->Uo, h->UTo,
-                     h->Vo, h->VTo, h->ws_g, h->ws_a, h->ws_x, h->ws_svd};
+                     h->Vo, h->VTo, h->ws_g, h->ws_a, h->ws_x, h->ws_svd, h->PL, h->PR};
     for (float *p : bufs)
         if (p) cudaFree(p);
 }
@@ -161,6 +165,7 @@ extern "C" int specoptim_create(specoptim_t **out, const specoptim_config *cfg, 
         {&h->m1, mn}, {&h->m2, mn}, {&h->Uo, mr}, {&h->UTo, mr}, {&h->Vo, nr}, {&h->VTo, nr},
         {&h->ws_g, h->tall ? mn : 4}, {&h->ws_a, h->tall ? (size_t)h->n * h->r : mr},
         {&h->ws_x, rr}, {&h->ws_svd, svd_workspace_floats(h->m, h->n)},
+        {&h->PL, h->m <= h->n ? (size_t)h->m * h->m : 4}, {&h->PR, h->m >= h->n ? (size_t)h->n * h->n : 4},
     };
     for (auto &b : plan) {
         cudaError_t e = cudaMalloc(reinterpret_cast<void **>(b.p), b.count * sizeof(float));
@@ -191,6 +196,26 @@ extern "C" int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void 
     return ema_run(h->M, G_anc, (int64_t)h->m * h->n, h->cfg.beta_anc,
                    static_cast<cudaStream_t>(stream));
 }
+
+namespace {
+
+// P = X diag(d) X^T (rows x rows) for a factor X (rows x r): X diag(d) into
+// `tmp`, then one fp32-accurate 3xTF32 product, rounded to TF32 when it feeds
+// the tensor-core step
+int form_projector(const float *X, const float *d, int rows, int r, float *P, float *tmp, bool round,
+                   cudaStream_t st) {
+    int rc = scale_cols_run(X, d, rows, r, tmp, st);
+    if (rc) return rc;
+    float *ws = nullptr;
+    if ((rc = scratch_floats(gemm3_workspace_floats(rows, rows, r), &ws))) return rc;
+    Epilogue e;
+    e.C = P;
+    e.ldc = rows;
+    e.round_tf32 = round;
+    return gemm_fp32x3(rows, rows, r, Operand{X, r, false}, Operand{tmp, r, true}, e, ws, st);
+}
+
+}  // namespace
 
 extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
                                           int32_t *sweeps_out) {
@@ -236,6 +261,8 @@ extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t c
         if ((r2 = transpose_run(h->V, h->VTo, h->n, h->r, round, st))) return r2;
         if ((r2 = transpose_run(h->UTo, h->Uo, h->r, h->m, false, st))) return r2;
         if ((r2 = transpose_run(h->VTo, h->Vo, h->r, h->n, false, st))) return r2;
+        if (h->m <= h->n && (r2 = form_projector(h->U, h->d, h->m, h->r, h->PL, h->ws_svd, round, st))) return r2;
+        if (h->m >= h->n && (r2 = form_projector(h->V, h->d, h->n, h->r, h->PR, h->ws_svd, round, st))) return r2;
         h->have_factors = true;
     }
     int r3 = check_device_flag(st);
@@ -250,10 +277,13 @@ extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *swee
 
 namespace {
 
-// The four products of one handle's step, in the order they must run, with
-// their epilogues; `transpose` is set when G^T must be formed first (m > n).
+// The products of one handle's step (two or three) with their epilogues, in
+// slots 3 - count .. 2 so that every handle's last (AdamW) product is slot 2;
+// `transpose` is set when G^T must be formed first (m > n).
+constexpr int kSlots = 3;
 struct StepPlan {
-    GemmProblem stage[4];
+    GemmProblem stage[kSlots];
+    int first;  // first used slot
     bool transpose;
     const float *G;
     float *GT;
@@ -312,30 +342,37 @@ StepPlan plan_step(specoptim_t *h, float *W, const float *G_mask, float lr, floa
                  int64_t ldb, const Epilogue &e) {
         return GemmProblem{M, N, K, Operand{A, lda, false}, Operand{B, ldb, true}, e};
     };
-    if (h->tall) {
-        float *T1 = h->ws_a, *Xf = h->ws_x, *ZT = h->ws_a;
-        plain.C = T1;
-        plain.ldc = n;
-        P.stage[0] = nt(r, n, m, h->UTo, m, P.GT, m, plain);      // T1  = U^T G
-        scaled.C = Xf;
-        scaled.ldc = r;
-        P.stage[1] = nt(r, r, n, T1, n, h->VTo, n, scaled);       // Xf  = (T1 V) o dd^T
-        plain.C = ZT;
-        plain.ldc = r;
-        P.stage[2] = nt(n, r, r, h->Vo, r, Xf, r, plain);         // Z^T = V Xf^T
-        P.stage[3] = nt(m, n, r, h->Uo, r, ZT, r, last);          // G_filt = U Z -> AdamW
-    } else {
-        float *TT = h->ws_a, *XfT = h->ws_x, *Y = h->ws_a;
+    Epilogue cols = plain;  // diag(d) on the columns
+    cols.mode = EPI_SCALE;
+    cols.col_scale = h->d;
+    if (m == n) {
+        float *TT = h->ws_a;
         plain.C = TT;
         plain.ldc = m;
-        P.stage[0] = nt(r, m, n, h->VTo, n, G_mask, n, plain);    // T^T = V^T G^T
-        scaled.C = XfT;
-        scaled.ldc = r;
-        P.stage[1] = nt(r, r, m, TT, m, h->UTo, m, scaled);       // Xf^T = (T^T U) o dd^T
-        plain.C = Y;
-        plain.ldc = r;
-        P.stage[2] = nt(m, r, r, h->Uo, r, XfT, r, plain);        // Y = U Xf
-        P.stage[3] = nt(m, n, r, Y, r, h->Vo, r, last);           // G_filt = Y V^T -> AdamW
+        P.first = 1;
+        P.transpose = false;
+        P.stage[1] = nt(n, m, n, h->PR, n, G_mask, n, plain);     // T^T = P_R G^T
+        P.stage[2] = nt(m, n, m, h->PL, m, TT, m, last);          // G_filt = P_L T -> AdamW
+    } else if (h->tall) {
+        float *T1 = h->ws_a, *T2T = h->ws_x;
+        plain.C = T1;
+        plain.ldc = n;
+        P.first = 0;
+        P.stage[0] = nt(r, n, m, h->UTo, m, P.GT, m, plain);      // T1 = U^T G
+        cols.C = T2T;
+        cols.ldc = r;
+        P.stage[1] = nt(n, r, n, h->PR, n, T1, n, cols);          // T2^T = P_R T1^T D
+        P.stage[2] = nt(m, n, r, h->Uo, r, T2T, r, last);         // G_filt = U T2 -> AdamW
+    } else {
+        float *T1T = h->ws_a, *T2 = h->ws_x;
+        plain.C = T1T;
+        plain.ldc = m;
+        P.first = 0;
+        P.stage[0] = nt(r, m, n, h->VTo, n, G_mask, n, plain);    // T1^T = V^T G^T
+        cols.C = T2;
+        cols.ldc = r;
+        P.stage[1] = nt(m, r, m, h->PL, m, T1T, m, cols);         // T2 = P_L T1 D
+        P.stage[2] = nt(m, n, r, T2, r, h->Vo, r, last);          // G_filt = T2 V^T -> AdamW
     }
     return P;
 }
@@ -356,7 +393,7 @@ extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, flo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const StepPlan P = plan_step(h, W, G_mask, lr, G_filt_out, G_proj_out);
     if (P.transpose && (rc = transpose_run(P.G, P.GT, P.m, P.n, P.round, st))) return rc;
-    for (int s = 0; s < 4; ++s)
+    for (int s = P.first; s < kSlots; ++s)
         if ((rc = run_problem(h->cfg.precision, P.stage[s], st))) return rc;
     return SPECOPTIM_OK;
 }
@@ -379,13 +416,14 @@ extern "C" int specoptim_step_many(specoptim_t *const *handles, int32_t count, f
         if (plans[i].transpose &&
             (rc = transpose_run(plans[i].G, plans[i].GT, plans[i].m, plans[i].n, plans[i].round, st)))
             return rc;
-    for (int s = 0; s < 4; ++s) {
-        // tensor-core problems of this stage share launches (largest first, 8 per launch);
+    for (int s = 0; s < kSlots; ++s) {
+        // tensor-core problems of this slot share launches (largest first, 8 per launch);
         // the rest run one by one on the SIMT path
         GemmProblem group[16];
         double work[16];
         int ng = 0;
         for (int i = 0; i < count; ++i) {
+            if (s < plans[i].first) continue;
             const GemmProblem &q = plans[i].stage[s];
             if (handles[i]->cfg.precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(q.M, q.N, q.K, q.A, q.B)) {
                 group[ng] = q;

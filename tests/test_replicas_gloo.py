@@ -59,6 +59,7 @@ def test_reference_arm_prints_only_on_rank_zero():
 def test_single_rank_helpers_need_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, False) == 3.5
-    assert bench.gemm_flops(2048, 2048) == 4.0 * 2048 ** 3 + 4.0 * 2048 ** 3
-    # tall and wide shapes use the cheaper association: 4 r^2 max(m,n) + 4 r^3
-    assert bench.gemm_flops(8192, 2048) == bench.gemm_flops(2048, 8192)
+    # square: P_R G^T then P_L T (two n^3 products)
+    assert bench.gemm_flops(2048, 2048) == 2 * (2.0 * 2048 ** 3)
+    # tall and wide are mirror images: 2 r L n + 2 r^3 + 2 L n r with r = min, L = max
+    assert bench.gemm_flops(8192, 2048) == bench.gemm_flops(2048, 8192) == 4.0 * 8192 * 2048 ** 2 + 2.0 * 2048 ** 3
