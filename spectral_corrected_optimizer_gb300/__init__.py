@@ -8,7 +8,8 @@ library every call raises.
 
 Method: "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes"
 (arXiv 2609.14339), key designs 1 (activation mask), 2 (anchor EMA) and 3
-(spectral-correction optimizer).
+(spectral-correction optimizer); key design 4 (PowerSGD-compressed outer
+synchronisation) is bound in the ``dpsync`` submodule.
 """
 from __future__ import annotations
 
@@ -40,7 +41,16 @@ class Config(ctypes.Structure):
                 ("svd_tol", ctypes.c_float), ("svd_inner_sweeps", ctypes.c_int32)]
 
 
-# (name, restype, argtypes) of every exported entry point of include/specoptim.h
+class DPConfig(ctypes.Structure):
+    """dpsync_config of include/dpsync.h."""
+    _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("ratio", ctypes.c_float), ("error_feedback", ctypes.c_int32),
+                ("outer_lr", ctypes.c_float), ("outer_momentum", ctypes.c_float),
+                ("mix", ctypes.c_float)]
+
+
+# (name, restype, argtypes) of every exported entry point of include/specoptim.h and
+# include/dpsync.h
 _vp, _i32, _i64, _u32, _u64, _f32, _f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                            ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float,
                                            ctypes.c_double)
@@ -70,6 +80,18 @@ SIGNATURES = [
     ("mask_pack", _int, [_vp, _vp, _i64, _i32, _i32, _i32, _u32, _u64, _u64, _vp]),
     ("mask_unpack", _int, [_vp, _vp, _i64, _i32, _i32, _i32, _u32, _u64, _u64, _vp]),
     ("mask_indices", _int, [_vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
+    ("dpsync_rank", _i32, [_i32, _i32, _f32]),
+    ("dpsync_config_default", _int, [ctypes.POINTER(DPConfig), _i32, _i32]),
+    ("dpsync_create", _int, [ctypes.POINTER(_vp), ctypes.POINTER(DPConfig), _vp, _vp, _vp]),
+    ("dpsync_handle_rank", _i32, [_vp]),
+    ("dpsync_destroy", _int, [_vp]),
+    ("dpsync_set_outer", _int, [_vp, _vp, _vp]),
+    ("dpsync_compress_p_many", _int, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp]),
+    ("dpsync_orthogonalize_many", _int, [ctypes.POINTER(_vp), _i32, _vp]),
+    ("dpsync_compress_q_many", _int, [ctypes.POINTER(_vp), _i32, _vp]),
+    ("dpsync_decompress_many", _int, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _f32, _vp]),
+    ("dpsync_outer_step_many", _int, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _f32, _vp]),
+    ("dpsync_get_state", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
 ]
 
 _lib = None

@@ -13,6 +13,9 @@ Readings of the workload text (stated once, used everywhere):
     gradient + N(0,1e-2) noise, fresh noise for every steady step.
   * Activations / activation gradients for the mask: ~N(0,1), rounded to bf16
     (round to nearest even) where the workload says bf16.
+  * Data-parallel outer synchronisation: the starting PowerSGD Q ~N(0,1) (the
+    same on every worker); a worker's weights after one outer period are the
+    outer weights minus a drift ~N(0, 1e-3), fresh per worker and period.
 
 Every stream is keyed by ``numpy.random.SeedSequence([seed, tag, index])`` so
 that any single tensor can be regenerated on its own.
@@ -24,6 +27,7 @@ import numpy as np
 # tags that separate independent random streams
 _TAG_W, _TAG_SIG_A, _TAG_SIG_B, _TAG_ANC_NOISE, _TAG_MASK_NOISE = 1, 2, 3, 4, 5
 _TAG_H, _TAG_GRAD = 6, 7
+_TAG_DP_Q, _TAG_DP_DRIFT = 8, 9
 
 # shapes (out_features m, in_features n) of one Llama-3.2-1B decoder layer
 LLAMA_1B_LAYER = {
@@ -126,3 +130,14 @@ def act_grads_f32(rows: int, H: int, seed: int = 0, index: int = 0) -> np.ndarra
 
 def act_grads_bf16(rows: int, H: int, seed: int = 0, index: int = 0) -> np.ndarray:
     return f32_to_bf16_bits(act_grads_f32(rows, H, seed, index))
+
+
+def dp_q0(n: int, k: int, seed: int = 0, index: int = 0) -> np.ndarray:
+    """Starting Q (n x k) of the PowerSGD power step, ~N(0, 1)."""
+    return normal_f32(seed, _TAG_DP_Q, index, (n, k), 1.0)
+
+
+def dp_drift(m: int, n: int, seed: int = 0, worker: int = 0, period: int = 0,
+             scale: float = 1e-3) -> np.ndarray:
+    """Change of one worker's weights over one outer period, ~N(0, scale)."""
+    return normal_f32(seed, _TAG_DP_DRIFT, worker * 1_000_003 + period, (m, n), scale)

@@ -79,3 +79,23 @@ def test_null_handles_are_rejected(lib):
     assert lib.specoptim_step(None, None, None, 1e-3, None, None, None) == so.ERR_INVALID_ARG
     assert lib.specoptim_svd_refresh(None, None, None) == so.ERR_INVALID_ARG
     assert lib.specoptim_destroy(None) == so.OK
+
+
+def test_dpsync_rank_matches_the_oracle(lib):
+    for m, n in [(2048, 2048), (512, 2048), (8192, 2048), (2048, 8192), (14336, 4096), (256, 128),
+                 (4, 4), (1, 7), (100, 3)]:
+        assert lib.dpsync_rank(m, n, 64.0) == oracle.dpsync_rank(m, n, 64.0)
+    assert lib.dpsync_rank(0, 4, 64.0) == -1 and lib.dpsync_rank(4, 4, 0.0) == -1
+
+
+@pytest.mark.parametrize("field,value", [("m", 0), ("n", 6), ("rank", 65), ("rank", -1), ("mix", 1.5)])
+def test_dpsync_create_rejects_bad_config_before_touching_the_gpu(lib, field, value):
+    cfg = so.DPConfig()
+    assert lib.dpsync_config_default(ctypes.byref(cfg), 256, 128) == so.OK
+    assert (cfg.ratio, cfg.error_feedback, cfg.mix) == (64.0, 1, 0.0)
+    setattr(cfg, field, value)
+    h = ctypes.c_void_p()
+    dummy = ctypes.c_void_p(1 << 20)
+    assert lib.dpsync_create(ctypes.byref(h), ctypes.byref(cfg), dummy, dummy, None) == so.ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.dpsync_compress_p_many(None, 1, None, None, None) == so.ERR_INVALID_ARG
