@@ -407,6 +407,76 @@ def mask_sweep(layer: Layer, p: float):
     return out
 
 
+def dp_sync_bytes(m: int, n: int, k: int) -> dict:
+    """Algorithmic HBM bytes of one outer synchronisation of an m x n matrix at
+    rank k, per kernel: compress_p reads theta, W_local and E and writes E
+    (16 B per element) with P written and Q read once; compress_q reads M once
+    and P^ once and writes Q; the outer step reads and writes E, theta and the
+    momentum and writes W_local (28 B per element) with P^ and Q read once; the
+    orthogonalisation reads P three times and writes P^."""
+    lo = 4.0 * (m + n) * k
+    return {"compress_p": 16.0 * m * n + lo, "compress_q": 4.0 * m * n + lo,
+            "outer_step": 28.0 * m * n + lo, "orth": 16.0 * m * k}
+
+
+def run_dp_sync(shapes, K: int, W: int, peaks: dict, peak_src: str, seed: int = 0) -> dict:
+    """PowerSGD-compressed outer synchronisation (key design 4) of the matrices
+    `shapes` on this GPU: W warm-up and K timed syncs, then one traced sync for
+    the per-kernel split.  One worker per GPU (replicas: the sums over workers
+    are the identity), 64x rank rule."""
+    import torch
+
+    import spectral_corrected_optimizer_gb300 as so
+    import spectral_corrected_optimizer_gb300.dpsync as dp
+    import synthetic
+
+    Q0 = [torch.from_numpy(synthetic.dp_q0(n, dp.rank_for(m, n), seed=seed, index=i))
+          for i, (m, n) in enumerate(shapes)]
+    g = dp.DPSyncGroup(shapes, Q0=Q0)
+    theta = [torch.from_numpy(synthetic.normal_f32(seed, 1, i, (m, n), 0.02)).cuda() for i, (m, n) in enumerate(shapes)]
+    g.set_outer(theta)
+    drift = [torch.from_numpy(synthetic.dp_drift(m, n, seed=seed, worker=0, period=i)).cuda()
+             for i, (m, n) in enumerate(shapes)]
+    W_local = [t - d for t, d in zip(theta, drift)]
+
+    for _ in range(W):
+        g.outer_sync(W_local)
+    torch.cuda.synchronize()
+    so.trace_reset()
+    ms = timed(torch, lambda: [g.outer_sync(W_local) for _ in range(K)], False)
+    launches = so.launch_count()
+    so.trace_enable(True)
+    traced_ms = timed(torch, lambda: g.outer_sync(W_local), False)
+    rep = so.trace_report()
+    so.trace_enable(False)
+    byts = {key: sum(dp_sync_bytes(m, n, k)[key] for (m, n), k in zip(shapes, g.ranks))
+            for key in ("compress_p", "compress_q", "outer_step", "orth")}
+    hbm = peaks["hbm_gbs"]
+
+    def roof(kernel, trace_name, b):
+        n_l, t = rep.get(trace_name, (0, 0.0))
+        ach = b / (t * 1e-3) / 1e9 if t > 0 else None
+        return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm if ach else None, "avg_launch_ms": t / max(n_l, 1),
+                "algorithmic_bytes_per_launch": b}
+
+    total_bytes = sum(byts.values())
+    values = sum(m * n for m, n in shapes)
+    sent = sum((m + n) * k for (m, n), k in zip(shapes, g.ranks))
+    out = {"syncs_per_s": K / (ms * 1e-3), "ms_per_sync": ms / K, "gpu_launches_per_sync": launches / K,
+           "ranks": g.ranks, "compression": values / sent,
+           "hbm_bound_ms": 1e3 * total_bytes / (hbm * 1e9), "frac_of_hbm_bound": 1e3 * total_bytes / (hbm * 1e9) / (ms / K),
+           "rooflines": [roof("dp_compress_p", "dp_compress_p", byts["compress_p"]),
+                         roof("dp_compress_q", "dp_compress_q", byts["compress_q"]),
+                         roof("dp_update (outer step)", "dp_outer_step", byts["outer_step"])],
+           "kernels_traced_ms": {k: round(v[1], 4) for k, v in rep.items()}, "traced_sync_ms": traced_ms,
+           "peak_source": "%s HBM copy bandwidth" % peak_src,
+           "note": "one worker per GPU: the all-reduces of P and Q are the identity; the outer step "
+                   "(Nesterov, lr 0.7, momentum 0.9) and error feedback run every sync"}
+    g.close()
+    return out
+
+
 def run_ours(args, rank, world, local_rank, dist_ok):
     import torch
 
@@ -449,6 +519,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     refresh_rep = so.trace_report()
     so.trace_enable(False)
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
+    import synthetic as _syn
+    dp_sync = run_dp_sync(list(_syn.LLAMA_1B_LAYER.values()), max(5, min(K, 20)), 3, peaks, peak_src, seed=rank)
     others = {}
     if not args.no_configs:
         import synthetic
@@ -535,6 +607,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                       "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()},
                       "refresh_kernels": {k: {"launches": v[0], "ms": round(v[1], 3)} for k, v in refresh_rep.items()}},
         "mask": dict(mask, frac_of_hbm=mask_frac, hbm_peak_GBps=peaks["hbm_gbs"]),
+        "dp_outer_sync": dict(dp_sync, workload="PowerSGD-compressed Streaming DiLoCo outer sync of the "
+                                                "llama-3.2-1b decoder layer (7 matrices, rank for 64x)"),
         "other_configs": others,
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak},
     }
@@ -717,7 +791,8 @@ def run_profile_case(args):
     'gate': steady spectral steps of one 8192x2048 matrix (transpose + 4 GEMMs per step);
     'mask': pack / unpack of one bf16 [65536, 2048] boundary at p = 0.95;
     'refresh': anchor EMA + SVD refresh of one 2048x2048 matrix, twice (the second warm);
-    'layer': batched refresh, then grouped steady steps of the 7-matrix 1B layer."""
+    'layer': batched refresh, then grouped steady steps of the 7-matrix 1B layer;
+    'dpsync': PowerSGD-compressed outer syncs of the 7-matrix 1B layer."""
     import numpy as np
     import torch
 
@@ -739,6 +814,16 @@ def run_profile_case(args):
         layer.refresh(0)
         for i in range(n_iter):
             layer.spectral(i)
+    elif args.profile == "dpsync":
+        import spectral_corrected_optimizer_gb300.dpsync as dp
+        shapes = list(synthetic.LLAMA_1B_LAYER.values())
+        g = dp.DPSyncGroup(shapes, seed=0)
+        theta = [torch.from_numpy(synthetic.normal_f32(0, 1, i, (m, n), 0.02)).cuda() for i, (m, n) in enumerate(shapes)]
+        g.set_outer(theta)
+        W_local = [t - torch.from_numpy(synthetic.dp_drift(m, n, period=i)).cuda()
+                   for i, (t, (m, n)) in enumerate(zip(theta, shapes))]
+        for i in range(n_iter):
+            g.outer_sync(W_local)
     elif args.profile == "refresh":
         inp = synthetic.MatrixInputs(2048, 2048, seed=0, rank=32)
         opt = so.SpectralOptimizer(2048, 2048)
@@ -768,7 +853,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the full-1B and 7B-layer measurements reported beside the headline")
-    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer"], default=None,
+    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync"], default=None,
                     help="run a small case for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -2,19 +2,24 @@
 // "Communication-Efficient LLM Adaptation over Decentralized GPU Meshes": the
 // Streaming DiLoCo outer step travels PowerSGD-compressed, 64x).
 //
-// Every kernel here streams the m x n matrices once and does O(k) fp32 work
-// per element (k <= 64), so they are HBM-bound: fp32 FMA on the SIMT cores
-// from operands staged in shared memory with cp.async, 8 x 8 register tiles
-// (one shared-memory load per four FMAs), grids sized by rows / tiles, and
-// deterministic split reductions (partials + last-arriving CTA, fixed order).
+// The m x n streams are HBM-bound with O(k) fp32 work per element (k <= 64):
+// persistent CTAs fed by 1D bulk copies (cp.async.bulk) into a ring of
+// shared-memory stages, fp32 FMA on the SIMT cores in 8 x 8 (or 4 x 8)
+// register tiles, and deterministic split reductions in a fixed order.  The
+// k x k orthogonalisation never touches fp64 (slow on this part): products and
+// sums are carried in two floats (hi + lo) and the triangular factors are
+// applied in fp32.
 //
-//   dp_compress_p_kernel   M = E + X - Y -> E;  P = M Q
-//   dp_gram_kernel         Gram matrix of P (or of P T1) in two-float precision,
-//                          then (last CTA) Cholesky in fp64 and T = R^-1
-//   dp_orth_apply_kernel   P^ = (P T1) T2      (two passes of Cholesky QR)
-//   dp_compress_q_kernel   Q = M^T P^
-//   dp_update_kernel       D = s P^ Q^T;  E <- M - D;  out = D  or the outer
-//                          Nesterov step and the restart of W_local
+//   dp_pad_q_kernel      Q (n x k) -> Qp (n x (kp+4)), zero padded, for bulk copies
+//   dp_compress_p_kernel M = E + X - Y -> E;  P = M Q
+//   dp_gram_kernel       Gram matrix of P (pass 0) or of P R1^-1 (pass 1) in two
+//                        floats; the last CTA of a matrix factors it (Cholesky,
+//                        two floats) and stores R with its reciprocal diagonal
+//   dp_orth_apply_kernel P^ = (P R1^-1) R2^-1 by forward substitution
+//   dp_compress_q_kernel partial Q = M^T P^ per row range
+//   dp_q_reduce_kernel   Q = sum of the partials (range order)
+//   dp_update_kernel     D = s P^ Q^T;  E <- M - D;  out = D, or the outer
+//                        Nesterov step and the restart of W_local
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,7 +29,7 @@
 #include <vector>
 
 #include "../../include/dpsync.h"
-#include "common.cuh"
+#include "tc.cuh"
 
 struct dpsync {
     dpsync_config cfg;
@@ -33,10 +38,13 @@ struct dpsync {
     float *E;              // m x n: M between compress_p and decompress, then the error
     float *theta, *mom;    // m x n each, allocated by set_outer
     float *Ph;             // m x kp orthonormal basis (padded columns are zero)
-    float *T;              // 2 x kp x kp: R1^-1, R2^-1 of the two Cholesky QR passes
-    double *Gpart;         // gram tasks x kp(kp+1)/2 partial Gram matrices
+    float *Qp;             // n x (kp + 4) padded copy of Q for compress_p
+    float *T;              // 2 x kp x kp: R1, R2 (strict upper part) with reciprocal diagonals
+    float *Gpart;          // gram tasks x blocks x 16 x 2 partial Gram matrices (hi, lo)
     float *Qpart;          // q row ranges x ncb*128 x kp partial Q
-    int *counters;         // [0, 2): gram passes; [2, 2 + ncb): Q column blocks
+    int *counters;         // [0, 2): gram passes
+    CUtensorMap *maps;     // device: X, Y, E (compress_p boxes), Qp, E (compress_q boxes), P^
+    const float *map_x, *map_y;  // the X and Y the first two maps describe
     int gram_tasks, q_ranges, ncb;
     bool have_outer;
 };
@@ -45,47 +53,33 @@ namespace spco {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxJobs = DPSYNC_MAX_BATCH;
+constexpr int kPBC = 64;         // compress_p columns per stage
+constexpr int kPMaxStages = 6;
 constexpr int kGramRows = 128;   // rows per Gram task
 constexpr int kQRows = 512;      // rows per compress_q task
 constexpr int kQCols = 128;      // columns per compress_q task
 constexpr int kQChunk = 16;      // rows per compress_q stage
 constexpr int kQStages = 4;
-constexpr int kPStages = 2;
-constexpr int kTileRows = 64;    // dp_update tile
-constexpr int kTileCols = 256;
-constexpr double kDrop = 1e-10;  // dependent column: residual^2 <= kDrop * norm^2
+constexpr int kURows = 256;      // rows per dp_update task
+constexpr int kUTile = 32;       // rows per dp_update tile (8 warps x 4 rows)
+constexpr int kUCols = 128;      // columns per dp_update task
+constexpr int kApplyRows = 256;  // rows per dp_orth_apply CTA (one per thread)
+constexpr float kDrop = 1e-10f;  // dependent column: residual^2 <= kDrop * norm^2
 
 inline int pad_rank(int k) { return k <= 8 ? 8 : k <= 16 ? 16 : k <= 32 ? 32 : 64; }
 
-// compress_p tiling per padded rank: R rows per CTA streamed in BC-column chunks.
-struct PCfg {
-    int R, BC, tiles, cs;
-};
-__host__ __device__ inline PCfg p_cfg(int kp) {
-    // 8 x 8 register tiles: (R/8)(kp/8) tiles over 8 warps, cs warps per tile
-    // split the columns
-    PCfg c;
-    c.R = kp == 64 ? 8 : 16;
-    c.BC = 128;
-    c.tiles = (c.R / 8) * (kp / 8);
-    c.cs = 8 / c.tiles;
-    return c;
-}
-inline int p_stage_floats(int kp) { return 3 * 2048 + 128 * (kp + 4); }
+__host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
-// ---------------------------------------------------------------------------
-// cp.async (sm_80+): 16-byte and 4-byte asynchronous copies global -> shared;
-// a source size of 0 fills the destination with zeros.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
+__device__ __forceinline__ int find_job(const int *begins, int count, int b) {
+    int j = 0;
+    while (j + 1 < count && b >= begins[j + 1]) ++j;
+    return j;
 }
-__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
+
+// cp.async (sm_80+): 16-byte asynchronous copy global -> shared
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -109,353 +103,385 @@ __device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// compress_p:  M = E + X - Y -> E (global);  P = M Q
+// two-float arithmetic (x = hi + lo, |lo| <= ulp(hi) / 2): error-free sum
+// (Knuth) and product (fma), with every operation rounded explicitly so that
+// the compiler cannot contract them.
 // ---------------------------------------------------------------------------
-struct PJob {
-    const float *X, *Y;
-    float *E;
-    const float *Q;
-    float *P;
-    int m, n, k, kp, ef, cta_begin;
+struct df {
+    float hi, lo;
 };
-struct PBatch {
-    PJob job[DPSYNC_MAX_BATCH];
-    int count, stage_floats;
+__device__ __forceinline__ df two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ df quick_two_sum(float a, float b) {  // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ df df_add(df x, df y) {
+    const df s = two_sum(x.hi, y.hi);
+    return quick_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ df df_neg(df x) { return {-x.hi, -x.lo}; }
+__device__ __forceinline__ df df_mul(df x, df y) {
+    const float p = __fmul_rn(x.hi, y.hi);
+    float e = __fmaf_rn(x.hi, y.hi, -p);
+    e = __fmaf_rn(x.hi, y.lo, e);
+    e = __fmaf_rn(x.lo, y.hi, e);
+    return quick_two_sum(p, e);
+}
+// 1 / x: fp32 estimate and one Newton step in two floats (x > 0)
+__device__ __forceinline__ df df_recip(df x) {
+    const float r = __frcp_rn(x.hi);
+    const df xr = df_mul(x, df{r, 0.f});                     // x r ~ 1
+    const df one_minus = df_add(df{1.f, 0.f}, df_neg(xr));  // 1 - x r
+    return df_add(df{r, 0.f}, df_mul(df{r, 0.f}, one_minus));
+}
+// sqrt(x): fp32 estimate and one Newton step in two floats (x > 0)
+__device__ __forceinline__ df df_sqrt(df x) {
+    const float r = __fsqrt_rn(x.hi);
+    const df rr = df_mul(df{r, 0.f}, df{r, 0.f});
+    const df d = df_add(x, df_neg(rr));                      // x - r^2
+    return df_add(df{r, 0.f}, df{__fdiv_rn(d.hi, __fmul_rn(2.f, r)), 0.f});
+}
+// (hi, lo) accumulation of a product of two floats: the product split exactly
+// by an fma, the running sum by TwoSum; lo collects all rounding errors.
+__device__ __forceinline__ void df_acc(float &hi, float &lo, float a, float b) {
+    const float p = __fmul_rn(a, b);
+    const float pe = __fmaf_rn(a, b, -p);
+    const df s = two_sum(hi, p);
+    hi = s.hi;
+    lo = __fadd_rn(lo, __fadd_rn(s.lo, pe));
+}
+
+// ---------------------------------------------------------------------------
+// dp_pad_q_kernel: Qp[j][c] = Q[j][c] for c < k, 0 for k <= c < kp + 4
+// ---------------------------------------------------------------------------
+struct PadJob {
+    const float *Q;
+    float *Qp;
+    int n, k, kp;
+    int64_t begin;
+};
+struct PadBatch {
+    PadJob job[kMaxJobs];
+    int count;
+    int64_t total;
 };
 
-__device__ __forceinline__ int find_job(const int *begins, int count, int b) {
-    int j = 0;
-    while (j + 1 < count && b >= begins[j + 1]) ++j;
-    return j;
+__global__ void __launch_bounds__(kThreads) dp_pad_q_kernel(const __grid_constant__ PadBatch B) {
+    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < B.total; e += (int64_t)gridDim.x * kThreads) {
+        int j = 0;
+        while (j + 1 < B.count && e >= B.job[j + 1].begin) ++j;
+        const PadJob &J = B.job[j];
+        const int64_t f = e - J.begin;
+        const int w = J.kp + 4;
+        const int64_t row = f / w;
+        const int c = (int)(f % w);
+        J.Qp[f] = c < J.k ? J.Q[row * J.k + c] : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// compress_p:  M = E + X - Y -> E (global);  P = M Q
+// Task: R rows (16; 8 for kp = 64) of one matrix over all its columns, in
+// stages of 64 columns.  Thread 0 keeps a ring of stages in flight: per stage
+// one 2D TMA box (64 columns x R rows) of each of X, Y, E and one of Qp (the
+// stage's 64 rows of Q, padded), all completing on the stage's mbarrier; the
+// boxes are zero-filled outside the matrices.  The warps form M (written to
+// global E from registers and in place of the E box), and the 8 warps
+// accumulate P in 8 x 8 register tiles ((R/8)(kp/8) tiles, cs warps per tile
+// splitting the columns); the task's last stage reduces the tiles over lanes
+// and warps.  A stage is refilled as soon as it is consumed.
+// ---------------------------------------------------------------------------
+constexpr int kPRows = 16;
+struct PJob {
+    const CUtensorMap *mx, *my, *me, *mq;
+    float *E, *P;
+    int m, n, k, kp, hasY, ef, R, nch, task_begin;
+};
+struct PBatch {
+    PJob job[kMaxJobs];
+    int count, total_tasks, stages;
+    uint32_t stage_bytes;
+    unsigned *flag;
+};
+constexpr int kPBuf = kPRows * kPBC;  // floats of one input box (R x 64)
+
+struct PCursor {
+    int task, chunk, job;  // task < 0: past the end
+};
+__device__ __forceinline__ void p_first(PCursor &c, const PBatch &B, const int *begins) {
+    c.task = blockIdx.x < (unsigned)B.total_tasks ? (int)blockIdx.x : -1;
+    c.chunk = 0;
+    c.job = c.task >= 0 ? find_job(begins, B.count, c.task) : 0;
+}
+__device__ __forceinline__ void p_advance(PCursor &c, const PBatch &B, const int *begins) {
+    if (c.task < 0) return;
+    if (++c.chunk < B.job[c.job].nch) return;
+    c.chunk = 0;
+    c.task += gridDim.x;
+    if (c.task >= B.total_tasks) {
+        c.task = -1;
+        return;
+    }
+    c.job = find_job(begins, B.count, c.task);
+}
+
+__device__ __forceinline__ void p_issue(const PBatch &B, const PCursor &c, unsigned char *stage, uint64_t *bar) {
+    const PJob &J = B.job[c.job];
+    const int row0 = (c.task - J.task_begin) * J.R, col0 = c.chunk * kPBC;
+    const uint32_t box = (uint32_t)J.R * kPBC * 4u, qbox = (uint32_t)kPBC * (J.kp + 4) * 4u;
+    const uint32_t nin = 1u + (J.hasY ? 1u : 0u) + (J.ef ? 1u : 0u);
+    float *xs = reinterpret_cast<float *>(stage), *ys = xs + kPBuf, *es = ys + kPBuf, *qs = es + kPBuf;
+    mbar_arrive_expect_tx(bar, box * nin + qbox);
+    tma_load_2d(xs, J.mx, col0, row0, bar);
+    if (J.hasY) tma_load_2d(ys, J.my, col0, row0, bar);
+    if (J.ef) tma_load_2d(es, J.me, col0, row0, bar);
+    tma_load_2d(qs, J.mq, 0, col0, bar);
+}
+
+// P tile += M_stage Q_stage (zero outside the matrix) for padded rank KP
+template <int KP>
+__device__ __forceinline__ void p_fma(const float *es, const float *qs, float (&acc)[64], int warp, int lane) {
+    constexpr int R = KP == 64 ? 8 : 16, TILES = (R / 8) * (KP / 8), CS = 8 / TILES, GS = 32 * CS;
+    constexpr int QS = KP + 4, U = (kPBC + GS - 1) / GS;
+    const int tile = warp % TILES, csplit = warp / TILES;
+    const int rt = tile % (R / 8), kt = tile / (R / 8);
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+        const int j = csplit * 32 + lane + GS * v;
+        if (GS * (v + 1) > kPBC && j >= kPBC) break;
+        float a[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) a[r] = es[(rt * 8 + r) * kPBC + j];
+        const float4 b0 = *reinterpret_cast<const float4 *>(qs + j * QS + kt * 8);
+        const float4 b1 = *reinterpret_cast<const float4 *>(qs + j * QS + kt * 8 + 4);
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[r * 8 + q] = fmaf(a[r], b[q], acc[r * 8 + q]);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 2) dp_compress_p_kernel(const __grid_constant__ PBatch B) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int begins[DPSYNC_MAX_BATCH];
-    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].cta_begin;
-    __syncthreads();
-    const int ji = find_job(begins, B.count, blockIdx.x);
-    const PJob &J = B.job[ji];
-    const PCfg C = p_cfg(J.kp);
-    const int row0 = (blockIdx.x - J.cta_begin) * C.R;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int begins[kMaxJobs];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    float *red = reinterpret_cast<float *>(smem + 128);  // 8 warps x 64
+    unsigned char *ring = smem + 128 + 8 * 64 * sizeof(float);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int qs = J.kp + 4;  // Q row stride in shared memory
-    float *red = smem + kPStages * B.stage_floats;  // 8 warps x 64
-
-    // zero the Q buffers once: cp.async writes only columns < k
-    for (int i = tid; i < kPStages * B.stage_floats; i += kThreads) smem[i] = 0.f;
+    if (tid < B.count) begins[tid] = B.job[tid].task_begin;
+    if (tid == 0) {
+        for (int s = 0; s < B.stages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        for (int j = 0; j < B.count; ++j) {
+            prefetch_tmap(B.job[j].mx);
+            prefetch_tmap(B.job[j].mq);
+        }
+    }
     __syncthreads();
-
-    const bool hasY = J.Y != nullptr, ef = J.ef != 0;
-    const int nch = (J.n + C.BC - 1) / C.BC;
-    const int f4_per_row = C.BC / 4, nf4 = C.R * f4_per_row;
-
-    auto issue = [&](int c) {
-        float *st = smem + (c % kPStages) * B.stage_floats;
-        float *xs = st, *ys = st + 2048, *es = st + 4096, *qsm = st + 6144;
-        const int col0 = c * C.BC;
-        for (int f = tid; f < nf4; f += kThreads) {
-            const int r = f / f4_per_row, c4 = f % f4_per_row;
-            const int gr = row0 + r, gc = col0 + 4 * c4;
-            const bool ok = gr < J.m && gc < J.n;
-            const size_t off = ok ? (size_t)gr * J.n + gc : 0;
-            cp_async16(xs + 4 * f, J.X + off, ok);
-            if (hasY) cp_async16(ys + 4 * f, J.Y + off, ok);
-            if (ef) cp_async16(es + 4 * f, J.E + off, ok);
+    PCursor cur, pc;
+    p_first(cur, B, begins);
+    pc = cur;
+    if (tid == 0)
+        for (int s = 0; s < B.stages && pc.task >= 0; ++s) {
+            p_issue(B, pc, ring + (size_t)s * B.stage_bytes, &bar[s]);
+            p_advance(pc, B, begins);
         }
-        const int nq = C.BC * J.k;
-        for (int e = tid; e < nq; e += kThreads) {
-            const int j = e / J.k, cc = e % J.k;
-            const bool ok = col0 + j < J.n;
-            cp_async4(qsm + j * qs + cc, J.Q + (ok ? (size_t)(col0 + j) * J.k + cc : 0), ok);
-        }
-    };
-
-    const int tile = warp % C.tiles, csplit = warp / C.tiles;
-    const int rt = tile % (C.R / 8), kt = tile / (C.R / 8);
-    const int g = csplit * 32 + lane, gstride = 32 * C.cs, u = C.BC / gstride;
     float acc[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-
-    issue(0);
-    cp_async_commit();
-    for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) issue(c + 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        float *st = smem + (c % kPStages) * B.stage_floats;
-        float *xs = st, *ys = st + 2048, *es = st + 4096, *qsm = st + 6144;
-        const int col0 = c * C.BC;
-        // M = E + X - Y into es and global E
-        for (int f = tid; f < nf4; f += kThreads) {
-            float4 x = reinterpret_cast<float4 *>(xs)[f];
-            if (hasY) {
-                const float4 y = reinterpret_cast<float4 *>(ys)[f];
-                x.x -= y.x; x.y -= y.y; x.z -= y.z; x.w -= y.w;
+    bool ok = true;
+    for (int it = 0; cur.task >= 0; ++it) {
+        const int s = it % B.stages;
+        unsigned char *stage = ring + (size_t)s * B.stage_bytes;
+        float *xs = reinterpret_cast<float *>(stage), *ys = xs + kPBuf, *es = ys + kPBuf, *qs = es + kPBuf;
+        const PJob &J = B.job[cur.job];
+        const int R = J.R, row0 = (cur.task - J.task_begin) * R, col0 = cur.chunk * kPBC;
+        if (ok) ok = mbar_wait_bounded(&bar[s], (uint32_t)(it / B.stages) & 1u, B.flag, 3u);
+        if (ok) {
+            // M = E + X - Y over the box: to global E (inside the matrix) and in place of the E box
+            for (int f = tid; f < R * (kPBC / 4); f += kThreads) {
+                float4 x = reinterpret_cast<const float4 *>(xs)[f];
+                if (J.hasY) {
+                    const float4 y = reinterpret_cast<const float4 *>(ys)[f];
+                    x.x -= y.x; x.y -= y.y; x.z -= y.z; x.w -= y.w;
+                }
+                if (J.ef) {
+                    const float4 e = reinterpret_cast<const float4 *>(es)[f];
+                    x.x = e.x + x.x; x.y = e.y + x.y; x.z = e.z + x.z; x.w = e.w + x.w;
+                }
+                reinterpret_cast<float4 *>(es)[f] = x;
+                const int r = row0 + f / (kPBC / 4), c = col0 + 4 * (f % (kPBC / 4));
+                if (r < J.m && c < J.n) __stcs(reinterpret_cast<float4 *>(J.E + (size_t)r * J.n + c), x);
             }
-            if (ef) {
-                const float4 e = reinterpret_cast<float4 *>(es)[f];
-                x.x = e.x + x.x; x.y = e.y + x.y; x.z = e.z + x.z; x.w = e.w + x.w;
+        }
+        ok = __syncthreads_and(ok) != 0;
+        if (!ok) break;
+        switch (J.kp) {
+            case 8: p_fma<8>(es, qs, acc, warp, lane); break;
+            case 16: p_fma<16>(es, qs, acc, warp, lane); break;
+            case 32: p_fma<32>(es, qs, acc, warp, lane); break;
+            default: p_fma<64>(es, qs, acc, warp, lane); break;
+        }
+        const bool last = cur.chunk == J.nch - 1;
+        __syncthreads();  // this stage is consumed: refill it
+        if (tid == 0 && pc.task >= 0) {
+            p_issue(B, pc, stage, &bar[s]);
+            p_advance(pc, B, begins);
+        }
+        if (last) {
+            // task done: sum the tiles over lanes (shuffles) and column-split warps (smem)
+            const int tiles = (R / 8) * (J.kp / 8), cs = 8 / tiles;
+            warp_reduce64(acc, lane);
+            red[warp * 64 + 2 * lane] = acc[0];
+            red[warp * 64 + 2 * lane + 1] = acc[1];
+            __syncthreads();
+            for (int e = tid; e < tiles * 64; e += kThreads) {
+                const int tt = e / 64, idx = e % 64;
+                float sum = 0.f;
+                for (int q = 0; q < cs; ++q) sum += red[(tt + q * tiles) * 64 + idx];
+                const int row = row0 + (tt % (R / 8)) * 8 + idx / 8, col = (tt / (R / 8)) * 8 + idx % 8;
+                if (row < J.m && col < J.k) J.P[(size_t)row * J.k + col] = sum;
             }
-            reinterpret_cast<float4 *>(es)[f] = x;
-            const int r = f / f4_per_row, c4 = f % f4_per_row;
-            const int gr = row0 + r, gc = col0 + 4 * c4;
-            if (gr < J.m && gc < J.n) *reinterpret_cast<float4 *>(J.E + (size_t)gr * J.n + gc) = x;
+            __syncthreads();  // red is free again
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
         }
-        __syncthreads();
-        // P_tile += M_chunk Q_chunk over this thread's columns
-        for (int v = 0; v < u; ++v) {
-            const int j = g + gstride * v;
-            float a[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) a[r] = es[(rt * 8 + r) * C.BC + j];
-            const float4 b0 = *reinterpret_cast<const float4 *>(qsm + j * qs + kt * 8);
-            const float4 b1 = *reinterpret_cast<const float4 *>(qsm + j * qs + kt * 8 + 4);
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[r * 8 + q] = fmaf(a[r], b[q], acc[r * 8 + q]);
-        }
-        __syncthreads();
+        p_advance(cur, B, begins);
     }
-    cp_async_wait<0>();
-
-    warp_reduce64(acc, lane);
-    red[warp * 64 + 2 * lane] = acc[0];
-    red[warp * 64 + 2 * lane + 1] = acc[1];
-    __syncthreads();
-    for (int e = tid; e < C.tiles * 64; e += kThreads) {
-        const int t = e / 64, idx = e % 64;
-        float s = 0.f;
-        for (int q = 0; q < C.cs; ++q) s += red[(t + q * C.tiles) * 64 + idx];
-        const int trt = t % (C.R / 8), tkt = t / (C.R / 8);
-        const int row = row0 + trt * 8 + idx / 8, col = tkt * 8 + idx % 8;
-        if (row < J.m && col < J.k) J.P[(size_t)row * J.k + col] = s;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// compress_q:  Q = M^T P^.  Task (column block of 128, row range of 512): the
-// partial of its rows into Qpart; the last task of a column block to finish
-// sums the partials in row-range order into the caller's Q.
-// ---------------------------------------------------------------------------
-struct QJob {
-    const float *M, *Ph;
-    float *Qpart, *Q;
-    int *counter;
-    int m, n, k, kp, ranges, ncb, task_begin;
-};
-struct QBatch {
-    QJob job[DPSYNC_MAX_BATCH];
-    int count, stage_floats;
-};
-
-__global__ void __launch_bounds__(kThreads, 2) dp_compress_q_kernel(const __grid_constant__ QBatch B) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int begins[DPSYNC_MAX_BATCH];
-    __shared__ int is_last;
-    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].task_begin;
-    __syncthreads();
-    const QJob &J = B.job[find_job(begins, B.count, blockIdx.x)];
-    const int task = blockIdx.x - J.task_begin;
-    const int cb = task % J.ncb, range = task / J.ncb;
-    const int col0 = cb * kQCols, rbeg = range * kQRows, rend = min(J.m, rbeg + kQRows);
-    const int nch = (rend - rbeg + kQChunk - 1) / kQChunk;
-    const int tid = threadIdx.x;
-    const int kp = J.kp;
-
-    auto issue = [&](int c) {
-        float *st = smem + (c % kQStages) * B.stage_floats;
-        float *ms = st, *ps = st + kQChunk * kQCols;
-        const int r0 = rbeg + c * kQChunk;
-        for (int f = tid; f < kQChunk * kQCols / 4; f += kThreads) {
-            const int r = f / (kQCols / 4), c4 = f % (kQCols / 4);
-            const int gr = r0 + r, gc = col0 + 4 * c4;
-            const bool ok = gr < rend && gc < J.n;
-            cp_async16(ms + 4 * f, J.M + (ok ? (size_t)gr * J.n + gc : 0), ok);
-        }
-        for (int f = tid; f < kQChunk * kp / 4; f += kThreads) {
-            const int r = f / (kp / 4), c4 = f % (kp / 4);
-            const bool ok = r0 + r < rend;
-            cp_async16(ps + 4 * f, J.Ph + (ok ? (size_t)(r0 + r) * kp + 4 * c4 : 0), ok);
-        }
-    };
-
-    const int tiles = 2 * kp, rg_count = kThreads / tiles;
-    const int tile = tid % tiles, rg = tid / tiles;
-    const int ct = tile % 16, kt = tile / 16;
-    float acc[64];  // [8 columns][8 ranks]
-#pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-
-#pragma unroll
-    for (int s = 0; s < kQStages - 1; ++s) {
-        if (s < nch) issue(s);
-        cp_async_commit();
-    }
-    for (int c = 0; c < nch; ++c) {
-        cp_async_wait<kQStages - 2>();
-        __syncthreads();
-        const float *st = smem + (c % kQStages) * B.stage_floats;
-        const float *ms = st, *ps = st + kQChunk * kQCols;
-        for (int i = rg; i < kQChunk; i += rg_count) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 4 * ct);
-            const float4 a1 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 64 + 4 * ct);
-            const float4 b0 = *reinterpret_cast<const float4 *>(ps + i * kp + kt * 8);
-            const float4 b1 = *reinterpret_cast<const float4 *>(ps + i * kp + kt * 8 + 4);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[x * 8 + q] = fmaf(a[x], b[q], acc[x * 8 + q]);
-        }
-        if (c + kQStages - 1 < nch) issue(c + kQStages - 1);
-        cp_async_commit();
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // sum the row groups in the (now idle) stage ring: halving steps
-    for (int half = rg_count / 2; half >= 1; half /= 2) {
-        const int nt = half * tiles;
-        if (rg >= half && rg < 2 * half) {
-            const int idx = (rg - half) * tiles + tile;
-#pragma unroll
-            for (int v = 0; v < 64; ++v) smem[v * nt + idx] = acc[v];
-        }
-        __syncthreads();
-        if (rg < half) {
-            const int idx = rg * tiles + tile;
-#pragma unroll
-            for (int v = 0; v < 64; ++v) acc[v] += smem[v * nt + idx];
-        }
-        __syncthreads();
-    }
-    const int ldp = J.ncb * kQCols;  // Qpart: [ranges][ldp][kp]
-    if (rg == 0) {
-        float *dst = J.Qpart + ((size_t)range * ldp + col0) * kp + kt * 8;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int col = x < 4 ? 4 * ct + x : 64 + 4 * ct + (x - 4);
-            float4 *d = reinterpret_cast<float4 *>(dst + (size_t)col * kp);
-            d[0] = make_float4(acc[x * 8 + 0], acc[x * 8 + 1], acc[x * 8 + 2], acc[x * 8 + 3]);
-            d[1] = make_float4(acc[x * 8 + 4], acc[x * 8 + 5], acc[x * 8 + 6], acc[x * 8 + 7]);
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) is_last = atomicAdd(J.counter + cb, 1) == J.ranges - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const int ncols = min(kQCols, J.n - col0);
-    for (int e = tid; e < ncols * J.k; e += kThreads) {
-        const int j = e / J.k, q = e % J.k;
-        float s = 0.f;
-        for (int r = 0; r < J.ranges; ++r) s += __ldcg(J.Qpart + ((size_t)r * ldp + col0 + j) * kp + q);
-        J.Q[(size_t)(col0 + j) * J.k + q] = s;
-    }
-    if (tid == 0) J.counter[cb] = 0;
 }
 
 // ---------------------------------------------------------------------------
 // orthogonalisation: two passes of Cholesky QR.  Pass p forms the Gram matrix
-// of Y = P (p = 0) or Y = P T1 (p = 1) with every product and sum carried in
-// two floats (hi + lo, error-free product and sum), factors it in fp64 as
-// R^T R (a pivot <= kDrop x the column's own squared norm marks the column
-// dependent: its row of R and column of R^-1 are zero) and stores T = R^-1.
+// of Y = P (p = 0) or Y = P R1^-1 (p = 1) with every product and sum carried in
+// two floats, factors it as R^T R in two floats (a pivot <= kDrop x the
+// column's own squared norm marks the column dependent: its row of R is zero
+// and its reciprocal pivot 0) and stores R in fp32: strict upper part and the
+// reciprocal pivots on the diagonal.
 // ---------------------------------------------------------------------------
 
-// y_c = sum_{a <= c} x_a T[a][c] in a fixed order: the gram pass and the apply
-// kernel evaluate P T1 through this one function, so the second pass sees
-// exactly the rows the apply kernel produces.
-__device__ __forceinline__ float upper_times(const float *x, const float *T, int kp, int c) {
-    float s = 0.f;
-    for (int a = 0; a <= c; ++a) s = fmaf(x[a], T[a * kp + c], s);
-    return s;
-}
-
-// (hi, lo) += a * b with the product split exactly (fma) and the sum by TwoSum
-__device__ __forceinline__ void df_acc(float &hi, float &lo, float a, float b) {
-    const float p = __fmul_rn(a, b);
-    const float pe = fmaf(a, b, -p);
-    const float s = __fadd_rn(hi, p);
-    const float bb = __fsub_rn(s, hi);
-    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
-    hi = s;
-    lo = __fadd_rn(lo, __fadd_rn(err, pe));
+// y <- y R^-1 for one row held in registers (forward substitution), R as
+// stored above.  The Gram pass and the apply kernel both go through this
+// function, so the second pass factors exactly the rows the apply kernel
+// produces.
+template <int KP>
+__device__ __forceinline__ void tri_solve_row(float (&y)[KP], const float *R) {
+#pragma unroll
+    for (int c = 0; c < KP; ++c) {
+        float s = y[c];
+#pragma unroll
+        for (int a = 0; a < c; ++a) s = fmaf(-y[a], R[a * KP + c], s);
+        y[c] = s * R[c * KP + c];
+    }
 }
 
 struct GJob {
-    const float *P, *T1;
-    double *Gpart;
-    float *Tout;
+    const float *P, *R1;
+    float *Gpart, *Rout;
     int *counter;
     int m, k, kp, tasks, task_begin;
 };
 struct GBatch {
-    GJob job[DPSYNC_MAX_BATCH];
+    GJob job[kMaxJobs];
     int count, pass;
 };
-constexpr int kMaxEntries = (64 * 65 / 2 + kThreads - 1) / kThreads;  // 9
 
-__global__ void __launch_bounds__(kThreads, 1) dp_gram_kernel(const __grid_constant__ GBatch B) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int begins[DPSYNC_MAX_BATCH];
+// (bi, bj) of upper-triangular 4 x 4 block b of an nb x nb block grid
+__device__ __forceinline__ void block_pair(int b, int nb, int &bi, int &bj) {
+    bi = 0;
+    while (b >= nb - bi) {
+        b -= nb - bi;
+        ++bi;
+    }
+    bj = bi + b;
+}
+
+template <int KP>
+__device__ void gram_task(const GBatch &B, const GJob &J, int task, unsigned char *smem) {
+    constexpr int NB = KP / 4, NBLK = NB * (NB + 1) / 2;
+    constexpr int RG = NBLK >= kThreads ? 1 : kThreads / NBLK;
+    constexpr int XS = KP + 1;  // row stride of the staged rows (odd: conflict-free per-row access)
     __shared__ int is_last;
-    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].task_begin;
-    __syncthreads();
-    const GJob &J = B.job[find_job(begins, B.count, blockIdx.x)];
-    const int task = blockIdx.x - J.task_begin;
-    const int kp = J.kp, tid = threadIdx.x;
+    float *xs = reinterpret_cast<float *>(smem);  // kGramRows x XS
+    float *r1 = xs + kGramRows * XS;              // KP x KP
+    float *red = r1 + KP * KP;                    // 32 x kThreads
+    const int tid = threadIdx.x;
     const int r0 = task * kGramRows, rows = min(kGramRows, J.m - r0);
-    float *xs = smem;                       // kGramRows x kp
-    float *ys = xs + kGramRows * kp;        // kGramRows x kp
-    float *t1 = ys + kGramRows * kp;        // kp x kp
-
-    for (int e = tid; e < kGramRows * kp; e += kThreads) {
-        const int r = e / kp, c = e % kp;
-        xs[e] = (r < rows && c < J.k) ? J.P[(size_t)(r0 + r) * J.k + c] : 0.f;
+    for (int e = tid; e < kGramRows * KP; e += kThreads) {
+        const int r = e / KP, c = e % KP;
+        xs[r * XS + c] = (r < rows && c < J.k) ? J.P[(size_t)(r0 + r) * J.k + c] : 0.f;
     }
     if (B.pass == 1)
-        for (int e = tid; e < kp * kp; e += kThreads) t1[e] = J.T1[e];
+        for (int e = tid; e < KP * KP; e += kThreads) r1[e] = J.R1[e];
     __syncthreads();
-    const float *y = xs;
     if (B.pass == 1) {
-        for (int e = tid; e < kGramRows * kp; e += kThreads) {
-            const int r = e / kp, c = e % kp;
-            ys[e] = upper_times(xs + r * kp, t1, kp, c);
+        if (tid < rows) {
+            float y[KP];
+#pragma unroll
+            for (int c = 0; c < KP; ++c) y[c] = xs[tid * XS + c];
+            tri_solve_row<KP>(y, r1);
+#pragma unroll
+            for (int c = 0; c < KP; ++c) xs[tid * XS + c] = y[c];
         }
         __syncthreads();
-        y = ys;
     }
-    // this thread's entries (a <= b) of the upper triangle, row-major order
-    const int E = kp * (kp + 1) / 2;
-    int ea[kMaxEntries], eb[kMaxEntries];
-    float hi[kMaxEntries], lo[kMaxEntries];
+    // 4 x 4 blocks of the upper triangle, RG row groups per block
+    const int blk = tid % NBLK, rg = tid / NBLK;
+    const bool active = rg < RG && tid < NBLK * RG;
+    int bi, bj;
+    block_pair(blk, NB, bi, bj);
+    float hi[16], lo[16];
 #pragma unroll
-    for (int v = 0; v < kMaxEntries; ++v) {
-        int e = tid + v * kThreads, a = 0;
-        if (e >= E) e = -1;
-        if (e >= 0)
-            while (e >= kp - a) { e -= kp - a; ++a; }
-        ea[v] = e >= 0 ? a : -1;
-        eb[v] = e >= 0 ? a + e : 0;
-        hi[v] = lo[v] = 0.f;
+    for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0.f;
+    if (active)
+        for (int r = rg; r < rows; r += RG) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = xs[r * XS + 4 * bi + i];
+                b[i] = xs[r * XS + 4 * bj + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) df_acc(hi[i * 4 + j], lo[i * 4 + j], a[i], b[j]);
+        }
+    // tree over the row groups: slot = rg * NBLK + blk, element-major in red
+    for (int cnt = RG; cnt > 1;) {
+        const int h = (cnt + 1) / 2;
+        if (active && rg >= h && rg < cnt) {
+            const int slot = (rg - h) * NBLK + blk;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                red[(2 * e) * kThreads + slot] = hi[e];
+                red[(2 * e + 1) * kThreads + slot] = lo[e];
+            }
+        }
+        __syncthreads();
+        if (active && rg < cnt - h) {
+            const int slot = rg * NBLK + blk;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const df s = df_add(df{hi[e], lo[e]}, df{red[(2 * e) * kThreads + slot], red[(2 * e + 1) * kThreads + slot]});
+                hi[e] = s.hi;
+                lo[e] = s.lo;
+            }
+        }
+        __syncthreads();
+        cnt = h;
     }
-    for (int r = 0; r < rows; ++r) {
+    if (active && rg == 0) {
+        float2 *gp = reinterpret_cast<float2 *>(J.Gpart) + ((size_t)task * NBLK + blk) * 16;
 #pragma unroll
-        for (int v = 0; v < kMaxEntries; ++v)
-            if (ea[v] >= 0) df_acc(hi[v], lo[v], y[r * kp + ea[v]], y[r * kp + eb[v]]);
+        for (int e = 0; e < 16; ++e) {
+            const df s = quick_two_sum(hi[e], lo[e]);
+            gp[e] = make_float2(s.hi, s.lo);
+        }
     }
-    double *gp = J.Gpart + (size_t)task * E;
-#pragma unroll
-    for (int v = 0; v < kMaxEntries; ++v)
-        if (ea[v] >= 0) gp[tid + v * kThreads] = (double)hi[v] + (double)lo[v];
     __threadfence();
     __syncthreads();
     if (tid == 0) is_last = atomicAdd(J.counter, 1) == J.tasks - 1;
@@ -463,102 +489,352 @@ __global__ void __launch_bounds__(kThreads, 1) dp_gram_kernel(const __grid_const
     if (!is_last) return;
     __threadfence();
 
-    // last CTA: G = sum of the partials (task order), Cholesky, T = R^-1
-    double *G = reinterpret_cast<double *>(smem);  // kp x kp (upper triangle used)
-    double *Ti = G + kp * kp;                       // kp x kp
-    double *piv = Ti + kp * kp;                     // kp
-    double *dg = piv + kp;                          // kp: original diagonal
-    for (int e = tid; e < E; e += kThreads) {
-        double s = 0.0;
-        for (int t = 0; t < J.tasks; ++t) s += __ldcg(J.Gpart + (size_t)t * E + e);
-        int a = 0, f = e;
-        while (f >= kp - a) { f -= kp - a; ++a; }
-        G[a * kp + a + f] = s;
-        if (f == 0) dg[a] = s;
+    // last CTA of the matrix: G = sum of the partials in task order, then Cholesky
+    float *gh = reinterpret_cast<float *>(smem);  // KP x KP (upper triangle)
+    float *gl = gh + KP * KP;
+    float *dg = gl + KP * KP;                      // original diagonal (hi)
+    float *pinv = dg + KP;                         // reciprocal pivots (0: dependent)
+    for (int e = tid; e < NBLK * 16; e += kThreads) {
+        const int b = e / 16, w = e % 16;
+        df s{0.f, 0.f};
+        const float2 *src = reinterpret_cast<const float2 *>(J.Gpart) + (size_t)b * 16 + w;
+        const size_t stride = (size_t)NBLK * 16;
+        int t = 0;
+        for (; t + 8 <= J.tasks; t += 8) {  // eight loads in flight, then the ordered sums
+            float2 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(t + u) * stride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s = df_add(s, df{v[u].x, v[u].y});
+        }
+        for (; t < J.tasks; ++t) {
+            const float2 v = __ldcg(src + (size_t)t * stride);
+            s = df_add(s, df{v.x, v.y});
+        }
+        int pbi, pbj;
+        block_pair(b, NB, pbi, pbj);
+        const int r = 4 * pbi + w / 4, c = 4 * pbj + w % 4;
+        if (r <= c) {
+            gh[r * KP + c] = s.hi;
+            gl[r * KP + c] = s.lo;
+            if (r == c) dg[r] = s.hi;
+        }
     }
     __syncthreads();
-    for (int j = 0; j < kp; ++j) {
-        const double d = G[j * kp + j];
-        const bool dep = !(d > kDrop * dg[j]);
-        const double pj = dep ? 0.0 : sqrt(d);
-        for (int c = j + 1 + tid; c < kp; c += kThreads) G[j * kp + c] = dep ? 0.0 : G[j * kp + c] / pj;
-        if (tid == 0) piv[j] = pj;
-        __syncthreads();
-        if (!dep) {
-            const int L = kp - j - 1;
-            for (int idx = tid; idx < L * L; idx += kThreads) {
-                const int a = j + 1 + idx / L, b = j + 1 + idx % L;
-                if (a <= b) G[a * kp + b] -= G[j * kp + a] * G[j * kp + b];
-            }
+    // pivot j: 1 / sqrt(d), or 0 when the residual d is at most kDrop of the column's norm^2
+    auto recip_pivot = [&](df d, int j) -> df {
+        return d.hi > kDrop * dg[j] ? df_recip(df_sqrt(d)) : df{0.f, 0.f};
+    };
+    // row 0 of R
+    {
+        const df inv = recip_pivot(df{gh[0], gl[0]}, 0);
+        for (int c = 1 + tid; c < KP; c += kThreads) {
+            const df r = df_mul(df{gh[c], gl[c]}, inv);
+            gh[c] = r.hi;
+            gl[c] = r.lo;
         }
-        __syncthreads();
+        if (tid == 0) pinv[0] = inv.hi;
     }
-    // columns of R^-1 by back substitution, one thread per column
-    if (tid < kp) {
-        const int c = tid;
-        for (int i = c; i >= 0; --i) {
-            double t;
-            if (piv[i] == 0.0) {
-                t = 0.0;
-            } else if (i == c) {
-                t = 1.0 / piv[i];
+    __syncthreads();
+    // step j: trailing update with row j of R; the threads holding row j + 1
+    // finish it in the same pass (each recomputes the new pivot), so one
+    // barrier per step
+    for (int j = 0; j + 1 < KP; ++j) {
+        const int L = KP - j - 1;
+        for (int idx = tid; idx < L * L; idx += kThreads) {
+            const int a = j + 1 + idx / L, c = j + 1 + idx % L;
+            if (a > c) continue;
+            const df rja{gh[j * KP + a], gl[j * KP + a]};
+            const df g = df_add(df{gh[a * KP + c], gl[a * KP + c]},
+                                df_neg(df_mul(rja, df{gh[j * KP + c], gl[j * KP + c]})));
+            if (a == j + 1) {
+                const df d = df_add(df{gh[a * KP + a], gl[a * KP + a]}, df_neg(df_mul(rja, rja)));
+                const df inv = recip_pivot(d, a);
+                if (c == a) {
+                    pinv[a] = inv.hi;
+                } else {
+                    const df r = df_mul(g, inv);
+                    gh[a * KP + c] = r.hi;
+                    gl[a * KP + c] = r.lo;
+                }
             } else {
-                double s = 0.0;
-                for (int p = i + 1; p <= c; ++p) s += G[i * kp + p] * Ti[p * kp + c];
-                t = -s / piv[i];
+                gh[a * KP + c] = g.hi;
+                gl[a * KP + c] = g.lo;
             }
-            Ti[i * kp + c] = t;
         }
+        __syncthreads();
     }
-    __syncthreads();
-    for (int e = tid; e < kp * kp; e += kThreads) {
-        const int i = e / kp, c = e % kp;
-        J.Tout[e] = i <= c ? (float)Ti[e] : 0.f;
+    for (int e = tid; e < KP * KP; e += kThreads) {
+        const int r = e / KP, c = e % KP;
+        J.Rout[e] = r < c ? gh[e] : r == c ? pinv[r] : 0.f;
     }
     if (tid == 0) *J.counter = 0;
 }
 
-// P^ = (P T1) T2 into the handle's m x kp basis.
+__global__ void __launch_bounds__(kThreads, 1) dp_gram_kernel(const __grid_constant__ GBatch B) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int begins[kMaxJobs];
+    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].task_begin;
+    __syncthreads();
+    const GJob &J = B.job[find_job(begins, B.count, blockIdx.x)];
+    const int task = blockIdx.x - J.task_begin;
+    switch (J.kp) {
+        case 8: gram_task<8>(B, J, task, smem); break;
+        case 16: gram_task<16>(B, J, task, smem); break;
+        case 32: gram_task<32>(B, J, task, smem); break;
+        default: gram_task<64>(B, J, task, smem); break;
+    }
+}
+
+inline size_t gram_smem_bytes(int kp) {
+    const size_t p1 = sizeof(float) * ((size_t)kGramRows * (kp + 1) + (size_t)kp * kp + 32 * kThreads);
+    const size_t p2 = sizeof(float) * (2 * (size_t)kp * kp + 2 * kp);
+    return std::max(p1, p2);
+}
+
+// P^ = (P R1^-1) R2^-1 into the handle's m x kp basis, one row per thread.
 struct AJob {
-    const float *P, *T;  // T: T1 then T2, kp x kp each
+    const float *P, *R;  // R: R1 then R2, kp x kp each
     float *Ph;
     int m, k, kp, cta_begin;
 };
 struct ABatch {
-    AJob job[DPSYNC_MAX_BATCH];
+    AJob job[kMaxJobs];
     int count;
 };
-constexpr int kApplyRows = 64;
+
+template <int KP>
+__device__ void orth_apply_rows(const AJob &J, unsigned char *smem_raw) {
+    const int tid = threadIdx.x;
+    const int r0 = (blockIdx.x - J.cta_begin) * kApplyRows, rows = min(kApplyRows, J.m - r0);
+    float *r12 = reinterpret_cast<float *>(smem_raw);  // R1, R2
+    for (int e = tid; e < 2 * KP * KP; e += kThreads) r12[e] = J.R[e];
+    __syncthreads();
+    if (tid >= rows) return;
+    const int row = r0 + tid;
+    float y[KP];
+#pragma unroll
+    for (int c = 0; c < KP; ++c) y[c] = c < J.k ? J.P[(size_t)row * J.k + c] : 0.f;
+    tri_solve_row<KP>(y, r12);
+    tri_solve_row<KP>(y, r12 + KP * KP);
+    float4 *dst = reinterpret_cast<float4 *>(J.Ph + (size_t)row * KP);
+#pragma unroll
+    for (int c = 0; c < KP; c += 4) dst[c / 4] = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
+}
 
 __global__ void __launch_bounds__(kThreads) dp_orth_apply_kernel(const __grid_constant__ ABatch B) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int begins[DPSYNC_MAX_BATCH];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ int begins[kMaxJobs];
     if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].cta_begin;
     __syncthreads();
     const AJob &J = B.job[find_job(begins, B.count, blockIdx.x)];
-    const int kp = J.kp, tid = threadIdx.x;
-    const int r0 = (blockIdx.x - J.cta_begin) * kApplyRows, rows = min(kApplyRows, J.m - r0);
-    float *xs = smem, *ys = xs + kApplyRows * kp, *t1 = ys + kApplyRows * kp, *t2 = t1 + kp * kp;
-    for (int e = tid; e < kApplyRows * kp; e += kThreads) {
-        const int r = e / kp, c = e % kp;
-        xs[e] = (r < rows && c < J.k) ? J.P[(size_t)(r0 + r) * J.k + c] : 0.f;
-    }
-    for (int e = tid; e < 2 * kp * kp; e += kThreads) t1[e] = J.T[e];
-    __syncthreads();
-    for (int e = tid; e < kApplyRows * kp; e += kThreads) {
-        const int r = e / kp, c = e % kp;
-        ys[e] = upper_times(xs + r * kp, t1, kp, c);
-    }
-    __syncthreads();
-    for (int e = tid; e < rows * kp; e += kThreads) {
-        const int r = e / kp, c = e % kp;
-        J.Ph[(size_t)(r0 + r) * kp + c] = upper_times(ys + r * kp, t2, kp, c);
+    switch (J.kp) {
+        case 8: orth_apply_rows<8>(J, smem_raw); break;
+        case 16: orth_apply_rows<16>(J, smem_raw); break;
+        case 32: orth_apply_rows<32>(J, smem_raw); break;
+        default: orth_apply_rows<64>(J, smem_raw); break;
     }
 }
 
 // ---------------------------------------------------------------------------
-// decompress / outer step over 64 x 256 tiles:  D = s P^ Q^T (8 x 8 per thread,
-// P^ and Q staged transposed in shared memory), then per element
+// compress_q:  partial Q = M^T P^ over one row range.  Task (column block of
+// 128, row range of 512); the ring holds stages of one TMA box of M (128
+// columns x 16 rows) and the matching box of P^ (kp x 16), zero outside the
+// matrices.  Thread tile: 8 columns x 8 ranks; row groups split each stage's
+// rows and are summed in a halving tree at the end of the task.
+// ---------------------------------------------------------------------------
+struct QJob {
+    const CUtensorMap *mm, *mp;
+    float *Qpart;
+    int m, n, kp, ranges, ncb, task_begin;
+};
+struct QBatch {
+    QJob job[kMaxJobs];
+    int count, total_tasks, stages;
+    uint32_t stage_bytes;
+    unsigned *flag;
+};
+
+struct QCursor {
+    int task, chunk, job, nch;
+};
+__device__ __forceinline__ int q_nch(const QJob &J, int task) {
+    const int range = (task - J.task_begin) / J.ncb;
+    const int rows = min(kQRows, J.m - range * kQRows);
+    return (rows + kQChunk - 1) / kQChunk;
+}
+__device__ __forceinline__ void q_first(QCursor &c, const QBatch &B, const int *begins) {
+    c.task = blockIdx.x < (unsigned)B.total_tasks ? (int)blockIdx.x : -1;
+    c.chunk = 0;
+    c.job = c.task >= 0 ? find_job(begins, B.count, c.task) : 0;
+    c.nch = c.task >= 0 ? q_nch(B.job[c.job], c.task) : 0;
+}
+__device__ __forceinline__ void q_advance(QCursor &c, const QBatch &B, const int *begins) {
+    if (c.task < 0) return;
+    if (++c.chunk < c.nch) return;
+    c.chunk = 0;
+    c.task += gridDim.x;
+    if (c.task >= B.total_tasks) {
+        c.task = -1;
+        return;
+    }
+    c.job = find_job(begins, B.count, c.task);
+    c.nch = q_nch(B.job[c.job], c.task);
+}
+__device__ __forceinline__ void q_issue(const QBatch &B, const QCursor &c, unsigned char *stage, uint64_t *bar) {
+    const QJob &J = B.job[c.job];
+    const int t = c.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
+    const int r0 = range * kQRows + c.chunk * kQChunk;
+    float *ms = reinterpret_cast<float *>(stage), *ps = ms + kQChunk * kQCols;
+    mbar_arrive_expect_tx(bar, (uint32_t)kQChunk * (kQCols + J.kp) * 4u);
+    tma_load_2d(ms, J.mm, cb * kQCols, r0, bar);
+    tma_load_2d(ps, J.mp, 0, r0, bar);
+}
+
+// acc[8 columns][8 ranks] += M_stage^T P^_stage for padded rank KP: tiles of
+// 8 columns x 8 ranks, 256 / (2 KP) row groups each taking every RGN-th row
+template <int KP>
+__device__ __forceinline__ void q_fma(const float *ms, float (&acc)[64], int tid) {
+    constexpr int TILES = 2 * KP, RGN = kThreads / TILES;
+    const float *ps = ms + kQChunk * kQCols;
+    const int tile = tid % TILES, rg = tid / TILES, ct = tile % 16, kt = tile / 16;
+#pragma unroll
+    for (int i0 = 0; i0 < kQChunk; i0 += RGN) {
+        const int i = i0 + rg;
+        const float4 a0 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 4 * ct);
+        const float4 a1 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 64 + 4 * ct);
+        const float4 b0 = *reinterpret_cast<const float4 *>(ps + i * KP + kt * 8);
+        const float4 b1 = *reinterpret_cast<const float4 *>(ps + i * KP + kt * 8 + 4);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[x * 8 + q] = fmaf(a[x], b[q], acc[x * 8 + q]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) dp_compress_q_kernel(const __grid_constant__ QBatch B) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int begins[kMaxJobs];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    float *red = reinterpret_cast<float *>(smem + 128);  // 128 x 64 floats
+    unsigned char *ring = smem + 128 + 128 * 64 * sizeof(float);
+    const int tid = threadIdx.x;
+    if (tid < B.count) begins[tid] = B.job[tid].task_begin;
+    if (tid == 0) {
+        for (int s = 0; s < B.stages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        for (int j = 0; j < B.count; ++j) {
+            prefetch_tmap(B.job[j].mm);
+            prefetch_tmap(B.job[j].mp);
+        }
+    }
+    __syncthreads();
+    QCursor cur, pc;
+    q_first(cur, B, begins);
+    pc = cur;
+    if (tid == 0)
+        for (int s = 0; s < B.stages && pc.task >= 0; ++s) {
+            q_issue(B, pc, ring + (size_t)s * B.stage_bytes, &bar[s]);
+            q_advance(pc, B, begins);
+        }
+    float acc[64];  // [8 columns][8 ranks]
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+    bool ok = true;
+    for (int it = 0; cur.task >= 0; ++it) {
+        const int s = it % B.stages;
+        const QJob &J = B.job[cur.job];
+        const int kp = J.kp, tiles = 2 * kp, rgn = kThreads / tiles;
+        const int tile = tid % tiles, rg = tid / tiles, ct = tile % 16, kt = tile / 16;
+        const int t = cur.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
+        if (ok) ok = mbar_wait_bounded(&bar[s], (uint32_t)(it / B.stages) & 1u, B.flag, 4u);
+        if (ok) {
+            const float *ms = reinterpret_cast<const float *>(ring + (size_t)s * B.stage_bytes);
+            switch (kp) {
+                case 8: q_fma<8>(ms, acc, tid); break;
+                case 16: q_fma<16>(ms, acc, tid); break;
+                case 32: q_fma<32>(ms, acc, tid); break;
+                default: q_fma<64>(ms, acc, tid); break;
+            }
+        }
+        ok = __syncthreads_and(ok) != 0;  // this stage is consumed
+        if (!ok) break;
+        if (tid == 0 && pc.task >= 0) {
+            q_issue(B, pc, ring + (size_t)s * B.stage_bytes, &bar[s]);
+            q_advance(pc, B, begins);
+        }
+        if (cur.chunk == cur.nch - 1) {
+            // task done: halving tree over the row groups, then the partial to Qpart
+            for (int half = rgn / 2; half >= 1; half /= 2) {
+                const int nt = half * tiles;
+                if (rg >= half && rg < 2 * half) {
+                    const int idx = (rg - half) * tiles + tile;
+#pragma unroll
+                    for (int v = 0; v < 64; ++v) red[v * nt + idx] = acc[v];
+                }
+                __syncthreads();
+                if (rg < half) {
+                    const int idx = rg * tiles + tile;
+#pragma unroll
+                    for (int v = 0; v < 64; ++v) acc[v] += red[v * nt + idx];
+                }
+                __syncthreads();
+            }
+            if (rg == 0) {
+                const int ldp = J.ncb * kQCols;
+                float *dst = J.Qpart + ((size_t)range * ldp + cb * kQCols) * kp + kt * 8;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int col = x < 4 ? 4 * ct + x : 64 + 4 * ct + (x - 4);
+                    float4 *d = reinterpret_cast<float4 *>(dst + (size_t)col * kp);
+                    d[0] = make_float4(acc[x * 8 + 0], acc[x * 8 + 1], acc[x * 8 + 2], acc[x * 8 + 3]);
+                    d[1] = make_float4(acc[x * 8 + 4], acc[x * 8 + 5], acc[x * 8 + 6], acc[x * 8 + 7]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        }
+        q_advance(cur, B, begins);
+    }
+}
+
+// Q[j][c] = sum over the row ranges (in order) of the partials
+struct RJob {
+    const float *Qpart;
+    float *Q;
+    int n, k, kp, ranges, ldp;
+    int64_t begin;
+};
+struct RBatch {
+    RJob job[kMaxJobs];
+    int count;
+    int64_t total;
+};
+
+__global__ void __launch_bounds__(kThreads) dp_q_reduce_kernel(const __grid_constant__ RBatch B) {
+    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < B.total; e += (int64_t)gridDim.x * kThreads) {
+        int j = 0;
+        while (j + 1 < B.count && e >= B.job[j + 1].begin) ++j;
+        const RJob &J = B.job[j];
+        const int64_t f = e - J.begin;
+        const int64_t col = f / J.k;
+        const int c = (int)(f % J.k);
+        float s = 0.f;
+        for (int r = 0; r < J.ranges; ++r) s += J.Qpart[((size_t)r * J.ldp + col) * J.kp + c];
+        J.Q[f] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decompress / outer step.  Task (row block of 256, column block of 128) of a
+// persistent CTA (two per SM): the task's Q rows go transposed into shared
+// memory once, the P^ rows of each 32-row tile arrive by cp.async one tile
+// ahead, and each thread holds a 4 x 4 tile of D = s P^ Q^T (rows 4w..4w+3 of
+// the tile, columns 4l..4l+3).  The thread's E (and theta, momentum) values
+// are loaded before D is formed, so the FMA work covers the memory latency;
+// then per element
 //   E <- M - D (error feedback);  out <- D                       (mode 0)
 //   b <- mu b + D;  theta <- theta - lr (D + mu b);
 //   W <- (1 - mix) theta + mix W                                 (mode 1)
@@ -566,81 +842,108 @@ __global__ void __launch_bounds__(kThreads) dp_orth_apply_kernel(const __grid_co
 struct UJob {
     const float *Ph, *Q;
     float *E, *out, *theta, *mom, *W;
-    int m, n, k, kp, ef, tiles_n, cta_begin;
+    int m, n, k, kp, ef, tiles_c, task_begin;
     float lr, mu, mix;
 };
 struct UBatch {
-    UJob job[DPSYNC_MAX_BATCH];
-    int count, mode;
+    UJob job[kMaxJobs];
+    int count, mode, total_tasks;
     float q_scale;
 };
-constexpr int kPsStride = kTileRows + 4;
-constexpr int kQsStride = kTileCols + 4;
+constexpr int kQsStride = kUCols + 4;
 
 __global__ void __launch_bounds__(kThreads, 2) dp_update_kernel(const __grid_constant__ UBatch B) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int begins[DPSYNC_MAX_BATCH];
-    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].cta_begin;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int begins[kMaxJobs];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < B.count) begins[tid] = B.job[tid].task_begin;
     __syncthreads();
-    const UJob &J = B.job[find_job(begins, B.count, blockIdx.x)];
-    const int t = blockIdx.x - J.cta_begin;
-    const int r0 = (t / J.tiles_n) * kTileRows, c0 = (t % J.tiles_n) * kTileCols;
-    const int kp = J.kp, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float *ps = smem;                   // kp x kPsStride: P^ rows of the tile, transposed
-    float *qs = ps + kp * kPsStride;    // kp x kQsStride: Q rows of the tile, transposed
-    for (int e = tid; e < kTileRows * kp; e += kThreads) {
-        const int r = e / kp, c = e % kp;
-        ps[c * kPsStride + r] = r0 + r < J.m ? J.Ph[(size_t)(r0 + r) * kp + c] : 0.f;
-    }
-    for (int e = tid; e < kTileCols * kp; e += kThreads) {
-        const int j = e / kp, c = e % kp;
-        qs[c * kQsStride + j] = (c < J.k && c0 + j < J.n) ? J.Q[(size_t)(c0 + j) * J.k + c] : 0.f;
-    }
-    __syncthreads();
-    float acc[64];  // [8 rows][8 columns]
-#pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-    for (int c = 0; c < kp; ++c) {
-        const float4 p0 = *reinterpret_cast<const float4 *>(ps + c * kPsStride + 8 * warp);
-        const float4 p1 = *reinterpret_cast<const float4 *>(ps + c * kPsStride + 8 * warp + 4);
-        const float4 q0 = *reinterpret_cast<const float4 *>(qs + c * kQsStride + 4 * lane);
-        const float4 q1 = *reinterpret_cast<const float4 *>(qs + c * kQsStride + 128 + 4 * lane);
-        const float a[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        const float b[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int x = 0; x < 8; ++x) acc[r * 8 + x] = fmaf(a[r], b[x], acc[r * 8 + x]);
-    }
+    float *qs = reinterpret_cast<float *>(smem);  // kp x kQsStride (kp of the largest job)
     const float s = B.q_scale;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int task = blockIdx.x; task < B.total_tasks; task += gridDim.x) {
+        const UJob &J = B.job[find_job(begins, B.count, task)];
+        const int kp = J.kp, t = task - J.task_begin;
+        const int rbeg = (t / J.tiles_c) * kURows, c0 = (t % J.tiles_c) * kUCols;
+        const int rend = min(J.m, rbeg + kURows), ntile = (rend - rbeg + kUTile - 1) / kUTile;
+        const int col = c0 + 4 * lane;
+        const bool col_in = col < J.n;
+        float *ps = qs + kp * kQsStride;  // 2 x kUTile x kp
+        __syncthreads();                  // the previous task is done with qs and ps
+        for (int e = tid; e < kUCols * kp; e += kThreads) {
+            const int j = e / kp, c = e % kp;
+            qs[c * kQsStride + j] = (c < J.k && c0 + j < J.n) ? J.Q[(size_t)(c0 + j) * J.k + c] : 0.f;
+        }
+        auto load_ph = [&](int tile) {
+            const int r = rbeg + tile * kUTile, rows = min(kUTile, rend - r);
+            float *dst = ps + (tile & 1) * kUTile * kp;
+            const float *src = J.Ph + (size_t)r * kp;
+            for (int f = tid; f < rows * kp / 4; f += kThreads) cp_async16(dst + 4 * f, src + 4 * f);
+            cp_async_commit();
+        };
+        load_ph(0);
+        for (int tl = 0; tl < ntile; ++tl) {
+            const int rowb = rbeg + tl * kUTile + 4 * warp;
+            // this thread's operands, loaded ahead of the FMA work
+            float4 ev[4], tv[4], bv[4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int row = r0 + 8 * warp + r;
-        if (row >= J.m) break;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = c0 + 128 * h + 4 * lane;
-            if (col >= J.n) continue;
-            const size_t idx = (size_t)row * J.n + col;
-            const float4 D = make_float4(s * acc[r * 8 + 4 * h], s * acc[r * 8 + 4 * h + 1],
-                                         s * acc[r * 8 + 4 * h + 2], s * acc[r * 8 + 4 * h + 3]);
-            if (J.ef) {
-                float4 M = *reinterpret_cast<const float4 *>(J.E + idx);
-                M.x -= D.x; M.y -= D.y; M.z -= D.z; M.w -= D.w;
-                *reinterpret_cast<float4 *>(J.E + idx) = M;
+            for (int i = 0; i < 4; ++i) {
+                const bool in = col_in && rowb + i < rend;
+                const size_t idx = in ? (size_t)(rowb + i) * J.n + col : 0;
+                ev[i] = (in && J.ef) ? __ldcs(reinterpret_cast<const float4 *>(J.E + idx)) : zero;
+                tv[i] = (in && B.mode == 1) ? __ldcs(reinterpret_cast<const float4 *>(J.theta + idx)) : zero;
+                bv[i] = (in && B.mode == 1) ? __ldcs(reinterpret_cast<const float4 *>(J.mom + idx)) : zero;
             }
-            if (B.mode == 0) {
-                if (J.out) *reinterpret_cast<float4 *>(J.out + idx) = D;
+            if (tl + 1 < ntile) {
+                load_ph(tl + 1);
+                cp_async_wait<1>();
             } else {
-                float4 th = *reinterpret_cast<const float4 *>(J.theta + idx);
-                float4 b = *reinterpret_cast<const float4 *>(J.mom + idx);
+                cp_async_wait<0>();
+            }
+            __syncthreads();  // P^ rows of this tile (and qs) are visible
+            const float *pr = ps + (tl & 1) * kUTile * kp + 4 * warp * kp;
+            float acc[16];  // [4 rows][4 columns]
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int c4 = 0; c4 < kp; c4 += 4) {
+                float4 p[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[i] = *reinterpret_cast<const float4 *>(pr + i * kp + c4);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const float4 q = *reinterpret_cast<const float4 *>(qs + (c4 + cc) * kQsStride + 4 * lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float pv = cc == 0 ? p[i].x : cc == 1 ? p[i].y : cc == 2 ? p[i].z : p[i].w;
+                        acc[i * 4 + 0] = fmaf(pv, q.x, acc[i * 4 + 0]);
+                        acc[i * 4 + 1] = fmaf(pv, q.y, acc[i * 4 + 1]);
+                        acc[i * 4 + 2] = fmaf(pv, q.z, acc[i * 4 + 2]);
+                        acc[i * 4 + 3] = fmaf(pv, q.w, acc[i * 4 + 3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = rowb + i;
+                if (!col_in || row >= rend) continue;
+                const size_t idx = (size_t)row * J.n + col;
+                const float4 D = make_float4(s * acc[i * 4], s * acc[i * 4 + 1], s * acc[i * 4 + 2], s * acc[i * 4 + 3]);
+                if (J.ef) {
+                    const float4 M = ev[i];
+                    __stcs(reinterpret_cast<float4 *>(J.E + idx), make_float4(M.x - D.x, M.y - D.y, M.z - D.z, M.w - D.w));
+                }
+                if (B.mode == 0) {
+                    if (J.out) __stcs(reinterpret_cast<float4 *>(J.out + idx), D);
+                    continue;
+                }
                 const float mu = J.mu, lr = J.lr;
+                float4 b = bv[i], th = tv[i];
                 b.x = fmaf(mu, b.x, D.x); b.y = fmaf(mu, b.y, D.y);
                 b.z = fmaf(mu, b.z, D.z); b.w = fmaf(mu, b.w, D.w);
                 th.x = fmaf(-lr, fmaf(mu, b.x, D.x), th.x); th.y = fmaf(-lr, fmaf(mu, b.y, D.y), th.y);
                 th.z = fmaf(-lr, fmaf(mu, b.z, D.z), th.z); th.w = fmaf(-lr, fmaf(mu, b.w, D.w), th.w);
-                *reinterpret_cast<float4 *>(J.mom + idx) = b;
-                *reinterpret_cast<float4 *>(J.theta + idx) = th;
+                __stcs(reinterpret_cast<float4 *>(J.mom + idx), b);
+                __stcs(reinterpret_cast<float4 *>(J.theta + idx), th);
                 float4 w = th;
                 if (J.mix != 0.f) {
                     const float4 wl = *reinterpret_cast<const float4 *>(J.W + idx);
@@ -648,8 +951,9 @@ __global__ void __launch_bounds__(kThreads, 2) dp_update_kernel(const __grid_con
                     w.x = fmaf(J.mix, wl.x, keep * th.x); w.y = fmaf(J.mix, wl.y, keep * th.y);
                     w.z = fmaf(J.mix, wl.z, keep * th.z); w.w = fmaf(J.mix, wl.w, keep * th.w);
                 }
-                *reinterpret_cast<float4 *>(J.W + idx) = w;
+                __stcs(reinterpret_cast<float4 *>(J.W + idx), w);
             }
+            __syncthreads();  // this tile's P^ buffer may be refilled
         }
     }
 }
@@ -663,6 +967,8 @@ __global__ void __launch_bounds__(kThreads, 2) dp_update_kernel(const __grid_con
 using namespace spco;
 
 namespace {
+
+constexpr size_t kSmemBudget = 232448;  // 227 KB: one CTA per SM
 
 int validate_batch(dpsync_t *const *hs, int32_t count, const char *what) {
     if (!hs || count < 1 || count > DPSYNC_MAX_BATCH)
@@ -680,15 +986,22 @@ int set_smem(const void *fn, size_t bytes) {
                        "cudaFuncSetAttribute");
 }
 
-int gram_smem_bytes(int kp) {
-    const size_t p1 = sizeof(float) * (2 * (size_t)kGramRows * kp + (size_t)kp * kp);
-    const size_t p2 = sizeof(double) * (2 * (size_t)kp * kp + 2 * (size_t)kp);
-    return (int)std::max(p1, p2);
+int gram_blocks(int kp) { return (kp / 4) * (kp / 4 + 1) / 2; }
+int p_rows(int kp) { return kp == 64 ? 8 : 16; }
+
+// launch order of a batch: largest work first, so the tail of the grid is short
+std::vector<int> by_size(dpsync_t *const *hs, int count) {
+    std::vector<int> order(count);
+    for (int i = 0; i < count; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        return (int64_t)hs[a]->m * hs[a]->n > (int64_t)hs[b]->m * hs[b]->n;
+    });
+    return order;
 }
 
 void free_all(dpsync *h) {
-    for (void *p : {(void *)h->E, (void *)h->theta, (void *)h->mom, (void *)h->Ph, (void *)h->T,
-                    (void *)h->Gpart, (void *)h->Qpart, (void *)h->counters})
+    for (void *p : {(void *)h->E, (void *)h->theta, (void *)h->mom, (void *)h->Ph, (void *)h->Qp, (void *)h->T,
+                    (void *)h->Gpart, (void *)h->Qpart, (void *)h->counters, (void *)h->maps})
         if (p) cudaFree(p);
 }
 
@@ -739,23 +1052,39 @@ extern "C" int dpsync_create(dpsync_t **out, const dpsync_config *cfg, float *P,
     h->gram_tasks = (h->m + kGramRows - 1) / kGramRows;
     h->q_ranges = (h->m + kQRows - 1) / kQRows;
     h->ncb = (h->n + kQCols - 1) / kQCols;
-    const size_t mn = (size_t)h->m * h->n, E = (size_t)h->kp * (h->kp + 1) / 2;
+    const size_t mn = (size_t)h->m * h->n, kp = h->kp;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMalloc(&h->E, sizeof(float) * mn);
-    if (e == cudaSuccess) e = cudaMalloc(&h->Ph, sizeof(float) * (size_t)h->m * h->kp);
-    if (e == cudaSuccess) e = cudaMalloc(&h->T, sizeof(float) * 2 * (size_t)h->kp * h->kp);
-    if (e == cudaSuccess) e = cudaMalloc(&h->Gpart, sizeof(double) * E * h->gram_tasks);
-    if (e == cudaSuccess)
-        e = cudaMalloc(&h->Qpart, sizeof(float) * (size_t)h->q_ranges * h->ncb * kQCols * h->kp);
-    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * (2 + h->ncb));
+    if (e == cudaSuccess) e = cudaMalloc(&h->Ph, sizeof(float) * (size_t)h->m * kp);
+    if (e == cudaSuccess) e = cudaMalloc(&h->Qp, sizeof(float) * (size_t)h->n * (kp + 4));
+    if (e == cudaSuccess) e = cudaMalloc(&h->T, sizeof(float) * 2 * kp * kp);
+    if (e == cudaSuccess) e = cudaMalloc(&h->Gpart, sizeof(float) * 32 * (size_t)gram_blocks(h->kp) * h->gram_tasks);
+    if (e == cudaSuccess) e = cudaMalloc(&h->Qpart, sizeof(float) * (size_t)h->q_ranges * h->ncb * kQCols * kp);
+    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&h->maps, sizeof(CUtensorMap) * 6);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->E, 0, sizeof(float) * mn, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->Ph, 0, sizeof(float) * (size_t)h->m * h->kp, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->T, 0, sizeof(float) * 2 * (size_t)h->kp * h->kp, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->counters, 0, sizeof(int) * (2 + h->ncb), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->Ph, 0, sizeof(float) * (size_t)h->m * kp, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->T, 0, sizeof(float) * 2 * kp * kp, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->counters, 0, sizeof(int) * 2, st);
     if (e != cudaSuccess) {
         free_all(h);
         delete h;
         return cuda_status(e, "dpsync_create");
+    }
+    // tensor maps of the handle's own buffers (those of X and Y follow each call)
+    CUtensorMap hm[4];
+    const uint32_t R = (uint32_t)p_rows(h->kp);
+    int rc = make_tmap_2d_ex(&hm[0], h->E, h->m, h->n, h->n, kPBC, R, false);
+    if (!rc) rc = make_tmap_2d_ex(&hm[1], h->Qp, h->n, h->kp + 4, h->kp + 4, h->kp + 4, kPBC, false);
+    if (!rc) rc = make_tmap_2d_ex(&hm[2], h->E, h->m, h->n, h->n, kQCols, kQChunk, false);
+    if (!rc) rc = make_tmap_2d_ex(&hm[3], h->Ph, h->m, h->kp, h->kp, h->kp, kQChunk, false);
+    if (!rc) rc = cuda_status(cudaMemcpyAsync(h->maps + 2, hm, sizeof(hm), cudaMemcpyHostToDevice, st),
+                              "dpsync_create: tensor maps");
+    if (!rc) rc = cuda_status(cudaStreamSynchronize(st), "dpsync_create");
+    if (rc) {
+        free_all(h);
+        delete h;
+        return rc;
     }
     *out = h;
     return SPECOPTIM_OK;
@@ -792,10 +1121,15 @@ extern "C" int dpsync_compress_p_many(dpsync_t *const *hs, int32_t count, const 
     clear_error();
     int rc;
     if ((rc = validate_batch(hs, count, "dpsync_compress_p_many"))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    PadBatch pad{};
     PBatch b{};
-    b.count = count;
-    int total = 0, kpmax = 8;
-    for (int i = 0; i < count; ++i) {
+    pad.count = b.count = count;
+    int64_t pad_total = 0;
+    int tasks = 0, kpmax = 8;
+    const std::vector<int> order = by_size(hs, count);
+    for (int slot = 0; slot < count; ++slot) {
+        const int i = order[slot];
         dpsync *h = hs[i];
         const float *x = X ? X[i] : nullptr;
         if (!x) {
@@ -806,26 +1140,58 @@ extern "C" int dpsync_compress_p_many(dpsync_t *const *hs, int32_t count, const 
         const float *y = Y ? Y[i] : nullptr;
         if (!aligned16(x) || (y && !aligned16(y)))
             return fail(SPECOPTIM_ERR_MISALIGNED, "dpsync_compress_p_many: X and Y must be 16-byte aligned");
-        PJob &j = b.job[i];
-        j.X = x;
-        j.Y = y;
+        PadJob &pj = pad.job[slot];
+        pj.Q = h->Q;
+        pj.Qp = h->Qp;
+        pj.n = h->n;
+        pj.k = h->k;
+        pj.kp = h->kp;
+        pj.begin = pad_total;
+        pad_total += (int64_t)h->n * (h->kp + 4);
+        if (x != h->map_x || (y && y != h->map_y)) {
+            CUtensorMap xm[2];
+            const uint32_t R = (uint32_t)p_rows(h->kp);
+            int r2 = make_tmap_2d_ex(&xm[0], x, h->m, h->n, h->n, kPBC, R, false);
+            if (!r2) r2 = make_tmap_2d_ex(&xm[1], y ? y : x, h->m, h->n, h->n, kPBC, R, false);
+            if (r2) return r2;
+            SPECOPTIM_CUDA(cudaMemcpyAsync(h->maps, xm, sizeof(xm), cudaMemcpyHostToDevice, st));
+            h->map_x = x;
+            h->map_y = y ? y : x;
+        }
+        PJob &j = b.job[slot];
+        j.mx = h->maps;
+        j.my = h->maps + 1;
+        j.me = h->maps + 2;
+        j.mq = h->maps + 3;
+        j.hasY = y ? 1 : 0;
         j.E = h->E;
-        j.Q = h->Q;
         j.P = h->P;
         j.m = h->m;
         j.n = h->n;
         j.k = h->k;
         j.kp = h->kp;
         j.ef = h->cfg.error_feedback ? 1 : 0;
-        j.cta_begin = total;
-        total += (h->m + p_cfg(h->kp).R - 1) / p_cfg(h->kp).R;
+        j.R = p_rows(h->kp);
+        j.nch = (h->n + kPBC - 1) / kPBC;
+        j.task_begin = tasks;
+        tasks += (h->m + j.R - 1) / j.R;
         kpmax = std::max(kpmax, h->kp);
     }
-    b.stage_floats = p_stage_floats(kpmax);
-    const size_t smem = sizeof(float) * ((size_t)kPStages * b.stage_floats + 8 * 64);
+    pad.total = pad_total;
+    b.total_tasks = tasks;
+    b.stage_bytes = (uint32_t)align128(sizeof(float) * (3 * (size_t)kPBuf + (size_t)kPBC * (kpmax + 4)));
+    // two CTAs per SM when two stages each fit in half of shared memory, else one with more stages
+    const size_t fixed = 128 + 8 * 64 * sizeof(float);
+    const int per_sm = fixed + 2 * (size_t)b.stage_bytes <= kSmemBudget / 2 ? 2 : 1;
+    b.stages = (int)std::min<size_t>(kPMaxStages, (kSmemBudget / per_sm - fixed) / b.stage_bytes);
+    b.flag = device_flag_ptr();
+    const size_t smem = fixed + (size_t)b.stages * b.stage_bytes;
     if ((rc = set_smem((const void *)dp_compress_p_kernel, smem))) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SPCO_LAUNCH("dp_compress_p", st, dp_compress_p_kernel<<<total, kThreads, smem, st>>>(b));
+    const int pad_grid = (int)std::min<int64_t>((pad_total + kThreads - 1) / kThreads, 4 * num_sms());
+    SPCO_LAUNCH("dp_pad_q", st, dp_pad_q_kernel<<<pad_grid, kThreads, 0, st>>>(pad));
+    SPECOPTIM_LAUNCHED("dp_pad_q_kernel");
+    const int grid = std::min(tasks, per_sm * num_sms());
+    SPCO_LAUNCH("dp_compress_p", st, dp_compress_p_kernel<<<grid, kThreads, smem, st>>>(b));
     SPECOPTIM_LAUNCHED("dp_compress_p_kernel");
     return SPECOPTIM_OK;
 }
@@ -837,6 +1203,7 @@ extern "C" int dpsync_orthogonalize_many(dpsync_t *const *hs, int32_t count, voi
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int kpmax = 8;
     for (int i = 0; i < count; ++i) kpmax = std::max(kpmax, hs[i]->kp);
+    const std::vector<int> order = by_size(hs, count);
     const size_t gsmem = gram_smem_bytes(kpmax);
     if ((rc = set_smem((const void *)dp_gram_kernel, gsmem))) return rc;
     for (int pass = 0; pass < 2; ++pass) {
@@ -844,13 +1211,13 @@ extern "C" int dpsync_orthogonalize_many(dpsync_t *const *hs, int32_t count, voi
         g.count = count;
         g.pass = pass;
         int total = 0;
-        for (int i = 0; i < count; ++i) {
-            dpsync *h = hs[i];
-            GJob &j = g.job[i];
+        for (int slot = 0; slot < count; ++slot) {
+            dpsync *h = hs[order[slot]];
+            GJob &j = g.job[slot];
             j.P = h->P;
-            j.T1 = h->T;
+            j.R1 = h->T;
             j.Gpart = h->Gpart;
-            j.Tout = h->T + (size_t)pass * h->kp * h->kp;
+            j.Rout = h->T + (size_t)pass * h->kp * h->kp;
             j.counter = h->counters + pass;
             j.m = h->m;
             j.k = h->k;
@@ -865,11 +1232,11 @@ extern "C" int dpsync_orthogonalize_many(dpsync_t *const *hs, int32_t count, voi
     ABatch a{};
     a.count = count;
     int total = 0;
-    for (int i = 0; i < count; ++i) {
-        dpsync *h = hs[i];
-        AJob &j = a.job[i];
+    for (int slot = 0; slot < count; ++slot) {
+        dpsync *h = hs[order[slot]];
+        AJob &j = a.job[slot];
         j.P = h->P;
-        j.T = h->T;
+        j.R = h->T;
         j.Ph = h->Ph;
         j.m = h->m;
         j.k = h->k;
@@ -877,7 +1244,7 @@ extern "C" int dpsync_orthogonalize_many(dpsync_t *const *hs, int32_t count, voi
         j.cta_begin = total;
         total += (h->m + kApplyRows - 1) / kApplyRows;
     }
-    const size_t asmem = sizeof(float) * (2 * (size_t)kApplyRows * kpmax + 2 * (size_t)kpmax * kpmax);
+    const size_t asmem = sizeof(float) * 2 * (size_t)kpmax * kpmax;
     if ((rc = set_smem((const void *)dp_orth_apply_kernel, asmem))) return rc;
     SPCO_LAUNCH("dp_orth_apply", st, dp_orth_apply_kernel<<<total, kThreads, asmem, st>>>(a));
     SPECOPTIM_LAUNCHED("dp_orth_apply_kernel");
@@ -888,33 +1255,53 @@ extern "C" int dpsync_compress_q_many(dpsync_t *const *hs, int32_t count, void *
     clear_error();
     int rc;
     if ((rc = validate_batch(hs, count, "dpsync_compress_q_many"))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     QBatch b{};
-    b.count = count;
-    int total = 0, kpmax = 8;
-    for (int i = 0; i < count; ++i) {
-        dpsync *h = hs[i];
-        QJob &j = b.job[i];
-        j.M = h->E;
-        j.Ph = h->Ph;
+    RBatch r{};
+    b.count = r.count = count;
+    int tasks = 0, kpmax = 8;
+    int64_t rtotal = 0;
+    const std::vector<int> order = by_size(hs, count);
+    for (int slot = 0; slot < count; ++slot) {
+        dpsync *h = hs[order[slot]];
+        QJob &j = b.job[slot];
+        j.mm = h->maps + 4;
+        j.mp = h->maps + 5;
         j.Qpart = h->Qpart;
-        j.Q = h->Q;
-        j.counter = h->counters + 2;
         j.m = h->m;
         j.n = h->n;
-        j.k = h->k;
         j.kp = h->kp;
         j.ranges = h->q_ranges;
         j.ncb = h->ncb;
-        j.task_begin = total;
-        total += h->q_ranges * h->ncb;
+        j.task_begin = tasks;
+        tasks += h->q_ranges * h->ncb;
         kpmax = std::max(kpmax, h->kp);
+        RJob &rj = r.job[slot];
+        rj.Qpart = h->Qpart;
+        rj.Q = h->Q;
+        rj.n = h->n;
+        rj.k = h->k;
+        rj.kp = h->kp;
+        rj.ranges = h->q_ranges;
+        rj.ldp = h->ncb * kQCols;
+        rj.begin = rtotal;
+        rtotal += (int64_t)h->n * h->k;
     }
-    b.stage_floats = kQChunk * kQCols + kQChunk * kpmax;
-    const size_t smem = sizeof(float) * (size_t)kQStages * b.stage_floats;
+    b.total_tasks = tasks;
+    r.total = rtotal;
+    b.stage_bytes = (uint32_t)align128(sizeof(float) * ((size_t)kQChunk * kQCols + (size_t)kQChunk * kpmax));
+    b.stages = kQStages;
+    b.flag = device_flag_ptr();
+    const size_t smem = 128 + 128 * 64 * sizeof(float) + (size_t)b.stages * b.stage_bytes;
     if ((rc = set_smem((const void *)dp_compress_q_kernel, smem))) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SPCO_LAUNCH("dp_compress_q", st, dp_compress_q_kernel<<<total, kThreads, smem, st>>>(b));
+    int per_sm = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dp_compress_q_kernel, kThreads, smem);
+    const int grid = std::min(tasks, std::max(1, per_sm) * num_sms());
+    SPCO_LAUNCH("dp_compress_q", st, dp_compress_q_kernel<<<grid, kThreads, smem, st>>>(b));
     SPECOPTIM_LAUNCHED("dp_compress_q_kernel");
+    const int rgrid = (int)std::min<int64_t>((rtotal + kThreads - 1) / kThreads, 4 * num_sms());
+    SPCO_LAUNCH("dp_q_reduce", st, dp_q_reduce_kernel<<<rgrid, kThreads, 0, st>>>(r));
+    SPECOPTIM_LAUNCHED("dp_q_reduce_kernel");
     return SPECOPTIM_OK;
 }
 
@@ -929,13 +1316,15 @@ int launch_update(dpsync_t *const *hs, int32_t count, float *const *ptrs, float 
     b.mode = mode;
     b.q_scale = q_scale;
     int total = 0, kpmax = 8;
-    for (int i = 0; i < count; ++i) {
+    const std::vector<int> order = by_size(hs, count);
+    for (int slot = 0; slot < count; ++slot) {
+        const int i = order[slot];
         dpsync *h = hs[i];
         float *p = ptrs ? ptrs[i] : nullptr;
         if (mode == 1 && (!p || !h->have_outer))
             return fail(SPECOPTIM_ERR_INVALID_ARG, std::string(what) + ": needs W_local and set_outer");
         if (p && !aligned16(p)) return fail(SPECOPTIM_ERR_MISALIGNED, std::string(what) + ": 16-byte alignment");
-        UJob &j = b.job[i];
+        UJob &j = b.job[slot];
         j.Ph = h->Ph;
         j.Q = h->Q;
         j.E = h->E;
@@ -948,19 +1337,23 @@ int launch_update(dpsync_t *const *hs, int32_t count, float *const *ptrs, float 
         j.k = h->k;
         j.kp = h->kp;
         j.ef = h->cfg.error_feedback ? 1 : 0;
-        j.tiles_n = (h->n + kTileCols - 1) / kTileCols;
-        j.cta_begin = total;
+        j.tiles_c = (h->n + kUCols - 1) / kUCols;
+        j.task_begin = total;
         j.lr = h->cfg.outer_lr;
         j.mu = h->cfg.outer_momentum;
         j.mix = h->cfg.mix;
-        total += ((h->m + kTileRows - 1) / kTileRows) * j.tiles_n;
+        total += ((h->m + kURows - 1) / kURows) * j.tiles_c;
         kpmax = std::max(kpmax, h->kp);
     }
-    const size_t smem = sizeof(float) * (size_t)kpmax * (kPsStride + kQsStride);
+    b.total_tasks = total;
+    const size_t smem = sizeof(float) * (size_t)kpmax * (kQsStride + 2 * kUTile);
     if ((rc = set_smem((const void *)dp_update_kernel, smem))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int per_sm = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dp_update_kernel, kThreads, smem);
+    const int grid = std::min(total, std::max(1, per_sm) * num_sms());
     SPCO_LAUNCH(mode == 0 ? "dp_decompress" : "dp_outer_step", st,
-                dp_update_kernel<<<total, kThreads, smem, st>>>(b));
+                dp_update_kernel<<<grid, kThreads, smem, st>>>(b));
     SPECOPTIM_LAUNCHED("dp_update_kernel");
     return SPECOPTIM_OK;
 }
@@ -984,9 +1377,9 @@ extern "C" int dpsync_get_state(const dpsync_t *h, float *E, float *theta, float
     if (!h) return fail(SPECOPTIM_ERR_INVALID_ARG, "dpsync_get_state: null handle");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = sizeof(float) * (size_t)h->m * h->n;
-    if (E) SPECOPTIM_CUDA(cudaMemcpyAsync(E, h->E, bytes, cudaMemcpyDeviceToDevice, st));
     if ((theta || mom) && !h->have_outer)
         return fail(SPECOPTIM_ERR_INVALID_ARG, "dpsync_get_state: set_outer was not called");
+    if (E) SPECOPTIM_CUDA(cudaMemcpyAsync(E, h->E, bytes, cudaMemcpyDeviceToDevice, st));
     if (theta) SPECOPTIM_CUDA(cudaMemcpyAsync(theta, h->theta, bytes, cudaMemcpyDeviceToDevice, st));
     if (mom) SPECOPTIM_CUDA(cudaMemcpyAsync(mom, h->mom, bytes, cudaMemcpyDeviceToDevice, st));
     if (P_hat)

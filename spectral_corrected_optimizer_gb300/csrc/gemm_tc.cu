@@ -374,6 +374,11 @@ bool tmap_encoder_available() { return encode_fn() != nullptr; }
 
 int make_tmap_2d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
                  uint32_t box_cols, uint32_t box_rows) {
+    return make_tmap_2d_ex(map, ptr, rows, cols, ld, box_cols, box_rows, true);
+}
+
+int make_tmap_2d_ex(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(SPECOPTIM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -381,7 +386,8 @@ int make_tmap_2d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols,
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(SPECOPTIM_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");

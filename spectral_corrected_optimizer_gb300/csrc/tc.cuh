@@ -117,6 +117,10 @@ constexpr uint32_t tf32_idesc(int M, int N) {
 // x box_rows.  Fails with SPECOPTIM_ERR_CUDA if the driver entry point is missing.
 int make_tmap_2d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
                  uint32_t box_cols, uint32_t box_rows);
+// Same with the swizzle chosen: 128-byte swizzle (box_cols * 4 <= 128) or none
+// (rows of the box land densely in shared memory, box_cols * 4 a multiple of 16).
+int make_tmap_2d_ex(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 bool tmap_encoder_available();
 
 }  // namespace spco
