@@ -54,7 +54,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxJobs = DPSYNC_MAX_BATCH;
-constexpr int kPBC = 64;         // compress_p columns per stage
+constexpr int kPBC = 128;        // compress_p columns per stage
 constexpr int kPMaxStages = 6;
 constexpr int kGramRows = 128;   // rows per Gram task
 constexpr int kQRows = 512;      // rows per compress_q task
@@ -186,9 +186,11 @@ __global__ void __launch_bounds__(kThreads) dp_pad_q_kernel(const __grid_constan
 // ---------------------------------------------------------------------------
 // compress_p:  M = E + X - Y -> E (global);  P = M Q
 // Task: R rows (16; 8 for kp = 64) of one matrix over all its columns, in
-// stages of 64 columns.  Thread 0 keeps a ring of stages in flight: per stage
-// one 2D TMA box (64 columns x R rows) of each of X, Y, E and one of Qp (the
-// stage's 64 rows of Q, padded), all completing on the stage's mbarrier; the
+// stages of 128 columns (512-byte row segments: narrower boxes cost DRAM
+// efficiency, wider ones leave no room for the Q box).  Thread 0 keeps a ring
+// of stages in flight: per stage one 2D TMA box (128 columns x R rows) of each
+// of X, Y, E and one of Qp (the stage's 128 rows of Q, padded), all
+// completing on the stage's mbarrier; the
 // boxes are zero-filled outside the matrices.  The warps form M (written to
 // global E from registers and in place of the E box), and the 8 warps
 // accumulate P in 8 x 8 register tiles ((R/8)(kp/8) tiles, cs warps per tile
@@ -207,7 +209,7 @@ struct PBatch {
     uint32_t stage_bytes;
     unsigned *flag;
 };
-constexpr int kPBuf = kPRows * kPBC;  // floats of one input box (R x 64)
+constexpr int kPBuf = kPRows * kPBC;  // floats of one input box (R x 128)
 
 struct PCursor {
     int task, chunk, job;  // task < 0: past the end
