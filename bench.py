@@ -57,9 +57,10 @@ def env_int(name, default):
         return default
 
 
-def profiled_traffic(profile: str, sources):
+def profiled_traffic(profile: str, sources, key: str = ""):
     """DRAM bytes per launch from a committed ncu summary under profiles/, or None
-    when one of the kernel's sources changed since the counters were taken."""
+    when one of the kernel's sources changed since the counters were taken
+    (`key`: the kernel name in front of the figure, for summaries of several kernels)."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "spectral_corrected_optimizer_gb300", "csrc")
@@ -72,7 +73,8 @@ def profiled_traffic(profile: str, sources):
             text = f.read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch=([0-9.e+]+) sources_sha256_16=([0-9a-f]+)", text)
+    m = re.search((re.escape(key) + " " if key else "") +
+                  r"traffic_bytes_per_launch=([0-9.e+]+) sources_sha256_16=([0-9a-f]+)", text)
     if not m or m.group(2) != h.hexdigest()[:16]:
         return None
     return float(m.group(1))
@@ -81,6 +83,7 @@ def profiled_traffic(profile: str, sources):
 GEMM_PROFILE = ("gemm_tf32_layer_step.md", ("gemm_tc.cu", "gemm.cuh", "tc.cuh", "specoptim.cu"))
 ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh"))
 APPLY_PROFILE = ("jacobi_apply_layer_refresh.md", ("jacobi_apply_tc.cu", "jacobi.cuh", "tc.cuh"))
+DPSYNC_PROFILE = ("dpsync_layer_outer_sync.md", ("dpsync.cu", "tc.cuh", "common.cuh"))
 
 
 def padded_order(r: int) -> int:
@@ -458,7 +461,9 @@ def run_dp_sync(shapes, K: int, W: int, peaks: dict, peak_src: str, seed: int = 
         ach = b / (t * 1e-3) / 1e9 if t > 0 else None
         return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm if ach else None, "avg_launch_ms": t / max(n_l, 1),
-                "algorithmic_bytes_per_launch": b}
+                "algorithmic_bytes_per_launch": b,
+                "traffic": profiled_traffic(*DPSYNC_PROFILE, key=kernel.split()[0]),
+                "traffic_source": "profiles/" + DPSYNC_PROFILE[0]}
 
     total_bytes = sum(byts.values())
     values = sum(m * n for m, n in shapes)
