@@ -29,7 +29,11 @@ design notes):
     compressed by one warm-started PowerSGD power step with error feedback;
     the rank k of each matrix gives mn / ((m + n) k) = 64; the orthonormal
     basis is Gram-Schmidt with dependent columns set to zero; workers' P and Q
-    are summed and the decompressed update scaled by 1 / workers.
+    are summed and the decompressed update scaled by 1 / workers;
+  * the mask fused with the layer boundary (key design 1 with the decoder
+    layer around it): a bf16 sum is the float32 sum rounded to bf16 (nearest
+    even); RMSNorm (Llama form, x = h / sqrt(mean(h^2) + eps) * gamma) is
+    computed in float64 and rounded once.
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py``
 against closed forms, brute force, published test vectors or independent
@@ -412,3 +416,80 @@ class DPSync:
         self.theta, self.mom, W_new = outer_nesterov(self.theta, self.mom, D, self.outer_lr,
                                                      self.outer_momentum, W_local, self.mix)
         return W_new
+
+
+# ---------------------------------------------------------------------------
+# key design 1 at the layer boundary: the mask folded into the ops next to it.
+# The page sends only the K kept values of the boundary activation and of its
+# gradient; on the sender the boundary value is the decoder layer's residual
+# sum h = a + b, on the receiver the next layer starts with RMSNorm of h~
+# (Llama: x = h / sqrt(mean(h^2) + eps) * gamma) and keeps h~ for its residual
+# branch.  All tensors bf16 (uint16 bit patterns here).  Readings: a bf16 sum
+# is the float32 sum rounded to bf16 (nearest even); RMSNorm is computed in
+# float64 here and rounded once to bf16 at the end.
+# ---------------------------------------------------------------------------
+
+def bf16_bits(x) -> np.ndarray:
+    """Round to bfloat16, nearest with ties to even (via float32), as uint16 bits."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return np.where(np.isnan(x), np.uint16(0x7FC0), r)
+
+
+def bf16_value(bits) -> np.ndarray:
+    """float64 value of bf16 bit patterns."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16)).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def mask_pack_add(a, b, K: int, layer: int, step: int, batch_id: int = 0) -> np.ndarray:
+    """Sender: packed[r, k] = bf16(a + b)[r, pi_r(k)] (the residual sum is formed at
+    the kept dims only)."""
+    s = (bf16_value(a).astype(np.float32) + bf16_value(b).astype(np.float32))
+    return mask_pack(bf16_bits(s), K, layer, step, batch_id)
+
+
+def mask_unpack_rmsnorm(packed, gamma, eps: float, H: int, layer: int, step: int, batch_id: int = 0):
+    """Receiver: h~ = unpack(packed) and x = RMSNorm(h~) * gamma.  Returns
+    (h~ bits, x bits, x in float64 before rounding)."""
+    h = mask_unpack(np.ascontiguousarray(packed, dtype=np.uint16), H, layer, step, batch_id)
+    hv = bf16_value(h)
+    r = 1.0 / np.sqrt(np.mean(hv * hv, axis=1, keepdims=True) + eps)
+    x = hv * r * bf16_value(gamma)[None, :]
+    return h, bf16_bits(x), x
+
+
+def mask_rmsnorm_backward_pack(packed_h, gamma, eps: float, dx, g_res, layer: int, step: int,
+                               batch_id: int = 0):
+    """Receiver backward: dL/dh~ = g_res + RMSNorm backward of the upstream gradient
+    dx, sent at the kept dims only:
+      dL/dh~_j = g_res_j + gamma_j dx_j / r - h~_j (sum_i gamma_i dx_i h~_i) / (H r^3),
+    r = sqrt(mean(h~^2) + eps).  Returns (packed bits, float64 values)."""
+    packed_h = np.ascontiguousarray(packed_h, dtype=np.uint16)
+    rows, K = packed_h.shape
+    H = np.asarray(gamma).shape[0]
+    h = bf16_value(mask_unpack(packed_h, H, layer, step, batch_id))
+    g = bf16_value(gamma)[None, :]
+    dxv = bf16_value(dx)
+    rr = np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps)
+    s = np.sum(g * dxv * h, axis=1, keepdims=True)
+    dh = g * dxv / rr - h * s / (H * rr ** 3)
+    if g_res is not None:
+        dh = dh + bf16_value(g_res)
+    idx = mask_indices(rows, H, K, layer, step, batch_id).astype(np.int64)
+    vals = np.take_along_axis(dh, idx, axis=1)
+    return bf16_bits(vals), vals
+
+
+def mask_unpack_add(packed, g, layer: int, step: int, batch_id: int = 0) -> np.ndarray:
+    """Sender backward: g[r, pi_r(k)] <- bf16(g + packed[r, k]); every other entry of g
+    unchanged (the returned array is a new one)."""
+    g = np.array(g, dtype=np.uint16, copy=True)
+    packed = np.ascontiguousarray(packed, dtype=np.uint16)
+    rows, K = packed.shape
+    idx = mask_indices(rows, g.shape[1], K, layer, step, batch_id).astype(np.int64)
+    cur = np.take_along_axis(g, idx, axis=1)
+    s = bf16_value(cur).astype(np.float32) + bf16_value(packed).astype(np.float32)
+    np.put_along_axis(g, idx, bf16_bits(s), axis=1)
+    return g
