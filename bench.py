@@ -410,6 +410,73 @@ def mask_sweep(layer: Layer, p: float):
     return out
 
 
+def sector_coverage(H: int, K: int, elems: int = 16) -> float:
+    """Expected fraction of a row's 32-byte sectors (16 bf16) that hold at least one
+    of K kept dims drawn without replacement from H (what a gather at the kept dims
+    costs in DRAM traffic)."""
+    miss = 1.0
+    for i in range(elems):
+        miss *= max(0.0, (H - K - i) / (H - i))
+    return 1.0 - miss
+
+
+def mask_fused_bench(peaks: dict, peak_src: str, p: float = 0.95, reps: int = 20) -> dict:
+    """The mask ops fused with the layer boundary on the workload's bf16 [65536, 2048]
+    boundary tensor: each op timed alone (CUDA events, `reps` launches, inputs larger
+    than L2), its algorithmic bytes (sector coverage for the gathers at kept dims) and
+    the unfused chain it replaces (plain mask ops + torch elementwise) for context."""
+    import torch
+
+    import spectral_corrected_optimizer_gb300 as so
+
+    rows, H = MASK_ROWS, MASK_H
+    K = so.mask_keep_count(p, H)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    a = torch.randn(rows, H, device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randn(rows, H, device="cuda", generator=g).to(torch.bfloat16)
+    gamma = torch.randn(H, device="cuda", generator=g).to(torch.bfloat16)
+    packed = so.mask_pack_add(a, b, K, 1, 0)
+    h_out, x_out = torch.empty_like(a), torch.empty_like(a)
+    pg = torch.empty_like(packed)
+    gg = b.clone()
+    cov = sector_coverage(H, K)
+    dense, pk = rows * H * 2.0, rows * K * 2.0
+
+    def t_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    ops = {
+        "pack_add": (lambda: so.mask_pack_add(a, b, K, 1, 0, out=packed), 2 * cov * dense + pk,
+                     lambda: so.mask_pack(a + b, K, 1, 0, 0, out=packed)),
+        "unpack_rmsnorm": (lambda: so.mask_unpack_rmsnorm(packed, gamma, 1e-5, H, 1, 0, h_out=h_out, x_out=x_out),
+                           pk + 2 * dense,
+                           lambda: torch.nn.functional.rms_norm(so.mask_unpack(packed, H, 1, 0, 0, out=h_out),
+                                                                (H,), gamma, 1e-5)),
+        "rmsnorm_backward_pack": (lambda: so.mask_rmsnorm_backward_pack(packed, gamma, 1e-5, a, b, 1, 0, out=pg),
+                                  2 * cov * dense + 2 * pk, None),
+        "unpack_add": (lambda: so.mask_unpack_add(packed, gg, 1, 0), pk + 2 * cov * dense,
+                       lambda: gg.add_(so.mask_unpack(packed, H, 1, 0, 0, out=h_out))),
+    }
+    out = {"rows": rows, "H": H, "p": p, "K": K, "sector_coverage": cov, "ops": {}}
+    for name, (fn, byts, unfused) in ops.items():
+        ms = t_ms(fn)
+        ach = byts / (ms * 1e-3) / 1e9
+        rec = {"ms": ms, "algorithmic_bytes": byts, "achieved_GBps": ach, "frac_of_hbm": ach / peaks["hbm_gbs"]}
+        if unfused is not None:
+            rec["unfused_ms"] = t_ms(unfused)
+        out["ops"][name] = rec
+    out["peak_source"] = "%s HBM copy bandwidth" % peak_src
+    return out
+
+
 def dp_sync_bytes(m: int, n: int, k: int) -> dict:
     """Algorithmic HBM bytes of one outer synchronisation of an m x n matrix at
     rank k, per kernel: compress_p reads theta, W_local and E and writes E
@@ -524,6 +591,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     refresh_rep = so.trace_report()
     so.trace_enable(False)
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
+    mask_fused = mask_fused_bench(peaks, peak_src)
     import synthetic as _syn
     dp_sync = run_dp_sync(list(_syn.LLAMA_1B_LAYER.values()), max(5, min(K, 20)), 3, peaks, peak_src, seed=rank)
     others = {}
@@ -612,6 +680,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                       "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()},
                       "refresh_kernels": {k: {"launches": v[0], "ms": round(v[1], 3)} for k, v in refresh_rep.items()}},
         "mask": dict(mask, frac_of_hbm=mask_frac, hbm_peak_GBps=peaks["hbm_gbs"]),
+        "mask_fused": dict(mask_fused, workload="mask fused with the layer boundary: bf16 [65536, 2048], p = 0.95"),
         "dp_outer_sync": dict(dp_sync, workload="PowerSGD-compressed Streaming DiLoCo outer sync of the "
                                                 "llama-3.2-1b decoder layer (7 matrices, rank for 64x)"),
         "other_configs": others,
@@ -797,7 +866,8 @@ def run_profile_case(args):
     'mask': pack / unpack of one bf16 [65536, 2048] boundary at p = 0.95;
     'refresh': anchor EMA + SVD refresh of one 2048x2048 matrix, twice (the second warm);
     'layer': batched refresh, then grouped steady steps of the 7-matrix 1B layer;
-    'dpsync': PowerSGD-compressed outer syncs of the 7-matrix 1B layer."""
+    'dpsync': PowerSGD-compressed outer syncs of the 7-matrix 1B layer;
+    'maskfused': the four mask ops fused with the layer boundary on bf16 [65536, 2048]."""
     import numpy as np
     import torch
 
@@ -819,6 +889,17 @@ def run_profile_case(args):
         layer.refresh(0)
         for i in range(n_iter):
             layer.spectral(i)
+    elif args.profile == "maskfused":
+        K = so.mask_keep_count(MASK_P, MASK_H)
+        gen = torch.Generator(device="cuda").manual_seed(3)
+        a = torch.randn(MASK_ROWS, MASK_H, device="cuda", generator=gen).to(torch.bfloat16)
+        b = torch.randn(MASK_ROWS, MASK_H, device="cuda", generator=gen).to(torch.bfloat16)
+        gamma = torch.randn(MASK_H, device="cuda", generator=gen).to(torch.bfloat16)
+        for i in range(n_iter):
+            packed = so.mask_pack_add(a, b, K, i, 0)
+            so.mask_unpack_rmsnorm(packed, gamma, 1e-5, MASK_H, i, 0)
+            so.mask_rmsnorm_backward_pack(packed, gamma, 1e-5, a, b, i, 0)
+            so.mask_unpack_add(packed, b, i, 0)
     elif args.profile == "dpsync":
         import spectral_corrected_optimizer_gb300.dpsync as dp
         shapes = list(synthetic.LLAMA_1B_LAYER.values())
@@ -858,7 +939,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the full-1B and 7B-layer measurements reported beside the headline")
-    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync"], default=None,
+    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync", "maskfused"], default=None,
                     help="run a small case for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -49,8 +49,8 @@ class DPConfig(ctypes.Structure):
                 ("mix", ctypes.c_float)]
 
 
-# (name, restype, argtypes) of every exported entry point of include/specoptim.h and
-# include/dpsync.h
+# (name, restype, argtypes) of every exported entry point of include/specoptim.h,
+# include/mask_fused.h and include/dpsync.h
 _vp, _i32, _i64, _u32, _u64, _f32, _f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                            ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float,
                                            ctypes.c_double)
@@ -80,6 +80,10 @@ SIGNATURES = [
     ("mask_pack", _int, [_vp, _vp, _i64, _i32, _i32, _i32, _u32, _u64, _u64, _vp]),
     ("mask_unpack", _int, [_vp, _vp, _i64, _i32, _i32, _i32, _u32, _u64, _u64, _vp]),
     ("mask_indices", _int, [_vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
+    ("mask_pack_add", _int, [_vp, _vp, _vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
+    ("mask_unpack_rmsnorm", _int, [_vp, _vp, _f32, _vp, _vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
+    ("mask_rmsnorm_backward_pack", _int, [_vp, _vp, _f32, _vp, _vp, _vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
+    ("mask_unpack_add", _int, [_vp, _vp, _i64, _i32, _i32, _u32, _u64, _u64, _vp]),
     ("dpsync_rank", _i32, [_i32, _i32, _f32]),
     ("dpsync_config_default", _int, [ctypes.POINTER(DPConfig), _i32, _i32]),
     ("dpsync_create", _int, [ctypes.POINTER(_vp), ctypes.POINTER(DPConfig), _vp, _vp, _vp]),
@@ -336,3 +340,63 @@ def mask_indices(rows: int, H: int, K: int, layer: int, step: int, batch_id: int
     _check(lib().mask_indices(_ptr(out), rows, H, K, layer, step, batch_id, _stream(stream)),
            "mask_indices")
     return out
+
+
+# ---------------------------------------------------------------- mask fused with the layer boundary
+
+def _bf16(t, shape, name):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be bfloat16 of shape %s, got %s %s" % (name, shape, t.dtype, tuple(t.shape)))
+    return _ptr(t)
+
+
+def mask_pack_add(a, b, K: int, layer: int, step: int, batch_id: int = 0, out=None, stream=None):
+    """packed = pack(a + b) for bf16 CUDA tensors a, b [rows, H] (the sum is formed at the kept dims only)."""
+    torch = _torch()
+    rows, H = a.shape
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.bfloat16, device=a.device)
+    _check(lib().mask_pack_add(_bf16(a, (rows, H), "a"), _bf16(b, (rows, H), "b"), _bf16(out, (rows, K), "out"),
+                               rows, H, K, layer, step, batch_id, _stream(stream)), "mask_pack_add")
+    return out
+
+
+def mask_unpack_rmsnorm(packed, gamma, eps: float, H: int, layer: int, step: int, batch_id: int = 0,
+                        h_out=None, x_out=None, stream=None):
+    """(h~, x): h~ = unpack(packed), x = RMSNorm(h~) * gamma, bf16 [rows, H] each."""
+    torch = _torch()
+    rows, K = packed.shape
+    if h_out is None:
+        h_out = torch.empty((rows, H), dtype=torch.bfloat16, device=packed.device)
+    if x_out is None:
+        x_out = torch.empty((rows, H), dtype=torch.bfloat16, device=packed.device)
+    _check(lib().mask_unpack_rmsnorm(_bf16(packed, (rows, K), "packed"), _bf16(gamma, (H,), "gamma"), float(eps),
+                                     _bf16(h_out, (rows, H), "h_out"), _bf16(x_out, (rows, H), "x_out"), rows, H, K,
+                                     layer, step, batch_id, _stream(stream)), "mask_unpack_rmsnorm")
+    return h_out, x_out
+
+
+def mask_rmsnorm_backward_pack(packed_h, gamma, eps: float, dx, g_res, layer: int, step: int, batch_id: int = 0,
+                               out=None, stream=None):
+    """Packed dL/dh~ (bf16 [rows, K]) from the packed h~, gamma, dx [rows, H] and g_res [rows, H] or None."""
+    torch = _torch()
+    rows, K = packed_h.shape
+    H = gamma.shape[0]
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.bfloat16, device=packed_h.device)
+    _check(lib().mask_rmsnorm_backward_pack(_bf16(packed_h, (rows, K), "packed_h"), _bf16(gamma, (H,), "gamma"),
+                                            float(eps), _bf16(dx, (rows, H), "dx"),
+                                            None if g_res is None else _bf16(g_res, (rows, H), "g_res"),
+                                            _bf16(out, (rows, K), "out"), rows, H, K, layer, step, batch_id,
+                                            _stream(stream)), "mask_rmsnorm_backward_pack")
+    return out
+
+
+def mask_unpack_add(packed, g, layer: int, step: int, batch_id: int = 0, stream=None):
+    """g[r, pi_r(k)] += packed[r, k] in place (bf16), other entries unchanged."""
+    rows, K = packed.shape
+    H = g.shape[1]
+    _check(lib().mask_unpack_add(_bf16(packed, (rows, K), "packed"), _bf16(g, (rows, H), "g"), rows, H, K,
+                                 layer, step, batch_id, _stream(stream)), "mask_unpack_add")
+    return g

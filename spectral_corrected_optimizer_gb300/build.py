@@ -37,7 +37,8 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
-        os.path.join(INCLUDE, "specoptim.h"), os.path.join(INCLUDE, "dpsync.h")]
+        os.path.join(INCLUDE, "specoptim.h"), os.path.join(INCLUDE, "dpsync.h"),
+        os.path.join(INCLUDE, "mask_fused.h")]
 
 
 def needs_build() -> bool:

@@ -23,76 +23,10 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "mask_g.cuh"
 
 namespace spco {
 namespace {
-
-// ---- g: keyed permutation ---------------------------------------------------
-
-__host__ __device__ __forceinline__ uint64_t splitmix_out(uint64_t state) {
-    uint64_t z = state + 0x9e3779b97f4a7c15ULL;
-    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
-    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
-    return z ^ (z >> 31);
-}
-
-__device__ __forceinline__ uint32_t murmur_fmix(uint32_t x) {
-    x ^= x >> 16;
-    x *= 0x85ebca6bu;
-    x ^= x >> 13;
-    x *= 0xc2b2ae35u;
-    x ^= x >> 16;
-    return x;
-}
-
-struct RowKeys {
-    uint32_t k[4];
-};
-
-__device__ __forceinline__ RowKeys row_keys(uint64_t seed, uint64_t row) {
-    uint64_t rk = splitmix_out(seed ^ row);
-    RowKeys out;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out.k[i] = static_cast<uint32_t>(splitmix_out(rk + (uint64_t)i));
-    return out;
-}
-
-// permutation geometry for a given H
-struct PermShape {
-    uint32_t H;
-    int lo_bits;
-    uint32_t hi_mask, lo_mask;
-    uint32_t walk_limit;
-};
-
-__host__ __device__ inline PermShape perm_shape(uint32_t H) {
-    int w = 0;
-    while ((1ull << w) < (unsigned long long)H) ++w;
-    PermShape s;
-    s.H = H;
-    s.lo_bits = w - w / 2;
-    s.hi_mask = (1u << (w / 2)) - 1u;
-    s.lo_mask = (1u << s.lo_bits) - 1u;
-    s.walk_limit = 1u << w;
-    return s;
-}
-
-__device__ __forceinline__ uint32_t feistel4(const RowKeys &key, const PermShape &ps, uint32_t x) {
-    uint32_t lo = x & ps.lo_mask;
-    uint32_t hi = x >> ps.lo_bits;
-    hi ^= murmur_fmix(lo ^ key.k[0]) & ps.hi_mask;
-    lo ^= murmur_fmix(hi ^ key.k[1]) & ps.lo_mask;
-    hi ^= murmur_fmix(lo ^ key.k[2]) & ps.hi_mask;
-    lo ^= murmur_fmix(hi ^ key.k[3]) & ps.lo_mask;
-    return (hi << ps.lo_bits) | lo;
-}
-
-// pi_r(k): the k-th kept dim of the row (cycle walking bounded by the domain size)
-__device__ __forceinline__ uint32_t kept_dim(const RowKeys &key, const PermShape &ps, uint32_t k) {
-    uint32_t x = feistel4(key, ps, k);
-    for (uint32_t g = 0; x >= ps.H && g < ps.walk_limit; ++g) x = feistel4(key, ps, x);
-    return x;
-}
 
 // ---- pipelined bulk-copy kernels --------------------------------------------
 //
@@ -288,10 +222,6 @@ __global__ void indices_kernel(int32_t *__restrict__ idx, int64_t rows, int H, i
         for (int k = threadIdx.x; k < K; k += blockDim.x)
             idx[r * K + k] = (int32_t)kept_dim(key, ps, (uint32_t)k);
     }
-}
-
-uint64_t mask_seed(uint32_t layer, uint64_t step, uint64_t batch_id) {
-    return splitmix_out(splitmix_out(splitmix_out((uint64_t)layer) ^ step) ^ batch_id);
 }
 
 int check_args(int64_t rows, int32_t H, int32_t K, int32_t elem_bytes) {
