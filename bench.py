@@ -411,9 +411,9 @@ def mask_sweep(layer: Layer, p: float):
 
 
 def sector_coverage(H: int, K: int, elems: int = 16) -> float:
-    """Expected fraction of a row's 32-byte sectors (16 bf16) that hold at least one
-    of K kept dims drawn without replacement from H (what a gather at the kept dims
-    costs in DRAM traffic)."""
+    """Expected fraction of a row's `elems`-element blocks (16 bf16 = one 32-byte
+    sector, 64 bf16 = one 128-byte line) that hold at least one of K kept dims drawn
+    without replacement from H."""
     miss = 1.0
     for i in range(elems):
         miss *= max(0.0, (H - K - i) / (H - i))
@@ -439,7 +439,10 @@ def mask_fused_bench(peaks: dict, peak_src: str, p: float = 0.95, reps: int = 20
     h_out, x_out = torch.empty_like(a), torch.empty_like(a)
     pg = torch.empty_like(packed)
     gg = b.clone()
-    cov = sector_coverage(H, K)
+    # reads at the kept dims come from DRAM in whole 128-byte lines (ncu: the gathers'
+    # DRAM reads equal the line coverage), writes of single elements in 32-byte sectors
+    cov = sector_coverage(H, K, 64)
+    wcov = sector_coverage(H, K, 16)
     dense, pk = rows * H * 2.0, rows * K * 2.0
 
     def t_ms(fn):
@@ -462,10 +465,10 @@ def mask_fused_bench(peaks: dict, peak_src: str, p: float = 0.95, reps: int = 20
                                                                 (H,), gamma, 1e-5)),
         "rmsnorm_backward_pack": (lambda: so.mask_rmsnorm_backward_pack(packed, gamma, 1e-5, a, b, 1, 0, out=pg),
                                   2 * cov * dense + 2 * pk, None),
-        "unpack_add": (lambda: so.mask_unpack_add(packed, gg, 1, 0), pk + 2 * cov * dense,
+        "unpack_add": (lambda: so.mask_unpack_add(packed, gg, 1, 0), pk + (cov + wcov) * dense,
                        lambda: gg.add_(so.mask_unpack(packed, H, 1, 0, 0, out=h_out))),
     }
-    out = {"rows": rows, "H": H, "p": p, "K": K, "sector_coverage": cov, "ops": {}}
+    out = {"rows": rows, "H": H, "p": p, "K": K, "line_coverage": cov, "sector_coverage": wcov, "ops": {}}
     for name, (fn, byts, unfused) in ops.items():
         ms = t_ms(fn)
         ach = byts / (ms * 1e-3) / 1e9

@@ -41,6 +41,11 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Gathers at the kept dims take them in batches of kBatch per lane: all the
+// batch's indices are hashed first, then all its loads are issued, so each lane
+// keeps kBatch independent loads in flight per tensor.
+constexpr int kBatch = 8;
+
 __global__ void __launch_bounds__(kThreadsF) pack_add_kernel(const uint16_t *__restrict__ a, const uint16_t *__restrict__ b,
                                                            uint16_t *__restrict__ packed, int64_t rows, int H,
                                                            int K, uint64_t seed) {
@@ -49,9 +54,25 @@ __global__ void __launch_bounds__(kThreadsF) pack_add_kernel(const uint16_t *__r
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * kWarps) {
         const RowKeys key = row_keys(seed, (uint64_t)r);
         const uint16_t *ar = a + r * H, *br = b + r * H;
-        for (int k = lane; k < K; k += 32) {
-            const uint32_t j = kept_dim(key, ps, (uint32_t)k);
-            packed[r * K + k] = bf16_rne(bf16_val(__ldg(ar + j)) + bf16_val(__ldg(br + j)));
+        for (int k0 = 0; k0 < K; k0 += 32 * kBatch) {
+            uint32_t j[kBatch];
+            uint16_t va[kBatch], vb[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const bool in = k0 + 32 * u + lane < K;
+                va[u] = in ? __ldg(ar + j[u]) : (uint16_t)0;
+                vb[u] = in ? __ldg(br + j[u]) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                if (k < K) packed[r * K + k] = bf16_rne(bf16_val(va[u]) + bf16_val(vb[u]));
+            }
         }
     }
 }
@@ -118,23 +139,96 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * kWarps) {
         const RowKeys key = row_keys(seed, (uint64_t)r);
         const uint16_t *pr = packed_h + r * K, *dr = dx + r * H;
+        const uint16_t *gr = g_res ? g_res + r * H : nullptr;
+        if (K <= 32 * kBatch) {
+            // one batch: the kept dims' operands stay in registers between the two passes
+            uint32_t j[kBatch];
+            float hv[kBatch], gd[kBatch], rv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = 32 * u + lane;
+                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+            }
+            float ss = 0.f, s = 0.f;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = 32 * u + lane;
+                const bool in = k < K;
+                hv[u] = in ? bf16_val(__ldg(pr + k)) : 0.f;
+                gd[u] = in ? bf16_val(__ldg(gamma + j[u])) * bf16_val(__ldg(dr + j[u])) : 0.f;
+                rv[u] = (in && gr) ? bf16_val(__ldg(gr + j[u])) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                ss = fmaf(hv[u], hv[u], ss);
+                s = fmaf(gd[u], hv[u], s);
+            }
+            ss = warp_sum(ss);
+            s = warp_sum(s);
+            const float rr = sqrtf(fmaf(ss, inv_h, eps)), rinv = 1.f / rr;
+            const float c = s * inv_h * rinv * rinv * rinv;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = 32 * u + lane;
+                if (k < K) out[r * K + k] = bf16_rne(gd[u] * rinv - hv[u] * c + rv[u]);
+            }
+            continue;
+        }
+        // pass 1: mean of squares of h~ and sum_i gamma_i dx_i h~_i over the kept dims
         float ss = 0.f, s = 0.f;
-        for (int k = lane; k < K; k += 32) {
-            const uint32_t j = kept_dim(key, ps, (uint32_t)k);
-            const float hv = bf16_val(__ldg(pr + k));
-            ss = fmaf(hv, hv, ss);
-            s = fmaf(bf16_val(__ldg(gamma + j)) * bf16_val(__ldg(dr + j)), hv, s);
+        for (int k0 = 0; k0 < K; k0 += 32 * kBatch) {
+            uint32_t j[kBatch];
+            uint16_t hv[kBatch], gv[kBatch], dv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                const bool in = k < K;
+                hv[u] = in ? __ldg(pr + k) : (uint16_t)0;
+                gv[u] = in ? __ldg(gamma + j[u]) : (uint16_t)0;
+                dv[u] = in ? __ldg(dr + j[u]) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float h = bf16_val(hv[u]);
+                ss = fmaf(h, h, ss);
+                s = fmaf(bf16_val(gv[u]) * bf16_val(dv[u]), h, s);
+            }
         }
         ss = warp_sum(ss);
         s = warp_sum(s);
         const float rr = sqrtf(fmaf(ss, inv_h, eps)), rinv = 1.f / rr;
         const float c = s * inv_h * rinv * rinv * rinv;
-        for (int k = lane; k < K; k += 32) {
-            const uint32_t j = kept_dim(key, ps, (uint32_t)k);
-            const float hv = bf16_val(__ldg(pr + k));
-            float v = bf16_val(__ldg(gamma + j)) * bf16_val(__ldg(dr + j)) * rinv - hv * c;
-            if (g_res) v += bf16_val(__ldg(g_res + r * H + j));
-            out[r * K + k] = bf16_rne(v);
+        // pass 2: the kept dims' gradient (the operands come back from L1 / L2)
+        for (int k0 = 0; k0 < K; k0 += 32 * kBatch) {
+            uint32_t j[kBatch];
+            uint16_t hv[kBatch], gv[kBatch], dv[kBatch], rv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                const bool in = k < K;
+                hv[u] = in ? __ldg(pr + k) : (uint16_t)0;
+                gv[u] = in ? __ldg(gamma + j[u]) : (uint16_t)0;
+                dv[u] = in ? __ldg(dr + j[u]) : (uint16_t)0;
+                rv[u] = (in && gr) ? __ldg(gr + j[u]) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                if (k < K) {
+                    const float v = bf16_val(gv[u]) * bf16_val(dv[u]) * rinv - bf16_val(hv[u]) * c + bf16_val(rv[u]);
+                    out[r * K + k] = bf16_rne(v);
+                }
+            }
         }
     }
 }
@@ -146,9 +240,27 @@ __global__ void __launch_bounds__(kThreadsF) unpack_add_kernel(const uint16_t *_
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * kWarps) {
         const RowKeys key = row_keys(seed, (uint64_t)r);
         uint16_t *gr = g + r * H;
-        for (int k = lane; k < K; k += 32) {
-            const uint32_t j = kept_dim(key, ps, (uint32_t)k);
-            gr[j] = bf16_rne(bf16_val(gr[j]) + bf16_val(__ldg(packed + r * K + k)));
+        const uint16_t *pr = packed + r * K;
+        for (int k0 = 0; k0 < K; k0 += 32 * kBatch) {
+            uint32_t j[kBatch];
+            uint16_t gv[kBatch], pv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                const bool in = k < K;
+                gv[u] = in ? gr[j[u]] : (uint16_t)0;
+                pv[u] = in ? __ldg(pr + k) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + 32 * u + lane;
+                if (k < K) gr[j[u]] = bf16_rne(bf16_val(gv[u]) + bf16_val(pv[u]));
+            }
         }
     }
 }
