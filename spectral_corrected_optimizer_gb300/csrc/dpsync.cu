@@ -59,8 +59,6 @@ constexpr int kPMaxStages = 6;
 constexpr int kGramRows = 128;   // rows per Gram task
 constexpr int kQRows = 512;      // rows per compress_q task
 constexpr int kQCols = 128;      // columns per compress_q task
-constexpr int kQChunk = 16;      // rows per compress_q stage
-constexpr int kQStages = 4;
 constexpr int kURows = 256;      // rows per dp_update task
 constexpr int kUTile = 32;       // rows per dp_update tile (8 warps x 4 rows)
 constexpr int kUCols = 128;      // columns per dp_update task
@@ -153,6 +151,14 @@ __device__ __forceinline__ void df_acc(float &hi, float &lo, float a, float b) {
     const df s = two_sum(hi, p);
     hi = s.hi;
     lo = __fadd_rn(lo, __fadd_rn(s.lo, pe));
+}
+
+// tf32 hi (round to nearest, ties away) and lo = tf32(x - hi) of four floats
+__device__ __forceinline__ float tf32_rna(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
+__device__ __forceinline__ float4 split_hi4(float4 v, float4 &lo) {
+    const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    lo = make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+    return h;
 }
 
 // ---------------------------------------------------------------------------
@@ -639,12 +645,49 @@ __global__ void __launch_bounds__(kThreads) dp_orth_apply_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// compress_q:  partial Q = M^T P^ over one row range.  Task (column block of
-// 128, row range of 512); the ring holds stages of one TMA box of M (128
-// columns x 16 rows) and the matching box of P^ (kp x 16), zero outside the
-// matrices.  Thread tile: 8 columns x 8 ranks; row groups split each stage's
-// rows and are summed in a halving tree at the end of the task.
+// compress_q on the tcgen05 tensor cores:  partial Q = M^T P^ over one row
+// range, 3xTF32 (hi.hi + hi.lo + lo.hi, fp32-accurate).
+// Task (column block of 128, row range of 512) accumulates
+//   D (128 x NP, TMEM) += A (128 x 32) . B (NP x 32)^T   per chunk of 32 rows,
+// A[j][i] = M[r0 + i][col0 + j], B[c][i] = P^[r0 + i][c] (NP = kp, at least 16).
+// The raw chunk arrives by TMA (boxes of 128 x 32 of M and kp x 32 of P^,
+// zero outside the matrices) into a ring of kQtRaw stages; four split warps
+// transpose it into the K-major, 128-byte-swizzled operand tiles, split into
+// tf32 hi and lo, in a ring of kQtOps stages (the raw ring runs further ahead
+// than the operands, which only wait for the MMAs).  Warp roles:
+//   warp 0      TMA producer
+//   warp 1      TMEM (two accumulators) and the MMA issuer (12 MMAs per chunk)
+//   warps 2-9   transpose + split
+//   warps 10-13 epilogue: the task's accumulator to its partial in Qpart
+// Every mbarrier wait is bounded; a wait that gives up records a code in the
+// library's device flag and that role stops.
 // ---------------------------------------------------------------------------
+constexpr int kQtK = 32;                       // rows of M per chunk (the MMA K of one atom)
+constexpr int kQtMaxRaw = 8, kQtOps = 2;
+constexpr int kQtThreads = 448;
+constexpr int kQtSplitThreads = 256;  // warps 2-9
+constexpr uint32_t kQtRawM = kQtK * kQCols * 4;       // 16 KB
+constexpr uint32_t kQtA = kQCols * 128;               // 16 KB: 128 rows of 128 bytes
+constexpr size_t kQtSmem = 232448 - 1024;             // all of shared memory but the static part
+// ring layout for the largest padded rank of a launch: raw stages (M box, P^ box),
+// then two operand stages (A hi, A lo, B hi, B lo); as many raw stages as fit
+struct QtLayout {
+    uint32_t raw_stage, op_stage, b_bytes, op_base;
+    int raw;
+};
+__host__ __device__ inline QtLayout qt_layout(int kpmax) {
+    QtLayout L;
+    const int np = kpmax < 16 ? 16 : kpmax;
+    L.raw_stage = (kQtRawM + (uint32_t)kQtK * kpmax * 4 + 1023) & ~1023u;
+    L.b_bytes = (uint32_t)np * 128;
+    L.op_stage = (2 * kQtA + 2 * L.b_bytes + 1023) & ~1023u;
+    L.raw = (int)((kQtSmem - 1024 - 256 - kQtOps * (size_t)L.op_stage) / L.raw_stage);
+    if (L.raw > kQtMaxRaw) L.raw = kQtMaxRaw;
+    L.op_base = (uint32_t)L.raw * L.raw_stage;
+    return L;
+}
+constexpr uint32_t kQtTmemCols = 128;                 // two accumulators of up to 64 columns
+
 struct QJob {
     const CUtensorMap *mm, *mp;
     float *Qpart;
@@ -652,8 +695,7 @@ struct QJob {
 };
 struct QBatch {
     QJob job[kMaxJobs];
-    int count, total_tasks, stages;
-    uint32_t stage_bytes;
+    int count, total_tasks, kpmax;
     unsigned *flag;
 };
 
@@ -663,7 +705,7 @@ struct QCursor {
 __device__ __forceinline__ int q_nch(const QJob &J, int task) {
     const int range = (task - J.task_begin) / J.ncb;
     const int rows = min(kQRows, J.m - range * kQRows);
-    return (rows + kQChunk - 1) / kQChunk;
+    return (rows + kQtK - 1) / kQtK;
 }
 __device__ __forceinline__ void q_first(QCursor &c, const QBatch &B, const int *begins) {
     c.task = blockIdx.x < (unsigned)B.total_tasks ? (int)blockIdx.x : -1;
@@ -671,134 +713,192 @@ __device__ __forceinline__ void q_first(QCursor &c, const QBatch &B, const int *
     c.job = c.task >= 0 ? find_job(begins, B.count, c.task) : 0;
     c.nch = c.task >= 0 ? q_nch(B.job[c.job], c.task) : 0;
 }
-__device__ __forceinline__ void q_advance(QCursor &c, const QBatch &B, const int *begins) {
-    if (c.task < 0) return;
-    if (++c.chunk < c.nch) return;
+__device__ __forceinline__ bool q_advance(QCursor &c, const QBatch &B, const int *begins) {  // true: new task
+    if (c.task < 0) return false;
+    if (++c.chunk < c.nch) return false;
     c.chunk = 0;
     c.task += gridDim.x;
     if (c.task >= B.total_tasks) {
         c.task = -1;
-        return;
+        return true;
     }
     c.job = find_job(begins, B.count, c.task);
     c.nch = q_nch(B.job[c.job], c.task);
-}
-__device__ __forceinline__ void q_issue(const QBatch &B, const QCursor &c, unsigned char *stage, uint64_t *bar) {
-    const QJob &J = B.job[c.job];
-    const int t = c.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
-    const int r0 = range * kQRows + c.chunk * kQChunk;
-    float *ms = reinterpret_cast<float *>(stage), *ps = ms + kQChunk * kQCols;
-    mbar_arrive_expect_tx(bar, (uint32_t)kQChunk * (kQCols + J.kp) * 4u);
-    tma_load_2d(ms, J.mm, cb * kQCols, r0, bar);
-    tma_load_2d(ps, J.mp, 0, r0, bar);
+    return true;
 }
 
-// acc[8 columns][8 ranks] += M_stage^T P^_stage for padded rank KP: tiles of
-// 8 columns x 8 ranks, 256 / (2 KP) row groups each taking every RGN-th row
-template <int KP>
-__device__ __forceinline__ void q_fma(const float *ms, float (&acc)[64], int tid) {
-    constexpr int TILES = 2 * KP, RGN = kThreads / TILES;
-    const float *ps = ms + kQChunk * kQCols;
-    const int tile = tid % TILES, rg = tid / TILES, ct = tile % 16, kt = tile / 16;
-#pragma unroll
-    for (int i0 = 0; i0 < kQChunk; i0 += RGN) {
-        const int i = i0 + rg;
-        const float4 a0 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 4 * ct);
-        const float4 a1 = *reinterpret_cast<const float4 *>(ms + i * kQCols + 64 + 4 * ct);
-        const float4 b0 = *reinterpret_cast<const float4 *>(ps + i * KP + kt * 8);
-        const float4 b1 = *reinterpret_cast<const float4 *>(ps + i * KP + kt * 8 + 4);
-        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[x * 8 + q] = fmaf(a[x], b[q], acc[x * 8 + q]);
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 2) dp_compress_q_kernel(const __grid_constant__ QBatch B) {
-    extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kQtThreads, 1) dp_compress_q_kernel(const __grid_constant__ QBatch B) {
+    extern __shared__ __align__(1024) unsigned char qt_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(qt_raw) + 1023) & ~uintptr_t(1023));
+    const QtLayout L = qt_layout(B.kpmax);
+    const int kQtRaw = L.raw;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.op_base + kQtOps * L.op_stage);
+    uint64_t *full = bars;                   // [kQtMaxRaw] raw chunk landed
+    uint64_t *rfree = full + kQtMaxRaw;      // [kQtMaxRaw] raw chunk consumed
+    uint64_t *ready = rfree + kQtRaw;        // [kQtOps] operands written (128 arrivals)
+    uint64_t *ofree = ready + kQtOps;        // [kQtOps] MMAs done with the operands
+    uint64_t *tfull = ofree + kQtOps;        // [2] accumulator complete
+    uint64_t *tempty = tfull + 2;            // [2] accumulator read (128 arrivals)
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
     __shared__ int begins[kMaxJobs];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 128);  // 128 x 64 floats
-    unsigned char *ring = smem + 128 + 128 * 64 * sizeof(float);
-    const int tid = threadIdx.x;
-    if (tid < B.count) begins[tid] = B.job[tid].task_begin;
-    if (tid == 0) {
-        for (int s = 0; s < B.stages; ++s) mbar_init(&bar[s], 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x < B.count) begins[threadIdx.x] = B.job[threadIdx.x].task_begin;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQtRaw; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&rfree[s], kQtSplitThreads);
+        }
+        for (int o = 0; o < kQtOps; ++o) {
+            mbar_init(&ready[o], kQtSplitThreads);
+            mbar_init(&ofree[o], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
         fence_mbar_init();
-        for (int j = 0; j < B.count; ++j) {
-            prefetch_tmap(B.job[j].mm);
-            prefetch_tmap(B.job[j].mp);
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, kQtTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    unsigned *flag = B.flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            for (int j = 0; j < B.count; ++j) {
+                prefetch_tmap(B.job[j].mm);
+                prefetch_tmap(B.job[j].mp);
+            }
+            QCursor c;
+            q_first(c, B, begins);
+            int i = 0;
+            for (; c.task >= 0; ++i, q_advance(c, B, begins)) {
+                const int s = i % kQtRaw;
+                if (!mbar_wait_bounded(&rfree[s], ((uint32_t)(i / kQtRaw) & 1u) ^ 1u, flag, 0x301u)) break;
+                const QJob &J = B.job[c.job];
+                const int t = c.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
+                const int r0 = range * kQRows + c.chunk * kQtK;
+                unsigned char *st = smem + s * L.raw_stage;
+                mbar_arrive_expect_tx(&full[s], kQtRawM + (uint32_t)kQtK * J.kp * 4u);
+                tma_load_2d(st, J.mm, cb * kQCols, r0, &full[s]);
+                tma_load_2d(st + kQtRawM, J.mp, 0, r0, &full[s]);
+            }
+            if (c.task >= 0)  // gave up: let the loads already issued land before the CTA exits
+                for (int q = (i > kQtRaw ? i - kQtRaw : 0); q < i; ++q)
+                    mbar_wait_bounded(&full[q % kQtRaw], (uint32_t)(q / kQtRaw) & 1u, flag, 0x305u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            QCursor c;
+            q_first(c, B, begins);
+            int i = 0, task_i = 0;
+            bool ok = true;
+            for (; c.task >= 0; ++i) {
+                const int o = i % kQtOps, a = task_i & 1;
+                const QJob &J = B.job[c.job];
+                const int np = J.kp < 16 ? 16 : J.kp;
+                if (!(ok = mbar_wait_bounded(&ready[o], (uint32_t)(i / kQtOps) & 1u, flag, 0x302u))) break;
+                if (c.chunk == 0 && !(ok = mbar_wait_bounded(&tempty[a], ((uint32_t)(task_i >> 1) & 1u) ^ 1u, flag, 0x303u)))
+                    break;
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + L.op_base + o * L.op_stage);
+                const uint32_t ah = st, al = st + kQtA, bh = st + 2 * kQtA, bl = bh + L.b_bytes;
+                const uint32_t as[3] = {ah, ah, al}, bs[3] = {bh, bl, bh};
+                const uint32_t d = tmem + (uint32_t)(a * 64);
+                const uint32_t idesc = tf32_idesc(128, np);
+#pragma unroll
+                for (int u = 0; u < 3; ++u)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        mma_tf32(d, smem_desc_sw128(as[u] + q * 32), smem_desc_sw128(bs[u] + q * 32), idesc,
+                                 (c.chunk > 0 || u > 0 || q > 0) ? 1u : 0u);
+                mma_commit(&ofree[o]);
+                const bool last = c.chunk == c.nch - 1;
+                if (last) mma_commit(&tfull[a]);
+                if (q_advance(c, B, begins)) ++task_i;
+            }
+            if (!ok && i > 0)  // gave up: the MMAs issued finish before TMEM is freed
+                mbar_wait_bounded(&ofree[(i - 1) % kQtOps], (uint32_t)((i - 1) / kQtOps) & 1u, flag, 0x306u);
+        }
+    } else if (warp < 10) {
+        // ---------------- transpose + split: raw M (32 x 128) -> A[j][i], raw P^ (32 x kp) -> B[c][i]
+        const int tid = threadIdx.x - 64;
+        QCursor c;
+        q_first(c, B, begins);
+        for (int i = 0; c.task >= 0; ++i, q_advance(c, B, begins)) {
+            const int s = i % kQtRaw, o = i % kQtOps;
+            if (!mbar_wait_bounded(&full[s], (uint32_t)(i / kQtRaw) & 1u, flag, 0x304u)) break;
+            if (!mbar_wait_bounded(&ofree[o], ((uint32_t)(i / kQtOps) & 1u) ^ 1u, flag, 0x308u)) break;
+            const unsigned char *rs = smem + s * L.raw_stage;
+            unsigned char *st = smem + L.op_base + o * L.op_stage;
+            const float *rm = reinterpret_cast<const float *>(rs), *rp = reinterpret_cast<const float *>(rs + kQtRawM);
+            const int kp = B.job[c.job].kp;
+#pragma unroll 4
+            for (int e = tid; e < kQCols * 8; e += kQtSplitThreads) {  // (row j of A, 16-byte chunk cc: i = 4 cc .. 4 cc + 3)
+                const int j = e % kQCols, cc = e / kQCols;
+                float4 lo;
+                const float4 hi = split_hi4(make_float4(rm[(4 * cc) * kQCols + j], rm[(4 * cc + 1) * kQCols + j],
+                                                        rm[(4 * cc + 2) * kQCols + j], rm[(4 * cc + 3) * kQCols + j]), lo);
+                const uint32_t off = (uint32_t)j * 128 + ((uint32_t)(cc ^ (j & 7)) << 4);
+                *reinterpret_cast<float4 *>(st + off) = hi;
+                *reinterpret_cast<float4 *>(st + kQtA + off) = lo;
+            }
+            for (int e = tid; e < kp * 8; e += kQtSplitThreads) {  // (row r of B, chunk cc)
+                const int r = e % kp, cc = e / kp;
+                float4 lo;
+                const float4 hi = split_hi4(make_float4(rp[(4 * cc) * kp + r], rp[(4 * cc + 1) * kp + r],
+                                                        rp[(4 * cc + 2) * kp + r], rp[(4 * cc + 3) * kp + r]), lo);
+                const uint32_t off = (uint32_t)r * 128 + ((uint32_t)(cc ^ (r & 7)) << 4);
+                *reinterpret_cast<float4 *>(st + 2 * kQtA + off) = hi;
+                *reinterpret_cast<float4 *>(st + 2 * kQtA + L.b_bytes + off) = lo;
+            }
+            fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+            mbar_arrive(&rfree[s]);
+            mbar_arrive(&ready[o]);
+        }
+    } else {
+        // ---------------- epilogue: TMEM lane quarter q = columns 32q .. 32q+31 of the block
+        const int q = warp % 4;
+        QCursor c;
+        q_first(c, B, begins);
+        for (int task_i = 0; c.task >= 0; ++task_i) {
+            const int a = task_i & 1;
+            const QJob &J = B.job[c.job];
+            const int t = c.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
+            if (!mbar_wait_bounded(&tfull[a], (uint32_t)(task_i >> 1) & 1u, flag, 0x307u)) break;
+            tc_fence_after();
+            float v0[32], v1[32];
+            const uint32_t taddr = tmem + (uint32_t)(a * 64) + ((uint32_t)(q * 32) << 16);
+            tmem_ld32(taddr, v0);
+            if (J.kp > 32) tmem_ld32(taddr + 32, v1);
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+            const int ldp = J.ncb * kQCols, col = cb * kQCols + q * 32 + lane;
+            float4 *dst = reinterpret_cast<float4 *>(J.Qpart + ((size_t)range * ldp + col) * J.kp);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                if (4 * x < J.kp) dst[x] = make_float4(v0[4 * x], v0[4 * x + 1], v0[4 * x + 2], v0[4 * x + 3]);
+            if (J.kp > 32) {
+#pragma unroll
+                for (int x = 0; x < 8; ++x) dst[8 + x] = make_float4(v1[4 * x], v1[4 * x + 1], v1[4 * x + 2], v1[4 * x + 3]);
+            }
+            // next task (the cursor walks chunk by chunk)
+            do {
+            } while (!q_advance(c, B, begins));
         }
     }
+    tc_fence_before();
     __syncthreads();
-    QCursor cur, pc;
-    q_first(cur, B, begins);
-    pc = cur;
-    if (tid == 0)
-        for (int s = 0; s < B.stages && pc.task >= 0; ++s) {
-            q_issue(B, pc, ring + (size_t)s * B.stage_bytes, &bar[s]);
-            q_advance(pc, B, begins);
-        }
-    float acc[64];  // [8 columns][8 ranks]
-#pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-    bool ok = true;
-    for (int it = 0; cur.task >= 0; ++it) {
-        const int s = it % B.stages;
-        const QJob &J = B.job[cur.job];
-        const int kp = J.kp, tiles = 2 * kp, rgn = kThreads / tiles;
-        const int tile = tid % tiles, rg = tid / tiles, ct = tile % 16, kt = tile / 16;
-        const int t = cur.task - J.task_begin, cb = t % J.ncb, range = t / J.ncb;
-        if (ok) ok = mbar_wait_bounded(&bar[s], (uint32_t)(it / B.stages) & 1u, B.flag, 4u);
-        if (ok) {
-            const float *ms = reinterpret_cast<const float *>(ring + (size_t)s * B.stage_bytes);
-            switch (kp) {
-                case 8: q_fma<8>(ms, acc, tid); break;
-                case 16: q_fma<16>(ms, acc, tid); break;
-                case 32: q_fma<32>(ms, acc, tid); break;
-                default: q_fma<64>(ms, acc, tid); break;
-            }
-        }
-        ok = __syncthreads_and(ok) != 0;  // this stage is consumed
-        if (!ok) break;
-        if (tid == 0 && pc.task >= 0) {
-            q_issue(B, pc, ring + (size_t)s * B.stage_bytes, &bar[s]);
-            q_advance(pc, B, begins);
-        }
-        if (cur.chunk == cur.nch - 1) {
-            // task done: halving tree over the row groups, then the partial to Qpart
-            for (int half = rgn / 2; half >= 1; half /= 2) {
-                const int nt = half * tiles;
-                if (rg >= half && rg < 2 * half) {
-                    const int idx = (rg - half) * tiles + tile;
-#pragma unroll
-                    for (int v = 0; v < 64; ++v) red[v * nt + idx] = acc[v];
-                }
-                __syncthreads();
-                if (rg < half) {
-                    const int idx = rg * tiles + tile;
-#pragma unroll
-                    for (int v = 0; v < 64; ++v) acc[v] += red[v * nt + idx];
-                }
-                __syncthreads();
-            }
-            if (rg == 0) {
-                const int ldp = J.ncb * kQCols;
-                float *dst = J.Qpart + ((size_t)range * ldp + cb * kQCols) * kp + kt * 8;
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const int col = x < 4 ? 4 * ct + x : 64 + 4 * ct + (x - 4);
-                    float4 *d = reinterpret_cast<float4 *>(dst + (size_t)col * kp);
-                    d[0] = make_float4(acc[x * 8 + 0], acc[x * 8 + 1], acc[x * 8 + 2], acc[x * 8 + 3]);
-                    d[1] = make_float4(acc[x * 8 + 4], acc[x * 8 + 5], acc[x * 8 + 6], acc[x * 8 + 7]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-        }
-        q_advance(cur, B, begins);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kQtTmemCols);
     }
 }
 
@@ -1078,8 +1178,8 @@ extern "C" int dpsync_create(dpsync_t **out, const dpsync_config *cfg, float *P,
     const uint32_t R = (uint32_t)p_rows(h->kp);
     int rc = make_tmap_2d_ex(&hm[0], h->E, h->m, h->n, h->n, kPBC, R, false);
     if (!rc) rc = make_tmap_2d_ex(&hm[1], h->Qp, h->n, h->kp + 4, h->kp + 4, h->kp + 4, kPBC, false);
-    if (!rc) rc = make_tmap_2d_ex(&hm[2], h->E, h->m, h->n, h->n, kQCols, kQChunk, false);
-    if (!rc) rc = make_tmap_2d_ex(&hm[3], h->Ph, h->m, h->kp, h->kp, h->kp, kQChunk, false);
+    if (!rc) rc = make_tmap_2d_ex(&hm[2], h->E, h->m, h->n, h->n, kQCols, kQtK, false);
+    if (!rc) rc = make_tmap_2d_ex(&hm[3], h->Ph, h->m, h->kp, h->kp, h->kp, kQtK, false);
     if (!rc) rc = cuda_status(cudaMemcpyAsync(h->maps + 2, hm, sizeof(hm), cudaMemcpyHostToDevice, st),
                               "dpsync_create: tensor maps");
     if (!rc) rc = cuda_status(cudaStreamSynchronize(st), "dpsync_create");
@@ -1291,15 +1391,11 @@ extern "C" int dpsync_compress_q_many(dpsync_t *const *hs, int32_t count, void *
     }
     b.total_tasks = tasks;
     r.total = rtotal;
-    b.stage_bytes = (uint32_t)align128(sizeof(float) * ((size_t)kQChunk * kQCols + (size_t)kQChunk * kpmax));
-    b.stages = kQStages;
     b.flag = device_flag_ptr();
-    const size_t smem = 128 + 128 * 64 * sizeof(float) + (size_t)b.stages * b.stage_bytes;
-    if ((rc = set_smem((const void *)dp_compress_q_kernel, smem))) return rc;
-    int per_sm = 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dp_compress_q_kernel, kThreads, smem);
-    const int grid = std::min(tasks, std::max(1, per_sm) * num_sms());
-    SPCO_LAUNCH("dp_compress_q", st, dp_compress_q_kernel<<<grid, kThreads, smem, st>>>(b));
+    b.kpmax = kpmax;
+    if ((rc = set_smem((const void *)dp_compress_q_kernel, kQtSmem))) return rc;
+    const int grid = std::min(tasks, num_sms());
+    SPCO_LAUNCH("dp_compress_q", st, dp_compress_q_kernel<<<grid, kQtThreads, kQtSmem, st>>>(b));
     SPECOPTIM_LAUNCHED("dp_compress_q_kernel");
     const int rgrid = (int)std::min<int64_t>((rtotal + kThreads - 1) / kThreads, 4 * num_sms());
     SPCO_LAUNCH("dp_q_reduce", st, dp_q_reduce_kernel<<<rgrid, kThreads, 0, st>>>(r));
