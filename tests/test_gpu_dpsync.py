@@ -199,3 +199,57 @@ def test_host_argument_checks():
         dp().DPSyncGroup([(64, 130)], ranks=[4])                  # n not a multiple of 4
     with pytest.raises(Exception):
         dp().DPSyncGroup([(640, 1280)], ranks=[65])               # rank above 64
+
+
+def test_full_layer_sync_sampled():
+    """The bench's workload: one outer sync of the 7 matrices of a Llama-3.2-1B
+    layer (64x rank rule) in one batch, each call checked on sampled rows and
+    columns that the oracle computes one by one."""
+    shapes = list(synthetic.LLAMA_1B_LAYER.values())
+    ranks = [oracle.dpsync_rank(m, n) for m, n in shapes]
+    Q0 = [synthetic.dp_q0(n, k, seed=2, index=i) for i, ((m, n), k) in enumerate(zip(shapes, ranks))]
+    g = dp().DPSyncGroup(shapes, Q0=[torch.from_numpy(q) for q in Q0])
+    assert g.ranks == ranks
+    theta = [synthetic.normal_f32(3, 1, i, (m, n), 0.02) for i, (m, n) in enumerate(shapes)]
+    W = [theta[i] - synthetic.dp_drift(m, n, seed=3, period=i) for i, (m, n) in enumerate(shapes)]
+    g.set_outer([dev(t) for t in theta])
+    Wd = [dev(w) for w in W]
+    g.compress_p(None, Wd)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    Ms, Ps = [], []
+    for i, ((m, n), k) in enumerate(zip(shapes, ranks)):
+        M = state(g, i)[0]
+        rows = rng.choice(m, 16, replace=False)
+        M_ref = theta[i][rows].astype(np.float64) - W[i][rows]
+        assert rel(M[rows], M_ref) < 1e-6
+        assert rel(host(g.P[i])[rows], M_ref @ Q0[i].astype(np.float64)) < TOL
+        Ms.append(M)
+        Ps.append(host(g.P[i]).astype(np.float64))
+    g.orthogonalize()
+    Phs = []
+    for i, ((m, n), k) in enumerate(zip(shapes, ranks)):
+        Ph = state(g, i)[3].astype(np.float64)
+        assert np.abs(Ph.T @ Ph - np.eye(k)).max() < 1e-5
+        assert rel(Ph, oracle.orthogonalize(Ps[i])) < TOL
+        Phs.append(Ph)
+    g.compress_q()
+    torch.cuda.synchronize()
+    Qs = []
+    for i, ((m, n), k) in enumerate(zip(shapes, ranks)):
+        cols = rng.choice(n, 16, replace=False)
+        Q = host(g.Q[i]).astype(np.float64)
+        assert rel(Q[cols], Ms[i][:, cols].astype(np.float64).T @ Phs[i]) < TOL
+        Qs.append(Q)
+    g.outer_step(Wd, 1.0)
+    torch.cuda.synchronize()
+    for i, ((m, n), k) in enumerate(zip(shapes, ranks)):
+        E, th, mo, _ = state(g, i)
+        rows = rng.choice(m, 8, replace=False)
+        D = Phs[i][rows] @ Qs[i].T
+        assert rel(E[rows], Ms[i][rows] - D) < TOL
+        th_ref, mo_ref, W_ref = oracle.outer_nesterov(theta[i][rows], np.zeros((8, n)), D, 0.7, 0.9)
+        assert rel(mo[rows], mo_ref) < TOL
+        assert rel(th[rows] - theta[i][rows], th_ref - theta[i][rows]) < TOL
+        assert np.array_equal(host(Wd[i])[rows], th[rows])
+    g.close()
