@@ -129,19 +129,14 @@ __device__ __forceinline__ df df_mul(df x, df y) {
     e = __fmaf_rn(x.lo, y.hi, e);
     return quick_two_sum(p, e);
 }
-// 1 / x: fp32 estimate and one Newton step in two floats (x > 0)
-__device__ __forceinline__ df df_recip(df x) {
-    const float r = __frcp_rn(x.hi);
-    const df xr = df_mul(x, df{r, 0.f});                     // x r ~ 1
-    const df one_minus = df_add(df{1.f, 0.f}, df_neg(xr));  // 1 - x r
-    return df_add(df{r, 0.f}, df_mul(df{r, 0.f}, one_minus));
-}
-// sqrt(x): fp32 estimate and one Newton step in two floats (x > 0)
-__device__ __forceinline__ df df_sqrt(df x) {
-    const float r = __fsqrt_rn(x.hi);
-    const df rr = df_mul(df{r, 0.f}, df{r, 0.f});
-    const df d = df_add(x, df_neg(rr));                      // x - r^2
-    return df_add(df{r, 0.f}, df{__fdiv_rn(d.hi, __fmul_rn(2.f, r)), 0.f});
+// 1 / sqrt(x): fp32 estimate y and one Newton step y + y (1 - x y^2) / 2 in two floats (x > 0)
+__device__ __forceinline__ df df_rsqrt(df x) {
+    const float y = rsqrtf(x.hi);
+    const float yy = __fmul_rn(y, y);
+    const df y2{yy, __fmaf_rn(y, y, -yy)};                              // y^2 exactly
+    const df e = df_add(df{1.f, 0.f}, df_neg(df_mul(x, y2)));          // 1 - x y^2
+    const df c = df_mul(df{y, 0.f}, e);
+    return df_add(df{y, 0.f}, df{__fmul_rn(0.5f, c.hi), __fmul_rn(0.5f, c.lo)});
 }
 // (hi, lo) accumulation of a product of two floats: the product split exactly
 // by an fma, the running sum by TwoSum; lo collects all rounding errors.
@@ -531,7 +526,7 @@ __device__ void gram_task(const GBatch &B, const GJob &J, int task, unsigned cha
     __syncthreads();
     // pivot j: 1 / sqrt(d), or 0 when the residual d is at most kDrop of the column's norm^2
     auto recip_pivot = [&](df d, int j) -> df {
-        return d.hi > kDrop * dg[j] ? df_recip(df_sqrt(d)) : df{0.f, 0.f};
+        return d.hi > kDrop * dg[j] ? df_rsqrt(d) : df{0.f, 0.f};
     };
     // row 0 of R
     {
@@ -549,9 +544,14 @@ __device__ void gram_task(const GBatch &B, const GJob &J, int task, unsigned cha
     // barrier per step
     for (int j = 0; j + 1 < KP; ++j) {
         const int L = KP - j - 1;
-        for (int idx = tid; idx < L * L; idx += kThreads) {
-            const int a = j + 1 + idx / L, c = j + 1 + idx % L;
-            if (a > c) continue;
+        // the pairs j < a <= c, a-major: a = j + 1 + ra with ra from the triangular index
+        for (int idx = tid; idx < L * (L + 1) / 2; idx += kThreads) {
+            int ra = 0, rem = idx;
+            while (rem >= L - ra) {
+                rem -= L - ra;
+                ++ra;
+            }
+            const int a = j + 1 + ra, c = a + rem;
             const df rja{gh[j * KP + a], gl[j * KP + a]};
             const df g = df_add(df{gh[a * KP + c], gl[a * KP + c]},
                                 df_neg(df_mul(rja, df{gh[j * KP + c], gl[j * KP + c]})));
