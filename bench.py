@@ -254,7 +254,7 @@ class ModelWorkload:
     work; generating 16 distinct layers would take minutes of host time), plus
     plain-AdamW tensors (the full model's embedding and norm vectors)."""
 
-    def __init__(self, shapes: dict, n_layers: int, seed: int, plain=()):
+    def __init__(self, shapes: dict, n_layers: int, seed: int, plain=(), tau_p: float = 1e-3):
         import numpy as np
         import torch
 
@@ -267,7 +267,8 @@ class ModelWorkload:
         self.Ganc = {n: [torch.from_numpy(inputs[n].anchor_grad(i)).cuda() for i in range(2)] for n in self.names}
         self.Gm = {n: [torch.from_numpy(inputs[n].masked_grad(t)).cuda() for t in range(2)] for n in self.names}
         W0 = {n: torch.from_numpy(inputs[n].weights()).cuda() for n in self.names}
-        self.layers = [{n: so.SpectralOptimizer(*shapes[n]) for n in self.names} for _ in range(n_layers)]
+        self.layers = [{n: so.SpectralOptimizer(*shapes[n], tau_p=tau_p) for n in self.names}
+                       for _ in range(n_layers)]
         self.W = [{n: W0[n].clone() for n in self.names} for _ in range(n_layers)]
         self.plain = []
         for i, (rows, cols) in enumerate(plain):
@@ -606,11 +607,19 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                                        "embedding 128256x2048 + 33 norm vectors plain AdamW", full, 20, 3)
         del full
         torch.cuda.empty_cache()
-        l7 = ModelWorkload(synthetic.LLAMA_7B_LAYER, 1, seed=rank)
-        others["layer_7b"] = run_config("7B-shaped layer: q,o 4096x4096; k,v 1024x4096; gate,up 14336x4096; "
-                                        "down 4096x14336", l7, 20, 3, mask_shape=(8 * 4096, 4096, 0.95))
-        del l7
-        torch.cuda.empty_cache()
+        sweep = {}
+        for tau in (1e-4, 1e-3, 1e-2):  # the workload's tau_p values; tau changes d, not the work
+            l7 = ModelWorkload(synthetic.LLAMA_7B_LAYER, 1, seed=rank, tau_p=tau)
+            res7 = run_config("7B-shaped layer: q,o 4096x4096; k,v 1024x4096; gate,up 14336x4096; "
+                              "down 4096x14336", l7, 20, 3,
+                              mask_shape=(8 * 4096, 4096, 0.95) if tau == 1e-3 else None)
+            sweep["%g" % tau] = {"steps_per_s": res7["steps_per_s"], "refresh_ms": res7["refresh_ms"],
+                                 "refresh_sweeps_max": res7["refresh_sweeps_max"]}
+            if tau == 1e-3:
+                others["layer_7b"] = res7
+            del l7
+            torch.cuda.empty_cache()
+        others["layer_7b"]["tau_p_sweep"] = sweep
     mask_frac = mask["p0.95"]["effective_GBps"] / peaks["hbm_gbs"]
 
     # rooflines of the two heaviest kernels: the tensor-core GEMM of the steady

@@ -53,11 +53,11 @@ def check_matrix(opt, inp, G, Gf, Gp, W0, W1, lr, alpha=0.3, tau=1e-3):
     assert torch.linalg.norm(dW - dW_want) / torch.linalg.norm(dW_want) <= 1e-3
 
 
-def run_layer(shapes, seed):
+def run_layer(shapes, seed, tau=1e-3):
     ensure_lib()
     inps = synthetic.layer_inputs(shapes, seed=seed, rank=32)
     names = list(inps)
-    opts = [so.SpectralOptimizer(inps[k].m, inps[k].n) for k in names]
+    opts = [so.SpectralOptimizer(inps[k].m, inps[k].n, tau_p=tau) for k in names]
     for o, k in zip(opts, names):
         o.anchor_update(dev(inps[k].anchor_grad(0)))
     sweeps = so.svd_refresh_many(opts)
@@ -72,7 +72,7 @@ def run_layer(shapes, seed):
         Gp = torch.empty_like(G)
         o.step(W, G, lr, Gf, Gp)
         torch.cuda.synchronize()
-        check_matrix(o, inp, G, Gf, Gp, W0, W, lr)
+        check_matrix(o, inp, G, Gf, Gp, W0, W, lr, tau=tau)
     return opts, inps
 
 
@@ -80,9 +80,11 @@ def test_llama_1b_layer_properties():
     run_layer(synthetic.LLAMA_1B_LAYER, seed=0)
 
 
-def test_7b_class_matrices_properties():
+@pytest.mark.parametrize("tau", [1e-4, 1e-3, 1e-2])
+def test_7b_class_matrices_properties(tau):
+    """The 7B-shaped workload at each of its tau_p values."""
     run_layer({"q": synthetic.LLAMA_7B_LAYER["q"], "k": synthetic.LLAMA_7B_LAYER["k"],
-               "gate": synthetic.LLAMA_7B_LAYER["gate"]}, seed=3)
+               "gate": synthetic.LLAMA_7B_LAYER["gate"]}, seed=3, tau=tau)
 
 
 def test_kv_shape_against_the_oracle():
