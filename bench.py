@@ -842,13 +842,30 @@ class OracleSample:
                 "p=0.95 mask round trip; steps/s = 1 / seconds per sample")
 
 
+def oracle_toy_seconds():
+    """The oracle's whole path on the toy workload (256 x 128: anchor EMA, its own
+    Jacobi SVD, filter, step; a 64 x 256 bf16 mask round trip), seconds."""
+    import oracle
+    import synthetic
+    inp = synthetic.toy_matrix_inputs()
+    t = time.perf_counter()
+    opt = oracle.SpectralOptimizer(inp.m, inp.n)
+    opt.anchor_update(inp.anchor_grad(0))
+    opt.svd_refresh()
+    opt.step(inp.weights().astype("float64"), inp.masked_grad(0), 2e-5)
+    h = synthetic.activations_bf16(64, 256)
+    K = oracle.mask_K(0.95, 256)
+    oracle.mask_unpack(oracle.mask_pack(h, K, 3, 7), 256, 3, 7)
+    return time.perf_counter() - t
+
+
 def cpu_baseline():
     s = OracleSample()
     t = time.perf_counter()
     s.step(0)
     dt = time.perf_counter() - t
     return {"value": 1.0 / dt, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": s.describe(), "seconds": dt}
+            "sample": s.describe(), "seconds": dt, "toy_whole_path_seconds": oracle_toy_seconds()}
 
 
 def run_reference(args, rank, world):
