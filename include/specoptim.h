@@ -211,6 +211,13 @@ int specoptim_trace_report(char *buf, int64_t len);
  * Any other return value means the mechanism is broken. */
 int specoptim_selftest_wait_timeout(uint32_t spin_limit, void *stream);
 
+/* Synchronises `stream` and reports whether a bounded device-side wait of any
+ * of the library's kernels (the asynchronous calls of this header, of
+ * mask_fused.h and of dpsync.h) gave up since the last check:
+ * SPECOPTIM_ERR_TIMEOUT (the flag is cleared; the results of the kernels
+ * launched since the last check are not to be trusted) or SPECOPTIM_OK. */
+int specoptim_check_device(void *stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *specoptim_last_error(void);
 

@@ -71,6 +71,7 @@ SIGNATURES = [
     ("specoptim_gemm_nt", _int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     ("specoptim_filter_noalloc", _int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]),
     ("specoptim_selftest_wait_timeout", _int, [_u32, _vp]),
+    ("specoptim_check_device", _int, [_vp]),
     ("specoptim_trace_enable", _int, [_i32]),
     ("specoptim_launch_count", _i64, []),
     ("specoptim_trace_reset", _int, []),
@@ -270,6 +271,11 @@ def gemm_nt(A, B, precision: int = PREC_TF32, out=None, stream=None):
     _check(lib().specoptim_gemm_nt(M, N, K, _ptr(A), K, _ptr(B), K, _ptr(out), N, precision,
                                    _stream(stream)), "specoptim_gemm_nt")
     return out
+
+
+def check_device(stream=None):
+    """Synchronise the stream; raise if a bounded device-side wait of the library gave up."""
+    _check(lib().specoptim_check_device(_stream(stream)), "specoptim_check_device")
 
 
 def trace_enable(on: bool = True):

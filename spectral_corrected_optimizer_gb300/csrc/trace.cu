@@ -109,6 +109,11 @@ extern "C" int specoptim_selftest_wait_timeout(uint32_t spin_limit, void *stream
     return check_device_flag(st);
 }
 
+extern "C" int specoptim_check_device(void *stream) {
+    clear_error();
+    return check_device_flag(static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int specoptim_trace_enable(int32_t enable) {
     clear_error();
     std::lock_guard<std::mutex> lk(g_mu);

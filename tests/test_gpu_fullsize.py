@@ -142,3 +142,6 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     assert float(x.sum()) == 1024.0
     idx = so.mask_indices(4, 256, 13, 3, 7)
     assert np.array_equal(host(idx), oracle.mask_indices(4, 256, 13, 3, 7))
+    # the public check after asynchronous work finds nothing to report
+    assert lib.specoptim_check_device(torch.cuda.current_stream().cuda_stream) == so.OK
+    so.check_device()
