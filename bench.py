@@ -219,27 +219,44 @@ class Layer:
         self.hd = torch.empty_like(self.h)
         self.gd = torch.empty_like(self.g)
         self.lr = 2e-5
+        self.last_sweeps = None
         self.flops = sum(gemm_flops(i.m, i.n) for i in self.inputs.values())
         self.bytes = sum(step_bytes(i.m, i.n) for i in self.inputs.values())
         self.params = sum(i.m * i.n for i in self.inputs.values())
+
+    def reset_state(self):
+        """Fresh optimizer state and the initial weights: a loop run after this
+        one replays the same refresh history (the Jacobi sweep count of a warm-
+        started refresh depends on how many refreshes came before it)."""
+        for name, inp in self.inputs.items():
+            self.opt[name].close()
+            self.opt[name] = self.so.SpectralOptimizer(inp.m, inp.n)
+            self.W[name].copy_(self.torch.from_numpy(inp.weights()))
 
     def refresh(self, idx: int, G=None):
         """Anchor EMA + batched SVD refresh of the 7 matrices; returns the Jacobi
         sweeps each one took."""
         for name in self.names:
             self.opt[name].anchor_update(G[name] if G else self.Ganc[name][idx % 2])
-        return self.so.svd_refresh_many([self.opt[name] for name in self.names])
+        self.last_sweeps = self.so.svd_refresh_many([self.opt[name] for name in self.names])
+        return self.last_sweeps
 
     def spectral(self, i: int, G=None):
         self.so.step_many([self.opt[n] for n in self.names], [self.W[n] for n in self.names],
                           [G[n] if G else self.Gpool[n][i % POOL] for n in self.names], self.lr)
 
-    def mask_round_trip(self, i: int, h=None, g=None):
+    def mask_round_trip(self, i: int, hp_out=None, gp_out=None, hp_in=None, gp_in=None):
+        """Pack the boundary activation and its gradient, and unpack the packed
+        values of the neighbouring stages.  On one device the unpack reads the
+        values this step packed; a loop that exchanges them over a link passes
+        the received ones (hp_in, gp_in) and its own send buffers."""
         so, layer = self.so, i % MASK_BOUNDARIES
-        so.mask_pack(self.h if h is None else h, self.K, layer, i, 0, out=self.hp)
-        so.mask_unpack(self.hp, MASK_H, layer, i, 0, out=self.hd)
-        so.mask_pack(self.g if g is None else g, self.K, layer, i, 0, out=self.gp)
-        so.mask_unpack(self.gp, MASK_H, layer, i, 0, out=self.gd)
+        hp = self.hp if hp_out is None else hp_out
+        gp = self.gp if gp_out is None else gp_out
+        so.mask_pack(self.h, self.K, layer, i, 0, out=hp)
+        so.mask_unpack(hp if hp_in is None else hp_in, MASK_H, layer, i, 0, out=self.hd)
+        so.mask_pack(self.g, self.K, layer, i, 0, out=gp)
+        so.mask_unpack(gp if gp_in is None else gp_in, MASK_H, layer, i, 0, out=self.gd)
 
     def step(self, i: int):
         if i % REFRESH_EVERY == 0:
@@ -577,9 +594,11 @@ def run_ours(args, rank, world, local_rank, dist_ok):
 
     # ---- the timed region: K whole-hot-path steps
     so.trace_reset()
+    layer.last_sweeps = None
     with ClockSampler(local_rank) as clocks:
         ms = timed(torch, lambda: [layer.step(W + i) for i in range(K)], dist_ok)
     launches = so.launch_count()
+    timed_sweeps = layer.last_sweeps
     ms_max = max_over_ranks(ms, dist_ok)
     value = world * K / (ms_max * 1e-3)
 
@@ -679,7 +698,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world, "parallelism": "replicas (one layer per GPU)",
                    "l2": "inputs larger than L2: each step streams 0.97 GB of distinct gradients and "
-                         "optimizer state and 1 GB of activations"},
+                         "optimizer state and 1 GB of activations",
+                   "timed_refresh_sweeps": timed_sweeps},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "roofline": roof,
@@ -704,31 +724,42 @@ def run_ours(args, rank, world, local_rank, dist_ok):
 
 
 def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
-    """Same steps with host buffers, as a training loop would drive them: every
-    step's masked gradients and activations (and, every 20th step, the anchor
-    gradients) come host -> device from pinned memory, and every step's updated
-    weights go device -> host (the parameter snapshot the anchor circuit pulls).
-    The copies run on two more streams (one per direction), double-buffered: step
-    i+1's inputs travel while step i computes, and step i's weights leave from a
-    device-side snapshot while step i+1 computes.  All of it is inside the timed
-    region."""
+    """Same steps with host buffers, as a pipeline stage's training loop would
+    drive them.  What crosses the host link each step is what the method sends:
+    host -> device, the step's masked gradients (every 20th step also the anchor
+    gradients) and the packed boundary values received from the neighbouring
+    stages (the activation from the previous stage, the gradient from the next);
+    device -> host, the step's updated weights (the parameter snapshot the anchor
+    circuit pulls) and the packed values this stage sends.  The dense boundary
+    activation and its gradient are produced and consumed on the device by the
+    model's own layers, so they stay resident, as in training.  The copies run on
+    two more streams (one per direction), double-buffered: step i+1's inputs
+    travel while step i computes, and step i's outputs leave from device-side
+    buffers while step i+1 computes.  All of it is inside the timed region."""
     torch = layer.torch
     names = layer.names
     hostG = {n: [g.cpu().pin_memory() for g in layer.Gpool[n][:2]] for n in names}
     hostA = {n: [g.cpu().pin_memory() for g in layer.Ganc[n]] for n in names}
-    host_h, host_g = layer.h.cpu().pin_memory(), layer.g.cpu().pin_memory()
     hostW = {n: torch.empty(layer.W[n].shape, dtype=torch.float32).pin_memory() for n in names}
+    # received packed values: one boundary's pack of the synthetic activations
+    host_hp = layer.so.mask_pack(layer.h, layer.K, 0, 0, 0).cpu().pin_memory()
+    host_gp = layer.so.mask_pack(layer.g, layer.K, 0, 0, 0).cpu().pin_memory()
+    sent_hp = [torch.empty_like(host_hp).pin_memory() for _ in range(2)]
+    sent_gp = [torch.empty_like(host_gp).pin_memory() for _ in range(2)]
     devG = [{n: torch.empty_like(layer.Gpool[n][0]) for n in names} for _ in range(2)]
     devA = [{n: torch.empty_like(layer.Ganc[n][0]) for n in names} for _ in range(2)]
-    dev_h = [torch.empty_like(layer.h) for _ in range(2)]
-    dev_g = [torch.empty_like(layer.g) for _ in range(2)]
+    in_hp = [torch.empty_like(layer.hp) for _ in range(2)]
+    in_gp = [torch.empty_like(layer.gp) for _ in range(2)]
+    out_hp = [torch.empty_like(layer.hp) for _ in range(2)]
+    out_gp = [torch.empty_like(layer.gp) for _ in range(2)]
     snapW = {n: torch.empty_like(layer.W[n]) for n in names}
     compute, copy, back = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     stats = {"h2d": 0, "d2h": 0}
     freed = [torch.cuda.Event(), torch.cuda.Event()]  # compute done with input buffer b
     loaded = [torch.cuda.Event(), torch.cuda.Event()]  # inputs of buffer b landed
+    out_free = [torch.cuda.Event(), torch.cuda.Event()]  # packed send buffer b has left
     snapped, sent = torch.cuda.Event(), torch.cuda.Event()
-    for e in freed + [sent]:
+    for e in freed + out_free + [sent]:
         e.record(compute)
 
     def load(i):  # on the copy stream: step i's inputs into buffer i % 2
@@ -742,9 +773,9 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
             for n in names:
                 devG[b][n].copy_(hostG[n][i % 2], non_blocking=True)
                 stats["h2d"] += devG[b][n].numel() * 4
-            dev_h[b].copy_(host_h, non_blocking=True)
-            dev_g[b].copy_(host_g, non_blocking=True)
-            stats["h2d"] += 2 * dev_h[b].numel() * 2
+            in_hp[b].copy_(host_hp, non_blocking=True)
+            in_gp[b].copy_(host_gp, non_blocking=True)
+            stats["h2d"] += (in_hp[b].numel() + in_gp[b].numel()) * 2
             loaded[b].record(copy)
 
     def one(i, last):
@@ -755,14 +786,19 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
         if i % REFRESH_EVERY == 0:
             layer.refresh(0, G=devA[b])
         layer.spectral(i, G=devG[b])
-        layer.mask_round_trip(i, h=dev_h[b], g=dev_g[b])
+        compute.wait_event(out_free[b])  # step i-2's packed values have left
+        layer.mask_round_trip(i, hp_out=out_hp[b], gp_out=out_gp[b], hp_in=in_hp[b], gp_in=in_gp[b])
         freed[b].record(compute)
-        compute.wait_event(sent)  # the previous snapshot has left
+        compute.wait_event(sent)  # the previous weight snapshot has left
         for n in names:
             snapW[n].copy_(layer.W[n], non_blocking=True)
         snapped.record(compute)
         with torch.cuda.stream(back):
             back.wait_event(snapped)
+            sent_hp[b].copy_(out_hp[b], non_blocking=True)
+            sent_gp[b].copy_(out_gp[b], non_blocking=True)
+            stats["d2h"] += (out_hp[b].numel() + out_gp[b].numel()) * 2
+            out_free[b].record(back)
             for n in names:
                 hostW[n].copy_(snapW[n], non_blocking=True)
                 stats["d2h"] += snapW[n].numel() * 4
@@ -775,14 +811,19 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
         compute.wait_stream(copy)
         compute.wait_stream(back)
 
-    run(10_000, W)
+    layer.reset_state()  # the same steps as the device-resident timed region, same refresh history
+    run(0, W)
     stats["h2d"] = stats["d2h"] = 0
-    ms = timed(torch, lambda: run(10_000 + W, K), dist_ok)
+    layer.last_sweeps = None
+    ms = timed(torch, lambda: run(W, K), dist_ok)
     ms = max_over_ranks(ms, dist_ok)
     return {"value": world * K / (ms * 1e-3), "unit": "steps/s",
             "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K,
-            "pipeline": "copies on two more streams (one per direction), double-buffered inputs, weights "
-                        "read back from a device-side snapshot; every copy inside the timed region",
+            "timed_refresh_sweeps": layer.last_sweeps,
+            "pipeline": "copies on two more streams (one per direction), double-buffered inputs and packed "
+                        "sends, weights read back from a device-side snapshot; every copy inside the timed region",
+            "link_traffic": "gradients in, weights out, packed boundary values (K of H per row) both ways; "
+                            "the dense boundary tensors stay on the device",
             "link": link_bandwidth(torch)}
 
 
