@@ -327,23 +327,59 @@ __global__ void init_q_kernel(float *__restrict__ Q, int Np, int r, const float 
     }
 }
 
-// sums of squares: out[0] = off-diagonal, out[1] = all (double atomics)
-__global__ void offnorm_kernel(const float *__restrict__ A, int Np, double *out) {
-    double off = 0.0, all = 0.0;
-    const int64_t total = (int64_t)Np * Np;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const double v = A[e];
-        all += v * v;
-        if (e / Np != e % Np) off += v * v;
+// Sums of squares of A (Np x Np, Np a multiple of 4): out[0] += off-diagonal,
+// out[1] += all.  A is a Gram matrix rotated by orthogonal similarities, so no
+// entry exceeds its largest diagonal entry in magnitude: each block scales by
+// the power of two just above that entry (exact, no overflow, underflow only
+// below 2^-75 of it) and sums the scaled squares in fp32 per thread (a few
+// hundred terms each); the per-thread sums are combined in double, one pair of
+// atomics per block.  fp64 arithmetic, slow on this part, is kept out of the
+// per-element loop.
+__global__ void __launch_bounds__(256) offnorm_kernel(const float *__restrict__ A, int Np, double *out) {
+    __shared__ float smax[8];
+    __shared__ double sred[2][8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float dm = 0.f;
+    for (int i = tid; i < Np; i += blockDim.x) dm = fmaxf(dm, fabsf(A[(size_t)i * Np + i]));
+    for (int o = 16; o > 0; o >>= 1) dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+    if (lane == 0) smax[warp] = dm;
+    __syncthreads();
+    dm = smax[0];
+    for (int w = 1; w < 8; ++w) dm = fmaxf(dm, smax[w]);
+    int e = 0;
+    frexpf(dm, &e);  // dm = f 2^e, f in [0.5, 1)
+    const float sc = (dm > 0.f && isfinite(dm)) ? ldexpf(1.f, -e) : 1.f;
+    float off = 0.f, all = 0.f;
+    const int n4 = Np >> 2;
+    for (int i = blockIdx.x; i < Np; i += gridDim.x) {
+        const float4 *row = reinterpret_cast<const float4 *>(A + (size_t)i * Np);
+        for (int c = tid; c < n4; c += blockDim.x) {
+            const float4 v = row[c];
+            const float x = v.x * sc, y = v.y * sc, z = v.z * sc, w = v.w * sc;
+            const float sx = x * x, sy = y * y, sz = z * z, sw = w * w;
+            all += (sx + sy) + (sz + sw);
+            const int d = i - 4 * c;  // position of the diagonal entry in this float4, if any
+            off += ((d == 0 ? 0.f : sx) + (d == 1 ? 0.f : sy)) + ((d == 2 ? 0.f : sz) + (d == 3 ? 0.f : sw));
+        }
     }
+    double doff = off, dall = all;
     for (int o = 16; o > 0; o >>= 1) {
-        off += __shfl_xor_sync(0xffffffffu, off, o);
-        all += __shfl_xor_sync(0xffffffffu, all, o);
+        doff += __shfl_xor_sync(0xffffffffu, doff, o);
+        dall += __shfl_xor_sync(0xffffffffu, dall, o);
     }
-    if ((threadIdx.x & 31) == 0) {
-        atomicAdd(&out[0], off);
-        atomicAdd(&out[1], all);
+    if (lane == 0) {
+        sred[0][warp] = doff;
+        sred[1][warp] = dall;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double so = 0.0, sa = 0.0;
+        for (int w = 0; w < 8; ++w) {
+            so += sred[0][w];
+            sa += sred[1][w];
+        }
+        atomicAdd(&out[0], so);
+        atomicAdd(&out[1], sa);
     }
 }
 
@@ -722,8 +758,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             if (!jb.active[i]) continue;
             jobs[i].sweeps = sweep + 1;
             SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), hi));
-            const int64_t NN = (int64_t)b[i].Np * b[i].Np;
-            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<grid_for(NN, 256), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
+            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<std::min(b[i].Np, 2 * num_sms()), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
             SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
                                            cudaMemcpyDeviceToHost, hi));
         }

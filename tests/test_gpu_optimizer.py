@@ -201,6 +201,26 @@ def test_batched_and_warm_started_refresh(prec):
             assert np.abs(host(d_) - o.d).max() <= 1e-3
 
 
+@pytest.mark.parametrize("prec", PRECS)
+def test_refresh_is_scale_covariant(prec):
+    # scaling the anchor gradient by 2^k is exact through the EMA, the Gram
+    # product, the rotations (their angles are ratios) and the convergence test,
+    # so the refresh takes the same sweeps and s scales by exactly 2^k; k = +-40
+    # puts the Gram matrix's entries 2^+-80 away from those at k = 0
+    inp = synthetic.MatrixInputs(384, 256, seed=77, rank=6)
+    G = inp.anchor_grad(0)
+    out = {}
+    for k in (0, -40, 40):
+        g = so.SpectralOptimizer(inp.m, inp.n, precision=prec)
+        g.anchor_update(dev(np.ldexp(G, k).astype(np.float32)))
+        sweeps = g.svd_refresh()
+        _, s_, _, _ = g.get_factors()
+        out[k] = (sweeps, host(s_).astype(np.float64))
+    for k in (-40, 40):
+        assert out[k][0] == out[0][0]
+        np.testing.assert_allclose(np.ldexp(out[k][1], -k), out[0][1], rtol=1e-6, atol=0)
+
+
 def test_refresh_many_rejects_bad_batches():
     a = so.SpectralOptimizer(32, 16)
     with pytest.raises(so.SpecOptimError):
