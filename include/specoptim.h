@@ -21,6 +21,11 @@
  *   - Every call returns a status code and never throws or aborts.  On a
  *     non-zero status, specoptim_last_error() gives a message (per thread).
  *   - A handle serves one weight matrix and is not thread-safe.
+ *   - One device per process: the library's shared state (kernel launch
+ *     limits, a scratch buffer, the flag of its bounded device-side waits)
+ *     belongs to the device that is current at its first use.  Creating a
+ *     handle, or a call that reaches that state, while another device is
+ *     current returns SPECOPTIM_ERR_INVALID_ARG.
  */
 #ifndef SPECOPTIM_H
 #define SPECOPTIM_H

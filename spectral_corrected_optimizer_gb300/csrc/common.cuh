@@ -71,6 +71,17 @@ void trace_end(int token, cudaStream_t st);
         ::spco::trace_end(_tk, st);                                          \
     } while (0)
 
+// The library serves one device per process: its shared state (kernel
+// shared-memory limits, the scratch buffer below, the device-side error flag)
+// belongs to the device that is current at its first use.  bind_device()
+// records that device and fails with SPECOPTIM_ERR_INVALID_ARG when another
+// one is current.
+int bind_device();
+
+// Raises `fn`'s dynamic shared-memory limit to at least `bytes` (once per
+// kernel and size; thread-safe).
+int set_smem_limit(const void *fn, size_t bytes);
+
 // Library-wide scratch for transient operands (the split copies of 3xTF32
 // products in the SVD refresh): grown on demand with cudaMalloc on the current
 // device, never shrunk, shared by all handles.  Callers use it only between

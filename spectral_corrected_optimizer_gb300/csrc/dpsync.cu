@@ -1084,8 +1084,7 @@ int validate_batch(dpsync_t *const *hs, int32_t count, const char *what) {
 }
 
 int set_smem(const void *fn, size_t bytes) {
-    return cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
-                       "cudaFuncSetAttribute");
+    return set_smem_limit(fn, bytes);
 }
 
 int gram_blocks(int kp) { return (kp / 4) * (kp / 4 + 1) / 2; }
@@ -1143,6 +1142,7 @@ extern "C" int dpsync_create(dpsync_t **out, const dpsync_config *cfg, float *P,
         return fail(SPECOPTIM_ERR_INVALID_ARG, "dpsync_create: rank above 64 or min(m, n)");
     if ((reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(Q)) & 3u)
         return fail(SPECOPTIM_ERR_MISALIGNED, "dpsync_create: P and Q must be 4-byte aligned");
+    if (int rc = bind_device()) return rc;
     dpsync *h = new dpsync();
     h->cfg = *cfg;
     h->m = cfg->m;

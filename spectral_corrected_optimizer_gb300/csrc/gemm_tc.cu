@@ -333,13 +333,7 @@ int gemm_tc_group(int count, const GemmProblem *probs, cudaStream_t stream) {
         g.tile_off[p + 1] = g.tile_off[p] + g.tiles_n[p] * (int)((q.M + BM - 1) / BM);
         mode_mask |= 1 << q.epi.mode;
     }
-    static bool attr = false;
-    if (!attr) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(gemm_tf32_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)SMEM_BYTES));
-        attr = true;
-    }
+    if (int rc = set_smem_limit(reinterpret_cast<const void *>(&gemm_tf32_kernel), SMEM_BYTES)) return rc;
     const int grid = std::min(g.tile_off[count], num_sms());
     const char *name = (mode_mask & (1 << EPI_ADAMW)) ? "gemm_tf32_adamw"
                        : (mode_mask & (1 << EPI_SCALE)) ? "gemm_tf32_scale"

@@ -374,12 +374,7 @@ int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st) {
     }
     if (ab.count == 0) return SPECOPTIM_OK;
     ab.total = ab.task_off[ab.count];
-    static bool attr = false;
-    if (!attr) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kApSmem));
-        attr = true;
-    }
+    if (int rc = set_smem_limit(reinterpret_cast<const void *>(&jacobi_apply_kernel), kApSmem)) return rc;
     const int grid = std::min(num_sms(), ab.total);
     SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<grid, kApThreads, kApSmem, st>>>(ab, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("jacobi_apply_kernel");

@@ -290,12 +290,8 @@ int jacobi_rotate(const CtJob *jobs, int count, cudaStream_t st, int max_ctas) {
     }
     if (cb.count == 0) return SPECOPTIM_OK;
     cb.total = cb.task_off[cb.count];
-    static bool attr = false;
-    if (!attr) {
-        SPECOPTIM_CUDA(cudaFuncSetAttribute(jacobi_rotate_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)ct_smem(kStages)));
-        attr = true;
-    }
+    if (int rc = set_smem_limit(reinterpret_cast<const void *>(&jacobi_rotate_kernel<kStages>), ct_smem(kStages)))
+        return rc;
     // one CTA per SM (or per SM of the share given) with at least two tasks each
     int grid = std::max(1, std::min(max_ctas > 0 ? max_ctas : num_sms(), cb.total / 2));
     SPCO_LAUNCH("svd_jacobi_rotate", st,

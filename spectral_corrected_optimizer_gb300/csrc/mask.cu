@@ -265,13 +265,7 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
         size_t smem = ring_layout(in_b, out_b, stages).total;
-        static bool attr = false;
-        if (!attr) {
-            SPECOPTIM_CUDA(cudaFuncSetAttribute(pack_bulk_kernel<T>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kSmemBudget));
-            attr = true;
-        }
+        if (int rc = set_smem_limit(reinterpret_cast<const void *>(&pack_bulk_kernel<T>), kSmemBudget)) return rc;
         int grid = (int)std::min<int64_t>(nfull, (int64_t)num_sms() * plan.ctas_per_sm);
         SPCO_LAUNCH("mask_pack_bulk", st, pack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(d, p, nfull, H, K, seed, stages,
                                                           device_flag_ptr()));
@@ -296,13 +290,7 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
     int64_t nfull = (aligned16(dense) && aligned16(packed) && stages > 0) ? rows / CH : 0;
     if (nfull > 0) {
         size_t smem = ring_layout(in_b, out_b, stages).total;
-        static bool attr = false;
-        if (!attr) {
-            SPECOPTIM_CUDA(cudaFuncSetAttribute(unpack_bulk_kernel<T>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kSmemBudget));
-            attr = true;
-        }
+        if (int rc = set_smem_limit(reinterpret_cast<const void *>(&unpack_bulk_kernel<T>), kSmemBudget)) return rc;
         int grid = (int)std::min<int64_t>(nfull, (int64_t)num_sms() * plan.ctas_per_sm);
         SPCO_LAUNCH("mask_unpack_bulk", st, unpack_bulk_kernel<T><<<grid, kThreads, smem, st>>>(p, d, nfull, H, K, seed, stages,
                                                             device_flag_ptr()));

@@ -317,7 +317,7 @@ extern "C" int mask_unpack_rmsnorm(const void *packed, const void *gamma, float 
     const int warps = (int)std::min<size_t>(kWarps, 200 * 1024 / row_bytes);
     if (warps < 1) return fail(SPECOPTIM_ERR_NOT_IMPLEMENTED, "mask_unpack_rmsnorm: H too large for the row buffers");
     const size_t smem = row_bytes * warps;
-    SPECOPTIM_CUDA(cudaFuncSetAttribute(unpack_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    if (int rc = set_smem_limit(reinterpret_cast<const void *>(&unpack_rmsnorm_kernel), smem)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     SPCO_LAUNCH("mask_unpack_rmsnorm", st,
                 unpack_rmsnorm_kernel<<<grid_rows(rows, warps), kThreadsF, smem, st>>>(

@@ -63,6 +63,7 @@ unsigned *device_flag_ptr() {
 }
 
 int check_device_flag(cudaStream_t st) {
+    if (int rc = bind_device()) return rc;
     unsigned *p = device_flag_ptr();
     if (!p) return SPECOPTIM_OK;
     unsigned v = 0;
@@ -147,6 +148,7 @@ extern "C" int specoptim_create(specoptim_t **out, const specoptim_config *cfg, 
     *out = nullptr;
     int rc = validate_cfg(cfg);
     if (rc) return rc;
+    if ((rc = bind_device())) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     specoptim_t *h = new specoptim_t();
     std::memset(h, 0, sizeof(*h));

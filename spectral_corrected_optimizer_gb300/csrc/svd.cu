@@ -625,13 +625,7 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
 }  // namespace
 
 int set_solve_attributes() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(jacobi_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSolveSmem);
-    });
-    SPECOPTIM_CUDA(err);
-    return SPECOPTIM_OK;
+    return set_smem_limit(reinterpret_cast<const void *>(&jacobi_solve_kernel), kSolveSmem);
 }
 
 // Streams and events of one refresh call's Jacobi loop (created per call: a few

@@ -65,9 +65,39 @@ namespace {
 std::mutex g_scratch_mu;
 float *g_scratch = nullptr;
 size_t g_scratch_n = 0;
+std::mutex g_dev_mu;
+int g_device = -1;
+std::mutex g_smem_mu;
+std::map<const void *, size_t> g_smem;
 }  // namespace
 
+int bind_device() {
+    int dev = 0;
+    SPECOPTIM_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_device < 0) g_device = dev;
+    if (dev != g_device)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "the library serves one device per process (device " +
+                                                   std::to_string(g_device) + " at first use, device " +
+                                                   std::to_string(dev) + " current now)");
+    return SPECOPTIM_OK;
+}
+
+int set_smem_limit(const void *fn, size_t bytes) {
+    int rc = bind_device();
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    size_t &have = g_smem[fn];
+    if (bytes > have) {
+        SPECOPTIM_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+        have = bytes;
+    }
+    return SPECOPTIM_OK;
+}
+
 int scratch_floats(size_t n, float **out) {
+    int rc = bind_device();
+    if (rc) return rc;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (n > g_scratch_n) {
         if (g_scratch) {
