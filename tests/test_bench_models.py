@@ -1,0 +1,54 @@
+"""Host-side models behind bench.py's roofline and traffic figures, checked
+against independent counts: the expected fraction of 32-byte sectors and
+128-byte lines of a row that the kept dims touch (the fused mask ops' byte
+model) against the oracle's own index sets, and the lookup that reports ncu
+traffic only while the profiled kernel's sources are unchanged."""
+import hashlib
+
+import numpy as np
+import pytest
+
+import bench
+import oracle
+
+
+@pytest.mark.parametrize("H,K", [(256, 13), (2048, 102), (2048, 205), (4096, 205)])
+@pytest.mark.parametrize("elems", [16, 64])
+def test_coverage_model_matches_the_index_sets(H, K, elems):
+    rows = 4096
+    idx = oracle.mask_indices(rows, H, K, 3, 7)
+    touched = np.zeros((rows, H // elems), dtype=bool)
+    np.put_along_axis(touched, (idx // elems).astype(np.int64), True, axis=1)
+    expected = bench.sector_coverage(H, K, elems)
+    # the blocks a row touches are negatively correlated (K dims without
+    # replacement), so the binomial standard error bounds that of the mean
+    se = np.sqrt(expected * (1.0 - expected) / touched.size)
+    assert abs(touched.mean() - expected) <= 6.0 * se
+
+
+def test_coverage_model_limits():
+    assert bench.sector_coverage(2048, 0) == 0.0
+    assert bench.sector_coverage(2048, 2048) == 1.0
+    assert bench.sector_coverage(2048, 102, elems=1) == pytest.approx(102 / 2048, rel=1e-15)
+    # one block of H elements always holds a kept dim once K >= 1
+    assert bench.sector_coverage(64, 1, elems=64) == pytest.approx(1.0, rel=1e-15)
+
+
+def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
+    csrc = tmp_path / "spectral_corrected_optimizer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "a.cu").write_bytes(b"first kernel")
+    (csrc / "b.cuh").write_bytes(b"shared header")
+    sha = hashlib.sha256(b"first kernel" + b"shared header").hexdigest()[:16]
+    (tmp_path / "profiles" / "p.md").write_text(
+        "notes\nmachine-readable: k1 traffic_bytes_per_launch=12.5e6 sources_sha256_16=%s\n"
+        "machine-readable: k2 traffic_bytes_per_launch=3e6 sources_sha256_16=%s\n" % (sha, sha))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sources = ("a.cu", "b.cuh")
+    assert bench.profiled_traffic("p.md", sources, key="k1") == 12.5e6
+    assert bench.profiled_traffic("p.md", sources, key="k2") == 3e6
+    assert bench.profiled_traffic("p.md", sources, key="k3") is None
+    assert bench.profiled_traffic("missing.md", sources, key="k1") is None
+    (csrc / "b.cuh").write_bytes(b"shared header, edited")
+    assert bench.profiled_traffic("p.md", sources, key="k1") is None
