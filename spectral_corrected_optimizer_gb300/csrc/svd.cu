@@ -334,10 +334,19 @@ __global__ void init_q_kernel(float *__restrict__ Q, int Np, int r, const float 
 // below 2^-75 of it) and sums the scaled squares in fp32 per thread (a few
 // hundred terms each); the per-thread sums are combined in double, one pair of
 // atomics per block.  fp64 arithmetic, slow on this part, is kept out of the
-// per-element loop.
-__global__ void __launch_bounds__(256) offnorm_kernel(const float *__restrict__ A, int Np, double *out) {
+// per-element loop.  One launch covers the batch: blockIdx.y picks the matrix.
+struct OffBatch {
+    const float *A[kMaxBatch];
+    double *out[kMaxBatch];
+    int Np[kMaxBatch];
+};
+
+__global__ void __launch_bounds__(256) offnorm_kernel(const OffBatch ob) {
     __shared__ float smax[8];
     __shared__ double sred[2][8];
+    const float *__restrict__ A = ob.A[blockIdx.y];
+    double *out = ob.out[blockIdx.y];
+    const int Np = ob.Np[blockIdx.y];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float dm = 0.f;
     for (int i = tid; i < Np; i += blockDim.x) dm = fmaxf(dm, fabsf(A[(size_t)i * Np + i]));
@@ -350,16 +359,33 @@ __global__ void __launch_bounds__(256) offnorm_kernel(const float *__restrict__ 
     frexpf(dm, &e);  // dm = f 2^e, f in [0.5, 1)
     const float sc = (dm > 0.f && isfinite(dm)) ? ldexpf(1.f, -e) : 1.f;
     float off = 0.f, all = 0.f;
+    // this block's rows are i = blockIdx.x + r gridDim.x; its float4s are walked
+    // flat, four loads in flight per thread
     const int n4 = Np >> 2;
-    for (int i = blockIdx.x; i < Np; i += gridDim.x) {
-        const float4 *row = reinterpret_cast<const float4 *>(A + (size_t)i * Np);
-        for (int c = tid; c < n4; c += blockDim.x) {
-            const float4 v = row[c];
-            const float x = v.x * sc, y = v.y * sc, z = v.z * sc, w = v.w * sc;
+    const int nrows = Np > (int)blockIdx.x ? (Np - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = nrows * n4;
+    for (int e0 = tid; e0 < total; e0 += 4 * (int)blockDim.x) {
+        float4 v[4];
+        int d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * (int)blockDim.x;
+            if (e < total) {
+                const int r = e / n4, c = e - r * n4;
+                const int i = (int)blockIdx.x + r * (int)gridDim.x;
+                v[u] = reinterpret_cast<const float4 *>(A + (size_t)i * Np)[c];
+                d[u] = i - 4 * c;  // position of the diagonal entry in this float4, if any
+            } else {
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                d[u] = -1;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float x = v[u].x * sc, y = v[u].y * sc, z = v[u].z * sc, w = v[u].w * sc;
             const float sx = x * x, sy = y * y, sz = z * z, sw = w * w;
             all += (sx + sy) + (sz + sw);
-            const int d = i - 4 * c;  // position of the diagonal entry in this float4, if any
-            off += ((d == 0 ? 0.f : sx) + (d == 1 ? 0.f : sy)) + ((d == 2 ? 0.f : sz) + (d == 3 ? 0.f : sw));
+            off += ((d[u] == 0 ? 0.f : sx) + (d[u] == 1 ? 0.f : sy)) + ((d[u] == 2 ? 0.f : sz) + (d[u] == 3 ? 0.f : sw));
         }
     }
     double doff = off, dall = all;
@@ -634,13 +660,14 @@ int set_solve_attributes() {
 // returns, which the driver defers until their work completed).
 struct JacStreams {
     cudaStream_t hi = nullptr, lo = nullptr;
-    cudaEvent_t a_done[2] = {}, q_done[2] = {}, ev = nullptr;
+    cudaEvent_t a_done[2] = {}, q_done[2] = {}, ev = nullptr, norms = nullptr;
     ~JacStreams() {
         for (int k = 0; k < 2; ++k) {
             if (a_done[k]) cudaEventDestroy(a_done[k]);
             if (q_done[k]) cudaEventDestroy(q_done[k]);
         }
         if (ev) cudaEventDestroy(ev);
+        if (norms) cudaEventDestroy(norms);
         if (hi) cudaStreamDestroy(hi);
         if (lo) cudaStreamDestroy(lo);
     }
@@ -653,6 +680,7 @@ struct JacStreams {
             SPECOPTIM_CUDA(cudaEventCreateWithFlags(&q_done[k], cudaEventDisableTiming));
         }
         SPECOPTIM_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+        SPECOPTIM_CUDA(cudaEventCreateWithFlags(&norms, cudaEventDisableTiming));
         SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest));
         SPECOPTIM_CUDA(cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least));
         SPECOPTIM_CUDA(cudaEventRecord(ev, st));
@@ -731,7 +759,11 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
         return SPECOPTIM_OK;
     };
-    std::vector<double> host(2 * count);
+    // the convergence test's sums land in pinned host memory (one small buffer per
+    // host thread, kept for the life of the process), so the copies stay
+    // asynchronous and the host waits on an event, not on the stream
+    static thread_local double *host = nullptr;
+    if (!host) SPECOPTIM_CUDA(cudaMallocHost(reinterpret_cast<void **>(&host), 2 * kMaxBatch * sizeof(double)));
     int active = count;
     long g = 0;
     if ((rc2 = solve(0))) return rc2;
@@ -745,19 +777,35 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             // rotation of A finds SMs free sooner (measured best among 1/4 .. all)
             if ((rc2 = jacobi_rotate(qjob, count, lo, num_sms() * 3 / 8))) return rc2;
             SPECOPTIM_CUDA(cudaEventRecord(js_.q_done[g & 1], lo));
-            if ((rc2 = solve(g + 1))) return rc2;
+            // the sweep's last solve (the next sweep's first) goes after the convergence test
+            if (k + 1 < rounds && (rc2 = solve(g + 1))) return rc2;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
+        // convergence test of the active matrices: one launch, then the next
+        // sweep's first solve runs while the host waits for the sums
+        OffBatch ob;
+        int nt = 0, max_np = 0;
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             jobs[i].sweeps = sweep + 1;
             SPECOPTIM_CUDA(cudaMemsetAsync(b[i].norms, 0, 2 * sizeof(double), hi));
-            SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<std::min(b[i].Np, 2 * num_sms()), 256, 0, hi>>>(b[i].A, b[i].Np, b[i].norms));
-            SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
-                                           cudaMemcpyDeviceToHost, hi));
+            ob.A[nt] = b[i].A;
+            ob.out[nt] = b[i].norms;
+            ob.Np[nt] = b[i].Np;
+            max_np = std::max(max_np, b[i].Np);
+            ++nt;
         }
+        if (nt == 0) break;  // unreachable: the loop runs only while a matrix is active
+        const dim3 ogrid((unsigned)std::max(1, std::min(max_np, (2 * num_sms() + nt - 1) / nt)), (unsigned)nt);
+        SPCO_LAUNCH("svd_offnorm", hi, offnorm_kernel<<<ogrid, 256, 0, hi>>>(ob));
         SPECOPTIM_LAUNCHED("offnorm_kernel");
-        SPECOPTIM_CUDA(cudaStreamSynchronize(hi));
+        for (int i = 0; i < count; ++i)
+            if (jb.active[i])
+                SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
+                                               cudaMemcpyDeviceToHost, hi));
+        SPECOPTIM_CUDA(cudaEventRecord(js_.norms, hi));
+        if ((rc2 = solve(g))) return rc2;
+        SPECOPTIM_CUDA(cudaEventSynchronize(js_.norms));
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
             const double tol = jobs[i].tol;
