@@ -99,3 +99,24 @@ def test_dpsync_create_rejects_bad_config_before_touching_the_gpu(lib, field, va
     assert lib.dpsync_create(ctypes.byref(h), ctypes.byref(cfg), dummy, dummy, None) == so.ERR_INVALID_ARG
     assert h.value is None
     assert lib.dpsync_compress_p_many(None, 1, None, None, None) == so.ERR_INVALID_ARG
+
+
+def test_binding_refuses_tensors_it_cannot_pass_as_device_pointers(lib):
+    # the binding checks device, dtype, shape and element size before any
+    # pointer reaches the library (a host tensor would otherwise be read by a kernel)
+    torch = pytest.importorskip("torch")
+    h = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        so.mask_pack(h, 2, 0, 0)
+    with pytest.raises(ValueError, match="CUDA"):
+        so.mask_unpack(torch.zeros(4, 2, dtype=torch.bfloat16), 8, 0, 0)
+    with pytest.raises(ValueError, match="shape"):
+        so.mask_pack(h, 2, 0, 0, out=torch.zeros(4, 3, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="2- or 4-byte"):
+        so._elem_bytes(torch.zeros(4, 8, dtype=torch.float64))
+    with pytest.raises(ValueError, match="float32"):
+        so._f32_2d(torch.zeros(2, 3, dtype=torch.float64), (2, 3), "W")
+    with pytest.raises(ValueError, match="float32"):
+        so._f32_2d(torch.zeros(3, 2), (2, 3), "W")
+    with pytest.raises(ValueError, match="CUDA"):
+        so._f32_2d(torch.zeros(2, 3), (2, 3), "W")
