@@ -999,6 +999,48 @@ def run_profile_case(args):
     return {"profile": args.profile, "iterations": n_iter, "launches": so.launch_count()}
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_replicas(n: int) -> int:
+    """`bench.py --gpus N` started as one process: start N ranks of this script
+    (RANK / LOCAL_RANK / WORLD_SIZE / MASTER_ADDR / MASTER_PORT set as torchrun
+    would set them, one GPU each), pass rank 0's output through, and return the
+    worst exit status.  The ranks meet over a gloo group: barriers around the
+    timed region and the max over ranks of its duration."""
+    port = str(free_port())
+    procs = []
+    for rank in range(n):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=port)
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + sys.argv[1:], env=env,
+                                      stdout=None if rank == 0 else subprocess.DEVNULL))
+    rcs = [p.wait() for p in procs]
+    return max(rcs, key=abs)
+
+
+def run_dry(args, rank, world, dist_ok):
+    """Host-only stand-in for the GPU work (for checking the launcher and the
+    max-over-ranks timing without a GPU): rank r "works" for 20 + 10 r ms
+    between the two barriers."""
+    if dist_ok:
+        import torch.distributed as dist
+        dist.barrier()
+    t = time.perf_counter()
+    time.sleep((20 + 10 * rank) * 1e-3)
+    ms = (time.perf_counter() - t) * 1e3
+    if dist_ok:
+        dist.barrier()
+    ms_max = max_over_ranks(ms, dist_ok)
+    return {"metric": METRIC, "value": world * args.steps / (ms_max * 1e-3), "unit": "steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "dry_run": True, "rank_ms": ms, "scaling": "weak"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1011,9 +1053,15 @@ def main():
                     help="skip the full-1B and 7B-layer measurements reported beside the headline")
     ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync", "maskfused"], default=None,
                     help="run a small case for ncu captures instead of the benchmark")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="host-only stand-in for the GPU work (checks the launcher and the rank timing)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus))
 
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
@@ -1027,7 +1075,9 @@ def main():
     if args.profile:
         print(json.dumps(run_profile_case(args)), flush=True)
         return
-    if args.impl == "reference":
+    if args.dry_run:
+        res = run_dry(args, rank, world, dist_ok)
+    elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
         res = run_ours(args, rank, world, local_rank, dist_ok)

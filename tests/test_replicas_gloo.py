@@ -63,3 +63,20 @@ def test_single_rank_helpers_need_no_process_group():
     assert bench.gemm_flops(2048, 2048) == 2 * (2.0 * 2048 ** 3)
     # tall and wide are mirror images: 2 r L n + 2 r^3 + 2 L n r with r = min, L = max
     assert bench.gemm_flops(8192, 2048) == bench.gemm_flops(2048, 8192) == 4.0 * 8192 * 2048 ** 2 + 2.0 * 2048 ** 3
+
+
+def test_bench_gpus_flag_launches_the_ranks_itself():
+    """`bench.py --gpus 2` run as a single process starts two ranks over gloo;
+    rank 0 alone prints the line, with n_gpus = 2 and the slower rank's time
+    (rank 1 works 30 ms, rank 0 20 ms, in the host-only stand-in)."""
+    import json
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run",
+                          "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=180,
+                         env={k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK")})
+    assert res.returncode == 0, res.stderr
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["dry_run"]
+    assert out["ms_per_step"] * out["steps"] >= 30.0
+    assert out["value"] == pytest.approx(2 * out["steps"] / (out["ms_per_step"] * out["steps"] * 1e-3))
