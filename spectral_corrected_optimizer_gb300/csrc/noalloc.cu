@@ -19,7 +19,15 @@
 // Host code cannot use the array's name as a device address, so the first call
 // on each device looks the address up with cudaGetSymbolAddress (with that
 // device current) and caches it; that first call should therefore come before
-// any stream capture.
+// any stream capture.  The cached address belongs to the device's primary
+// context: after cudaDeviceReset (or any other teardown of that context) it
+// is stale, and this entry point must not be called again in that process.
+//
+// The products follow the projection equation's literal order (U^T G first,
+// then V, then U and V^T again), not the projector association that
+// specoptim_step runs; with SPECOPTIM_PREC_TF32 every operand is rounded to
+// TF32 (nearest) before it reaches the tensor cores, U and V included, as in
+// the step.
 #include <mutex>
 #include <string>
 
@@ -88,9 +96,10 @@ extern "C" int specoptim_filter_noalloc(const float *U, const float *V, const fl
         return fail(SPECOPTIM_ERR_MISALIGNED, "filter_noalloc: U, V, G, G_filt must be 16-byte aligned");
     const bool tall = m > n;
     const size_t r = (size_t)(tall ? n : m);
-    const size_t need = tall ? round_up64((size_t)n * m) + round_up64(r * m) + round_up64(r * n) +
+    // tall: G^T, U^T, U, V^T, V, T1, Xf; otherwise U^T, U, V^T, V, T^T, Xf^T
+    const size_t need = tall ? round_up64((size_t)n * m) + 2 * round_up64(r * m) + 2 * round_up64(r * n) +
                                    round_up64(r * n) + round_up64(r * r)
-                             : round_up64(r * m) + round_up64(r * n) + round_up64(r * m) +
+                             : 2 * round_up64(r * m) + 2 * round_up64(r * n) + round_up64(r * m) +
                                    round_up64(r * r);
     if (need > kScratchFloats)
         return fail(SPECOPTIM_ERR_INVALID_ARG,
@@ -119,12 +128,19 @@ extern "C" int specoptim_filter_noalloc(const float *U, const float *V, const fl
         p += round_up64(count);
         return q;
     };
+    // U^T and V^T (rounded on the way), and U, V back from them: the operands of
+    // the last two products then carry the same rounding as the first two
+    float *UT = take(r * m), *Ur = take(r * m), *VT = take(r * n), *Vr = take(r * n);
+    if ((rc = transpose_run(U, UT, m, (int)r, round, st))) return rc;
+    if ((rc = transpose_run(V, VT, n, (int)r, round, st))) return rc;
+    if ((rc = transpose_run(UT, Ur, (int)r, m, false, st))) return rc;
+    if ((rc = transpose_run(VT, Vr, (int)r, n, false, st))) return rc;
+    U = Ur;
+    V = Vr;
     if (tall) {  // T1 = U^T G, Xf = (T1 V) o dd^T, Z^T = V Xf^T, G_filt = U Z
-        float *GT = take((size_t)n * m), *UT = take(r * m), *VT = take(r * n);
+        float *GT = take((size_t)n * m);
         float *T1 = take(r * n), *Xf = take(r * r), *ZT = T1;
         if ((rc = transpose_run(G, GT, m, n, round, st))) return rc;
-        if ((rc = transpose_run(U, UT, m, (int)r, round, st))) return rc;
-        if ((rc = transpose_run(V, VT, n, (int)r, round, st))) return rc;
         plain.C = T1;
         plain.ldc = n;
         if ((rc = gemm_dispatch(precision, r, n, m, UT, m, GT, m, plain, st))) return rc;
@@ -137,9 +153,7 @@ extern "C" int specoptim_filter_noalloc(const float *U, const float *V, const fl
         return gemm_dispatch(precision, m, n, r, U, r, ZT, r, out, st);
     }
     // T^T = V^T G^T, Xf^T = (T^T U) o dd^T, Y = U Xf, G_filt = Y V^T
-    float *UT = take(r * m), *VT = take(r * n), *TT = take(r * m), *XfT = take(r * r), *Y = TT;
-    if ((rc = transpose_run(U, UT, m, (int)r, round, st))) return rc;
-    if ((rc = transpose_run(V, VT, n, (int)r, round, st))) return rc;
+    float *TT = take(r * m), *XfT = take(r * r), *Y = TT;
     plain.C = TT;
     plain.ldc = m;
     if ((rc = gemm_dispatch(precision, r, m, n, VT, n, G, n, plain, st))) return rc;
