@@ -44,6 +44,7 @@ extern "C" {
 #define SPECOPTIM_ERR_NOT_CONVERGED   4 /* SVD hit svd_max_sweeps; old factors kept   */
 #define SPECOPTIM_ERR_NOT_IMPLEMENTED 5
 #define SPECOPTIM_ERR_TIMEOUT         6 /* a bounded device-side wait gave up         */
+#define SPECOPTIM_ERR_BOUNDS          7 /* an index check failed (checked build only) */
 
 /* GEMM arithmetic of the projection (key design 3, projection equation) */
 #define SPECOPTIM_PREC_TF32 0  /* tcgen05 kind::tf32 tensor cores, fp32 accumulate */
@@ -94,7 +95,9 @@ int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void *stream);
  * side (fp32) by block Jacobi, re-orthonormalised by Newton-Schulz; then
  * s_i = |M v_i| and the long-side factor M V / s (or M^T U / s).  Columns
  * with s_i = 0 are left zero (their d_i is 0).
- * Synchronises `stream` once per Jacobi sweep to test convergence.
+ * The calling thread waits once per Jacobi sweep for its convergence test (an
+ * event on the library's streams, not a synchronisation of `stream`); the
+ * call returns with the factor recovery queued on `stream`.
  * sweeps_out (host pointer, may be NULL) receives the number of sweeps.
  * Returns SPECOPTIM_ERR_NOT_CONVERGED, keeping the previous factors, if the
  * off-diagonal norm is still above svd_tol after svd_max_sweeps sweeps. */
@@ -112,6 +115,30 @@ int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out);
 int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
                                int32_t *sweeps_out);
 
+/* The same batched refresh, split so that it runs beside the steps instead of
+ * in front of them -- the anchor of key design 2 is asynchronous: its
+ * momentum is decomposed off the fast replicas' critical path, and its
+ * factors take effect once they are ready.
+ *   begin: enqueues the Gram matrices and the Jacobi sweeps of the handles'
+ *     current anchor momenta on two streams of the library's own (ordered
+ *     after the work already on `stream`), and returns at once: a library
+ *     thread runs the sweep loop and waits on each sweep's convergence test,
+ *     so the calling thread never blocks.
+ *   end: waits (on the host) until that loop has finished -- the GPU keeps
+ *     running whatever the caller queued meanwhile -- then enqueues on
+ *     `stream` the factor recovery (s, d, U, V) and the step's operand copies
+ *     and projectors.  sweeps_out and the return value are those of
+ *     specoptim_svd_refresh_many.
+ * Steps of these handles enqueued between begin and end use the previous
+ * factors; steps enqueued after end use the new ones, so the results do not
+ * depend on timing.  end takes the same handles in the same order as begin.
+ * Between the two calls anchor_update, set_state, svd_refresh(_many), begin
+ * and destroy on these handles return SPECOPTIM_ERR_INVALID_ARG, and only one
+ * refresh (of any form) may be in progress per process. */
+int specoptim_svd_refresh_begin(specoptim_t *const *handles, int32_t count, void *stream);
+int specoptim_svd_refresh_end(specoptim_t *const *handles, int32_t count, void *stream,
+                              int32_t *sweeps_out);
+
 /* Spectral-corrected step, key design 3 (projection and blend equations)
  * followed by AdamW:
  *   X = U^T G V,  X_filt = diag(d) X diag(d),  G_filt = U X_filt V^T,
@@ -122,9 +149,14 @@ int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void 
  * W: device m x n, updated in place.  G_mask: device m x n, read only.
  * lr: this step's learning rate (a schedule stays on the host).
  * G_filt_out, G_proj_out: optional device m x n outputs (NULL to skip).
- * The four products are evaluated in the cheaper association for the shape
- * (U^T G first when m >= n, G V first when m < n); the blend and the AdamW
- * update run in the epilogue of the last product. */
+ * G_filt is evaluated as P_L G P_R with the projectors P_L = U diag(d) U^T
+ * and P_R = V diag(d) V^T (the same matrix, reassociated), formed at each
+ * refresh for the side that needs one: m = n runs P_R G^T, then P_L T (two
+ * products); m > n runs U^T G, then P_R (U^T G)^T diag(d), then U T2 (three);
+ * m < n runs V^T G^T, then P_L (.) diag(d), then T2 V^T (three).  With
+ * SPECOPTIM_PREC_TF32 the factors, the projectors and every intermediate are
+ * rounded to TF32 (nearest); G enters the products as given.  The blend and
+ * the AdamW update run in the epilogue of the last product. */
 int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr, void *stream,
                    float *G_filt_out, float *G_proj_out);
 
@@ -178,17 +210,26 @@ int specoptim_gemm_nt(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
  * memory through its own pool, or on a latency-critical path where the device
  * synchronisation of cudaMalloc / cudaFree is not acceptable.
  *   G_filt = U diag(d) U^T G V diag(d) V^T
- * U (m x r), V (n x r), d (r), G (m x n), G_filt (m x n, written) with
- * r = min(m, n): device pointers, fp32 row-major, U, V, G, G_filt 16-byte
- * aligned; precision SPECOPTIM_PREC_TF32 or SPECOPTIM_PREC_FP32 as in
- * specoptim_step (same association and rounding).
+ * U (m x r), V (n x r), d (r floats: exactly min(m, n) values, as
+ * specoptim_get_factors returns them), G (m x n), G_filt (m x n, written)
+ * with r = min(m, n): device pointers, fp32 row-major, U, V, G, G_filt
+ * 16-byte aligned (d needs no alignment).  The products run in the literal
+ * order of the projection equation (U^T G, then V, then U and V^T again),
+ * not in specoptim_step's projector association, so the two agree to the
+ * rounding of the products, not bit for bit.  precision SPECOPTIM_PREC_TF32
+ * rounds U, V and every intermediate to TF32 (nearest) before the tensor
+ * cores read them (G enters as given); SPECOPTIM_PREC_FP32 runs fp32 SIMT
+ * products.
  * Intermediates live in one 16 MiB file-scope device array that every GPU
  * loading the library holds until exit; shapes whose intermediates do not fit
- * (about r * (2 max(m,n) + 2 r) floats, plus m n when m > n) are rejected with
- * SPECOPTIM_ERR_INVALID_ARG.  All calls share the array: calls that overlap on
- * the GPU race and give wrong results.  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress) and should come before
- * any stream capture. */
+ * (2 r (m + n) + r (m + r) floats when m <= n, m n + 2 r (m + n) + r (n + r)
+ * when m > n; e.g. 512 x 2048 and 2048 x 512 fit, 2048 x 2048 does not) are
+ * rejected with SPECOPTIM_ERR_INVALID_ARG.  All calls share the array: calls
+ * that overlap on the GPU race and give wrong results.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and should
+ * come before any stream capture; the address is that of the device's primary
+ * context, so after cudaDeviceReset this entry point must not be called again
+ * in the process. */
 int specoptim_filter_noalloc(const float *U, const float *V, const float *d, const float *G,
                              float *G_filt, int32_t m, int32_t n, int32_t precision, void *stream);
 
@@ -220,7 +261,10 @@ int specoptim_selftest_wait_timeout(uint32_t spin_limit, void *stream);
  * of the library's kernels (the asynchronous calls of this header, of
  * mask_fused.h and of dpsync.h) gave up since the last check:
  * SPECOPTIM_ERR_TIMEOUT (the flag is cleared; the results of the kernels
- * launched since the last check are not to be trusted) or SPECOPTIM_OK. */
+ * launched since the last check are not to be trusted) or SPECOPTIM_OK.
+ * A library built with -DSPECOPTIM_CHECK (a test build) also verifies, in the
+ * mask kernels, that every kept index is below H; a failure skips the access
+ * and is reported here as SPECOPTIM_ERR_BOUNDS. */
 int specoptim_check_device(void *stream);
 
 /* Message of the last failed call on this thread ("" if none). */

@@ -20,11 +20,11 @@ from . import build as _build
 
 LIB_PATH = _build.LIB
 
-OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_CUDA, ERR_NOT_CONVERGED, ERR_NOT_IMPLEMENTED, ERR_TIMEOUT = range(7)
+OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_CUDA, ERR_NOT_CONVERGED, ERR_NOT_IMPLEMENTED, ERR_TIMEOUT, ERR_BOUNDS = range(8)
 PREC_TF32, PREC_FP32 = 0, 1
 
 _STATUS = {1: "invalid argument", 2: "misaligned pointer", 3: "CUDA error", 4: "SVD not converged",
-           5: "not implemented", 6: "device-side wait timed out"}
+           5: "not implemented", 6: "device-side wait timed out", 7: "index check failed (checked build)"}
 
 
 class SpecOptimError(RuntimeError):
@@ -62,6 +62,8 @@ SIGNATURES = [
     ("specoptim_anchor_update", _int, [_vp, _vp, _vp]),
     ("specoptim_svd_refresh", _int, [_vp, _vp, ctypes.POINTER(_i32)]),
     ("specoptim_svd_refresh_many", _int, [ctypes.POINTER(_vp), _i32, _vp, ctypes.POINTER(_i32)]),
+    ("specoptim_svd_refresh_begin", _int, [ctypes.POINTER(_vp), _i32, _vp]),
+    ("specoptim_svd_refresh_end", _int, [ctypes.POINTER(_vp), _i32, _vp, ctypes.POINTER(_i32)]),
     ("specoptim_step", _int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp]),
     ("specoptim_step_many", _int, [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _f32, _vp]),
     ("specoptim_get_factors", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
@@ -102,19 +104,25 @@ SIGNATURES = [
 _lib = None
 
 
+def load(path: str):
+    """Loads a build of the library from `path` with the C-ABI's signatures set
+    (lib() uses it for the library itself; tests use it for the checked build)."""
+    if not os.path.exists(path):
+        raise ImportError("libspecoptim.so is not built (%s); run "
+                          "spectral_corrected_optimizer_gb300.build.build()" % path)
+    handle = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        f = getattr(handle, name)
+        f.restype = res
+        f.argtypes = args
+    return handle
+
+
 def lib():
     """The loaded library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise ImportError("libspecoptim.so is not built (%s); run "
-                              "spectral_corrected_optimizer_gb300.build.build()" % LIB_PATH)
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, res, args in SIGNATURES:
-            f = getattr(handle, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = handle
+        _lib = load(LIB_PATH)
     return _lib
 
 
@@ -234,6 +242,23 @@ def svd_refresh_many(optimizers, stream=None):
     arr = (ctypes.c_void_p * n)(*[o._h.value for o in optimizers])
     sweeps = (ctypes.c_int32 * n)()
     _check(lib().specoptim_svd_refresh_many(arr, n, _stream(stream), sweeps), "specoptim_svd_refresh_many")
+    return list(sweeps)
+
+
+def svd_refresh_begin(optimizers, stream=None):
+    """Starts a batched SVD refresh that runs beside later work (returns at once);
+    steps enqueued before svd_refresh_end use the previous factors."""
+    n = len(optimizers)
+    arr = (ctypes.c_void_p * n)(*[o._h.value for o in optimizers])
+    _check(lib().specoptim_svd_refresh_begin(arr, n, _stream(stream)), "specoptim_svd_refresh_begin")
+
+
+def svd_refresh_end(optimizers, stream=None):
+    """Completes the refresh begun on the same optimizers (same order); returns the sweeps."""
+    n = len(optimizers)
+    arr = (ctypes.c_void_p * n)(*[o._h.value for o in optimizers])
+    sweeps = (ctypes.c_int32 * n)()
+    _check(lib().specoptim_svd_refresh_end(arr, n, _stream(stream), sweeps), "specoptim_svd_refresh_end")
     return list(sweeps)
 
 

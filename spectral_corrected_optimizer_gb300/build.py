@@ -4,6 +4,11 @@ nvcc compiles every csrc/*.cu for sm_103a only, in parallel, and links one
 shared library with the CUDA runtime linked statically, so the library needs
 no libcudart at load time.  Rebuilds only when a source is newer than the
 library.
+
+build(check=True) makes the checked test build instead
+(_build_check/libspecoptim_check.so, -DSPECOPTIM_CHECK): the same library
+whose mask kernels verify every kept index against H and report a failure
+through specoptim_check_device.
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libspecoptim.so")
+OUT_CHECK = os.path.join(HERE, "_build_check")
+LIB_CHECK = os.path.join(OUT_CHECK, "libspecoptim_check.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,23 +48,26 @@ def _deps():
         os.path.join(INCLUDE, "mask_fused.h")]
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(check: bool = False) -> bool:
+    lib = LIB_CHECK if check else LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, check: bool = False) -> str:
+    out_dir, lib = (OUT_CHECK, LIB_CHECK) if check else (OUT, LIB)
+    if not force and not needs_build(check):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
+    extra = ["-DSPECOPTIM_CHECK"] if check else []
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,12 +77,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

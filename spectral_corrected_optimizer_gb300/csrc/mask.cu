@@ -101,7 +101,7 @@ pack_bulk_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t nc
         T *out = reinterpret_cast<T *>(smem + L.out + (it % kOutBufs) * L.out_stride);
         if (ok) ok = mbar_wait_bounded(&bar[stage], parity, flag, 1u);
         if (ok)
-            for (int k = lane; k < K; k += 32) out[warp * K + k] = src[kept_dim(key, ps, (uint32_t)k)];
+            for (int k = lane; k < K; k += 32) out[warp * K + k] = src[kept_index(key, ps, (uint32_t)k, flag, 1u)];
         fence_proxy_async_smem();
         ok = __syncthreads_and(ok) != 0;  // row gathers done; block control flow stays uniform
         if (!ok) break;
@@ -167,7 +167,7 @@ unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t 
         if (ok) {
             const T *src = reinterpret_cast<const T *>(smem + L.in + stage * L.in_stride) + (size_t)warp * K;
             T *dst = reinterpret_cast<T *>(row);
-            for (int k = lane; k < K; k += 32) dst[kept_dim(key, ps, (uint32_t)k)] = src[k];
+            for (int k = lane; k < K; k += 32) dst[kept_index(key, ps, (uint32_t)k, flag, 2u)] = src[k];
         }
         fence_proxy_async_smem();
         ok = __syncthreads_and(ok) != 0;
@@ -191,36 +191,37 @@ unpack_bulk_kernel(const T *__restrict__ packed, T *__restrict__ dense, int64_t 
 
 template <typename T>
 __global__ void pack_rows_kernel(const T *__restrict__ dense, T *__restrict__ packed, int64_t row0,
-                                 int64_t rows, int H, int K, uint64_t seed) {
+                                 int64_t rows, int H, int K, uint64_t seed, unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     for (int64_t r = row0 + blockIdx.x; r < rows; r += gridDim.x) {
         RowKeys key = row_keys(seed, (uint64_t)r);
         for (int k = threadIdx.x; k < K; k += blockDim.x)
-            packed[r * K + k] = dense[r * H + kept_dim(key, ps, (uint32_t)k)];
+            packed[r * K + k] = dense[r * H + kept_index(key, ps, (uint32_t)k, flag, 3u)];
     }
 }
 
 template <typename T>
 __global__ void unpack_rows_kernel(const T *__restrict__ packed, T *__restrict__ dense,
-                                   int64_t row0, int64_t rows, int H, int K, uint64_t seed) {
+                                   int64_t row0, int64_t rows, int H, int K, uint64_t seed,
+                                   unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     for (int64_t r = row0 + blockIdx.x; r < rows; r += gridDim.x) {
         for (int j = threadIdx.x; j < H; j += blockDim.x) dense[r * H + j] = T(0);
         __syncthreads();
         RowKeys key = row_keys(seed, (uint64_t)r);
         for (int k = threadIdx.x; k < K; k += blockDim.x)
-            dense[r * H + kept_dim(key, ps, (uint32_t)k)] = packed[r * K + k];
+            dense[r * H + kept_index(key, ps, (uint32_t)k, flag, 4u)] = packed[r * K + k];
         __syncthreads();
     }
 }
 
 __global__ void indices_kernel(int32_t *__restrict__ idx, int64_t rows, int H, int K,
-                               uint64_t seed) {
+                               uint64_t seed, unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         RowKeys key = row_keys(seed, (uint64_t)r);
         for (int k = threadIdx.x; k < K; k += blockDim.x)
-            idx[r * K + k] = (int32_t)kept_dim(key, ps, (uint32_t)k);
+            idx[r * K + k] = (int32_t)kept_index(key, ps, (uint32_t)k, flag, 5u);
     }
 }
 
@@ -273,7 +274,8 @@ int run_pack(const void *dense, void *packed, int64_t rows, int H, int K, uint64
     }
     int64_t row0 = nfull * CH;
     if (row0 < rows) {
-        SPCO_LAUNCH("mask_pack_rows", st, pack_rows_kernel<T><<<row_grid(rows - row0), 128, 0, st>>>(d, p, row0, rows, H, K, seed));
+        SPCO_LAUNCH("mask_pack_rows", st, pack_rows_kernel<T><<<row_grid(rows - row0), 128, 0, st>>>(d, p, row0, rows, H, K, seed,
+                                                                             device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_pack row kernel");
     }
     return SPECOPTIM_OK;
@@ -298,7 +300,8 @@ int run_unpack(const void *packed, void *dense, int64_t rows, int H, int K, uint
     }
     int64_t row0 = nfull * CH;
     if (row0 < rows) {
-        SPCO_LAUNCH("mask_unpack_rows", st, unpack_rows_kernel<T><<<row_grid(rows - row0), 256, 0, st>>>(p, d, row0, rows, H, K, seed));
+        SPCO_LAUNCH("mask_unpack_rows", st, unpack_rows_kernel<T><<<row_grid(rows - row0), 256, 0, st>>>(p, d, row0, rows, H, K, seed,
+                                                                                 device_flag_ptr()));
         SPECOPTIM_LAUNCHED("mask_unpack row kernel");
     }
     return SPECOPTIM_OK;
@@ -358,7 +361,7 @@ extern "C" int mask_indices(int32_t *idx_out, int64_t rows, int32_t H, int32_t K
     if (!idx_out) return fail(SPECOPTIM_ERR_INVALID_ARG, "mask_indices: null pointer");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     SPCO_LAUNCH("mask_indices", st, indices_kernel<<<row_grid(rows), 128, 0, st>>>(idx_out, rows, H, K,
-                                                   mask_seed(layer, step, batch_id)));
+                                                   mask_seed(layer, step, batch_id), device_flag_ptr()));
     SPECOPTIM_LAUNCHED("mask_indices kernel");
     return SPECOPTIM_OK;
 }

@@ -48,7 +48,7 @@ constexpr int kBatch = 8;
 
 __global__ void __launch_bounds__(kThreadsF) pack_add_kernel(const uint16_t *__restrict__ a, const uint16_t *__restrict__ b,
                                                            uint16_t *__restrict__ packed, int64_t rows, int H,
-                                                           int K, uint64_t seed) {
+                                                           int K, uint64_t seed, unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     const int lane = threadIdx.x & 31;
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * kWarps) {
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreadsF) pack_add_kernel(const uint16_t *__r
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int k = k0 + 32 * u + lane;
-                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+                j[u] = k < K ? kept_index(key, ps, (uint32_t)k, flag, 6u) : 0u;
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kThreadsF) unpack_rmsnorm_kernel(const uint16_
                                                                  const uint16_t *__restrict__ gamma, float eps,
                                                                  uint16_t *__restrict__ h_out,
                                                                  uint16_t *__restrict__ x_out, int64_t rows,
-                                                                 int H, int K, uint64_t seed, int warps) {
+                                                                 int H, int K, uint64_t seed, int warps,
+                                                                 unsigned *flag) {
     extern __shared__ __align__(16) uint16_t rowbuf[];  // per warp: h row, x row (H + pad each)
     const PermShape ps = perm_shape((uint32_t)H);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kThreadsF) unpack_rmsnorm_kernel(const uint16_
         __syncwarp();
         const RowKeys key = row_keys(seed, (uint64_t)r);
         for (int k = lane; k < K; k += 32) {
-            const uint32_t j = kept_dim(key, ps, (uint32_t)k);
+            const uint32_t j = kept_index(key, ps, (uint32_t)k, flag, 7u);
             const uint16_t p = __ldg(pr + k);
             hb[j] = p;
             xb[j] = bf16_rne(bf16_val(p) * rinv * bf16_val(__ldg(gamma + j)));
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
                                                                    const uint16_t *__restrict__ dx,
                                                                    const uint16_t *__restrict__ g_res,
                                                                    uint16_t *__restrict__ out, int64_t rows, int H,
-                                                                   int K, uint64_t seed) {
+                                                                   int K, uint64_t seed, unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     const int lane = threadIdx.x & 31;
     const float inv_h = 1.f / (float)H;
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int k = 32 * u + lane;
-                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+                j[u] = k < K ? kept_index(key, ps, (uint32_t)k, flag, 8u) : 0u;
             }
             float ss = 0.f, s = 0.f;
 #pragma unroll
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int k = k0 + 32 * u + lane;
-                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+                j[u] = k < K ? kept_index(key, ps, (uint32_t)k, flag, 8u) : 0u;
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int k = k0 + 32 * u + lane;
-                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+                j[u] = k < K ? kept_index(key, ps, (uint32_t)k, flag, 8u) : 0u;
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsF) rmsnorm_bwd_pack_kernel(const uint1
 }
 
 __global__ void __launch_bounds__(kThreadsF) unpack_add_kernel(const uint16_t *__restrict__ packed, uint16_t *__restrict__ g,
-                                                             int64_t rows, int H, int K, uint64_t seed) {
+                                                             int64_t rows, int H, int K, uint64_t seed, unsigned *flag) {
     const PermShape ps = perm_shape((uint32_t)H);
     const int lane = threadIdx.x & 31;
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * kWarps) {
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kThreadsF) unpack_add_kernel(const uint16_t *_
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int k = k0 + 32 * u + lane;
-                j[u] = k < K ? kept_dim(key, ps, (uint32_t)k) : 0u;
+                j[u] = k < K ? kept_index(key, ps, (uint32_t)k, flag, 9u) : 0u;
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -296,7 +297,8 @@ extern "C" int mask_pack_add(const void *a, const void *b, void *packed, int64_t
     SPCO_LAUNCH("mask_pack_add", st,
                 pack_add_kernel<<<grid_rows(rows, kWarps), kThreadsF, 0, st>>>(
                     static_cast<const uint16_t *>(a), static_cast<const uint16_t *>(b),
-                    static_cast<uint16_t *>(packed), rows, H, K, mask_seed(layer, step, batch_id)));
+                    static_cast<uint16_t *>(packed), rows, H, K, mask_seed(layer, step, batch_id),
+                    device_flag_ptr()));
     SPECOPTIM_LAUNCHED("pack_add_kernel");
     return SPECOPTIM_OK;
 }
@@ -323,7 +325,7 @@ extern "C" int mask_unpack_rmsnorm(const void *packed, const void *gamma, float 
                 unpack_rmsnorm_kernel<<<grid_rows(rows, warps), kThreadsF, smem, st>>>(
                     static_cast<const uint16_t *>(packed), static_cast<const uint16_t *>(gamma), eps,
                     static_cast<uint16_t *>(h_out), static_cast<uint16_t *>(x_out), rows, H, K,
-                    mask_seed(layer, step, batch_id), warps));
+                    mask_seed(layer, step, batch_id), warps, device_flag_ptr()));
     SPECOPTIM_LAUNCHED("unpack_rmsnorm_kernel");
     return SPECOPTIM_OK;
 }
@@ -345,7 +347,8 @@ extern "C" int mask_rmsnorm_backward_pack(const void *packed_h, const void *gamm
                 rmsnorm_bwd_pack_kernel<<<grid_rows(rows, kWarps), kThreadsF, 0, st>>>(
                     static_cast<const uint16_t *>(packed_h), static_cast<const uint16_t *>(gamma), eps,
                     static_cast<const uint16_t *>(dx), static_cast<const uint16_t *>(g_res),
-                    static_cast<uint16_t *>(packed_grad), rows, H, K, mask_seed(layer, step, batch_id)));
+                    static_cast<uint16_t *>(packed_grad), rows, H, K, mask_seed(layer, step, batch_id),
+                    device_flag_ptr()));
     SPECOPTIM_LAUNCHED("rmsnorm_bwd_pack_kernel");
     return SPECOPTIM_OK;
 }
@@ -363,7 +366,7 @@ extern "C" int mask_unpack_add(const void *packed, void *g, int64_t rows, int32_
     SPCO_LAUNCH("mask_unpack_add", st,
                 unpack_add_kernel<<<grid_rows(rows, kWarps), kThreadsF, 0, st>>>(
                     static_cast<const uint16_t *>(packed), static_cast<uint16_t *>(g), rows, H, K,
-                    mask_seed(layer, step, batch_id)));
+                    mask_seed(layer, step, batch_id), device_flag_ptr()));
     SPECOPTIM_LAUNCHED("unpack_add_kernel");
     return SPECOPTIM_OK;
 }

@@ -79,6 +79,30 @@ __device__ __forceinline__ uint32_t kept_dim(const RowKeys &key, const PermShape
     return x;
 }
 
+// Flag value of a failed index check in the checked build (bit 31 set, the
+// check's site number in the low bits).
+constexpr unsigned kBoundsFlag = 0x80000000u;
+
+// kept_dim as an index into a row of H values.  The checked build
+// (-DSPECOPTIM_CHECK, for tests) verifies j < H -- the permutation's output
+// after cycle walking -- records a failure in *flag with its site number and
+// returns 0 instead, so the access it feeds stays inside the row; the normal
+// build returns kept_dim unchanged.
+__device__ __forceinline__ uint32_t kept_index(const RowKeys &key, const PermShape &ps, uint32_t k,
+                                               unsigned *flag, unsigned site) {
+    const uint32_t j = kept_dim(key, ps, k);
+#ifdef SPECOPTIM_CHECK
+    if (j >= ps.H) {
+        if (flag) atomicCAS(flag, 0u, kBoundsFlag | site);
+        return 0u;
+    }
+#else
+    (void)flag;
+    (void)site;
+#endif
+    return j;
+}
+
 // seed of one (layer, step, batch) boundary
 __host__ __device__ inline uint64_t mask_seed(uint32_t layer, uint64_t step, uint64_t batch_id) {
     return splitmix_out(splitmix_out(splitmix_out((uint64_t)layer) ^ step) ^ batch_id);

@@ -41,6 +41,16 @@ struct specoptim {
     float *ws_g, *ws_a, *ws_x;   // step workspace: G^T (tall), T1/Z^T or T^T/Y, Xf
     float *ws_svd;
     bool have_factors;
+    struct PendingRefresh *pending;  // refresh begun and not yet ended (svd_refresh_begin / _end)
+};
+
+// A refresh between specoptim_svd_refresh_begin and _end: its handles in call
+// order, their jobs and the run of svd.cu.
+struct PendingRefresh {
+    int count;
+    specoptim_t *h[16];
+    spco::SvdJob jobs[16];
+    spco::SvdRun *run;
 };
 
 namespace spco {
@@ -73,6 +83,9 @@ int check_device_flag(cudaStream_t st) {
         unsigned zero = 0;
         cudaMemcpyAsync(p, &zero, sizeof(zero), cudaMemcpyHostToDevice, st);
         cudaStreamSynchronize(st);
+        if (v & 0x80000000u)  // only the checked build (-DSPECOPTIM_CHECK) sets bit 31
+            return fail(SPECOPTIM_ERR_BOUNDS, "an index check of the checked build failed (site " +
+                                                  std::to_string(v & 0x7FFFFFFFu) + ")");
         return fail(SPECOPTIM_ERR_TIMEOUT, "a bounded device-side wait gave up (code " +
                                                std::to_string(v) + ")");
     }
@@ -185,6 +198,9 @@ extern "C" int specoptim_create(specoptim_t **out, const specoptim_config *cfg, 
 extern "C" int specoptim_destroy(specoptim_t *h) {
     clear_error();
     if (!h) return SPECOPTIM_OK;
+    if (h->pending)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "destroy: an SVD refresh of this handle is in progress "
+                                               "(end it with specoptim_svd_refresh_end first)");
     cudaDeviceSynchronize();
     free_all(h);
     delete h;
@@ -195,6 +211,9 @@ extern "C" int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void 
     clear_error();
     if (!h || !G_anc) return fail(SPECOPTIM_ERR_INVALID_ARG, "anchor_update: null argument");
     if (!aligned16(G_anc)) return fail(SPECOPTIM_ERR_MISALIGNED, "anchor_update: G_anc not 16-byte aligned");
+    if (h->pending)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "anchor_update: the anchor momentum is being decomposed "
+                                               "(call specoptim_svd_refresh_end first)");
     return ema_run(h->M, G_anc, (int64_t)h->m * h->n, h->cfg.beta_anc,
                    static_cast<cudaStream_t>(stream));
 }
@@ -219,18 +238,21 @@ int form_projector(const float *X, const float *d, int rows, int r, float *P, fl
 
 }  // namespace
 
-extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
-                                          int32_t *sweeps_out) {
-    clear_error();
+namespace {
+
+int check_handles(specoptim_t *const *handles, int32_t count, const char *what) {
     if (!handles || count < 1 || count > 16)
-        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: 1 to 16 handles");
+        return fail(SPECOPTIM_ERR_INVALID_ARG, std::string(what) + ": 1 to 16 handles");
     for (int i = 0; i < count; ++i) {
-        if (!handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: null handle");
+        if (!handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, std::string(what) + ": null handle");
         for (int k = 0; k < i; ++k)
-            if (handles[k] == handles[i]) return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: repeated handle");
+            if (handles[k] == handles[i])
+                return fail(SPECOPTIM_ERR_INVALID_ARG, std::string(what) + ": repeated handle");
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SvdJob jobs[16];
+    return SPECOPTIM_OK;
+}
+
+void fill_jobs(specoptim_t *const *handles, int32_t count, SvdJob *jobs) {
     for (int i = 0; i < count; ++i) {
         specoptim_t *h = handles[i];
         SvdJob &a = jobs[i];
@@ -247,8 +269,15 @@ extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t c
         a.tol = h->cfg.svd_tol;
         a.max_sweeps = h->cfg.svd_max_sweeps;
         a.inner_sweeps = h->cfg.svd_inner_sweeps;
+        a.sweeps = 0;
+        a.status = SPECOPTIM_OK;
     }
-    int rc = svd_refresh_batch(jobs, count, st);
+}
+
+// After the factors of a refresh are written (svd_refresh_complete returned
+// rc): the step's operand copies and projector of every converged handle.
+int install_factors(specoptim_t *const *handles, int32_t count, const SvdJob *jobs, int rc,
+                    cudaStream_t st, int32_t *sweeps_out) {
     if (sweeps_out)
         for (int i = 0; i < count; ++i) sweeps_out[i] = jobs[i].sweeps;
     if (rc && rc != SPECOPTIM_ERR_NOT_CONVERGED) return rc;
@@ -271,6 +300,62 @@ extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t c
     if (r3) return r3;
     if (rc) return fail(rc, err);
     return SPECOPTIM_OK;
+}
+
+}  // namespace
+
+extern "C" int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void *stream,
+                                          int32_t *sweeps_out) {
+    clear_error();
+    int rc = check_handles(handles, count, "svd_refresh_many");
+    if (rc) return rc;
+    for (int i = 0; i < count; ++i)
+        if (handles[i]->pending)
+            return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_many: a refresh of this handle is in progress");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SvdJob jobs[16];
+    fill_jobs(handles, count, jobs);
+    rc = svd_refresh_batch(jobs, count, st);
+    return install_factors(handles, count, jobs, rc, st, sweeps_out);
+}
+
+extern "C" int specoptim_svd_refresh_begin(specoptim_t *const *handles, int32_t count, void *stream) {
+    clear_error();
+    int rc = check_handles(handles, count, "svd_refresh_begin");
+    if (rc) return rc;
+    for (int i = 0; i < count; ++i)
+        if (handles[i]->pending)
+            return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_begin: a refresh of this handle is in progress");
+    PendingRefresh *P = new PendingRefresh();
+    P->count = count;
+    for (int i = 0; i < count; ++i) P->h[i] = handles[i];
+    fill_jobs(handles, count, P->jobs);
+    if ((rc = svd_refresh_start(P->jobs, count, static_cast<cudaStream_t>(stream), true, &P->run))) {
+        delete P;
+        return rc;
+    }
+    for (int i = 0; i < count; ++i) handles[i]->pending = P;
+    return SPECOPTIM_OK;
+}
+
+extern "C" int specoptim_svd_refresh_end(specoptim_t *const *handles, int32_t count, void *stream,
+                                         int32_t *sweeps_out) {
+    clear_error();
+    int rc = check_handles(handles, count, "svd_refresh_end");
+    if (rc) return rc;
+    PendingRefresh *P = handles[0]->pending;
+    bool same = P && P->count == count;
+    for (int i = 0; same && i < count; ++i) same = P->h[i] == handles[i];
+    if (!same)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh_end: the handles are not those of a refresh begun "
+                                               "with specoptim_svd_refresh_begin (same handles, same order)");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = svd_refresh_complete(P->run, P->jobs, st);
+    for (int i = 0; i < count; ++i) handles[i]->pending = nullptr;
+    SvdJob jobs[16];
+    std::memcpy(jobs, P->jobs, sizeof(SvdJob) * count);
+    delete P;
+    return install_factors(handles, count, jobs, rc, st, sweeps_out);
 }
 
 extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *sweeps_out) {
@@ -477,6 +562,9 @@ extern "C" int specoptim_set_state(specoptim_t *h, const float *M, const float *
     clear_error();
     if (!h || !M || !exp_avg || !exp_avg_sq || t < 0)
         return fail(SPECOPTIM_ERR_INVALID_ARG, "set_state: null argument or t < 0");
+    if (h->pending)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "set_state: an SVD refresh of this handle is in progress "
+                                               "(call specoptim_svd_refresh_end first)");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)h->m * h->n * 4;
     SPECOPTIM_CUDA(cudaMemcpyAsync(h->M, M, bytes, cudaMemcpyDeviceToDevice, st));

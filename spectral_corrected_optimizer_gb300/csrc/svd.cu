@@ -24,8 +24,11 @@
 // (d_i ~ s_i/tau_p for the small directions, so the error of those directions
 // enters G_filt multiplied by d_i).
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
+#include <string>
+#include <thread>
 #include <vector>
 
 #include "gemm.cuh"
@@ -699,17 +702,47 @@ struct JacStreams {
     }
 };
 
-int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
-    if (count < 1 || count > kMaxBatch)
-        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: 1 to 16 matrices per batch");
+// One batched refresh in flight: its jobs, buffers and streams, and (for the
+// asynchronous form) the library thread that runs its sweep loop.
+struct SvdRun {
+    int count = 0;
+    SvdJob jobs[kMaxBatch];
     JobBufs b[kMaxBatch];
-    int rc;
-    for (int i = 0; i < count; ++i) {
-        b[i] = carve(jobs[i]);
-        jobs[i].sweeps = 0;
-        jobs[i].status = SPECOPTIM_OK;
-        if ((rc = prepare(jobs[i], b[i], st))) return rc;
+    JacStreams js;
+    cudaEvent_t done = nullptr;  // recorded on `hi` once both chains' last kernels are queued
+    std::thread worker;
+    int device = 0;
+    int rc = SPECOPTIM_OK;
+    std::string err;
+    ~SvdRun() {
+        if (done) cudaEventDestroy(done);
     }
+};
+
+namespace {
+
+std::atomic<bool> g_run_active{false};
+
+// pinned host slots for the convergence test's sums (one run at a time)
+double *host_sums() {
+    static double *p = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        if (cudaMallocHost(reinterpret_cast<void **>(&p), 2 * kMaxBatch * sizeof(double)) != cudaSuccess)
+            p = nullptr;
+    });
+    return p;
+}
+
+// Gram matrices and the Jacobi sweeps of every job, on the run's two streams.
+int sweep_loop(SvdRun &R) {
+    const int count = R.count;
+    SvdJob *jobs = R.jobs;
+    JobBufs *b = R.b;
+    cudaStream_t hi = R.js.hi, lo = R.js.lo;
+    int rc;
+    for (int i = 0; i < count; ++i)
+        if ((rc = prepare(jobs[i], b[i], hi))) return rc;
     JacBatch jb;
     std::memset(&jb, 0, sizeof(jb));
     jb.count = count;
@@ -717,7 +750,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     ApJob ajob[kMaxBatch];
     CtJob qjob[kMaxBatch];
     for (int i = 0; i < count; ++i) {
-        if ((rc = upload_maps(b[i], st))) return rc;
+        if ((rc = upload_maps(b[i], hi))) return rc;
         jb.A[i] = b[i].A;
         jb.Np[i] = b[i].Np;
         jb.active[i] = 1;
@@ -732,8 +765,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     const int solve_grid = jb.pair_off[count];
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
-    int rc2 = set_solve_attributes();
-    if (rc2) return rc2;
+    if ((rc = set_solve_attributes())) return rc;
     auto set_round = [&](long g) {
         for (int i = 0; i < count; ++i) {
             const int round = (int)(g % (b[i].nb - 1));
@@ -749,9 +781,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
     // ...; `lo`: Q <- Q R for round g, released with solve(g+1) (which does not
     // need it) so that the two share the SMs.  Rotations of round g live in
     // slot g % 2; solve(g+1) rewrites the slot of round g-1 once Q(g-1) read it.
-    JacStreams js_;
-    if ((rc2 = js_.create(st))) return rc2;
-    cudaStream_t hi = js_.hi, lo = js_.lo;
+    JacStreams &js_ = R.js;
     auto solve = [&](long gg) -> int {
         set_round(gg);
         SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, js_.q_done[gg & 1], 0));
@@ -759,26 +789,25 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
         SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
         return SPECOPTIM_OK;
     };
-    // the convergence test's sums land in pinned host memory (one small buffer per
-    // host thread, kept for the life of the process), so the copies stay
+    // the convergence test's sums land in pinned host memory, so the copies stay
     // asynchronous and the host waits on an event, not on the stream
-    static thread_local double *host = nullptr;
-    if (!host) SPECOPTIM_CUDA(cudaMallocHost(reinterpret_cast<void **>(&host), 2 * kMaxBatch * sizeof(double)));
+    double *host = host_sums();
+    if (!host) return fail(SPECOPTIM_ERR_CUDA, "svd_refresh: pinned host memory for the convergence test");
     int active = count;
     long g = 0;
-    if ((rc2 = solve(0))) return rc2;
+    if ((rc = solve(0))) return rc;
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(g);
-            if ((rc2 = jacobi_apply(ajob, count, hi))) return rc2;
+            if ((rc = jacobi_apply(ajob, count, hi))) return rc;
             SPECOPTIM_CUDA(cudaEventRecord(js_.a_done[g & 1], hi));
             SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, js_.a_done[g & 1], 0));
             // on 3/8 of the SMs: the solves take the rest, and the next round's
             // rotation of A finds SMs free sooner (measured best among 1/4 .. all)
-            if ((rc2 = jacobi_rotate(qjob, count, lo, num_sms() * 3 / 8))) return rc2;
+            if ((rc = jacobi_rotate(qjob, count, lo, num_sms() * 3 / 8))) return rc;
             SPECOPTIM_CUDA(cudaEventRecord(js_.q_done[g & 1], lo));
             // the sweep's last solve (the next sweep's first) goes after the convergence test
-            if (k + 1 < rounds && (rc2 = solve(g + 1))) return rc2;
+            if (k + 1 < rounds && (rc = solve(g + 1))) return rc;
         }
         SPECOPTIM_LAUNCHED("jacobi sweep");
         // convergence test of the active matrices: one launch, then the next
@@ -804,7 +833,7 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
                 SPECOPTIM_CUDA(cudaMemcpyAsync(&host[2 * i], b[i].norms, 2 * sizeof(double),
                                                cudaMemcpyDeviceToHost, hi));
         SPECOPTIM_CUDA(cudaEventRecord(js_.norms, hi));
-        if ((rc2 = solve(g))) return rc2;
+        if ((rc = solve(g))) return rc;
         SPECOPTIM_CUDA(cudaEventSynchronize(js_.norms));
         for (int i = 0; i < count; ++i) {
             if (!jb.active[i]) continue;
@@ -822,20 +851,113 @@ int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
             }
         }
     }
-    if ((rc2 = js_.join(st))) return rc2;
-    int first_bad = SPECOPTIM_OK;
-    for (int i = 0; i < count; ++i) {
+    for (int i = 0; i < count; ++i)
         if (jb.active[i]) jobs[i].status = SPECOPTIM_ERR_NOT_CONVERGED;
+    return SPECOPTIM_OK;
+}
+
+// the run's loop, then `done` after both chains (also after a failure, so that
+// the caller can still order its stream after whatever was queued)
+void run_loop(SvdRun *R) {
+    R->rc = sweep_loop(*R);
+    if (R->rc) R->err = specoptim_last_error();
+    if (cudaEventRecord(R->js.ev, R->js.lo) != cudaSuccess ||
+        cudaStreamWaitEvent(R->js.hi, R->js.ev, 0) != cudaSuccess ||
+        cudaEventRecord(R->done, R->js.hi) != cudaSuccess) {
+        if (!R->rc) {
+            R->rc = SPECOPTIM_ERR_CUDA;
+            R->err = "svd_refresh: recording the end of the sweeps failed";
+        }
+    }
+}
+
+}  // namespace
+
+int svd_refresh_start(const SvdJob *jobs, int count, cudaStream_t st, bool async, SvdRun **out) {
+    *out = nullptr;
+    if (count < 1 || count > kMaxBatch)
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: 1 to 16 matrices per batch");
+    bool expected = false;
+    if (!g_run_active.compare_exchange_strong(expected, true))
+        return fail(SPECOPTIM_ERR_INVALID_ARG, "svd_refresh: another refresh is in progress in this process "
+                                               "(finish it with specoptim_svd_refresh_end first)");
+    SvdRun *R = new SvdRun();
+    R->count = count;
+    int rc = SPECOPTIM_OK;
+    size_t need = 0;
+    for (int i = 0; i < count; ++i) {
+        R->jobs[i] = jobs[i];
+        R->jobs[i].sweeps = 0;
+        R->jobs[i].status = SPECOPTIM_OK;
+        R->b[i] = carve(R->jobs[i]);
+        need = std::max(need, gemm3_workspace_floats(R->b[i].r, R->b[i].r, R->b[i].L));
+    }
+    float *ws = nullptr;
+    // the Gram products' scratch is grown here, on the calling thread, so that the
+    // sweep thread never reallocates it
+    if (!rc) rc = scratch_floats(need, &ws);
+    if (!rc) rc = cudaGetDevice(&R->device) == cudaSuccess ? R->js.create(st) : fail(SPECOPTIM_ERR_CUDA, "cudaGetDevice");
+    if (!rc && cudaEventCreateWithFlags(&R->done, cudaEventDisableTiming) != cudaSuccess)
+        rc = fail(SPECOPTIM_ERR_CUDA, "svd_refresh: cudaEventCreate");
+    if (rc) {
+        delete R;
+        g_run_active.store(false);
+        return rc;
+    }
+    if (async) {
+        try {
+            R->worker = std::thread([R] {
+                if (cudaSetDevice(R->device) != cudaSuccess) {
+                    R->rc = SPECOPTIM_ERR_CUDA;
+                    R->err = "svd_refresh: cudaSetDevice on the sweep thread failed";
+                    cudaEventRecord(R->done, R->js.hi);
+                    return;
+                }
+                run_loop(R);
+            });
+        } catch (...) {
+            run_loop(R);  // no thread could be started: run the loop here
+        }
+    } else {
+        run_loop(R);
+    }
+    *out = R;
+    return SPECOPTIM_OK;
+}
+
+int svd_refresh_complete(SvdRun *R, SvdJob *jobs, cudaStream_t st) {
+    if (R->worker.joinable()) R->worker.join();
+    int rc = R->rc;
+    std::string err = R->err;
+    if (cudaStreamWaitEvent(st, R->done, 0) != cudaSuccess && !rc) {
+        rc = SPECOPTIM_ERR_CUDA;
+        err = "svd_refresh: ordering the stream after the sweeps failed";
+    }
+    const int count = R->count;
+    int first_bad = SPECOPTIM_OK;
+    for (int i = 0; i < count && !rc; ++i) {
+        jobs[i].sweeps = R->jobs[i].sweeps;
+        jobs[i].status = R->jobs[i].status;
         if (jobs[i].status != SPECOPTIM_OK) {
             if (!first_bad) first_bad = jobs[i].status;
             continue;
         }
-        if ((rc = finish(jobs[i], b[i], st))) return rc;
+        if ((rc = finish(R->jobs[i], R->b[i], st))) err = specoptim_last_error();
     }
+    delete R;  // the streams go once their queued work is done
+    g_run_active.store(false);
+    if (rc) return fail(rc, err);
     if (first_bad)
         return fail(first_bad, "svd_refresh: Jacobi did not reach svd_tol within svd_max_sweeps; "
                                "previous factors kept for the matrices concerned");
     return SPECOPTIM_OK;
+}
+
+int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t st) {
+    SvdRun *R = nullptr;
+    int rc = svd_refresh_start(jobs, count, st, false, &R);
+    if (rc) return rc;
+    return svd_refresh_complete(R, jobs, st);
 }
 
 }  // namespace spco

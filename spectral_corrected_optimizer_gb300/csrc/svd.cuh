@@ -23,4 +23,15 @@ size_t svd_workspace_floats(int m, int n);
 // Refreshes up to 16 matrices; their Jacobi rounds share kernel launches.
 int svd_refresh_batch(SvdJob *jobs, int count, cudaStream_t stream);
 
+// The same refresh in two phases.  start: the Gram matrices and the Jacobi
+// sweeps of every job on the library's own streams, ordered after the work
+// already on `stream`; with `async` a library thread runs the sweep loop (it
+// waits on each sweep's convergence test) and the call returns at once.
+// complete: waits (host) for that loop, orders `stream` after its kernels,
+// writes the factors of the converged jobs on `stream`, fills jobs[i].sweeps
+// and .status and frees the run.  One run at a time per process.
+struct SvdRun;
+int svd_refresh_start(const SvdJob *jobs, int count, cudaStream_t stream, bool async, SvdRun **out);
+int svd_refresh_complete(SvdRun *run, SvdJob *jobs, cudaStream_t stream);
+
 }  // namespace spco

@@ -120,3 +120,13 @@ def test_binding_refuses_tensors_it_cannot_pass_as_device_pointers(lib):
         so._f32_2d(torch.zeros(3, 2), (2, 3), "W")
     with pytest.raises(ValueError, match="CUDA"):
         so._f32_2d(torch.zeros(2, 3), (2, 3), "W")
+
+
+def test_refresh_begin_end_argument_errors_without_a_gpu(lib):
+    null = (ctypes.c_void_p * 1)(None)
+    assert lib.specoptim_svd_refresh_begin(None, 1, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_svd_refresh_begin(null, 1, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_svd_refresh_begin(null, 0, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_svd_refresh_end(None, 1, None, None) == so.ERR_INVALID_ARG
+    assert lib.specoptim_svd_refresh_end(null, 17, None, None) == so.ERR_INVALID_ARG
+    assert b"handle" in lib.specoptim_last_error()

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import dev, ensure_lib, host, rel
+from gpu_util import Guarded, dev, ensure_lib, host, rel
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -76,9 +76,11 @@ def test_each_call_matches_the_oracle_on_the_gpu_inputs():
         torch.cuda.synchronize()
         for i in range(len(SHAPES)):
             assert rel(host(g.Q[i]), oracle.dpsync_compress_q(Ms[i], Phs[i])) < TOL, (sync, i)
-        outs = [torch.empty(m, n, device="cuda") for m, n, _ in SHAPES]
+        guarded = [Guarded((m, n)) for m, n, _ in SHAPES]
+        outs = [x.t for x in guarded]
         g.decompress(outs, q_scale=0.5)
         torch.cuda.synchronize()
+        assert all(x.intact() for x in guarded)
         for i in range(len(SHAPES)):
             D_ref, E_ref = oracle.dpsync_decompress(Ms[i], Phs[i], host(g.Q[i]), 0.5)
             assert rel(host(outs[i]), D_ref) < TOL, (sync, i)
@@ -102,9 +104,13 @@ def test_outer_sync_chain_matches_the_oracle(mix):
     for period in range(3):
         locals_ = [thetas[i] - synthetic.dp_drift(m, n, seed=2, worker=0, period=period)
                    for i, (m, n, _) in enumerate(shapes)]
-        W = [dev(w) for w in locals_]
+        guarded = [Guarded(w.shape) for w in locals_]
+        W = [x.t for x in guarded]
+        for w, x in zip(locals_, W):
+            x.copy_(dev(w))
         g.outer_sync(W)
         torch.cuda.synchronize()
+        assert all(x.intact() for x in guarded)
         for i, (m, n, k) in enumerate(shapes):
             th_before = refs[i].theta.copy()
             W_ref = refs[i].outer_sync(locals_[i])

@@ -9,7 +9,7 @@ import torch
 import oracle
 import spectral_corrected_optimizer_gb300 as so
 import synthetic
-from gpu_util import dev, ensure_lib, host
+from gpu_util import Guarded, dev, ensure_lib, host
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,11 @@ CASES = [  # rows, H, K, layer, step, batch_id
 def test_indices_bit_exact(rows, H, K, layer, step, batch):
     got = host(so.mask_indices(rows, H, K, layer, step, batch))
     assert np.array_equal(got, oracle.mask_indices(rows, H, K, layer, step, batch))
+    out = Guarded((rows, K), torch.int32)
+    lib = so.lib()
+    assert lib.mask_indices(out.t.data_ptr(), rows, H, K, layer, step, batch,
+                            torch.cuda.current_stream().cuda_stream) == so.OK
+    assert np.array_equal(host(out.t), got) and out.intact()
 
 
 @pytest.mark.parametrize("rows,H,K,layer,step,batch", CASES)
@@ -51,12 +56,17 @@ def test_pack_and_unpack_bit_exact(rows, H, K, layer, step, batch, kind):
         h[0, :] = -0.0
         if rows > 1:
             h[1, :] = np.nan
+    dt = torch.bfloat16 if kind == "bf16" else torch.float32
     want_p = oracle.mask_pack(h, K, layer, step, batch)
-    got_p = host(so.mask_pack(dev(h), K, layer, step, batch))
-    assert np.array_equal(got_p.view(np.uint8), want_p.view(np.uint8))
+    out_p = Guarded((rows, K), dt)
+    so.mask_pack(dev(h), K, layer, step, batch, out=out_p.t)
+    assert np.array_equal(host(out_p.t).view(np.uint8), want_p.view(np.uint8))
+    assert out_p.intact()
     want_u = oracle.mask_unpack(want_p, H, layer, step, batch)
-    got_u = host(so.mask_unpack(dev(want_p), H, layer, step, batch))
-    assert np.array_equal(got_u.view(np.uint8), want_u.view(np.uint8))
+    out_u = Guarded((rows, H), dt)
+    so.mask_unpack(dev(want_p), H, layer, step, batch, out=out_u.t)
+    assert np.array_equal(host(out_u.t).view(np.uint8), want_u.view(np.uint8))
+    assert out_u.intact()
 
 
 def test_unaligned_buffers_take_the_row_path():

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import dev, ensure_lib, host
+from gpu_util import Guarded, dev, ensure_lib, host
 
 pytestmark = pytest.mark.gpu
 
@@ -48,9 +48,11 @@ def ulp_diff(a_bits, b_bits):
 @pytest.mark.parametrize("rows,H,K,layer,step", CASES)
 def test_pack_add_bit_exact(rows, H, K, layer, step):
     a, b = bf(rows, H, 1, 0), bf(rows, H, 1, 1, 0.3)
-    got = so().mask_pack_add(dev(a), dev(b), K, layer, step)
+    out = Guarded((rows, K), torch.bfloat16)
+    got = so().mask_pack_add(dev(a), dev(b), K, layer, step, out=out.t)
     torch.cuda.synchronize()
     assert np.array_equal(host(got), oracle.mask_pack_add(a, b, K, layer, step))
+    assert out.intact()
 
 
 @pytest.mark.parametrize("rows,H,K,layer,step", CASES)
@@ -58,8 +60,10 @@ def test_unpack_rmsnorm(rows, H, K, layer, step):
     packed = bf(rows, K, 2, 0) if K else np.zeros((rows, 0), np.uint16)
     gamma = bf(1, H, 2, 1, 0.5)[0]
     eps = 1e-5
-    h, x = so().mask_unpack_rmsnorm(dev(packed), dev(gamma), eps, H, layer, step)
+    hg, xg = Guarded((rows, H), torch.bfloat16), Guarded((rows, H), torch.bfloat16)
+    h, x = so().mask_unpack_rmsnorm(dev(packed), dev(gamma), eps, H, layer, step, h_out=hg.t, x_out=xg.t)
     torch.cuda.synchronize()
+    assert hg.intact() and xg.intact()
     h_ref, x_ref_bits, _ = oracle.mask_unpack_rmsnorm(packed, gamma, eps, H, layer, step)
     assert np.array_equal(host(h), h_ref)
     assert ulp_diff(host(x), x_ref_bits).max() <= 1
@@ -73,9 +77,11 @@ def test_rmsnorm_backward_pack(rows, H, K, layer, step, with_res):
     dx = bf(rows, H, 3, 2)
     g_res = bf(rows, H, 3, 3, 0.2) if with_res else None
     eps = 1e-6
+    out = Guarded((rows, K), torch.bfloat16)
     got = so().mask_rmsnorm_backward_pack(dev(packed), dev(gamma), eps, dev(dx),
-                                          None if g_res is None else dev(g_res), layer, step)
+                                          None if g_res is None else dev(g_res), layer, step, out=out.t)
     torch.cuda.synchronize()
+    assert out.intact()
     _, ref = oracle.mask_rmsnorm_backward_pack(packed, gamma, eps, dx, g_res, layer, step)
     # magnitude of the terms at each kept dim
     h = oracle.bf16_value(oracle.mask_unpack(packed, H, layer, step))
@@ -94,10 +100,13 @@ def test_rmsnorm_backward_pack(rows, H, K, layer, step, with_res):
 def test_unpack_add_bit_exact(rows, H, K, layer, step):
     packed = bf(rows, K, 4, 0) if K else np.zeros((rows, 0), np.uint16)
     g = bf(rows, H, 4, 1)
-    gd = dev(g)
+    gg = Guarded((rows, H), torch.bfloat16)
+    gd = gg.t
+    gd.copy_(dev(g))
     so().mask_unpack_add(dev(packed), gd, layer, step)
     torch.cuda.synchronize()
     assert np.array_equal(host(gd), oracle.mask_unpack_add(packed, g, layer, step))
+    assert gg.intact()
 
 
 def test_full_boundary_sampled_rows():

@@ -19,7 +19,7 @@ import torch
 import oracle
 import spectral_corrected_optimizer_gb300 as so
 import synthetic
-from gpu_util import dev, ensure_lib, host, rel
+from gpu_util import Guarded, dev, ensure_lib, host, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -45,15 +45,19 @@ def run_case(inp, prec, steps=1, lr=2e-5, refresh=True, **cfg):
         gpu.svd_refresh()
         ora.svd_refresh()
     W0 = inp.weights()
-    Wd = dev(W0)
+    Wg = Guarded((m, n))  # every output between guard bytes (written past its ends -> caught)
+    Wd = Wg.t
+    Wd.copy_(dev(W0))
     Wo = W0.astype(np.float64)
     out = []
     for t in range(steps):
         G = inp.masked_grad(t)
-        gf = torch.empty(m, n, device="cuda")
-        gp = torch.empty(m, n, device="cuda")
+        gfg, gpg = Guarded((m, n)), Guarded((m, n))
+        gf, gp = gfg.t, gpg.t
         Wprev = host(Wd).copy()
         gpu.step(Wd, dev(G), lr, gf, gp)
+        torch.cuda.synchronize()
+        assert Wg.intact() and gfg.intact() and gpg.intact()
         Wo_prev = Wo
         Wo, Gf_o, Gp_o = ora.step(Wo, G, lr)
         out.append(dict(Gf=host(gf), Gp=host(gp), W=host(Wd), Wprev=Wprev, Gf_o=Gf_o, Gp_o=Gp_o,
@@ -253,3 +257,117 @@ def test_step_many_equals_single_steps(prec):
         assert torch.equal(wa, wb)
         for sa, sb in zip(x.get_state()[:3], y.get_state()[:3]):
             assert torch.equal(sa, sb)
+
+
+def test_refresh_that_does_not_converge_keeps_the_previous_factors():
+    """The refresh's failure path: with a one-sweep limit, a refresh whose
+    Jacobi cannot converge in one sweep returns SPECOPTIM_ERR_NOT_CONVERGED,
+    leaves U, s, V, d exactly as the previous refresh left them, and the next
+    step filters with those previous factors (checked against the oracle's
+    projection of them, key design 3)."""
+    m, n = 256, 128
+    inp = synthetic.toy_matrix_inputs(seed=4)
+    gpu = so.SpectralOptimizer(m, n, svd_max_sweeps=1)
+    # first anchor: orthogonal columns, so the Gram matrix is already diagonal
+    # and one sweep converges
+    G1 = np.zeros((m, n), np.float32)
+    G1[np.arange(n), np.arange(n)] = np.linspace(2e-2, 1e-3, n, dtype=np.float32)
+    gpu.anchor_update(dev(G1))
+    assert gpu.svd_refresh() == 1
+    before = [host(x).copy() for x in gpu.get_factors()]
+    assert (before[1] > 0).all()
+    # second anchor: a generic matrix; one sweep is not enough
+    gpu.anchor_update(dev(inp.anchor_grad(0)))
+    with pytest.raises(so.SpecOptimError) as err:
+        gpu.svd_refresh()
+    assert err.value.code == so.ERR_NOT_CONVERGED
+    after = [host(x) for x in gpu.get_factors()]
+    for a, b in zip(before, after):
+        assert np.array_equal(a, b)
+    # the next step still filters with the kept factors
+    G = inp.masked_grad(0)
+    gf = torch.empty(m, n, device="cuda")
+    gpu.step(dev(inp.weights()), dev(G), 2e-5, gf)
+    U, s, V, d = (x.astype(np.float64) for x in before)
+    want = oracle.project(U, V, d, G.astype(np.float64))[2]
+    assert rel(host(gf), want) <= TOL[so.PREC_TF32]
+    gpu.close()
+
+
+def _twins(shapes, seed):
+    inps = [synthetic.MatrixInputs(m, n, seed=seed + i, rank=4) for i, (m, n) in enumerate(shapes)]
+    mk = lambda: [so.SpectralOptimizer(i.m, i.n) for i in inps]
+    return inps, mk(), mk()
+
+
+def test_refresh_begin_end_gives_the_same_factors_and_orders_the_steps():
+    """The split refresh (key design 2: the anchor is asynchronous) computes the
+    same decomposition as the one-call refresh, bit for bit; a step enqueued
+    between begin and end uses the previous factors and one enqueued after end
+    the new ones, whatever the timing."""
+    shapes = [(256, 128), (96, 200), (130, 130)]
+    inps, a, b = _twins(shapes, 60)
+    for x, y, i in zip(a, b, inps):
+        g = dev(i.anchor_grad(0))
+        x.anchor_update(g)
+        y.anchor_update(g)
+    so.svd_refresh_many(a)
+    so.svd_refresh_many(b)
+    for x, y, i in zip(a, b, inps):
+        g = dev(i.anchor_grad(1))
+        x.anchor_update(g)
+        y.anchor_update(g)
+    Wa = [dev(i.weights()) for i in inps]
+    Wb = [w.clone() for w in Wa]
+    G = [dev(i.masked_grad(0)) for i in inps]
+    # a: begin, a step with the old factors, end, a step with the new ones
+    so.svd_refresh_begin(a)
+    so.step_many(a, Wa, G, 2e-5)
+    W_mid = [w.clone() for w in Wa]
+    sweeps_a = so.svd_refresh_end(a)
+    so.step_many(a, Wa, G, 2e-5)
+    # b: the same steps around a one-call refresh
+    so.step_many(b, Wb, G, 2e-5)
+    W_mid_b = [w.clone() for w in Wb]
+    sweeps_b = so.svd_refresh_many(b)
+    so.step_many(b, Wb, G, 2e-5)
+    torch.cuda.synchronize()
+    assert sweeps_a == sweeps_b
+    for x, y in zip(a, b):
+        for fa, fb in zip(x.get_factors(), y.get_factors()):
+            assert torch.equal(fa, fb)
+    for u, v in zip(W_mid, W_mid_b):
+        assert torch.equal(u, v)
+    for u, v in zip(Wa, Wb):
+        assert torch.equal(u, v)
+    for x in a + b:
+        x.close()
+
+
+def test_refresh_begin_end_argument_checks():
+    inps, a, _ = _twins([(64, 48), (48, 64)], 70)
+    for x, i in zip(a, inps):
+        x.anchor_update(dev(i.anchor_grad(0)))
+    so.svd_refresh_begin(a)
+    lib = so.lib()
+    g = dev(inps[0].anchor_grad(1))
+    # the momentum being decomposed cannot change, and the refresh cannot restart
+    with pytest.raises(so.SpecOptimError) as e:
+        a[0].anchor_update(g)
+    assert e.value.code == so.ERR_INVALID_ARG
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_begin(a[:1])
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_many(a)
+    # end takes the handles of the begin, in order
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_end(a[::-1])
+    with pytest.raises(so.SpecOptimError):
+        so.svd_refresh_end(a[:1])
+    assert lib.specoptim_destroy(a[0]._h) == so.ERR_INVALID_ARG
+    sweeps = so.svd_refresh_end(a)
+    assert all(s >= 1 for s in sweeps)
+    a[0].anchor_update(g)  # allowed again
+    torch.cuda.synchronize()
+    for x in a:
+        x.close()
