@@ -40,10 +40,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Llama-3.2-1B-shaped spectral-corrected steps/s; mask pack/unpack HBM GB/s"
 REFRESH_EVERY = 20
+# Overlapped schedule (measured in the breakdown): steps between an anchor's
+# arrival (its EMA and the start of its SVD refresh, which then runs beside the
+# steps on the library's own streams) and the first step that filters with its
+# factors (the end of the refresh).  The headline runs the refresh in one call
+# at the anchor's arrival (use_after = 0), which measured faster on one GPU: the
+# persistent step GEMMs and the Jacobi kernels each fill every SM, so running
+# them side by side gains nothing and costs the interleaving.
+REFRESH_USE_AFTER = 10
 MASK_ROWS, MASK_H, MASK_P = 32 * 2048, 2048, 0.95
 MASK_BOUNDARIES = 15
 POOL = 4               # distinct masked-gradient sets kept resident in HBM
-TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor throughput ratio
 
 WORKLOAD = ("llama-3.2-1b decoder layer (q,o 2048x2048; k,v 512x2048; gate,up 8192x2048; "
             "down 2048x8192), rank-32 anchor signal, SVD refresh every 20 steps, "
@@ -110,6 +117,33 @@ def read_peaks():
             return json.load(f), "measured"
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def measure_tf32_peak(torch) -> dict:
+    """The TF32 tensor-core peak measured the way the HBM and bf16 peaks of
+    MEASURED_PEAKS.json are: torch.matmul (cuBLAS) fp32 8192^3 with TF32
+    allowed, 2 N^3 flops; best of 10 (burst) and back to back for about 3 s
+    (sustained, under the power cap)."""
+    n = 8192
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn(n, n, device="cuda", generator=g)
+        b = torch.randn(n, n, device="cuda", generator=g)
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = min(timed(torch, lambda: torch.matmul(a, b, out=c), False) for _ in range(10))
+        reps = max(10, int(3000.0 / best))
+        sus = timed(torch, lambda: [torch.matmul(a, b, out=c) for _ in range(reps)], False) / reps
+        del a, b, c
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    f = 2.0 * n ** 3
+    return {"tf32_tflops": f / (best * 1e-3) / 1e12, "tf32_tflops_sustained": f / (sus * 1e-3) / 1e12,
+            "how": "torch.matmul fp32 8192^3 with allow_tf32 (cuBLAS), 2 N^3 flops: best of 10 (burst) and "
+                   "%d back to back (sustained), CUDA events" % reps}
 
 
 # ------------------------------------------------------------------ clocks
@@ -220,6 +254,8 @@ class Layer:
         self.gd = torch.empty_like(self.g)
         self.lr = 2e-5
         self.last_sweeps = None
+        self.pending = False
+        self.use_after = 0
         self.flops = sum(gemm_flops(i.m, i.n) for i in self.inputs.values())
         self.bytes = sum(step_bytes(i.m, i.n) for i in self.inputs.values())
         self.params = sum(i.m * i.n for i in self.inputs.values())
@@ -228,18 +264,46 @@ class Layer:
         """Fresh optimizer state and the initial weights: a loop run after this
         one replays the same refresh history (the Jacobi sweep count of a warm-
         started refresh depends on how many refreshes came before it)."""
+        self.refresh_end()
         for name, inp in self.inputs.items():
             self.opt[name].close()
             self.opt[name] = self.so.SpectralOptimizer(inp.m, inp.n)
             self.W[name].copy_(self.torch.from_numpy(inp.weights()))
 
     def refresh(self, idx: int, G=None):
-        """Anchor EMA + batched SVD refresh of the 7 matrices; returns the Jacobi
-        sweeps each one took."""
+        """Anchor EMA + batched SVD refresh of the 7 matrices in one call; returns
+        the Jacobi sweeps each one took."""
         for name in self.names:
             self.opt[name].anchor_update(G[name] if G else self.Ganc[name][idx % 2])
         self.last_sweeps = self.so.svd_refresh_many([self.opt[name] for name in self.names])
         return self.last_sweeps
+
+    def refresh_begin(self, idx: int, G=None):
+        """Anchor EMA, then the start of the batched SVD refresh: its Jacobi
+        sweeps run beside the following steps, which keep the previous factors."""
+        for name in self.names:
+            self.opt[name].anchor_update(G[name] if G else self.Ganc[name][idx % 2])
+        self.so.svd_refresh_begin([self.opt[name] for name in self.names])
+        self.pending = True
+
+    def refresh_end(self):
+        """The refresh's factors take effect for the steps enqueued from here on."""
+        if self.pending:
+            self.last_sweeps = self.so.svd_refresh_end([self.opt[name] for name in self.names])
+            self.pending = False
+
+    def schedule(self, i: int, t0: int):
+        """What step i does about the anchor, for a run whose timed steps start at
+        t0: before t0 (warm-up) a one-call refresh every REFRESH_EVERY steps;
+        from t0 on an anchor arrives every REFRESH_EVERY steps (the first at t0)
+        and is refreshed in one call (use_after = 0) or begun there and ended
+        use_after steps later."""
+        if i < t0:
+            return "refresh" if i % REFRESH_EVERY == 0 else None
+        k = (i - t0) % REFRESH_EVERY
+        if self.use_after == 0:
+            return "refresh" if k == 0 else None
+        return "begin" if k == 0 else ("end" if k == self.use_after else None)
 
     def spectral(self, i: int, G=None):
         self.so.step_many([self.opt[n] for n in self.names], [self.W[n] for n in self.names],
@@ -258,9 +322,20 @@ class Layer:
         so.mask_pack(self.g, self.K, layer, i, 0, out=gp)
         so.mask_unpack(gp if gp_in is None else gp_in, MASK_H, layer, i, 0, out=self.gd)
 
-    def step(self, i: int):
-        if i % REFRESH_EVERY == 0:
-            self.refresh(i // REFRESH_EVERY)
+    @staticmethod
+    def anchor_index(i: int, t0: int) -> int:
+        """Which anchor gradient arrives at step i (two alternate)."""
+        return (i // REFRESH_EVERY) if i < t0 else (i - t0) // REFRESH_EVERY + 1
+
+    def step(self, i: int, t0: int = 0):
+        what = self.schedule(i, t0)
+        if what == "refresh":
+            self.refresh(self.anchor_index(i, t0))
+        elif what == "begin":
+            self.refresh_end()
+            self.refresh_begin(self.anchor_index(i, t0))
+        elif what == "end":
+            self.refresh_end()
         self.spectral(i)
         self.mask_round_trip(i)
 
@@ -294,6 +369,7 @@ class ModelWorkload:
             self.plain.append((w, g, torch.zeros_like(w), torch.zeros_like(w)))
         self.t = 0
         self.flops = n_layers * sum(gemm_flops(*shapes[n]) for n in self.names)
+        self.bytes = n_layers * sum(step_bytes(*shapes[n]) for n in self.names) + 28.0 * sum(r * c for r, c in plain)
         self.params = n_layers * sum(m * n for m, n in shapes.values()) + sum(r * c for r, c in plain)
 
     def refresh(self, idx: int):
@@ -310,6 +386,11 @@ class ModelWorkload:
     def step(self, i: int):
         if i % REFRESH_EVERY == 0:
             self.refresh(i // REFRESH_EVERY)
+        self.steady(i)
+
+    def steady(self, i: int):
+        """One step without the refresh: the spectral step of every matrix and
+        the plain AdamW of the other tensors."""
         for layer, W in zip(self.layers, self.W):
             self.so.step_many([layer[n] for n in self.names], [W[n] for n in self.names],
                               [self.Gm[n][i % 2] for n in self.names], 2e-5)
@@ -318,21 +399,32 @@ class ModelWorkload:
             self.so.adamw(w, g, m, v, self.t, 2e-5)
 
 
-def run_config(name: str, workload, K: int, W: int, mask_shape=None):
+def run_config(name: str, workload, K: int, W: int, mask_shape=None, peaks=None):
     """Whole-path steps/s of another configuration: W warm-up steps (the first holds
-    the first refresh), then K timed steps holding one refresh; plus the refresh
-    alone and, where the configuration has one, its mask round trip."""
+    the first refresh), then K timed steps holding one refresh; the steady step
+    alone (no refresh) against its roofline max(F / P_tf32, B / BW) with F and B
+    the executed association's flops and bytes; the refresh alone; and, where the
+    configuration has one, its mask round trip."""
     torch = workload.torch
     for i in range(W):
         workload.step(i)
     torch.cuda.synchronize()
     ms = timed(torch, lambda: [workload.step(W + i) for i in range(K)], False)
+    steady_n = 10
+    steady_ms = timed(torch, lambda: [workload.steady(1000 + i) for i in range(steady_n)], False) / steady_n
     sweeps = []
     refresh_ms = timed(torch, lambda: sweeps.append(workload.refresh(7)), False)
     out = {"workload": name, "steps_per_s": K / (ms * 1e-3), "ms_per_step": ms / K, "steps": K, "warmup": W,
            "refreshes_in_timed_steps": sum(1 for i in range(W, W + K) if i % REFRESH_EVERY == 0),
            "refresh_ms": refresh_ms, "refresh_sweeps_max": max(sweeps[0]),
-           "params": workload.params, "gemm_tflop_per_step": workload.flops / 1e12}
+           "steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
+           "params": workload.params, "gemm_tflop_per_step": workload.flops / 1e12,
+           "hbm_gb_per_step": workload.bytes / 1e9}
+    if peaks is not None:
+        bound = 1e3 * max(workload.flops / (peaks["tf32_tflops"] * 1e12), workload.bytes / (peaks["hbm_gbs"] * 1e9))
+        out.update({"step_roofline_ms": bound, "step_frac": bound / steady_ms,
+                    "step_roofline_peaks": "%.0f TFLOP/s tf32 (%s), %.0f GB/s HBM" % (
+                        peaks["tf32_tflops"], peaks["tf32_source"], peaks["hbm_gbs"])})
     if mask_shape is not None:
         so = workload.so
         rows, H, p = mask_shape
@@ -589,14 +681,16 @@ def run_ours(args, rank, world, local_rank, dist_ok):
 
     # warm-up (step 0 carries the first anchor update + SVD refresh)
     for i in range(W):
-        layer.step(i)
+        layer.step(i, t0=W)
     torch.cuda.synchronize()
 
-    # ---- the timed region: K whole-hot-path steps
+    # ---- the timed region: K whole-hot-path steps; a refresh begins with the
+    # first of them and every REFRESH_EVERY steps, and ends REFRESH_USE_AFTER
+    # steps later (one still open after the last step ends inside the region)
     so.trace_reset()
     layer.last_sweeps = None
     with ClockSampler(local_rank) as clocks:
-        ms = timed(torch, lambda: [layer.step(W + i) for i in range(K)], dist_ok)
+        ms = timed(torch, lambda: ([layer.step(W + i, t0=W) for i in range(K)], layer.refresh_end()), dist_ok)
     launches = so.launch_count()
     timed_sweeps = layer.last_sweeps
     ms_max = max_over_ranks(ms, dist_ok)
@@ -613,6 +707,25 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     refresh_ms = timed(torch, lambda: sweeps.append(layer.refresh(7)), False)
     refresh_rep = so.trace_report()
     so.trace_enable(False)
+    # the overlapped schedule (the refresh begun at the anchor's arrival, running
+    # beside the next REFRESH_USE_AFTER steps), for comparison with the headline's
+    layer.use_after = REFRESH_USE_AFTER
+    layer.reset_state()
+    for i in range(W):
+        layer.step(i, t0=W)
+    torch.cuda.synchronize()
+    ov_ms = timed(torch, lambda: ([layer.step(W + i, t0=W) for i in range(K)], layer.refresh_end()), False)
+    overlap = {"steps_per_s": K / (ov_ms * 1e-3), "ms_per_step": ov_ms / K, "use_after": REFRESH_USE_AFTER,
+               "refresh_sweeps": layer.last_sweeps,
+               "schedule": "refresh begun at the anchor's arrival on the library's streams (specoptim_svd_refresh_"
+                           "begin), ended %d steps later; the steps in between use the previous factors" %
+                           REFRESH_USE_AFTER}
+    layer.use_after = 0
+    tf32 = measure_tf32_peak(torch)
+    tf32_peak = tf32["tf32_tflops_sustained"]
+    cfg_peaks = {"tf32_tflops": tf32_peak, "tf32_source": "measured cuBLAS sustained",
+                 "hbm_gbs": peaks["hbm_gbs"]}
+    elementwise = elementwise_bench(layer, peaks, peak_src)
     mask = {("p%.2f" % p): mask_sweep(layer, p) for p in (0.95, 0.90)}
     mask_fused = mask_fused_bench(peaks, peak_src)
     import synthetic as _syn
@@ -623,7 +736,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         full = ModelWorkload(synthetic.LLAMA_1B_LAYER, synthetic.LLAMA_1B_LAYERS, seed=rank,
                              plain=[synthetic.LLAMA_1B_EMBED] + [(1, 2048)] * synthetic.LLAMA_1B_NORMS)
         others["full_1b"] = run_config("llama-3.2-1b full model: 16 layers x 7 matrices spectral-corrected, "
-                                       "embedding 128256x2048 + 33 norm vectors plain AdamW", full, 20, 3)
+                                       "embedding 128256x2048 + 33 norm vectors plain AdamW", full, 20, 3,
+                                       peaks=cfg_peaks)
         del full
         torch.cuda.empty_cache()
         sweep = {}
@@ -631,9 +745,10 @@ def run_ours(args, rank, world, local_rank, dist_ok):
             l7 = ModelWorkload(synthetic.LLAMA_7B_LAYER, 1, seed=rank, tau_p=tau)
             res7 = run_config("7B-shaped layer: q,o 4096x4096; k,v 1024x4096; gate,up 14336x4096; "
                               "down 4096x14336", l7, 20, 3,
-                              mask_shape=(8 * 4096, 4096, 0.95) if tau == 1e-3 else None)
+                              mask_shape=(8 * 4096, 4096, 0.95) if tau == 1e-3 else None, peaks=cfg_peaks)
             sweep["%g" % tau] = {"steps_per_s": res7["steps_per_s"], "refresh_ms": res7["refresh_ms"],
-                                 "refresh_sweeps_max": res7["refresh_sweeps_max"]}
+                                 "refresh_sweeps_max": res7["refresh_sweeps_max"],
+                                 "steady_step_ms": res7["steady_step_ms"], "step_frac": res7["step_frac"]}
             if tau == 1e-3:
                 others["layer_7b"] = res7
             del l7
@@ -652,12 +767,11 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         a[0] += n
         a[1] += t
     total_ms = sum(v[1] for v in rep.values())
-    tf32_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
     g_launch, g_ms = fam.get("gemm_tf32", [0, 0.0])
     g_ach = layer.flops * steady_n / (g_ms * 1e-3) / 1e12 if g_ms > 0 else None
     roof_steady = {"kernel": "gemm_tf32", "bound": "tensor", "achieved": g_ach, "peak": tf32_peak,
                    "unit": "TFLOP/s", "frac": g_ach / tf32_peak if g_ach else None,
-                   "peak_source": "%s bf16 sustained x nominal tf32/bf16 %.3f" % (peak_src, TF32_OVER_BF16),
+                   "peak_source": "measured in this run: cuBLAS tf32 sustained (peaks.tf32)",
                    "launches_per_step": g_launch / steady_n, "avg_launch_ms": g_ms / max(g_launch, 1),
                    "share_of_step": g_ms / total_ms, "traffic": profiled_traffic(*GEMM_PROFILE),
                    "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"}
@@ -666,7 +780,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
     # second stream beside the solves, so its traced time includes sharing the SMs)
     nps = [padded_order(min(i.m, i.n)) for i in layer.inputs.values()]
     rounds = max(n // 32 for n in nps) - 1
-    period_ms = REFRESH_EVERY * steady_ms + refresh_ms
+    period_ms = REFRESH_EVERY * ms_max / K  # measured: the refresh overlaps the steps
 
     def hbm_roof(kernel, trace_name, per_matrix, profile):
         launches, ms = refresh_rep.get(trace_name, (0, 0.0))
@@ -699,7 +813,9 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "config": {"workload": WORKLOAD, "global_batch": world, "parallelism": "replicas (one layer per GPU)",
                    "l2": "inputs larger than L2: each step streams 0.97 GB of distinct gradients and "
                          "optimizer state and 1 GB of activations",
-                   "timed_refresh_sweeps": timed_sweeps},
+                   "timed_refresh_sweeps": timed_sweeps,
+                   "refresh_schedule": "every %d steps the anchor EMA and a batched SVD refresh of the 7 "
+                                       "matrices in one call, before that step's spectral step" % REFRESH_EVERY},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "roofline": roof,
@@ -707,6 +823,7 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                       "roofline_refresh_q_rotate": roof_rotate,"steady_step_ms": steady_ms, "steady_steps_per_s": 1e3 / steady_ms,
                       "step_roofline_ms": step_bound_ms, "step_frac": step_bound_ms / steady_ms,
                       "refresh_ms": refresh_ms, "refresh_sweeps": sweeps[0],
+                      "overlapped_refresh_schedule": overlap,
                       "refresh_note": "traced; one more refresh of the same layer (the Jacobi sweep count "
                                       "falls as the anchor EMA settles; the timed steps hold the second refresh)",
                       "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in rep.items()},
@@ -716,11 +833,45 @@ def run_ours(args, rank, world, local_rank, dist_ok):
         "dp_outer_sync": dict(dp_sync, workload="PowerSGD-compressed Streaming DiLoCo outer sync of the "
                                                 "llama-3.2-1b decoder layer (7 matrices, rank for 64x)"),
         "other_configs": others,
-        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak},
+        "elementwise": elementwise,
+        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops": tf32_peak,
+                  "tf32": tf32, "tf32_used": "sustained (the steady step and its GEMMs run in a loop)"},
     }
     if not args.no_e2e:
         result["e2e"] = run_e2e(layer, K, W, dist_ok, world)
     return result
+
+
+def elementwise_bench(layer: Layer, peaks: dict, peak_src: str, reps: int = 10) -> dict:
+    """HBM throughput of the two elementwise kernels: the anchor EMA of the 7
+    matrices of the layer (12 B per element: M and G_anc read, M written) and
+    the plain AdamW of the full model's embedding, 128256 x 2048 (28 B per
+    element: W, g, m, v read, W, m, v written)."""
+    torch, so = layer.torch, layer.so
+    names = layer.names
+    for n in names:
+        layer.opt[n].anchor_update(layer.Ganc[n][0])
+    ema_ms = timed(torch, lambda: [layer.opt[n].anchor_update(layer.Ganc[n][i % 2])
+                                   for i in range(reps) for n in names], False) / reps
+    ema_bytes = 12.0 * layer.params
+    rows, cols = 128256, 2048
+    g = torch.Generator(device="cuda").manual_seed(1)
+    W = torch.randn(rows, cols, device="cuda", generator=g) * 0.02
+    G = torch.randn(rows, cols, device="cuda", generator=g) * 1e-2
+    m, v = torch.zeros_like(W), torch.zeros_like(W)
+    so.adamw(W, G, m, v, 1, 2e-5)
+    ad_ms = timed(torch, lambda: [so.adamw(W, G, m, v, 2 + i, 2e-5) for i in range(reps)], False) / reps
+    ad_bytes = 28.0 * rows * cols
+    del W, G, m, v
+    torch.cuda.empty_cache()
+    hbm = peaks["hbm_gbs"]
+    return {"ema": {"kernel": "ema", "bound": "hbm", "ms": ema_ms, "GBps": ema_bytes / (ema_ms * 1e-3) / 1e9,
+                    "frac": ema_bytes / (ema_ms * 1e-3) / 1e9 / hbm, "bytes": ema_bytes,
+                    "workload": "anchor EMA of the 7 matrices of the llama-3.2-1b layer (7 launches)"},
+            "adamw": {"kernel": "adamw", "bound": "hbm", "ms": ad_ms, "GBps": ad_bytes / (ad_ms * 1e-3) / 1e9,
+                      "frac": ad_bytes / (ad_ms * 1e-3) / 1e9 / hbm, "bytes": ad_bytes,
+                      "workload": "plain AdamW of the 128256 x 2048 embedding"},
+            "peak_source": "%s HBM copy bandwidth" % peak_src}
 
 
 def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
@@ -729,8 +880,10 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
     host -> device, the step's masked gradients (every 20th step also the anchor
     gradients) and the packed boundary values received from the neighbouring
     stages (the activation from the previous stage, the gradient from the next);
-    device -> host, the step's updated weights (the parameter snapshot the anchor
-    circuit pulls) and the packed values this stage sends.  The dense boundary
+    device -> host, the packed values this stage sends, and once per anchor
+    period (at each anchor's arrival) the updated weights: the parameter
+    snapshot that the anchor circuit pulls periodically for its next unmasked
+    pass.  The dense boundary
     activation and its gradient are produced and consumed on the device by the
     model's own layers, so they stay resident, as in training.  The copies run on
     two more streams (one per direction), double-buffered: step i+1's inputs
@@ -762,13 +915,15 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
     for e in freed + out_free + [sent]:
         e.record(compute)
 
+    t0 = W  # the timed steps start here (the refresh schedule of Layer.schedule)
+
     def load(i):  # on the copy stream: step i's inputs into buffer i % 2
         b = i % 2
         with torch.cuda.stream(copy):
             copy.wait_event(freed[b])
-            if i % REFRESH_EVERY == 0:
+            if layer.schedule(i, t0) in ("refresh", "begin"):
                 for n in names:
-                    devA[b][n].copy_(hostA[n][(i // REFRESH_EVERY) % 2], non_blocking=True)
+                    devA[b][n].copy_(hostA[n][layer.anchor_index(i, t0) % 2], non_blocking=True)
                     stats["h2d"] += devA[b][n].numel() * 4
             for n in names:
                 devG[b][n].copy_(hostG[n][i % 2], non_blocking=True)
@@ -783,15 +938,24 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
         if not last:
             load(i + 1)
         compute.wait_event(loaded[b])
-        if i % REFRESH_EVERY == 0:
+        what = layer.schedule(i, t0)
+        if what == "refresh":
             layer.refresh(0, G=devA[b])
+        elif what == "begin":
+            layer.refresh_end()
+            layer.refresh_begin(0, G=devA[b])
+        elif what == "end":
+            layer.refresh_end()
         layer.spectral(i, G=devG[b])
         compute.wait_event(out_free[b])  # step i-2's packed values have left
         layer.mask_round_trip(i, hp_out=out_hp[b], gp_out=out_gp[b], hp_in=in_hp[b], gp_in=in_gp[b])
         freed[b].record(compute)
-        compute.wait_event(sent)  # the previous weight snapshot has left
-        for n in names:
-            snapW[n].copy_(layer.W[n], non_blocking=True)
+        # the anchor circuit pulls a parameter snapshot once per anchor period
+        snap = what in ("refresh", "begin")
+        if snap:
+            compute.wait_event(sent)  # the previous weight snapshot has left
+            for n in names:
+                snapW[n].copy_(layer.W[n], non_blocking=True)
         snapped.record(compute)
         with torch.cuda.stream(back):
             back.wait_event(snapped)
@@ -799,10 +963,11 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
             sent_gp[b].copy_(out_gp[b], non_blocking=True)
             stats["d2h"] += (out_hp[b].numel() + out_gp[b].numel()) * 2
             out_free[b].record(back)
-            for n in names:
-                hostW[n].copy_(snapW[n], non_blocking=True)
-                stats["d2h"] += snapW[n].numel() * 4
-            sent.record(back)
+            if snap:
+                for n in names:
+                    hostW[n].copy_(snapW[n], non_blocking=True)
+                    stats["d2h"] += snapW[n].numel() * 4
+                sent.record(back)
 
     def run(first, count):
         load(first)
@@ -815,15 +980,16 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
     run(0, W)
     stats["h2d"] = stats["d2h"] = 0
     layer.last_sweeps = None
-    ms = timed(torch, lambda: run(W, K), dist_ok)
+    ms = timed(torch, lambda: (run(W, K), layer.refresh_end()), dist_ok)
     ms = max_over_ranks(ms, dist_ok)
     return {"value": world * K / (ms * 1e-3), "unit": "steps/s",
             "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K,
             "timed_refresh_sweeps": layer.last_sweeps,
             "pipeline": "copies on two more streams (one per direction), double-buffered inputs and packed "
                         "sends, weights read back from a device-side snapshot; every copy inside the timed region",
-            "link_traffic": "gradients in, weights out, packed boundary values (K of H per row) both ways; "
-                            "the dense boundary tensors stay on the device",
+            "link_traffic": "every step: masked gradients in, packed boundary values (K of H per row) both ways; "
+                            "every %d steps: anchor gradients in and a weight snapshot out (the anchor circuit's "
+                            "periodic parameter pull); the dense boundary tensors stay on the device" % REFRESH_EVERY,
             "link": link_bandwidth(torch)}
 
 
@@ -900,13 +1066,51 @@ def oracle_toy_seconds():
     return time.perf_counter() - t
 
 
+SINGLE_THREAD_SAMPLE = r"""
+import json, os, sys, time
+sys.path.insert(0, %(root)r)
+import numpy as np
+import oracle, synthetic, bench
+out = {"toy_whole_path_seconds": bench.oracle_toy_seconds()}
+inp = synthetic.MatrixInputs(512, 2048, seed=0, rank=32)
+opt = oracle.SpectralOptimizer(512, 2048)
+rng = np.random.default_rng(0)
+opt.U = rng.standard_normal((512, 512)) / np.sqrt(512)
+opt.V = rng.standard_normal((2048, 512)) / np.sqrt(2048)
+opt.d = rng.uniform(0.0, 1.0, 512)
+W, G = inp.weights().astype(np.float64), inp.masked_grad(0)
+t = time.perf_counter()
+opt.step(W, G, 2e-5)
+out["kv_step_seconds"] = time.perf_counter() - t
+print(json.dumps(out))
+"""
+
+
+def single_thread_oracle():
+    """The oracle on one host thread (BLAS limited to one thread in a child
+    process): the toy whole path and one steady step of a 512 x 2048 (k / v)
+    matrix."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        env.pop(k, None)
+    try:
+        res = subprocess.run([sys.executable, "-c", SINGLE_THREAD_SAMPLE % {"root": ROOT}], env=env,
+                             capture_output=True, text=True, timeout=300)
+        return json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not a failure of the bench
+        return {"error": str(e)[:200]}
+
+
 def cpu_baseline():
     s = OracleSample()
     t = time.perf_counter()
     s.step(0)
     dt = time.perf_counter() - t
     return {"value": 1.0 / dt, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": s.describe(), "seconds": dt, "toy_whole_path_seconds": oracle_toy_seconds()}
+            "threads": "numpy's BLAS at its default thread count (one per host core); the C mask oracle "
+                       "on one thread",
+            "sample": s.describe(), "seconds": dt, "toy_whole_path_seconds": oracle_toy_seconds(),
+            "single_thread": single_thread_oracle()}
 
 
 def run_reference(args, rank, world):

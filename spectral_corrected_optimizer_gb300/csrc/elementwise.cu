@@ -3,6 +3,7 @@
 // plain AdamW for tensors outside the spectral correction.  128-bit loads and
 // stores, grid sized to a multiple of the SM count, scalar tail.
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "elementwise.cuh"
@@ -78,15 +79,31 @@ __device__ __forceinline__ float maybe_round(float v, int round) {
     return v;
 }
 
+// Up to kMaxTranspose transposes in one launch (the step's G^T of every tall
+// matrix): tiles numbered job by job.
+constexpr int kMaxTranspose = 16;
+struct TransposeBatch {
+    int count;
+    const float *src[kMaxTranspose];
+    float *dst[kMaxTranspose];
+    int rows[kMaxTranspose], cols[kMaxTranspose], round[kMaxTranspose];
+    int64_t tile_off[kMaxTranspose + 1];
+};
+
 __global__ void __launch_bounds__(256)
-transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows, int cols,
-                 int round) {
+transpose_kernel(const TransposeBatch tb) {
     __shared__ float tile[64][65];
     const int tid = threadIdx.x;
-    const int64_t tiles_c = (cols + 63) / 64, tiles = tiles_c * ((rows + 63) / 64);
-    const bool vec = ((rows | cols) & 3) == 0;
+    const int64_t tiles = tb.tile_off[tb.count];
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int r0 = (int)(t / tiles_c) * 64, c0 = (int)(t % tiles_c) * 64;
+        int j = 0;
+        while (j + 1 < tb.count && t >= tb.tile_off[j + 1]) ++j;
+        const float *__restrict__ src = tb.src[j];
+        float *__restrict__ dst = tb.dst[j];
+        const int rows = tb.rows[j], cols = tb.cols[j], round = tb.round[j];
+        const int64_t tiles_c = (cols + 63) / 64, local = t - tb.tile_off[j];
+        const bool vec = ((rows | cols) & 3) == 0;
+        const int r0 = (int)(local / tiles_c) * 64, c0 = (int)(local % tiles_c) * 64;
         __syncthreads();
         if (vec) {
             float4 v[4];
@@ -129,13 +146,33 @@ transpose_kernel(const float *__restrict__ src, float *__restrict__ dst, int row
 
 }  // namespace
 
-int transpose_run(const float *src, float *dst, int rows, int cols, bool round, cudaStream_t st) {
-    if (rows <= 0 || cols <= 0) return SPECOPTIM_OK;
-    const int64_t tiles = (int64_t)((rows + 63) / 64) * ((cols + 63) / 64);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 4));
-    SPCO_LAUNCH("transpose", st, transpose_kernel<<<grid, 256, 0, st>>>(src, dst, rows, cols, round ? 1 : 0));
+int transpose_many(int count, const TransposeJob *jobs, cudaStream_t st) {
+    if (count < 1 || count > kMaxTranspose) return fail(SPECOPTIM_ERR_INVALID_ARG, "transpose: 1 to 16 jobs");
+    TransposeBatch tb;
+    std::memset(&tb, 0, sizeof(tb));
+    for (int i = 0; i < count; ++i) {
+        const TransposeJob &q = jobs[i];
+        const int64_t tiles = (q.rows > 0 && q.cols > 0) ? (int64_t)((q.rows + 63) / 64) * ((q.cols + 63) / 64) : 0;
+        tb.src[tb.count] = q.src;
+        tb.dst[tb.count] = q.dst;
+        tb.rows[tb.count] = q.rows;
+        tb.cols[tb.count] = q.cols;
+        tb.round[tb.count] = q.round ? 1 : 0;
+        tb.tile_off[tb.count + 1] = tb.tile_off[tb.count] + tiles;
+        if (tiles) ++tb.count;
+    }
+    if (tb.count == 0) return SPECOPTIM_OK;
+    const int64_t tiles = tb.tile_off[tb.count];
+    // 8 CTAs of 256 threads per SM (16.6 KB of shared memory each)
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms() * 8));
+    SPCO_LAUNCH("transpose", st, transpose_kernel<<<grid, 256, 0, st>>>(tb));
     SPECOPTIM_LAUNCHED("transpose_kernel");
     return SPECOPTIM_OK;
+}
+
+int transpose_run(const float *src, float *dst, int rows, int cols, bool round, cudaStream_t st) {
+    const TransposeJob j{src, dst, rows, cols, round};
+    return transpose_many(1, &j, st);
 }
 
 AdamWScalars adamw_scalars(int64_t t, float lr, float beta1, float beta2, float eps, float wd) {

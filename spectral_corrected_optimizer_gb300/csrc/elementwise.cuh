@@ -19,6 +19,15 @@ AdamWScalars adamw_scalars(int64_t t, float lr, float beta1, float beta2, float 
 int ema_run(float *M, const float *G, int64_t n, float beta, cudaStream_t st);
 int adamw_run(float *W, const float *G, float *m1, float *m2, int64_t n, const AdamWScalars &s,
               cudaStream_t st);
+// dst (cols x rows) = src (rows x cols)^T, rounded to TF32 (nearest) when
+// `round`; up to 16 of them in one launch
+struct TransposeJob {
+    const float *src;
+    float *dst;
+    int rows, cols;
+    bool round;
+};
+int transpose_many(int count, const TransposeJob *jobs, cudaStream_t st);
 // out (rows x cols) = X diag(d): column j of X scaled by d[j]
 int scale_cols_run(const float *X, const float *d, int64_t rows, int cols, float *out, cudaStream_t st);
 

@@ -365,12 +365,15 @@ extern "C" int specoptim_svd_refresh(specoptim_t *h, void *stream, int32_t *swee
 namespace {
 
 // The products of one handle's step (two or three) with their epilogues, in
-// slots 3 - count .. 2 so that every handle's last (AdamW) product is slot 2;
-// `transpose` is set when G^T must be formed first (m > n).
+// slots first .. last: slot 0 holds every handle's first product, so that the
+// square matrices' last (AdamW) product shares slot 1 with the others' middle
+// products and slot 2 holds the AdamW products of the rest (grouped step_many
+// runs one launch per slot; this spreads the AdamW epilogue's memory traffic
+// over two of them).  `transpose` is set when G^T must be formed first (m > n).
 constexpr int kSlots = 3;
 struct StepPlan {
     GemmProblem stage[kSlots];
-    int first;  // first used slot
+    int first, last;  // used slots
     bool transpose;
     const float *G;
     float *GT;
@@ -436,15 +439,17 @@ StepPlan plan_step(specoptim_t *h, float *W, const float *G_mask, float lr, floa
         float *TT = h->ws_a;
         plain.C = TT;
         plain.ldc = m;
-        P.first = 1;
+        P.first = 0;
+        P.last = 1;
         P.transpose = false;
-        P.stage[1] = nt(n, m, n, h->PR, n, G_mask, n, plain);     // T^T = P_R G^T
-        P.stage[2] = nt(m, n, m, h->PL, m, TT, m, last);          // G_filt = P_L T -> AdamW
+        P.stage[0] = nt(n, m, n, h->PR, n, G_mask, n, plain);     // T^T = P_R G^T
+        P.stage[1] = nt(m, n, m, h->PL, m, TT, m, last);          // G_filt = P_L T -> AdamW
     } else if (h->tall) {
         float *T1 = h->ws_a, *T2T = h->ws_x;
         plain.C = T1;
         plain.ldc = n;
         P.first = 0;
+        P.last = 2;
         P.stage[0] = nt(r, n, m, h->UTo, m, P.GT, m, plain);      // T1 = U^T G
         cols.C = T2T;
         cols.ldc = r;
@@ -455,6 +460,7 @@ StepPlan plan_step(specoptim_t *h, float *W, const float *G_mask, float lr, floa
         plain.C = T1T;
         plain.ldc = m;
         P.first = 0;
+        P.last = 2;
         P.stage[0] = nt(r, m, n, h->VTo, n, G_mask, n, plain);    // T1^T = V^T G^T
         cols.C = T2;
         cols.ldc = r;
@@ -480,7 +486,7 @@ extern "C" int specoptim_step(specoptim_t *h, float *W, const float *G_mask, flo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const StepPlan P = plan_step(h, W, G_mask, lr, G_filt_out, G_proj_out);
     if (P.transpose && (rc = transpose_run(P.G, P.GT, P.m, P.n, P.round, st))) return rc;
-    for (int s = P.first; s < kSlots; ++s)
+    for (int s = P.first; s <= P.last; ++s)
         if ((rc = run_problem(h->cfg.precision, P.stage[s], st))) return rc;
     return SPECOPTIM_OK;
 }
@@ -499,10 +505,11 @@ extern "C" int specoptim_step_many(specoptim_t *const *handles, int32_t count, f
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     StepPlan plans[16];
     for (int i = 0; i < count; ++i) plans[i] = plan_step(handles[i], W[i], G_mask[i], lr, nullptr, nullptr);
+    TransposeJob tj[16];
+    int nt = 0;
     for (int i = 0; i < count; ++i)
-        if (plans[i].transpose &&
-            (rc = transpose_run(plans[i].G, plans[i].GT, plans[i].m, plans[i].n, plans[i].round, st)))
-            return rc;
+        if (plans[i].transpose) tj[nt++] = TransposeJob{plans[i].G, plans[i].GT, plans[i].m, plans[i].n, plans[i].round};
+    if (nt && (rc = transpose_many(nt, tj, st))) return rc;
     for (int s = 0; s < kSlots; ++s) {
         // tensor-core problems of this slot share launches (largest first, 8 per launch);
         // the rest run one by one on the SIMT path
@@ -510,7 +517,7 @@ extern "C" int specoptim_step_many(specoptim_t *const *handles, int32_t count, f
         double work[16];
         int ng = 0;
         for (int i = 0; i < count; ++i) {
-            if (s < plans[i].first) continue;
+            if (s < plans[i].first || s > plans[i].last) continue;
             const GemmProblem &q = plans[i].stage[s];
             if (handles[i]->cfg.precision == SPECOPTIM_PREC_TF32 && gemm_tc_supported(q.M, q.N, q.K, q.A, q.B)) {
                 group[ng] = q;

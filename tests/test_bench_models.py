@@ -52,3 +52,29 @@ def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("missing.md", sources, key="k1") is None
     (csrc / "b.cuh").write_bytes(b"shared header, edited")
     assert bench.profiled_traffic("p.md", sources, key="k1") is None
+
+
+@pytest.mark.parametrize("W,K", [(3, 20), (5, 20), (3, 40), (25, 20)])
+def test_refresh_schedule_of_the_timed_region(W, K):
+    """Warm-up steps refresh in one call every REFRESH_EVERY steps; the timed
+    steps begin a refresh with their first step and every REFRESH_EVERY steps
+    after, and end each one REFRESH_USE_AFTER steps after its begin, so a timed
+    region of K = multiple of REFRESH_EVERY steps holds whole refreshes only."""
+    class L:
+        use_after = bench.REFRESH_USE_AFTER
+    what = [bench.Layer.schedule(L, i, W) for i in range(W + K)]
+    L.use_after = 0
+    serial = [bench.Layer.schedule(L, i, W) for i in range(W + K)]
+    assert [i for i, x in enumerate(serial) if x] == [i for i in range(W) if i % bench.REFRESH_EVERY == 0] + \
+        list(range(W, W + K, bench.REFRESH_EVERY))
+    assert set(serial) <= {None, "refresh"}
+    assert what[0] == "refresh"
+    assert [i for i in range(W) if what[i]] == [i for i in range(W) if i % bench.REFRESH_EVERY == 0]
+    begins = [i for i in range(W, W + K) if what[i] == "begin"]
+    ends = [i for i in range(W, W + K) if what[i] == "end"]
+    assert begins == list(range(W, W + K, bench.REFRESH_EVERY))
+    assert ends == [b + bench.REFRESH_USE_AFTER for b in begins]
+    assert "refresh" not in what[W:]
+    # the anchors alternate, continuing after the warm-up's
+    idx = [bench.Layer.anchor_index(i, W) for i in begins]
+    assert idx == list(range(1, len(begins) + 1))
