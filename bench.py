@@ -91,6 +91,9 @@ GEMM_PROFILE = ("gemm_tf32_layer_step.md", ("gemm_tc.cu", "gemm.cuh", "tc.cuh", 
 ROTATE_PROFILE = ("jacobi_rotate_layer_refresh.md", ("jacobi_tc.cu", "jacobi.cuh", "tc.cuh"))
 APPLY_PROFILE = ("jacobi_apply_layer_refresh.md", ("jacobi_apply_tc.cu", "jacobi.cuh", "tc.cuh"))
 DPSYNC_PROFILE = ("dpsync_layer_outer_sync.md", ("dpsync.cu", "tc.cuh", "common.cuh"))
+ELEMENTWISE_PROFILE = ("elementwise_ema_adamw.md", ("elementwise.cu", "elementwise.cuh", "common.cuh"))
+# values per launch of the profiled elementwise case (bench.py --profile elementwise)
+ELEMENTWISE_PROFILE_VALUES = {"ema": 8192 * 2048, "adamw": 32768 * 2048}
 
 
 def padded_order(r: int) -> int:
@@ -774,7 +777,8 @@ def run_ours(args, rank, world, local_rank, dist_ok):
                    "peak_source": "measured in this run: cuBLAS tf32 sustained (peaks.tf32)",
                    "launches_per_step": g_launch / steady_n, "avg_launch_ms": g_ms / max(g_launch, 1),
                    "share_of_step": g_ms / total_ms, "traffic": profiled_traffic(*GEMM_PROFILE),
-                   "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch)"}
+                   "traffic_source": "profiles/gemm_tf32_layer_step.md (ncu DRAM bytes per grouped launch; "
+                                     "tensor-pipe activity of each launch in the same file)"}
     # the refresh's two tensor-core rotation kernels, both HBM-bound: A <- R^T A R
     # (jacobi_apply, on the critical chain) and Q <- Q R (jacobi_rotate, on a
     # second stream beside the solves, so its traced time includes sharing the SMs)
@@ -865,13 +869,21 @@ def elementwise_bench(layer: Layer, peaks: dict, peak_src: str, reps: int = 10) 
     del W, G, m, v
     torch.cuda.empty_cache()
     hbm = peaks["hbm_gbs"]
+
+    def per_value(key):  # ncu DRAM bytes per value of the profiled case (grows in proportion)
+        t = profiled_traffic(*ELEMENTWISE_PROFILE, key=key)
+        return None if t is None else t / ELEMENTWISE_PROFILE_VALUES[key]
+
     return {"ema": {"kernel": "ema", "bound": "hbm", "ms": ema_ms, "GBps": ema_bytes / (ema_ms * 1e-3) / 1e9,
                     "frac": ema_bytes / (ema_ms * 1e-3) / 1e9 / hbm, "bytes": ema_bytes,
+                    "traffic_bytes_per_value": per_value("ema"), "algorithmic_bytes_per_value": 12,
                     "workload": "anchor EMA of the 7 matrices of the llama-3.2-1b layer (7 launches)"},
             "adamw": {"kernel": "adamw", "bound": "hbm", "ms": ad_ms, "GBps": ad_bytes / (ad_ms * 1e-3) / 1e9,
                       "frac": ad_bytes / (ad_ms * 1e-3) / 1e9 / hbm, "bytes": ad_bytes,
+                      "traffic_bytes_per_value": per_value("adamw"), "algorithmic_bytes_per_value": 28,
                       "workload": "plain AdamW of the 128256 x 2048 embedding"},
-            "peak_source": "%s HBM copy bandwidth" % peak_src}
+            "peak_source": "%s HBM copy bandwidth" % peak_src,
+            "traffic_source": "profiles/" + ELEMENTWISE_PROFILE[0]}
 
 
 def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
@@ -1141,7 +1153,9 @@ def run_profile_case(args):
     'refresh': anchor EMA + SVD refresh of one 2048x2048 matrix, twice (the second warm);
     'layer': batched refresh, then grouped steady steps of the 7-matrix 1B layer;
     'dpsync': PowerSGD-compressed outer syncs of the 7-matrix 1B layer;
-    'maskfused': the four mask ops fused with the layer boundary on bf16 [65536, 2048]."""
+    'maskfused': the four mask ops fused with the layer boundary on bf16 [65536, 2048];
+    'elementwise': per iteration the anchor EMA of one 8192 x 2048 matrix and a plain AdamW
+    of 32768 x 2048 values (a quarter of the embedding)."""
     import numpy as np
     import torch
 
@@ -1184,6 +1198,17 @@ def run_profile_case(args):
                    for i, (t, (m, n)) in enumerate(zip(theta, shapes))]
         for i in range(n_iter):
             g.outer_sync(W_local)
+    elif args.profile == "elementwise":
+        inp = synthetic.MatrixInputs(8192, 2048, seed=0, rank=32)
+        opt = so.SpectralOptimizer(8192, 2048)
+        Ga = [torch.from_numpy(inp.anchor_grad(i)).cuda() for i in range(2)]
+        g = torch.Generator(device="cuda").manual_seed(1)
+        W = torch.randn(32768, 2048, device="cuda", generator=g) * 0.02
+        G = torch.randn(32768, 2048, device="cuda", generator=g) * 1e-2
+        m, v = torch.zeros_like(W), torch.zeros_like(W)
+        for i in range(n_iter):
+            opt.anchor_update(Ga[i % 2])
+            so.adamw(W, G, m, v, i + 1, 2e-5)
     elif args.profile == "refresh":
         inp = synthetic.MatrixInputs(2048, 2048, seed=0, rank=32)
         opt = so.SpectralOptimizer(2048, 2048)
@@ -1255,7 +1280,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the full-1B and 7B-layer measurements reported beside the headline")
-    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync", "maskfused"], default=None,
+    ap.add_argument("--profile", choices=["gate", "mask", "refresh", "layer", "dpsync", "maskfused", "elementwise"],
+                    default=None,
                     help="run a small case for ncu captures instead of the benchmark")
     ap.add_argument("--dry-run", action="store_true",
                     help="host-only stand-in for the GPU work (checks the launcher and the rank timing)")
