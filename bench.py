@@ -992,9 +992,17 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
     run(0, W)
     stats["h2d"] = stats["d2h"] = 0
     layer.last_sweeps = None
-    ms = timed(torch, lambda: (run(W, K), layer.refresh_end()), dist_ok)
+    host = []
+
+    def enqueue():
+        t = time.perf_counter()
+        run(W, K)
+        layer.refresh_end()
+        host.append((time.perf_counter() - t) * 1e3)
+
+    ms = timed(torch, enqueue, dist_ok)
     ms = max_over_ranks(ms, dist_ok)
-    return {"value": world * K / (ms * 1e-3), "unit": "steps/s",
+    return {"value": world * K / (ms * 1e-3), "unit": "steps/s", "host_enqueue_ms": host[0], "device_ms": ms,
             "h2d_bytes_per_step": stats["h2d"] // K, "d2h_bytes_per_step": stats["d2h"] // K,
             "timed_refresh_sweeps": layer.last_sweeps,
             "pipeline": "copies on two more streams (one per direction), double-buffered inputs and packed "

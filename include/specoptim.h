@@ -134,7 +134,9 @@ int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void 
  * depend on timing.  end takes the same handles in the same order as begin.
  * Between the two calls anchor_update, set_state, svd_refresh(_many), begin
  * and destroy on these handles return SPECOPTIM_ERR_INVALID_ARG, and only one
- * refresh (of any form) may be in progress per process. */
+ * refresh (of any form) may be in progress per process.  Every begin needs its
+ * end before the process exits (the library thread must not outlive the CUDA
+ * context). */
 int specoptim_svd_refresh_begin(specoptim_t *const *handles, int32_t count, void *stream);
 int specoptim_svd_refresh_end(specoptim_t *const *handles, int32_t count, void *stream,
                               int32_t *sweeps_out);
