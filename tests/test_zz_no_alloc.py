@@ -7,12 +7,14 @@ intermediates live in a 16 MiB static device array instead of memory the
 library allocates.
 
 The tests call it through the C-ABI with the factors of a real refresh,
-copied out, and check its filtered gradient against the oracle's projection
-(key design 3, projection equation, float64) of the same factors and
-gradient, on two calls in a row; both precisions; wide, tall, square and
-ragged shapes (r = 66 is not a multiple of 4, so the tensor-core path hands
-those products to the SIMT kernel).  Bars: relative Frobenius error 2e-3 for
-TF32 (the parity tests' bar) and 1e-4 for fp32.  They also check that a call
+copied out, and check its filtered gradient, on two calls in a row, against
+the filtered gradient the allocating entry point (specoptim_step with a
+G_filt output) gives for the same factors and gradient, within the parity
+tests' TF32 bar (relative Frobenius error 2e-3), and against the oracle's
+projection (key design 3, projection equation, float64) of the same factors
+and gradient: 2e-3 for TF32, 1e-4 for fp32.  Both precisions; wide, tall,
+square and ragged shapes (r = 66 is not a multiple of 4, so the tensor-core
+path hands those products to the SIMT kernel).  They also check that a call
 allocates no device memory and that a shape whose intermediates do not fit
 in the array is rejected with a clear error.
 
@@ -54,11 +56,14 @@ def test_noalloc_filter_matches_the_oracle(shape, prec):
     for call in range(2):
         Gh = inp.masked_grad(call)
         G = dev(Gh)
+        ref = torch.empty(m, n, device="cuda")
+        opt.step(dev(inp.weights()), G, 2e-5, G_filt_out=ref)  # the allocating entry point
         out = torch.full((m, n), float("nan"), device="cuda")
         noalloc(U, V, d, G, out, m, n, prec)
         torch.cuda.synchronize()
         got = host(out)
         assert np.isfinite(got).all()
+        assert rel(got, host(ref)) <= TOL[so.PREC_TF32], (call, rel(got, host(ref)))
         want = oracle.project(Uh, Vh, dh, Gh.astype(np.float64))[2]
         assert rel(got, want) <= TOL[prec], (call, rel(got, want))
     opt.close()
