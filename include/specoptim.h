@@ -96,8 +96,8 @@ int specoptim_anchor_update(specoptim_t *h, const float *G_anc, void *stream);
  * s_i = |M v_i| and the long-side factor M V / s (or M^T U / s).  Columns
  * with s_i = 0 are left zero (their d_i is 0).
  * The calling thread waits once per Jacobi sweep for its convergence test (an
- * event on the library's streams, not a synchronisation of `stream`); the
- * call returns with the factor recovery queued on `stream`.
+ * event on the library's streams), and at the end synchronises `stream` once,
+ * after the factor recovery, to read the device flag of the bounded waits.
  * sweeps_out (host pointer, may be NULL) receives the number of sweeps.
  * Returns SPECOPTIM_ERR_NOT_CONVERGED, keeping the previous factors, if the
  * off-diagonal norm is still above svd_tol after svd_max_sweeps sweeps. */
@@ -127,7 +127,8 @@ int specoptim_svd_refresh_many(specoptim_t *const *handles, int32_t count, void 
  *   end: waits (on the host) until that loop has finished -- the GPU keeps
  *     running whatever the caller queued meanwhile -- then enqueues on
  *     `stream` the factor recovery (s, d, U, V) and the step's operand copies
- *     and projectors.  sweeps_out and the return value are those of
+ *     and projectors, and synchronises `stream` once to read the device flag
+ *     of the bounded waits.  sweeps_out and the return value are those of
  *     specoptim_svd_refresh_many.
  * Steps of these handles enqueued between begin and end use the previous
  * factors; steps enqueued after end use the new ones, so the results do not
