@@ -64,25 +64,56 @@ def env_int(name, default):
         return default
 
 
-def profiled_traffic(profile: str, sources, key: str = ""):
-    """DRAM bytes per launch from a committed ncu summary under profiles/, or None
-    when one of the kernel's sources changed since the counters were taken
-    (`key`: the kernel name in front of the figure, for summaries of several kernels)."""
+def strip_comments(text: str) -> str:
+    """C/C++/CUDA source without its comments (string and character literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def code_digest(sources) -> str:
+    """First 16 hex digits of the sha256 of the kernel sources' code: comments and
+    runs of blank space removed, so that a comment edit keeps a profile valid."""
     import hashlib
-    import re
     csrc = os.path.join(ROOT, "spectral_corrected_optimizer_gb300", "csrc")
     h = hashlib.sha256()
     for name in sources:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(" ".join(strip_comments(f.read()).split()).encode())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile: str, sources, key: str = ""):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, or None
+    when the code of one of the kernel's sources changed since the counters were
+    taken (`key`: the kernel name in front of the figure, for summaries of several
+    kernels)."""
+    import re
     try:
         with open(os.path.join(ROOT, "profiles", profile)) as f:
             text = f.read()
     except OSError:
         return None
     m = re.search((re.escape(key) + " " if key else "") +
-                  r"traffic_bytes_per_launch=([0-9.e+]+) sources_sha256_16=([0-9a-f]+)", text)
-    if not m or m.group(2) != h.hexdigest()[:16]:
+                  r"traffic_bytes_per_launch=([0-9.e+]+) code_sha256_16=([0-9a-f]+)", text)
+    if not m or m.group(2) != code_digest(sources):
         return None
     return float(m.group(1))
 

@@ -165,10 +165,13 @@ int specoptim_step(specoptim_t *h, float *W, const float *G_mask, float lr, void
 
 /* The same step for 1 to 16 handles at once (e.g. the 7 weights of one
  * decoder layer), all with learning rate lr: W[i] and G_mask[i] (host arrays
- * of device pointers) belong to handles[i].  Each of the four products runs
- * for all handles in one persistent tensor-core launch (largest problems
- * first), so small matrices fill the SMs the large ones leave idle.  Same
- * results as calling specoptim_step on each handle (without debug outputs). */
+ * of device pointers) belong to handles[i].  The products are grouped by
+ * their position in each handle's chain (first, middle, last, as listed for
+ * specoptim_step): each position runs for all handles in persistent
+ * tensor-core launches of up to 8 products (largest first), so small
+ * matrices fill the SMs the large ones leave idle, and the transposes of G
+ * that the m > n handles need share one launch.  Same results as calling
+ * specoptim_step on each handle (without debug outputs). */
 int specoptim_step_many(specoptim_t *const *handles, int32_t count, float *const *W,
                         const float *const *G_mask, float lr, void *stream);
 

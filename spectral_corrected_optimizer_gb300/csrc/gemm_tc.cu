@@ -2,10 +2,12 @@
 //
 //   C (M x N) = A (M x K) . B (N x K)^T      A, B fp32 row-major, K contiguous
 //
-// These are the four products of the two-sided projection of key design 3
+// It runs the products of the two-sided projection of key design 3
 // ("Communication-Efficient LLM Adaptation over Decentralized GPU Meshes":
-// X = U^T G V, X_filt = diag(d) X diag(d), G_filt = U X_filt V^T), with the
-// diagonal scaling, the convex blend and the AdamW update as epilogues.
+// G_filt = U diag(d) U^T G V diag(d) V^T, evaluated through the projectors
+// U diag(d) U^T and V diag(d) V^T), with the diagonal scaling, the convex
+// blend and the AdamW update as epilogues, and the 3xTF32 products of the SVD
+// refresh (gemm3.cu).
 //
 // Design (one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0      TMA producer: 2D tiled loads (128B swizzle) of a 128 x 32 slab

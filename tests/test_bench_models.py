@@ -42,16 +42,24 @@ def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
     (csrc / "b.cuh").write_bytes(b"shared header")
     sha = hashlib.sha256(b"first kernel" + b"shared header").hexdigest()[:16]
     (tmp_path / "profiles" / "p.md").write_text(
-        "notes\nmachine-readable: k1 traffic_bytes_per_launch=12.5e6 sources_sha256_16=%s\n"
-        "machine-readable: k2 traffic_bytes_per_launch=3e6 sources_sha256_16=%s\n" % (sha, sha))
+        "notes\nmachine-readable: k1 traffic_bytes_per_launch=12.5e6 code_sha256_16=%s\n"
+        "machine-readable: k2 traffic_bytes_per_launch=3e6 code_sha256_16=%s\n" % (sha, sha))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     sources = ("a.cu", "b.cuh")
     assert bench.profiled_traffic("p.md", sources, key="k1") == 12.5e6
     assert bench.profiled_traffic("p.md", sources, key="k2") == 3e6
     assert bench.profiled_traffic("p.md", sources, key="k3") is None
     assert bench.profiled_traffic("missing.md", sources, key="k1") is None
+    # a comment or blank-space edit keeps the figure, a code edit drops it
+    (csrc / "b.cuh").write_bytes(b"shared  // a note\n/* more */ header")
+    assert bench.profiled_traffic("p.md", sources, key="k1") == 12.5e6
     (csrc / "b.cuh").write_bytes(b"shared header, edited")
     assert bench.profiled_traffic("p.md", sources, key="k1") is None
+
+
+def test_strip_comments_keeps_literals():
+    src = 'a = "x // y /* z */"; // line\nb = \'/\'; /* block\n */ c = "\\"//"; // end'
+    assert bench.strip_comments(src) == 'a = "x // y /* z */"; \nb = \'/\';   c = "\\"//"; '
 
 
 @pytest.mark.parametrize("W,K", [(3, 20), (5, 20), (3, 40), (25, 20)])
