@@ -190,6 +190,46 @@ def test_grouped_step_matches_single_steps_at_full_size():
         assert torch.equal(wa, wb)
 
 
+def test_split_refresh_schedule_over_several_periods_at_full_size():
+    """The bench's layer (7 matrices of the 1B layer) over three anchor periods of
+    six steps: refreshes begun at each anchor's arrival and ended three steps
+    later (the library thread runs the sweeps beside the steps) give bit for bit
+    the weights, factors and sweep counts of the one-call schedule whose refresh
+    sits at the same point of each period."""
+    ensure_lib()
+    shapes = synthetic.LLAMA_1B_LAYER
+    inps = synthetic.layer_inputs(shapes, seed=13, rank=32)
+    names = list(inps)
+    a = [so.SpectralOptimizer(*shapes[k]) for k in names]
+    b = [so.SpectralOptimizer(*shapes[k]) for k in names]
+    Wa = [dev(inps[k].weights()) for k in names]
+    Wb = [w.clone() for w in Wa]
+    G_sets = [[dev(inps[k].masked_grad(j)) for k in names] for j in range(2)]
+    sweeps_a, sweeps_b = [], []
+    for period in range(3):
+        for x, y, k in zip(a, b, names):
+            g = dev(inps[k].anchor_grad(period))
+            x.anchor_update(g)
+            y.anchor_update(g)
+        so.svd_refresh_begin(a)
+        for step in range(6):
+            Gs = G_sets[(period + step) % 2]
+            if step == 3:
+                sweeps_a.append(so.svd_refresh_end(a))
+                sweeps_b.append(so.svd_refresh_many(b))
+            so.step_many(a, Wa, Gs, 2e-5)
+            so.step_many(b, Wb, Gs, 2e-5)
+    torch.cuda.synchronize()
+    assert sweeps_a == sweeps_b and all(min(s) >= 1 for s in sweeps_a)
+    for wa, wb in zip(Wa, Wb):
+        assert torch.isfinite(wa).all() and torch.equal(wa, wb)
+    for x, y in zip(a, b):
+        for fa, fb in zip(x.get_factors(), y.get_factors()):
+            assert torch.equal(fa, fb)
+    for x in a + b:
+        x.close()
+
+
 def test_device_wait_timeout_is_reported_and_context_survives():
     ensure_lib()
     lib = so.lib()
