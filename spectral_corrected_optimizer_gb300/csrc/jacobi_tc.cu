@@ -99,7 +99,8 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
     extern __shared__ __align__(1024) unsigned char ct_smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(ct_smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes);
+    // barriers after the output staging tile (which starts at STAGES * kStageBytes)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes + kXBytes);
     uint64_t *full = bars;                 // [STAGES] TMA landed
     uint64_t *split = full + STAGES;      // [STAGES] X split (128 arrivals)
     uint64_t *empty = split + STAGES;     // [STAGES] MMAs done with the stage
