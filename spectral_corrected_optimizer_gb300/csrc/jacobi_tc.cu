@@ -3,20 +3,23 @@
 // Task = (matrix, 128-row slab, pair p):
 //   X (128 x 64)  = IN[slab rows, cols(p)]        two TMA boxes of 32 columns
 //   R_p^T hi / lo (64 x 64 each)                  four TMA boxes
-//   X is split in shared memory into hi = rna_tf32(x) and lo = rna_tf32(x - hi)
-//   (element-wise, so the 128-byte swizzle of the TMA layout is kept), then one
-//   thread issues 24 tcgen05.mma (M = 128, N = 64, K = 8) into a 64-column TMEM
-//   accumulator:  D = Xhi.Rhi + Xhi.Rlo + Xlo.Rhi  (3xTF32, fp32-accurate, the
-//   lo.lo term is below fp32 rounding).  D is staged in shared memory in the
-//   box layout of the output (as is, or transposed) and stored with TMA.
+//   X is split into hi = rna_tf32(x), kept in place in the swizzled shared
+//   tile, and lo = rna_tf32(x - hi), written to TMEM (lane = row of the slab);
+//   then one thread issues 24 tcgen05.mma (M = 128, N = 64, K = 8) into a
+//   64-column TMEM accumulator:  D = Xhi.Rhi + Xhi.Rlo + Xlo.Rhi  (3xTF32,
+//   fp32-accurate, the lo.lo term is below fp32 rounding), the last 8 with
+//   their A operand read from TMEM.  D is staged in shared memory in the box
+//   layout of the output (as is, or transposed) and stored with TMA.
+// Keeping X lo out of shared memory leaves room for three stages of 64 KB.
 // One persistent CTA per SM takes a contiguous range of tasks, with warp roles:
-//   warp 0      TMA producer into a two-stage ring (X, R hi, R lo, X lo per stage)
-//   warp 1      TMEM (two 64-column accumulators) and the MMA issuer
-//   warps 2-5   split X of the next stage into hi / lo
+//   warp 0      TMA producer into a three-stage ring (X, R hi, R lo per stage)
+//   warp 1      TMEM (two 64-column accumulators, X lo of each stage) and the
+//               MMA issuer
+//   warps 2-5   split X of the next stage: one thread per row, lo to its TMEM lane
 //   warps 6-9   epilogue: tcgen05.ld of their lane quarter, staging, TMA store
-// so the loads of task i+1, the split of task i+1, the MMAs of task i and the
-// stores of task i-1 overlap.  Every mbarrier wait is bounded; a wait that
-// gives up records a code in the library's device flag and the role stops.
+// so the loads of tasks i+1 and i+2, the split of task i+1, the MMAs of task i
+// and the stores of task i-1 overlap.  Every mbarrier wait is bounded; a wait
+// that gives up records a code in the library's device flag and the role stops.
 #include <algorithm>
 #include <cstring>
 
@@ -34,12 +37,14 @@ constexpr uint32_t kXBytes = 2 * kXAtom;        // the 64 columns of a pair
 constexpr uint32_t kRAtom = kP * 128;           // 32 columns x 64 rows: 8 KB
 constexpr uint32_t kRBytes = 2 * kRAtom;        // one part (hi or lo) of R_p^T
 constexpr uint32_t kLoadBytes = kXBytes + 2 * kRBytes;   // X raw + R hi + R lo
-constexpr uint32_t kStageBytes = kLoadBytes + kXBytes;   // + X lo
-constexpr uint32_t kTmemCols = 128;                      // two accumulators
+constexpr uint32_t kStageBytes = kLoadBytes;             // X lo lives in TMEM
+constexpr uint32_t kTmemCols = 512;                      // two accumulators + X lo of each stage
+constexpr uint32_t kLoCol = 128;                         // X lo of stage s at columns kLoCol + 64 s
 // stages, output staging (one 128 x 64 tile), barriers
 constexpr size_t ct_smem(int stages) { return (size_t)stages * kStageBytes + kXBytes + 1024 /*align*/ + 128; }
-constexpr int kStages = 2;
-static_assert(ct_smem(2) <= 232448, "shared memory budget of one CTA");
+constexpr int kStages = 3;
+static_assert(ct_smem(kStages) <= 232448, "shared memory budget of one CTA");
+static_assert(kLoCol + 64 * kStages <= kTmemCols, "TMEM columns");
 constexpr uint32_t kCtIdesc = tf32_idesc(kCtRows, kP);
 
 struct CtBatch {
@@ -91,6 +96,41 @@ __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo) {
     h.z = tf32_split(v.z, lo.z);
     h.w = tf32_split(v.w, lo.w);
     return h;
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&v)[64]) {
+    uint32_t u[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
+        "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, "
+        "%33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, "
+        "%49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};"
+        :
+        : "r"(taddr),
+          "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+          "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]),
+          "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]),
+          "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31]),
+          "r"(u[32]), "r"(u[33]), "r"(u[34]), "r"(u[35]), "r"(u[36]), "r"(u[37]), "r"(u[38]), "r"(u[39]),
+          "r"(u[40]), "r"(u[41]), "r"(u[42]), "r"(u[43]), "r"(u[44]), "r"(u[45]), "r"(u[46]), "r"(u[47]),
+          "r"(u[48]), "r"(u[49]), "r"(u[50]), "r"(u[51]), "r"(u[52]), "r"(u[53]), "r"(u[54]), "r"(u[55]),
+          "r"(u[56]), "r"(u[57]), "r"(u[58]), "r"(u[59]), "r"(u[60]), "r"(u[61]), "r"(u[62]), "r"(u[63])
+        : "memory");
+}
+
+// D (TMEM) += A . B^T with A (128 x 8 tf32) in TMEM (lane = row, column = k)
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 template <int STAGES>
@@ -169,21 +209,27 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
                 if (!mbar_wait_bounded(&tempty[a], ((uint32_t)(i >> 1) & 1u) ^ 1u, flag, 0x203u)) break;
                 tc_fence_after();
                 unsigned char *st = smem + s * kStageBytes;
-                const uint32_t a_hi = smem_u32(st), b_hi = a_hi + kXBytes, b_lo = b_hi + kRBytes,
-                               a_lo = a_hi + kLoadBytes;
-                const uint32_t as[3] = {a_hi, a_hi, a_lo}, bs[3] = {b_hi, b_lo, b_hi};
+                const uint32_t a_hi = smem_u32(st), b_hi = a_hi + kXBytes, b_lo = b_hi + kRBytes;
+                const uint32_t a_lo = tmem + kLoCol + 64u * (uint32_t)s;
+                const uint32_t bs[2] = {b_hi, b_lo};
                 const uint32_t d = tmem + (uint32_t)(a * kP);
                 uint32_t acc = 0;
 #pragma unroll
-                for (int u = 0; u < 3; ++u)
+                for (int u = 0; u < 2; ++u)
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            mma_tf32(d, smem_desc_sw128(as[u] + kk * kXAtom + q * 32),
+                            mma_tf32(d, smem_desc_sw128(a_hi + kk * kXAtom + q * 32),
                                      smem_desc_sw128(bs[u] + kk * kRAtom + q * 32), kCtIdesc, acc);
                             acc = 1;
                         }
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        mma_tf32_ta(d, a_lo + (uint32_t)(8 * (4 * kk + q)),
+                                    smem_desc_sw128(b_hi + kk * kRAtom + q * 32), kCtIdesc, 1u);
                 mma_commit(&empty[s]);  // stage free once these MMAs have read it
                 mma_commit(&tfull[a]);  // accumulator ready once they completed
             }
@@ -192,19 +238,30 @@ jacobi_rotate_kernel(const __grid_constant__ CtBatch cb, unsigned *flag) {
         }
     } else if (warp < 6) {
         // ---------------- split X into hi (in place) and lo
-        const int tid = threadIdx.x - 64;
+        // thread = row r of the slab = TMEM lane r (this warp's lane quarter)
+        const int q = warp & 3, r = 32 * q + lane;
         for (int i = 0; i < n; ++i) {
             const int s = i % STAGES;
             if (!mbar_wait_bounded(&full[s], (uint32_t)(i / STAGES) & 1u, flag, 0x204u)) break;
             unsigned char *st = smem + s * kStageBytes;
-            float4 *h4 = reinterpret_cast<float4 *>(st), *l4 = reinterpret_cast<float4 *>(st + kLoadBytes);
-#pragma unroll 4
-            for (int e = tid; e < (int)(kXBytes / 16); e += 128) {
-                float4 lo;
-                h4[e] = split_hi(h4[e], lo);
-                l4[e] = lo;
-            }
+            float lo[64];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    // 16-byte chunk c of row r of atom kk sits at chunk c ^ (r % 8) (128-byte swizzle)
+                    float4 *p = reinterpret_cast<float4 *>(st + kk * kXAtom + r * 128 + ((c ^ (r & 7)) << 4));
+                    float4 l;
+                    *p = split_hi(*p, l);
+                    lo[32 * kk + 4 * c] = l.x;
+                    lo[32 * kk + 4 * c + 1] = l.y;
+                    lo[32 * kk + 4 * c + 2] = l.z;
+                    lo[32 * kk + 4 * c + 3] = l.w;
+                }
+            tmem_st64(tmem + ((uint32_t)(32 * q) << 16) + kLoCol + 64u * (uint32_t)s, lo);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+            tc_fence_before();
             mbar_arrive(&split[s]);
         }
     } else {

@@ -62,7 +62,17 @@ __device__ __forceinline__ int find_job(const int *off, int count, int item) {
     return i;
 }
 
-constexpr int kSolveThreads = 256;
+constexpr int kSolveThreads = 256;  // threads per pair subproblem
+// Two pairs per CTA, each 256-thread half with a named barrier of its own: the
+// round's solves then hold half as many SMs (88 for the 1B layer's 176 pairs),
+// so the Q rotation launched beside them on 3/8 of the SMs finds its SMs free
+// (measured: two 256-thread CTAs on one SM run the solve as fast as one).
+constexpr int kSolvePairsPerCta = 2;
+
+// barrier of this thread's pair (id 0 is the CTA-wide __syncthreads)
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)(threadIdx.x / kSolveThreads)), "n"(kSolveThreads) : "memory");
+}
 
 // Rotation (c, s) of one pair from approximate reciprocal / square-root
 // intrinsics (a few ulp each): c^2 + s^2 = 1 to a few ulp, the same order as
@@ -115,7 +125,7 @@ constexpr int kSBuf = kP * kSP;  // floats per copy of S
 constexpr int kCsSlot = 36;  // float2 per slot (4 x 8 entries + skew, 16-byte multiple)
 __device__ __forceinline__ int cs_index(int k) { return (k >> 3) * 8 + (k & 7) + ((k >> 4) << 1); }
 
-// One CTA (8 warps) per pair: load the 64 x 64 subproblem S, run up to
+// 8 warps per pair (half a CTA): load the 64 x 64 subproblem S, run up to
 // `inner_sweeps` cyclic Jacobi sweeps (32 disjoint rotations per step) and
 // write the accumulated rotation R (64 x 64), split for 3xTF32.
 //  * Every warp computes all 32 rotations of a step itself (lane l owns pair
@@ -131,6 +141,7 @@ __device__ __forceinline__ int cs_index(int k) { return (k >> 3) * 8 + (k & 7) +
 //    values to the next positions, exchanging one value with each
 //    neighbouring quarter by shuffles.
 constexpr size_t kSolveSmem = (2 * (size_t)kSBuf + 2 * 2 * (size_t)kCsSlot) * 4 + 16;
+static_assert(kSolveSmem % 16 == 0, "each pair's shared memory starts 16-byte aligned");
 
 struct SolveState {
     float rt[8], rb[8];       // this thread's part of R (top / bottom positions of 8 pairs)
@@ -175,7 +186,7 @@ __device__ __forceinline__ void solve_step(float *S0, float2 *csb, SolveState &s
         Sn[st.wr_b[u] + st.wct] = z21;
         Sn[st.wr_b[u] + st.wcb] = sn * y21 + c * y22;
     }
-    __syncthreads();
+    pair_sync();
     // R <- R J_step on this thread's pairs, then the positions move on
     const float4 *cs4 = reinterpret_cast<const float4 *>(csb + FROM * kCsSlot + 8 * st.m + 2 * (st.m >> 1));
 #pragma unroll
@@ -213,7 +224,7 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
     const int Np = jb.Np[job], nb = Np / kB, round = jb.round[job];
     const int pair = item - jb.pair_off[job];
     const float *A = jb.A[job];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x % kSolveThreads, lane = tid & 31, warp = tid >> 5;
     // the subproblem in its start order (position = local index), copy 0
     for (int e = tid; e < kP * (kP / 4); e += kSolveThreads) {
         const int i = e / (kP / 4), j4 = (e % (kP / 4)) * 4;
@@ -246,7 +257,7 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
         st.wr_t[u] = cat_next(ka) * kSP;
         st.wr_b[u] = cat_next(kB + ka) * kSP;
     }
-    __syncthreads();
+    pair_sync();
     // A sweep has an odd number of steps (63): the copy holding S alternates
     // between sweeps.  The convergence test only matters with more than one sweep.
     const bool track = inner_sweeps > 1;
@@ -280,7 +291,7 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
                 red[1] = st.dmax;
             }
         }
-        __syncthreads();
+        pair_sync();
         // red is rewritten only after the next sweep's barriers
         if (red[0] <= 1e-7f * red[1]) break;
     }
@@ -294,7 +305,7 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
         Rs[ri * kTP + 8 * st.m + q] = st.rt[q];
         Rs[ri * kTP + kB + 8 * st.m + q] = st.rb[q];
     }
-    __syncthreads();
+    pair_sync();
     float *Rp = jb.R[job] + (size_t)pair * 2 * kP * kP;
     for (int e = tid; e < kP * kP / 2; e += kSolveThreads) {
         const int jj = e / (kP / 2), k2 = (e % (kP / 2)) * 2;
@@ -306,11 +317,14 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
     }
 }
 
-// Subproblem solves of one round: one CTA per pair.
-__global__ void __launch_bounds__(kSolveThreads)
-jacobi_solve_kernel(const JacBatch js, int inner_sweeps) {
+// Subproblem solves of one round: kSolvePairsPerCta pairs per CTA, each on its
+// own 256 threads and its own part of shared memory.
+__global__ void __launch_bounds__(kSolveThreads * kSolvePairsPerCta)
+jacobi_solve_kernel(const JacBatch js, int inner_sweeps, int pairs) {
     extern __shared__ __align__(16) unsigned char solve_smem[];
-    solve_pair(js, blockIdx.x, inner_sweeps, solve_smem);
+    const int half = threadIdx.x / kSolveThreads, item = blockIdx.x * kSolvePairsPerCta + half;
+    if (item >= pairs) return;  // a whole half: it takes part in no barrier
+    solve_pair(js, item, inner_sweeps, solve_smem + half * kSolveSmem);
 }
 
 __global__ void eye_kernel(float *__restrict__ Q, int Np) {
@@ -654,7 +668,7 @@ int finish(const SvdJob &a, const JobBufs &b, cudaStream_t st) {
 }  // namespace
 
 int set_solve_attributes() {
-    return set_smem_limit(reinterpret_cast<const void *>(&jacobi_solve_kernel), kSolveSmem);
+    return set_smem_limit(reinterpret_cast<const void *>(&jacobi_solve_kernel), kSolvePairsPerCta * kSolveSmem);
 }
 
 // Streams and events of one refresh call's Jacobi loop (created per call: a few
@@ -785,7 +799,10 @@ int sweep_loop(SvdRun &R) {
     auto solve = [&](long gg) -> int {
         set_round(gg);
         SPECOPTIM_CUDA(cudaStreamWaitEvent(hi, js_.q_done[gg & 1], 0));
-        SPCO_LAUNCH("svd_jacobi_solve", hi, jacobi_solve_kernel<<<solve_grid, kSolveThreads, kSolveSmem, hi>>>(jb, inner));
+        SPCO_LAUNCH("svd_jacobi_solve", hi,
+                    jacobi_solve_kernel<<<(solve_grid + kSolvePairsPerCta - 1) / kSolvePairsPerCta,
+                                          kSolveThreads * kSolvePairsPerCta, kSolvePairsPerCta * kSolveSmem, hi>>>(
+                        jb, inner, solve_grid));
         SPECOPTIM_LAUNCHED("jacobi_solve_kernel");
         return SPECOPTIM_OK;
     };
