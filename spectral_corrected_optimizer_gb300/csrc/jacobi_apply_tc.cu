@@ -28,9 +28,12 @@
 //               through a 32 x 33 shared tile per warp)
 // Every mbarrier wait is bounded; a wait that gives up records a code in the
 // library's device flag and that role stops (the producer and the MMA issuer
-// first let their last copies and MMAs land).
+// first let their last copies and MMAs land).  The kernel is launched as a
+// programmatic dependent of the round's solve: its set-up (barriers, TMEM)
+// runs on the SMs the solve's CTAs leave, before the solve has finished.
 #include <algorithm>
 #include <cstring>
+#include <string>
 
 #include "gemm.cuh"
 #include "jacobi.cuh"
@@ -203,6 +206,9 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // Launched as a programmatic dependent of the round's solve: the set-up above
+    // overlaps the solve's last CTAs; A and the rotations are read only past here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         if (lane == 0) {
@@ -376,7 +382,22 @@ int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st) {
     ab.total = ab.task_off[ab.count];
     if (int rc = set_smem_limit(reinterpret_cast<const void *>(&jacobi_apply_kernel), kApSmem)) return rc;
     const int grid = std::min(num_sms(), ab.total);
-    SPCO_LAUNCH("svd_jacobi_apply", st, jacobi_apply_kernel<<<grid, kApThreads, kApSmem, st>>>(ab, device_flag_ptr()));
+    // programmatic dependent launch: the CTAs may start on SMs the solve before it
+    // leaves, and wait (griddepcontrol.wait) for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kApThreads);
+    cfg.dynamicSmemBytes = kApSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    unsigned *flag = device_flag_ptr();
+    cudaError_t err = cudaSuccess;
+    SPCO_LAUNCH("svd_jacobi_apply", st, err = cudaLaunchKernelEx(&cfg, jacobi_apply_kernel, ab, flag));
+    if (err != cudaSuccess) return fail(SPECOPTIM_ERR_CUDA, std::string("jacobi_apply: ") + cudaGetErrorString(err));
     SPECOPTIM_LAUNCHED("jacobi_apply_kernel");
     return SPECOPTIM_OK;
 }

@@ -322,6 +322,8 @@ __device__ void solve_pair(const JacBatch &jb, int item, int inner_sweeps, unsig
 __global__ void __launch_bounds__(kSolveThreads * kSolvePairsPerCta)
 jacobi_solve_kernel(const JacBatch js, int inner_sweeps, int pairs) {
     extern __shared__ __align__(16) unsigned char solve_smem[];
+    // the apply that follows (a programmatic dependent) may set up on SMs this grid leaves
+    asm volatile("griddepcontrol.launch_dependents;");
     const int half = threadIdx.x / kSolveThreads, item = blockIdx.x * kSolvePairsPerCta + half;
     if (item >= pairs) return;  // a whole half: it takes part in no barrier
     solve_pair(js, item, inner_sweeps, solve_smem + half * kSolveSmem);
