@@ -78,8 +78,10 @@ struct ApJob {
 
 constexpr int kApMaxJobs = 16;
 
-// Launches the two-sided rotation of `count` (<= 16) matrices in one kernel.
-int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st);
+// Launches the two-sided rotation of `count` (<= 16) matrices in one kernel;
+// `after_solve`: as a programmatic dependent of the solve launched just before
+// it on `st` (the kernel waits for that solve's results before reading A).
+int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st, bool after_solve = false);
 
 // Launches the rotation of `count` (<= 32) matrices in one kernel on at most
 // `max_ctas` SMs (0: all of them).

@@ -29,8 +29,9 @@
 // Every mbarrier wait is bounded; a wait that gives up records a code in the
 // library's device flag and that role stops (the producer and the MMA issuer
 // first let their last copies and MMAs land).  The kernel is launched as a
-// programmatic dependent of the round's solve: its set-up (barriers, TMEM)
-// runs on the SMs the solve's CTAs leave, before the solve has finished.
+// programmatic dependent of the round's solve when the solve fits in one wave
+// beside the Q rotation: its set-up (barriers, TMEM) then runs on the SMs the
+// solve's CTAs leave, before the solve has finished.
 #include <algorithm>
 #include <cstring>
 #include <string>
@@ -365,7 +366,7 @@ jacobi_apply_kernel(const __grid_constant__ ApBatch ab, unsigned *flag) {
 
 }  // namespace
 
-int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st) {
+int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st, bool after_solve) {
     if (count < 1 || count > kApMaxJobs) return fail(SPECOPTIM_ERR_INVALID_ARG, "jacobi_apply: 1 to 16 matrices");
     ApBatch ab;
     std::memset(&ab, 0, sizeof(ab));
@@ -382,8 +383,8 @@ int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st) {
     ab.total = ab.task_off[ab.count];
     if (int rc = set_smem_limit(reinterpret_cast<const void *>(&jacobi_apply_kernel), kApSmem)) return rc;
     const int grid = std::min(num_sms(), ab.total);
-    // programmatic dependent launch: the CTAs may start on SMs the solve before it
-    // leaves, and wait (griddepcontrol.wait) for its results
+    // programmatic dependent launch (after_solve): the CTAs may start on SMs the
+    // solve before it leaves, and wait (griddepcontrol.wait) for its results
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kApThreads);
@@ -393,7 +394,7 @@ int jacobi_apply(const ApJob *jobs, int count, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_solve ? 1 : 0;
     unsigned *flag = device_flag_ptr();
     cudaError_t err = cudaSuccess;
     SPCO_LAUNCH("svd_jacobi_apply", st, err = cudaLaunchKernelEx(&cfg, jacobi_apply_kernel, ab, flag));

@@ -779,6 +779,12 @@ int sweep_loop(SvdRun &R) {
         qjob[i] = CtJob{&m[1], &m[1], &m[2], b[i].Np, 0, 0, 0, 1};
     }
     const int solve_grid = jb.pair_off[count];
+    // the apply starts as a programmatic dependent of the solve only while the
+    // solve's CTAs fit one per SM beside the Q rotation (measured: with more,
+    // e.g. a 14-matrix or a 7B-shaped batch, the early apply CTAs cost more
+    // than the launch they hide)
+    const int q_ctas = num_sms() * 3 / 8;
+    const bool apply_after_solve = (solve_grid + kSolvePairsPerCta - 1) / kSolvePairsPerCta <= num_sms() - q_ctas;
     int inner = 1;
     for (int i = 0; i < count; ++i) inner = std::max(inner, jobs[i].inner_sweeps);
     if ((rc = set_solve_attributes())) return rc;
@@ -818,12 +824,12 @@ int sweep_loop(SvdRun &R) {
     for (int sweep = 0; sweep < max_sweeps && active > 0; ++sweep) {
         for (int k = 0; k < rounds; ++k, ++g) {
             set_round(g);
-            if ((rc = jacobi_apply(ajob, count, hi))) return rc;
+            if ((rc = jacobi_apply(ajob, count, hi, apply_after_solve))) return rc;
             SPECOPTIM_CUDA(cudaEventRecord(js_.a_done[g & 1], hi));
             SPECOPTIM_CUDA(cudaStreamWaitEvent(lo, js_.a_done[g & 1], 0));
             // on 3/8 of the SMs: the solves take the rest, and the next round's
             // rotation of A finds SMs free sooner (measured best among 1/4 .. all)
-            if ((rc = jacobi_rotate(qjob, count, lo, num_sms() * 3 / 8))) return rc;
+            if ((rc = jacobi_rotate(qjob, count, lo, q_ctas))) return rc;
             SPECOPTIM_CUDA(cudaEventRecord(js_.q_done[g & 1], lo));
             // the sweep's last solve (the next sweep's first) goes after the convergence test
             if (k + 1 < rounds && (rc = solve(g + 1))) return rc;
