@@ -986,7 +986,9 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
         compute.wait_event(loaded[b])
         what = layer.schedule(i, t0)
         if what == "refresh":
+            t = time.perf_counter()
             layer.refresh(0, G=devA[b])
+            refresh_host.append((time.perf_counter() - t) * 1e3)
         elif what == "begin":
             layer.refresh_end()
             layer.refresh_begin(0, G=devA[b])
@@ -1023,23 +1025,27 @@ def run_e2e(layer: Layer, K: int, W: int, dist_ok: bool, world: int):
         compute.wait_stream(back)
 
     samples = []
-    for _ in range(E2E_REPEATS):
-        layer.reset_state()  # the same steps as the device-resident timed region, same refresh history
-        run(0, W)
-        stats["h2d"] = stats["d2h"] = 0
-        layer.last_sweeps = None
-        host = []
+    refresh_host = []
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for _ in range(E2E_REPEATS):
+            layer.reset_state()  # the same steps as the device-resident timed region, same refresh history
+            run(0, W)
+            stats["h2d"] = stats["d2h"] = 0
+            layer.last_sweeps = None
+            host = []
+            refresh_host.clear()
 
-        def enqueue():
-            t = time.perf_counter()
-            run(W, K)
-            layer.refresh_end()
-            host.append((time.perf_counter() - t) * 1e3)
+            def enqueue():
+                t = time.perf_counter()
+                run(W, K)
+                layer.refresh_end()
+                host.append((time.perf_counter() - t) * 1e3)
 
-        ms = max_over_ranks(timed(torch, enqueue, dist_ok), dist_ok)
-        samples.append((ms, host[0], dict(stats), layer.last_sweeps))
-    ms, host_ms, st, sweeps = sorted(samples, key=lambda x: x[0])[len(samples) // 2]
+            ms = max_over_ranks(timed(torch, enqueue, dist_ok), dist_ok)
+            samples.append((ms, host[0], dict(stats), layer.last_sweeps, list(refresh_host)))
+    ms, host_ms, st, sweeps, rh = sorted(samples, key=lambda x: x[0])[len(samples) // 2]
     return {"value": world * K / (ms * 1e-3), "unit": "steps/s", "host_enqueue_ms": host_ms, "device_ms": ms,
+            "refresh_call_ms": rh, "clocks": clocks.summary(),
             "h2d_bytes_per_step": st["h2d"] // K, "d2h_bytes_per_step": st["d2h"] // K,
             "timed_refresh_sweeps": sweeps,
             "samples_steps_per_s": [world * K / (x[0] * 1e-3) for x in samples],
