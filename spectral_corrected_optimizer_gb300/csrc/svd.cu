@@ -43,8 +43,8 @@ constexpr int kMaxBatch = 16;
 
 // All matrices of one batched refresh.  Each matrix i has Np[i] (a multiple of
 // 128) padded indices in nb = Np/32 blocks; in its round `round[i]` the blocks
-// meet in Np/64 pairs.  The solve kernel takes one CTA per pair, numbered over
-// the whole batch through pair_off.  R[i] points at the rotation slot of the
+// meet in Np/64 pairs.  The solve kernel takes 256 threads per pair (two pairs
+// per CTA), the pairs numbered over the whole batch through pair_off.  R[i] points at the rotation slot of the
 // round: per pair, R_p^T split for 3xTF32 (hi block, then lo block, 64 x 64 each).
 struct JacBatch {
     int count;
