@@ -4,12 +4,13 @@
 //
 // GPU formulation (fp32):
 //   1. Gram matrix of the short side, A = M^T M (m >= n) or M M^T (m < n),
-//      r x r, zero-padded to Np (a multiple of 64), in fp32-accurate 3xTF32
+//      r x r, zero-padded to Np (a multiple of 128), in fp32-accurate 3xTF32
 //      tensor-core products; with a previous factor W the start is W^T A W.
 //   2. Block-Jacobi eigen-decomposition A = Q diag(lambda) Q^T.  The Np/32
 //      blocks of 32 indices meet in round-robin order; in each round every
-//      pair of blocks forms a 64 x 64 subproblem that one CTA sweeps in shared
-//      memory (cyclic Jacobi, parallel order), giving a 64 x 64 rotation R_p
+//      pair of blocks forms a 64 x 64 subproblem that 256 threads sweep in
+//      shared memory (cyclic Jacobi, parallel order; two pairs per CTA),
+//      giving a 64 x 64 rotation R_p
 //      per pair (R = the block-diagonal of all R_p in the round's order).  The
 //      rotations are applied on the tensor cores (3xTF32): A <- R^T A R in one
 //      pass over its upper 128 x 128 super-tiles (jacobi_apply_tc.cu), and
